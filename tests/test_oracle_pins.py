@@ -1,0 +1,351 @@
+"""Pins for the CPU oracle: checks against things other than the oracle itself.
+
+- a hand-worked example whose every value was derived by hand (golden file);
+- the packed layout on hand-derived one-hot bytes (golden file);
+- exact rational arithmetic (Python Fractions / ints) on tiny random shapes;
+- a library routine (numpy int64 matmul) for the integer contraction;
+- a closed form (fraction of zero codes for Gaussian weights);
+- invariants and degenerate cases.
+
+Sources of the definitions: the 2B4T report translation on
+blog.csdn.net/soaring_casia ("原生1.58bit大模型"), section 2 "BitLinear层"
+items 1-3 (absmean ternary weights, per-token absmax int8 activations, subln);
+"BitNet b1.58 深度解析" (chenxutan.com) section 2.3(2) for the rescale.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+
+F32_EPS = Fraction(1, 2 ** 23)
+
+
+# ---------------------------------------------------------------- helpers
+def fl32(fr: Fraction) -> np.float32:
+    """Round an exact rational to the nearest binary32, ties to even."""
+    f = np.float32(float(fr))
+    cands = [np.nextafter(f, np.float32(-np.inf)), f,
+             np.nextafter(f, np.float32(np.inf))]
+    best, bestd = None, None
+    for c in cands:
+        d = abs(Fraction(float(c)) - fr)
+        if bestd is None or d < bestd or (
+                d == bestd and (np.array(c).view(np.uint32) & 1) == 0):
+            best, bestd = c, d
+    return np.float32(best)
+
+
+def rne(fr: Fraction) -> int:
+    fl = math.floor(fr)
+    diff = fr - fl
+    if diff > Fraction(1, 2):
+        return fl + 1
+    if diff < Fraction(1, 2):
+        return fl
+    return fl if fl % 2 == 0 else fl + 1
+
+
+def near_half(fr: Fraction, rel=Fraction(1, 2 ** 22)) -> bool:
+    """True if fr is within a couple of fp32 ulps of a rounding boundary."""
+    d = abs(fr - math.floor(fr) - Fraction(1, 2))
+    return d <= abs(fr) * rel + Fraction(1, 2 ** 40)
+
+
+FEPS = fl32(Fraction(1, 100000))  # the fp32 constant 1e-5f
+
+
+# ---------------------------------------------------------------- pin-1
+def test_hand_example(golden_dir):
+    with open(os.path.join(golden_dir, "hand_example.json")) as f:
+        gd = json.load(f)
+    W = np.array(gd["W"], np.float32)
+    x = np.array(gd["x"], np.float32)
+    g = oracle.gamma(W)
+    assert Fraction(float(W.__abs__().sum())) / W.size == Fraction(gd["mean_abs_W"])
+    assert g == fl32(Fraction(gd["mean_abs_W"]) + Fraction(float(FEPS)))
+    q = oracle.ternarize(W, g)
+    assert q.tolist() == gd["Wq"]
+    xq, s = oracle.quant_act(x)
+    assert s.tolist() == gd["s"]
+    assert xq.tolist() == gd["xq"]
+    acc = oracle.matmul_i32(q, xq)
+    assert acc.tolist() == gd["acc"]
+    packed = oracle.pack(q)
+    assert [bytes(r).hex() for r in packed] == gd["packed_rows_hex"]
+    y = oracle.forward_packed(packed, g, 2, 4, x)
+    for m in range(2):
+        for n in range(2):
+            a = gd["acc"][m][n]
+            exact_two_roundings = fl32(Fraction(float(fl32(a * Fraction(float(g)))))
+                                       / Fraction(gd["s"][m]))
+            assert y[m, n] == exact_two_roundings
+            e = a * Fraction(float(g)) / Fraction(gd["s"][m])
+            assert abs(Fraction(float(y[m, n])) - e) <= abs(e) * F32_EPS
+
+
+def test_weight_ties_round_half_to_even(golden_dir):
+    with open(os.path.join(golden_dir, "weight_tie_example.json")) as f:
+        gd = json.load(f)
+    W = np.array([[float.fromhex(v) for v in row] for row in gd["W_hex"]], np.float32)
+    g = oracle.gamma(W)
+    assert float(g) == float.fromhex(gd["gamma_hex"])
+    assert Fraction(float(W[0, 0])) / Fraction(float(g)) == Fraction(1, 2)
+    assert oracle.ternarize(W, g).tolist() == gd["Wq"]
+
+
+def test_pack_layout_onehot(golden_dir):
+    with open(os.path.join(golden_dir, "pack_layout_onehot.json")) as f:
+        gd = json.load(f)
+    K = gd["K"]
+    assert oracle.row_bytes(K) == gd["row_bytes"]
+    for c in gd["cases"]:
+        q = np.zeros((1, K), np.int8)
+        q[0, c["k"]] = c["q"]
+        p = oracle.pack(q)[0]
+        expect = np.full(gd["row_bytes"], 0x55, np.uint8)
+        expect[c["byte"]] = int(c["value"], 16)
+        assert p.tolist() == expect.tolist(), c
+        assert oracle.unpack(p[None, :], K).tolist() == q.tolist()
+
+
+@pytest.mark.parametrize("K", [1, 15, 16, 63, 64, 65, 100, 512])
+def test_pack_roundtrip_and_padding(K):
+    rng = np.random.default_rng(K)
+    q = rng.integers(-1, 2, size=(5, K)).astype(np.int8)
+    p = oracle.pack(q)
+    assert p.shape == (5, 16 * ((K + 63) // 64))
+    assert oracle.unpack(p, K).tolist() == q.tolist()
+    # no code 3 anywhere; padded weights decode to 0
+    bits = np.unpackbits(p, bitorder="little").reshape(5, -1, 2)
+    codes = bits[..., 0] + 2 * bits[..., 1]
+    assert codes.max() <= 2
+    Kp = 4 * p.shape[1]
+    qp = oracle.unpack(p, Kp)
+    assert (qp[:, K:] == 0).all()
+
+
+# ---------------------------------------------------------------- pin-3 brute force
+@pytest.mark.parametrize("seed", range(6))
+def test_bruteforce_rational(seed):
+    rng = np.random.default_rng(100 + seed)
+    N = int(rng.integers(1, 24))
+    K = int(rng.integers(1, 48))
+    M = int(rng.integers(1, 5))
+    W = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    x = rng.standard_normal((M, K)).astype(np.float32)
+    if seed % 2:
+        x[:, 0] *= 20
+    # gamma: exact rational mean, one rounding, then + 1e-5f with one rounding
+    S = sum(Fraction(abs(float(w))) for w in W.ravel())
+    g = oracle.gamma(W)
+    assert g == fl32(Fraction(float(fl32(S / (N * K)))) + Fraction(float(FEPS)))
+    # codes: exact rational round of W/gamma, except within ~1 ulp of a tie
+    q = oracle.ternarize(W, g)
+    G = Fraction(float(g))
+    skipped = 0
+    for (n, k), w in np.ndenumerate(W):
+        r = Fraction(float(w)) / G
+        if near_half(r):
+            skipped += 1
+            continue
+        assert q[n, k] == max(-1, min(1, rne(r)))
+    assert skipped <= 1
+    # activations
+    xq, s = oracle.quant_act(x)
+    for m in range(M):
+        amax = max(abs(Fraction(float(v))) for v in x[m])
+        assert s[m] == fl32(Fraction(127) / max(amax, Fraction(float(FEPS))))
+        S_ = Fraction(float(s[m]))
+        for k in range(K):
+            p = Fraction(float(x[m, k])) * S_
+            if near_half(p):
+                continue
+            assert xq[m, k] == max(-128, min(127, rne(p)))
+    # contraction: Python ints and numpy's int64 matmul
+    acc = oracle.matmul_i32(q, xq)
+    for m in range(M):
+        for n in range(N):
+            assert acc[m, n] == sum(int(q[n, k]) * int(xq[m, k]) for k in range(K))
+    assert (acc == xq.astype(np.int64) @ q.astype(np.int64).T).all()
+    # y within one fp32 ulp of the exact rational (acc * gamma / s)
+    y = oracle.rescale(acc, g, s)
+    for m in range(M):
+        for n in range(N):
+            e = int(acc[m, n]) * G / Fraction(float(s[m]))
+            assert abs(Fraction(float(y[m, n])) - e) <= abs(e) * F32_EPS
+            # the definition's two single roundings, evaluated exactly:
+            # fl32( fl32(acc * gamma) / s ) -- a divide, not a reciprocal-multiply
+            t = Fraction(float(fl32(int(acc[m, n]) * G)))
+            assert y[m, n] == fl32(t / Fraction(float(s[m])))
+    # forward from packed == the pieces
+    y2 = oracle.forward_packed(oracle.pack(q), g, N, K, x)
+    assert (y2.view(np.uint32) == y.view(np.uint32)).all()
+
+
+# ---------------------------------------------------------------- pin-4 closed form
+def test_zero_fraction_closed_form():
+    """For W ~ N(0, s^2), gamma ~ E|W| = s*sqrt(2/pi); a weight rounds to 0 iff
+    |W| < gamma/2, so P(0) = erf(sqrt(2/pi)/2/sqrt(2)) = 0.3101.  The
+    threshold-at-mean rule printed in the 深度解析 page's snippet (section 2.2)
+    would give erf(1/sqrt(pi)) = 0.5751 instead: this pins the round rule."""
+    rng = np.random.default_rng(7)
+    W = (rng.standard_normal((1024, 1024)) * 0.02).astype(np.float32)
+    q = oracle.ternarize(W, oracle.gamma(W))
+    p0 = float((q == 0).mean())
+    expect = math.erf(math.sqrt(2 / math.pi) / 2 / math.sqrt(2))
+    assert abs(expect - 0.3101) < 1e-4
+    assert abs(p0 - expect) < 0.004
+    assert abs(float((q == 1).mean()) - (1 - expect) / 2) < 0.004
+    assert abs(p0 - math.erf(1 / math.sqrt(math.pi))) > 0.2
+
+
+# ---------------------------------------------------------------- pin-2 invariants
+@pytest.mark.parametrize("density", [0.05, 0.5, 1.0])
+def test_ternary_representable_weights(density):
+    rng = np.random.default_rng(int(density * 100))
+    c = np.float32(0.037)
+    sign = rng.choice([-1, 1], size=(16, 96))
+    mask = rng.random((16, 96)) < density
+    mask[0, 0] = True
+    W = (sign * mask * c).astype(np.float32)
+    q = oracle.ternarize(W, oracle.gamma(W))
+    assert (q == np.sign(W).astype(np.int8)).all()
+
+
+def test_activation_invariants():
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((8, 333)).astype(np.float32)
+    xq, s = oracle.quant_act(x)
+    assert np.abs(xq.astype(int)).max() <= 127
+    for m in range(8):
+        i = int(np.argmax(np.abs(x[m])))
+        assert abs(int(xq[m, i])) == 127
+    # scaling a token by 2^e leaves its codes unchanged and scales s by 2^-e
+    for e in (-3, 5):
+        xq2, s2 = oracle.quant_act((x * np.float32(2.0 ** e)).astype(np.float32))
+        assert (xq2 == xq).all()
+        assert (s2 == (s * np.float32(2.0 ** -e))).all()
+
+
+def test_integer_activations_amax_127():
+    """Integer x with max|x| = 127: s = 1, xq = x, y = fl32(acc * gamma)."""
+    rng = np.random.default_rng(11)
+    x = rng.integers(-127, 128, size=(3, 200)).astype(np.float32)
+    x[:, 5] = 127
+    W = (rng.standard_normal((40, 200)) * 0.02).astype(np.float32)
+    y, packed, g = oracle.forward(W, x)
+    xq, s = oracle.quant_act(x)
+    assert (s == 1).all() and (xq == x).all()
+    q = oracle.unpack(packed, 200)
+    acc = x.astype(np.int64) @ q.astype(np.int64).T
+    for (m, n), a in np.ndenumerate(acc):
+        assert y[m, n] == fl32(int(a) * Fraction(float(g)))
+
+
+def test_power_of_two_scaling_of_x_scales_y_exactly():
+    rng = np.random.default_rng(5)
+    W = (rng.standard_normal((64, 128)) * 0.02).astype(np.float32)
+    x = rng.standard_normal((4, 128)).astype(np.float32)
+    y, packed, g = oracle.forward(W, x)
+    y4 = oracle.forward_packed(packed, g, 64, 128, (x * np.float32(4)).astype(np.float32))
+    assert (y4 == y * np.float32(4)).all()
+
+
+def test_token_rows_are_independent():
+    rng = np.random.default_rng(9)
+    W = (rng.standard_normal((32, 64)) * 0.02).astype(np.float32)
+    x = rng.standard_normal((6, 64)).astype(np.float32)
+    y, packed, g = oracle.forward(W, x)
+    perm = rng.permutation(6)
+    yp = oracle.forward_packed(packed, g, 32, 64, np.ascontiguousarray(x[perm]))
+    assert (yp == y[perm]).all()
+
+
+# ---------------------------------------------------------------- pin-5 special cases
+def test_single_weight_single_input():
+    W = np.array([[-0.3]], np.float32)
+    x = np.array([[0.75], [-2.0]], np.float32)
+    y, packed, g = oracle.forward(W, x)
+    assert g == fl32(Fraction(float(np.float32(0.3))) + Fraction(float(FEPS)))
+    assert oracle.unpack(packed, 1).tolist() == [[-1]]
+    xq, s = oracle.quant_act(x)
+    assert xq.tolist() == [[127], [-127]]
+    for m in range(2):
+        a = -int(xq[m, 0])
+        e = a * Fraction(float(g)) / Fraction(float(s[m]))
+        assert abs(Fraction(float(y[m, 0])) - e) <= abs(e) * F32_EPS
+    assert abs(float(y[0, 0]) - (-0.3 * 0.75)) < 1e-4
+
+
+def test_all_zero_weights_and_inputs():
+    W = np.zeros((3, 70), np.float32)
+    g = oracle.gamma(W)
+    assert g == FEPS
+    packed, _ = oracle.pack_weights(W)
+    assert (packed == 0x55).all()
+    x = np.zeros((2, 70), np.float32)
+    x[1, 3] = 1.5
+    y, _, _ = oracle.forward(W, x)
+    assert (y == 0).all()
+    xq, s = oracle.quant_act(x)
+    assert s[0] == fl32(Fraction(127) / Fraction(float(FEPS)))
+    assert (xq[0] == 0).all()
+    W2 = np.random.default_rng(1).standard_normal((3, 70)).astype(np.float32)
+    y2, _, _ = oracle.forward(W2, x)
+    assert (y2[0] == 0).all()
+
+
+def test_outputs_are_order_free_in_threads():
+    rng = np.random.default_rng(2)
+    q = rng.integers(-1, 2, size=(300, 257)).astype(np.int8)
+    xq = rng.integers(-127, 128, size=(3, 257)).astype(np.int8)
+    oracle.set_threads(1)
+    a1 = oracle.matmul_i32(q, xq)
+    oracle.set_threads(4)
+    a4 = oracle.matmul_i32(q, xq)
+    oracle.set_threads(1)
+    assert (a1 == a4).all()
+
+
+# ---------------------------------------------------------------- subln RMSNorm
+def test_rmsnorm_scale_against_high_precision():
+    rng = np.random.default_rng(21)
+    x = rng.standard_normal((5, 300)).astype(np.float32)
+    x[2] *= 1e-3
+    gain = (1 + 0.1 * rng.random(300)).astype(np.float32)
+    eps = 1e-5
+    xq, s, r = oracle.rmsnorm_quant_act(x, gain, eps)
+    for m in range(5):
+        ms = sum(Fraction(float(v)) ** 2 for v in x[m]) / 300
+        exact_r = 1.0 / math.sqrt(float(ms) + eps)
+        assert abs(float(r[m]) - exact_r) <= 3 * 2 ** -24 * exact_r
+    # codes are those of u = x * g (absmax quant is invariant under r_t > 0)
+    u = (x * gain).astype(np.float32)
+    xq_u, s_u = oracle.quant_act(u)
+    assert (xq == xq_u).all()
+    assert (s == (s_u / r).astype(np.float32)).all()
+    # the literal "normalise, then quantise" form agrees up to rounding
+    v = ((x * r[:, None]).astype(np.float32) * gain).astype(np.float32)
+    xq_v, s_v = oracle.quant_act(v)
+    diff = np.abs(xq_v.astype(int) - xq.astype(int))
+    assert diff.max() <= 1 and (diff > 0).mean() <= 0.001
+    assert np.allclose(s_v, s, rtol=1e-6, atol=0)
+
+
+def test_rmsnorm_constant_row_closed_form():
+    """x = c everywhere: r = 1/sqrt(c^2 + eps), every code is sign(c)*127."""
+    x = np.full((2, 64), 0.5, np.float32)
+    x[1] = -3.0
+    xq, s, r = oracle.rmsnorm_quant_act(x, None, 1e-5)
+    assert (xq[0] == 127).all() and (xq[1] == -127).all()
+    for m, c in enumerate((0.5, -3.0)):
+        assert abs(float(r[m]) - 1 / math.sqrt(c * c + 1e-5)) <= 2 ** -23 / abs(c)
+        s_u = np.float32(127) / np.float32(abs(c))
+        assert s[m] == np.float32(s_u / r[m])
