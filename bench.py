@@ -1,0 +1,488 @@
+#!/usr/bin/env python3
+"""BitLinear W1.58A8 forward benchmark (B300, sm_103a).
+
+Headline workload, one step: decode at M = 1 over a ~2B-class ternary model's
+projections -- 30 layers x {QKV 2560->3840, O 2560->2560, up 2560->6912,
+down 6912->2560} with distinct weights (388 MB packed, three times the 126 MB
+L2, so every step streams the weights from HBM; no L2 flush is needed).  A
+step is one bitlinear_forward per matrix (120 calls: fused activation
+quantisation + packed-ternary GEMV + rescale), captured once in a CUDA graph
+with launch overlap on and replayed.  Metric: GB/s of algorithmic bytes
+(packed weights + bf16 activations + fp32 outputs + gamma).
+
+Extra workloads reported under "extras": batched decode M in {8,16,32,64} on
+the same weights, prefill M = 2048 (tensor-core path; dense-equivalent
+2*M*N*K ops/s) and the 100B-class decode shapes (80 layers, 9.4 GB resident).
+
+--impl reference times the CPU oracle instead (the repository's plain C
+restatement of the method) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "BitLinear GB/s (decode, % HBM peak) and int8 TOPS (prefill, % INT8 peak)"
+WORKLOAD = "decode_2b"
+
+
+def load_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        d["source"] = "measured"
+        return d
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0,
+            "source": "fallback"}
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """Samples SM clock and throttle reasons through NVML while running."""
+
+    REASONS = {  # NVML clocks-event reason bits
+        0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+        0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+        0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+        0x100: "display_clock_setting"}
+
+    def __init__(self, index: int, period_s: float = 0.002):
+        self.index, self.period = index, period_s
+        self.samples: list[tuple[int, int]] = []
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._t = None
+        self.error = None
+
+    def __enter__(self):
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self._nv = pynvml
+            self._h = self._handle(pynvml)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
+        except Exception as e:  # NVML missing: report, do not fail the bench
+            self.error = repr(e)
+            return self
+        self._t = threading.Thread(target=self._run, daemon=True)
+        self._t.start()
+        return self
+
+    def _handle(self, nv):
+        # NVML numbers every GPU of the machine; match the CUDA device by UUID.
+        import torch
+        try:
+            want = str(torch.cuda.get_device_properties(self.index).uuid).lower()
+            for i in range(nv.nvmlDeviceGetCount()):
+                h = nv.nvmlDeviceGetHandleByIndex(i)
+                u = nv.nvmlDeviceGetUUID(h)
+                u = (u.decode() if isinstance(u, bytes) else u).lower()
+                if want and want in u:
+                    return h
+        except Exception:
+            pass
+        return nv.nvmlDeviceGetHandleByIndex(self.index)
+
+    def _run(self):
+        nv = self._nv
+        while not self._stop.is_set():
+            try:
+                mhz = nv.nvmlDeviceGetClockInfo(self._h, nv.NVML_CLOCK_SM)
+                rs = nv.nvmlDeviceGetCurrentClocksEventReasons(self._h)
+                self.samples.append((mhz, rs))
+            except Exception as e:
+                self.error = repr(e)
+                return
+            time.sleep(self.period)
+
+    def __exit__(self, *a):
+        self._stop.set()
+        if self._t is not None:
+            self._t.join()
+
+    def summary(self) -> dict:
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [],
+                    "samples": 0, "error": self.error}
+        mhz = [m for m, _ in self.samples]
+        bits = 0
+        for _, r in self.samples:
+            bits |= r
+        reasons = [n for b, n in self.REASONS.items() if bits & b and n != "gpu_idle"]
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(mhz)}
+
+
+# ------------------------------------------------------------------ helpers
+def algorithmic_bytes(M: int, N: int, K: int, x_bytes: int = 2) -> int:
+    """Bytes a BitLinear forward must move: packed weights, x, y and gamma."""
+    row = ((K + 63) // 64) * 16
+    return N * row + M * K * x_bytes + M * N * 4 + 4
+
+
+def prepare(bl, wl, mats, M: int, device, x_dtype):
+    """Pack each matrix's weights (seeded, drawn on the GPU) and draw x."""
+    import torch
+    out = []
+    for mt in mats:
+        W = wl.weight(mt.N, mt.K, mt.std, mt.seed, device)
+        packed, gamma = bl.bitlinear_pack_weights(W)
+        del W
+        x = wl.activations(M, mt.K, mt.x_kind if M == 1 else "outliers1pct",
+                           mt.seed + 500, device, x_dtype)
+        y = torch.empty((M, mt.N), dtype=torch.float32, device=device)
+        ws_n = bl.workspace_bytes(M, mt.N, mt.K)
+        ws = torch.empty(ws_n, dtype=torch.uint8, device=device) if ws_n else None
+        out.append(dict(mt=mt, packed=packed, gamma=gamma, x=x, y=y, ws=ws, M=M))
+    torch.cuda.synchronize()
+    return out
+
+
+def sweep_calls(bl, items):
+    for it in items:
+        mt = it["mt"]
+        bl.bitlinear_forward(it["packed"], it["gamma"], mt.N, mt.K, it["x"], y=it["y"],
+                             workspace=it["ws"])
+
+
+def capture(bl, items, stream):
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        sweep_calls(bl, items)  # warm (first launches set kernel attributes)
+        stream.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            sweep_calls(bl, items)
+    return g
+
+
+def time_graph(g, stream, steps: int, warmup: int, dist_mod, device) -> float:
+    """Seconds for `steps` replays, CUDA events on `stream`, barrier-bracketed."""
+    import torch
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            g.replay()
+        stream.synchronize()
+        dist_mod.barrier()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    dist_mod.barrier()
+    return e0.elapsed_time(e1) / 1e3
+
+
+def launches_per_call(bl, M: int, N: int, K: int) -> int:
+    return 1 if bl.workspace_bytes(M, N, K) == 0 else 2
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+def oracle_timing(items_host, budget_s: float, min_reps: int = 1):
+    """Time the CPU oracle's forward on host copies of (packed, gamma, x).
+    Returns (seconds, algorithmic bytes, calls, threads)."""
+    import oracle
+    oracle.set_threads(os.cpu_count() or 1)
+    t0 = time.perf_counter()
+    nbytes, calls = 0, 0
+    while True:
+        for (packed, g, N, K, x) in items_host:
+            oracle.forward_packed(packed, g, N, K, x)
+            nbytes += algorithmic_bytes(x.shape[0], N, K)
+            calls += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s and calls >= min_reps:
+            return el, nbytes, calls, oracle.get_threads()
+
+
+def host_items(items, limit: int):
+    out = []
+    for it in items[:limit]:
+        mt = it["mt"]
+        out.append((it["packed"].cpu().numpy(), float(it["gamma"].item()), mt.N, mt.K,
+                    it["x"].float().cpu().numpy()))
+    return out
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args, rank: int):
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    import torch
+    from w1_a8_bitlinear_02_b300 import workloads as wl
+    mats = wl.matrices(WORKLOAD, layers=1)  # one layer's four projections
+    items = []
+    for mt in mats:
+        W = wl.weight(mt.N, mt.K, mt.std, mt.seed, "cpu").numpy()
+        packed, g = oracle.pack_weights(W)
+        x = wl.activations(1, mt.K, mt.x_kind, mt.seed + 500, "cpu", torch.bfloat16)
+        items.append((packed, float(g), mt.N, mt.K, x.float().numpy()))
+    oracle.set_threads(os.cpu_count() or 1)
+    nb_step = [algorithmic_bytes(1, N, K) for (_, _, N, K, _) in items]
+    for i in range(args.warmup):
+        p, g, N, K, x = items[i % len(items)]
+        oracle.forward_packed(p, g, N, K, x)
+    t0 = time.perf_counter()
+    nbytes = 0
+    for i in range(args.steps):
+        p, g, N, K, x = items[i % len(items)]
+        oracle.forward_packed(p, g, N, K, x)
+        nbytes += nb_step[i % len(items)]
+    el = time.perf_counter() - t0
+    gbs = nbytes / el / 1e9
+    cores = oracle.get_threads()
+    sample = ("one BitLinear forward per step at M=1, cycling through layer 0's four "
+              "projections (QKV, O, up, down) of the ~2B decode workload")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int8", "data": "synthetic",
+        "config": {"workload": "decode_2b M=1 (CPU oracle, bounded sample)",
+                   "sample": sample},
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, rank: int, world: int, local: int):
+    import torch
+
+    import w1_a8_bitlinear_02_b300 as bl
+    from w1_a8_bitlinear_02_b300 import dist as D
+    from w1_a8_bitlinear_02_b300 import workloads as wl
+
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    peaks = load_peaks()
+    bl.set_launch_overlap(not args.no_overlap)
+    stream = torch.cuda.Stream(device)
+
+    mats = wl.matrices(WORKLOAD, layers=args.layers)
+    items = prepare(bl, wl, mats, 1, device, torch.bfloat16)
+    step_bytes = sum(algorithmic_bytes(1, it["mt"].N, it["mt"].K) for it in items)
+    packed_bytes = sum(it["packed"].numel() for it in items)
+    g = capture(bl, items, stream)
+    launches_step = sum(launches_per_call(bl, 1, it["mt"].N, it["mt"].K) for it in items)
+
+    with ClockSampler(local) as clk:
+        secs = time_graph(g, stream, args.steps, args.warmup, D, device)
+    secs_max, bytes_all = D.aggregate(secs, step_bytes * args.steps, device)
+    gbs = bytes_all / secs_max / 1e9
+    ms_step = secs_max / args.steps * 1e3
+    assert bl.device_error() == 0, "a kernel reported a device-side failure"
+
+    # the dominant kernel: the M=1 GEMV, one launch per matrix
+    per_launch_s = secs / (args.steps * len(items))
+    per_launch_bytes = step_bytes / len(items)
+    achieved = per_launch_bytes / per_launch_s / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                "kernel": "bl::gemv::gemv_kernel<1,*,bf16>",
+                "peak_source": f"{peaks['source']} (copy bandwidth)"}
+
+    # end to end: pinned host x -> device, the sweep, device y -> pinned host
+    xs_host = [it["x"].cpu().pin_memory() for it in items]
+    ys_host = [torch.empty_like(it["y"], device="cpu").pin_memory() for it in items]
+    h2d = sum(x.numel() * x.element_size() for x in xs_host)
+    d2h = sum(y.numel() * y.element_size() for y in ys_host)
+
+    def e2e_step():
+        for xh, it in zip(xs_host, items):
+            it["x"].copy_(xh, non_blocking=True)
+        g.replay()
+        for yh, it in zip(ys_host, items):
+            yh.copy_(it["y"], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        e2e_steps = max(1, min(args.steps, 200))
+        for _ in range(min(args.warmup, 5)):
+            e2e_step()
+        stream.synchronize()
+        D.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    e2e_s, e2e_bytes = D.aggregate(e0.elapsed_time(e1) / 1e3, step_bytes * e2e_steps, device)
+    e2e = {"value": e2e_bytes / e2e_s / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h,
+           "how": "per step: pinned-host x -> device, the 120-call graph, y -> pinned host"}
+
+    extras = {}
+    if not args.no_extras:
+        extras = run_extras(bl, wl, torch, device, stream, peaks, items, args)
+
+    cpu_baseline = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        hi = host_items(items, 4)
+        el, nb, calls, cores = oracle_timing(hi, args.cpu_seconds)
+        cpu_baseline = {"value": nb / el / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                        "sample": f"{calls} calls of the oracle's forward on layer 0's four "
+                                  "projections at M=1 (host copies of the same packed weights "
+                                  f"and activations), {el:.1f} s"}
+
+    del g
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "int8", "data": "synthetic",
+            "config": {"workload": "decode_2b: M=1 over 30 layers x {qkv 3840x2560, o 2560x2560, "
+                                   "up 6912x2560, down 2560x6912}, x bf16, fused act-quant",
+                       "M": 1, "layers": args.layers, "matrices": len(items),
+                       "packed_weight_bytes_per_step": packed_bytes,
+                       "algorithmic_bytes_per_step": step_bytes,
+                       "l2": "inputs larger than L2 (packed weights 388 MB vs 126 MB L2); no flush",
+                       "launch": "CUDA graph of one bitlinear_forward per matrix, launch overlap "
+                                 + ("off" if args.no_overlap else "on"),
+                       "parallelism": f"{world} independent replica(s), weak scaling"},
+            "roofline": roofline,
+            "cpu_baseline": cpu_baseline,
+            "e2e": e2e,
+            "gpu_launches": launches_step * args.steps,
+            "clocks": clk.summary(),
+            "frac_of_hbm_peak": gbs / peaks["hbm_gbs"],
+            "extras": extras,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def run_extras(bl, wl, torch, device, stream, peaks, items2b, args):
+    from w1_a8_bitlinear_02_b300 import dist as D
+    out = {}
+    reps = max(3, min(args.steps, 50))
+
+    def timed(fn, n):
+        for _ in range(3):
+            fn()
+        stream.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / 1e3 / n
+
+    with torch.cuda.stream(stream):
+        # batched decode on the same weights
+        mats = [it["mt"] for it in items2b]
+        bd = {}
+        for M in (8, 16, 32, 64):
+            its = []
+            for it in items2b:
+                mt = it["mt"]
+                x = wl.activations(M, mt.K, "outliers1pct", mt.seed + 600 + M, device, torch.bfloat16)
+                y = torch.empty((M, mt.N), dtype=torch.float32, device=device)
+                wsn = bl.workspace_bytes(M, mt.N, mt.K)
+                ws = torch.empty(wsn, dtype=torch.uint8, device=device) if wsn else None
+                its.append(dict(mt=mt, packed=it["packed"], gamma=it["gamma"], x=x, y=y, ws=ws))
+            g = capture(bl, its, stream)
+            s = timed(g.replay, reps)
+            nb = sum(algorithmic_bytes(M, m.N, m.K) for m in mats)
+            ops = sum(2 * M * m.N * m.K for m in mats)
+            bd[f"M={M}"] = {"GB/s": nb / s / 1e9, "frac_hbm": nb / s / 1e9 / peaks["hbm_gbs"],
+                            "TOPS_dense_equiv": ops / s / 1e12, "ms_per_sweep": s * 1e3}
+            del g, its
+        out["decode_2b_batch"] = bd
+
+        # prefill M = 2048 on the tensor-core path (forward = quant + GEMM)
+        pf = {}
+        for name, N, K, kind in (("up", 6912, 2560, "normal"), ("down", 2560, 6912, "relu2")):
+            W = wl.weight(N, K, 0.02, wl.weight_seed("prefill_2b", 0, 0) + N, device)
+            packed, gamma = bl.bitlinear_pack_weights(W)
+            del W
+            x = wl.activations(2048, K, kind, 4500 + K, device, torch.bfloat16)
+            y = torch.empty((2048, N), dtype=torch.float32, device=device)
+            ws = torch.empty(bl.workspace_bytes(2048, N, K), dtype=torch.uint8, device=device)
+            s = timed(lambda: bl.bitlinear_forward(packed, gamma, N, K, x, y=y, workspace=ws), reps)
+            ops = 2 * 2048 * N * K
+            tops = ops / s / 1e12
+            pf[name] = {"N": N, "K": K, "M": 2048, "ms": s * 1e3, "TOPS_dense_equiv": tops,
+                        "frac_bf16_peak": tops / peaks["bf16_tflops"],
+                        "note": "sm_103a has no integer MMA; int8 x ternary runs exactly as "
+                                "bf16 x bf16 -> fp32 on tcgen05 (kind::f16); peak = measured "
+                                "dense bf16 (burst)"}
+            del packed, gamma, x, y, ws
+        out["prefill_2b"] = pf
+
+        # 100B-class decode: 80 layers x {28672x8192, 8192x28672}, 9.4 GB resident
+        if not args.no_100b:
+            mats = wl.matrices("decode_100b")
+            its = prepare(bl, wl, mats, 1, device, torch.bfloat16)
+            res = {}
+            for M in (1, 8):
+                if M == 8:
+                    for it in its:
+                        mt = it["mt"]
+                        it["x"] = wl.activations(8, mt.K, "normal", mt.seed + 508, device,
+                                                 torch.bfloat16)
+                        it["y"] = torch.empty((8, mt.N), dtype=torch.float32, device=device)
+                        wsn = bl.workspace_bytes(8, mt.N, mt.K)
+                        it["ws"] = torch.empty(wsn, dtype=torch.uint8, device=device) if wsn else None
+                g = capture(bl, its, stream)
+                s = timed(g.replay, max(3, min(args.steps, 20)))
+                nb = sum(algorithmic_bytes(M, it["mt"].N, it["mt"].K) for it in its)
+                res[f"M={M}"] = {"GB/s": nb / s / 1e9, "frac_hbm": nb / s / 1e9 / peaks["hbm_gbs"],
+                                 "ms_per_sweep": s * 1e3,
+                                 "resident_packed_GB": sum(it["packed"].numel() for it in its) / 1e9}
+                del g
+            del its
+            out["decode_100b"] = res
+    torch.cuda.empty_cache()
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--layers", type=int, default=30)
+    ap.add_argument("--no-overlap", action="store_true")
+    ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--no-100b", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    from w1_a8_bitlinear_02_b300 import dist as D
+    rank, world, local = D.init()
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank)
+        else:
+            run_ours(args, rank, world, local)
+    finally:
+        D.finalize()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,211 @@
+/*
+ * bitlinear.h -- C ABI of the BitLinear W1.58A8 forward for NVIDIA B300
+ * (sm_103a).  libbitlinear.so exports exactly the functions declared here.
+ *
+ * The operation (BitNet b1.58; citations name the page and its section):
+ *   - Weights are ternarised by their absmean: gamma = mean|W| + 1e-5 (one
+ *     fp32 scale per weight tensor), Wq = clip(round(W / gamma), -1, +1).
+ *     ["20亿参数仅0.4GB…微软开源全球首个2B参数「原生1.58bit」大模型",
+ *     blog.csdn.net/soaring_casia, section 2 "BitLinear层", item 1.]
+ *   - Activations are quantised per token by their absmax:
+ *     s = 127 / max(max|x_t|, 1e-5), xq = clip(round(x * s), -128, 127).
+ *     [same page and section, item 2; "微软AI大模型炸场：0.4GB，CPU就能跑",
+ *     blog.csdn.net/2401_84494441, section 1 "激活8位量化".]
+ *   - y = (Wq @ xq) accumulated in int32, then y = acc * gamma / s in fp32.
+ *     ["BitNet b1.58 深度解析", chenxutan.com, section 2.3(2).]
+ *   - A subln RMSNorm precedes the quantised projection; no bias anywhere.
+ *     [soaring_casia page, section 2, item 3 and "偏置"; 0.4GB page, section 1
+ *     "归一化方法" and section 2 "偏置移除".]
+ *   - Weights are stored packed, several 2-bit codes per byte, and unpacked
+ *     on chip.  [0.4GB page, section 3 "软硬协同", GPU bullet; 深度解析
+ *     page, section 2.1: a 2-bit code has four states, one unused.]
+ * Rounding is half to even everywhere; every fp32 step is one IEEE op
+ * (divisions are true divisions).  The pages fix none of this; it is the
+ * reading this library takes, and the CPU oracle in the repository uses the
+ * same one.
+ *
+ * Conventions for every entry point:
+ *   - Pointers are DEVICE pointers unless marked (host).  The caller owns
+ *     and allocates every buffer, including workspaces; the library allocates
+ *     no device memory and holds no per-call state.
+ *   - All work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and is asynchronous: no call synchronises the host.
+ *   - Arguments are checked before anything is enqueued.  On any error the
+ *     call returns a non-zero bl_status and enqueues nothing (except
+ *     BL_ERR_CUDA, returned when a launch itself fails).  Nothing throws.
+ *   - Matrices are row-major and dense (row stride = number of columns).
+ *   - Limits: 1 <= N, M <= 2^31 - 1; 1 <= K <= 131072 (|acc| <= 127*K stays
+ *     below 2^24, so every partial sum is exact on every path).
+ *   - Inputs must be finite.  Results for NaN/Inf inputs are unspecified.
+ *
+ * Packed weight layout ("bl2" layout):
+ *   Row n of an [N, K] ternary matrix occupies row_bytes(K) = 16 * ceil(K/64)
+ *   bytes starting at n * row_bytes(K) (K is padded to a multiple of 64
+ *   weights with code 1 = weight 0).  Code c = Wq + 1 in {0, 1, 2}.  Weight k
+ *   lives in the little-endian 32-bit word w = k / 16 of its row at bit
+ *   8*j + 2*i, with i = (k % 16) / 4 and j = k % 4; equivalently in byte
+ *   4*w + j at bit 2*i.  So (word >> 2*i) & 0x03030303 holds the codes of
+ *   k = 16w+4i .. 16w+4i+3 as four bytes, in order.  Packed buffers must be
+ *   16-byte aligned.
+ */
+#ifndef BITLINEAR_H
+#define BITLINEAR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define BL_API __attribute__((visibility("default")))
+#else
+#define BL_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum bl_status {
+  BL_OK = 0,
+  BL_ERR_NULL = 1,        /* a required pointer is NULL                      */
+  BL_ERR_SHAPE = 2,       /* a size is outside the documented limits        */
+  BL_ERR_DTYPE = 3,       /* unknown bl_dtype code                           */
+  BL_ERR_ALIGN = 4,       /* a pointer violates its alignment requirement    */
+  BL_ERR_WORKSPACE = 5,   /* workspace NULL or smaller than required         */
+  BL_ERR_CUDA = 6,        /* a CUDA runtime call or kernel launch failed     */
+  BL_ERR_UNSUPPORTED = 7, /* current device is not an sm_103 GPU             */
+  BL_ERR_DEVICE = 8       /* a kernel gave up a bounded wait (see below)     */
+} bl_status;
+
+typedef enum bl_dtype {
+  BL_F32 = 0,  /* IEEE binary32                        */
+  BL_BF16 = 1  /* bfloat16 (widened to fp32 exactly)   */
+} bl_dtype;
+
+/* Library version, e.g. 100 for 0.1.0.  Host only; never fails. */
+BL_API int bitlinear_version(void);
+
+/* Static English text for a status code (host).  Never returns NULL. */
+BL_API const char *bitlinear_status_string(int status);
+
+/* Packed row length in bytes for K weights: 16 * ceil(K / 64).
+ * bytes: host pointer.  Errors: BL_ERR_NULL, BL_ERR_SHAPE. */
+BL_API bl_status bitlinear_packed_row_bytes(int64_t K, int64_t *bytes);
+
+/* Size of a whole packed [N, K] matrix: N * row_bytes(K).  Host output. */
+BL_API bl_status bitlinear_packed_bytes(int64_t N, int64_t K, size_t *bytes);
+
+/* Workspace needed by bitlinear_pack_weights: 8 * N bytes (one fp64 partial
+ * sum per row).  Host output. */
+BL_API bl_status bitlinear_pack_workspace_bytes(int64_t N, int64_t K, size_t *bytes);
+
+/* Ternarise and pack a weight matrix (offline step, off the hot path).
+ * [soaring_casia page, section 2 "BitLinear层", item 1: absmean weights.]
+ *   W       [N, K] of `dtype` (BL_F32 or BL_BF16), device.
+ *   packed  [N, row_bytes(K)] uint8 out, device, 16-byte aligned.
+ *   gamma   1 float out, device: fl32(fl32(S / (N*K)) + 1e-5f) where S is
+ *           sum |W| in fp64, added sequentially over k within each row and
+ *           then sequentially over the rows (a fixed, reproducible order).
+ *   ws      >= bitlinear_pack_workspace_bytes(N, K) bytes, device, 8-aligned.
+ * Codes: Wq = clip(rint(fl32(W / gamma)), -1, 1), stored as Wq + 1.
+ * Errors: BL_ERR_NULL, BL_ERR_SHAPE, BL_ERR_DTYPE, BL_ERR_ALIGN,
+ * BL_ERR_WORKSPACE, BL_ERR_UNSUPPORTED, BL_ERR_CUDA. */
+BL_API bl_status bitlinear_pack_weights(const void *W, int dtype, int64_t N, int64_t K,
+                                 uint8_t *packed, float *gamma, void *ws,
+                                 size_t ws_bytes, void *stream);
+
+/* Per-token absmax int8 quantisation of activations.
+ * [soaring_casia page, section 2, item 2; 0.4GB page, section 1 "激活8位量化".]
+ *   x      [M, K] of `dtype`, device.
+ *   xq     [M, K] int8 out, device: clip(rint(fl32(x * s_m)), -128, 127).
+ *   scale  [M] float out, device: s_m = fl32(127 / max(max_k |x_mk|, 1e-5f)).
+ * Consumers divide by s (s is the multiplicative quantisation scale).
+ * Errors: BL_ERR_NULL, BL_ERR_SHAPE, BL_ERR_DTYPE, BL_ERR_UNSUPPORTED,
+ * BL_ERR_CUDA. */
+BL_API bl_status bitlinear_quant_act(const void *x, int dtype, int64_t M, int64_t K,
+                              int8_t *xq, float *scale, void *stream);
+
+/* Fused subln RMSNorm + per-token absmax int8 quantisation.
+ * [soaring_casia page, section 2, item 3 (subln); 0.4GB page, section 1
+ * "归一化方法"; no bias (section 2 "偏置").]
+ *   x      [M, K] of `dtype`, device.
+ *   g      [K] float gain, device, or NULL for a gain of 1.
+ *   eps    added to mean(x^2) before the square root (e.g. 1e-5).
+ *   xq     [M, K] int8 out: the codes of v = x * r_m * g, computed as the
+ *          codes of u = fl32(x * g) (absmax codes do not change under the
+ *          positive per-token factor r_m).
+ *   scale  [M] float out: s_m = fl32(s_u / r_m), the scale of v, where
+ *          r_m = 1 / sqrt(fl32(mean_k x^2) + eps) and s_u is u's absmax
+ *          scale.  mean(x^2) is summed in compensated fp32 / fp64 on the GPU,
+ *          so r_m (hence s_m) may differ from a sequential fp64 sum by an ulp;
+ *          xq does not depend on r_m and is exact.
+ * Errors: as bitlinear_quant_act, plus BL_ERR_SHAPE for eps < 0. */
+BL_API bl_status bitlinear_rmsnorm_quant_act(const void *x, int dtype, const float *g,
+                                      float eps, int64_t M, int64_t K,
+                                      int8_t *xq, float *scale, void *stream);
+
+/* Workspace (device bytes) needed by bitlinear_forward, bitlinear_forward_q
+ * and bitlinear_matmul_i32 for these sizes; 0 when the chosen path needs
+ * none (small M).  Host output.  Errors: BL_ERR_NULL, BL_ERR_SHAPE. */
+BL_API bl_status bitlinear_workspace_bytes(int64_t M, int64_t N, int64_t K,
+                                    size_t *bytes);
+
+/* BitLinear forward: y = (Wq @ quant(x)) * gamma / s, with the activation
+ * quantisation fused in.  Equal, bit for bit, to bitlinear_quant_act followed
+ * by bitlinear_forward_q.
+ * [深度解析 page, section 2.3(2): y = (W_quant @ x_quant) * scale.]
+ *   packed [N, row_bytes(K)] packed codes, device, 16-byte aligned.
+ *   gamma  1 float, device (as written by bitlinear_pack_weights).
+ *   x      [M, K] of `dtype`, device.
+ *   y      [M, N] float out, device: y = fl32(fl32(float(acc) * gamma) / s_m),
+ *          acc = sum_k Wq[n,k] * xq[m,k] (exact int32).
+ *   ws     >= bitlinear_workspace_bytes(M, N, K) bytes, device, 256-aligned
+ *          (may be NULL when that size is 0).  Calls that share a workspace
+ *          must be ordered (same stream or synchronised).
+ * Errors: BL_ERR_NULL, BL_ERR_SHAPE, BL_ERR_DTYPE, BL_ERR_ALIGN,
+ * BL_ERR_WORKSPACE, BL_ERR_UNSUPPORTED, BL_ERR_CUDA. */
+BL_API bl_status bitlinear_forward(const uint8_t *packed, const float *gamma, int64_t N,
+                            int64_t K, const void *x, int dtype, int64_t M,
+                            float *y, void *ws, size_t ws_bytes, void *stream);
+
+/* BitLinear forward on pre-quantised activations.
+ *   xq     [M, K] int8 codes, device;  scale [M] float, device (s_m).
+ *   Other arguments and the result as bitlinear_forward. */
+BL_API bl_status bitlinear_forward_q(const uint8_t *packed, const float *gamma,
+                              int64_t N, int64_t K, const int8_t *xq,
+                              const float *scale, int64_t M, float *y, void *ws,
+                              size_t ws_bytes, void *stream);
+
+/* The bare ternary x int8 contraction: acc[m, n] = sum_k Wq[n,k] * xq[m,k]
+ * as exact int32 (no rescale).  Useful to split K across devices: int32
+ * partial sums add exactly, so a K-split needs one integer all-reduce before
+ * the rescale.  [0.4GB page, section 1: with ternary weights the matrix
+ * product reduces to additions.]
+ *   acc    [M, N] int32 out, device.  Other arguments as bitlinear_forward_q. */
+BL_API bl_status bitlinear_matmul_i32(const uint8_t *packed, int64_t N, int64_t K,
+                               const int8_t *xq, int64_t M, int32_t *acc,
+                               void *ws, size_t ws_bytes, void *stream);
+
+/* Launch overlap (programmatic dependent launch) for the forward kernels.
+ * When on (default off), forward / forward_q / matmul_i32 kernels are
+ * launched so that they may start while the previous kernel on the stream
+ * is still running; they prefetch `packed` and `gamma` before waiting for
+ * it and read everything else only after it has completed.  Precondition
+ * while on: `packed` and `gamma` are not written by the kernel launched
+ * immediately before on the same stream.  Process-wide; host only. */
+BL_API void bitlinear_set_launch_overlap(int on);
+BL_API int bitlinear_get_launch_overlap(void);
+
+/* Failure detection.  Every wait inside a kernel is bounded (about 2 s);
+ * a kernel that gives up sets a device-side flag, releases what it holds and
+ * returns early (its outputs are then invalid).  This reads (and, if
+ * `clear`, resets) the flag of the current device.  Synchronous: it waits
+ * for the device.  flags: host out, 0 = no error; bit 0 = pipeline wait
+ * timed out.  Returns BL_ERR_DEVICE when a flag was set, BL_OK otherwise,
+ * BL_ERR_CUDA if the device could not be read. */
+BL_API bl_status bitlinear_device_error(unsigned int *flags, int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BITLINEAR_H */

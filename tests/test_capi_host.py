@@ -1,0 +1,134 @@
+"""C-ABI checks that need no GPU: the library loads, exports every symbol the
+header declares, sizes and the path planner behave, and invalid arguments
+come back as status codes before anything touches a device."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "bitlinear.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from w1_a8_bitlinear_02_b300 import build, capi
+    build.build()
+    return capi.load()
+
+
+def header_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"BL_API[^;(]*?\b(bitlinear_\w+)\s*\(", text, re.S)))
+
+
+def test_header_declares_the_api():
+    syms = header_symbols()
+    for name in ("bitlinear_pack_weights", "bitlinear_quant_act", "bitlinear_rmsnorm_quant_act",
+                 "bitlinear_forward", "bitlinear_forward_q", "bitlinear_matmul_i32",
+                 "bitlinear_workspace_bytes", "bitlinear_device_error"):
+        assert name in syms
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from w1_a8_bitlinear_02_b300 import capi
+    for name in header_symbols():
+        assert hasattr(lib, name), name
+        assert name in capi.SIGNATURES, f"{name} has no ctypes declaration"
+    out = subprocess.run(["nm", "-D", "--defined-only", capi.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (bitlinear_\w+)", out))
+    assert exported == set(header_symbols())
+
+
+def test_library_targets_sm103a_only(lib):
+    from w1_a8_bitlinear_02_b300 import capi
+    out = subprocess.run(["/usr/local/cuda/bin/cuobjdump", "--list-elf", capi.LIB_PATH],
+                         capture_output=True, text=True)
+    if out.returncode != 0:
+        pytest.skip("cuobjdump unavailable")
+    arches = set(re.findall(r"sm_\w+", out.stdout))
+    assert arches == {"sm_103a"}, arches
+
+
+def test_version_and_status_strings(lib):
+    assert lib.bitlinear_version() >= 100
+    for s in range(9):
+        assert lib.bitlinear_status_string(s)
+    assert lib.bitlinear_status_string(99) == b"unknown status"
+
+
+def test_row_bytes_and_sizes(lib):
+    import w1_a8_bitlinear_02_b300 as bl
+    assert bl.packed_row_bytes(1) == 16
+    assert bl.packed_row_bytes(64) == 16
+    assert bl.packed_row_bytes(65) == 32
+    assert bl.packed_row_bytes(2560) == 640
+    assert bl.packed_bytes(3840, 2560) == 3840 * 640
+    assert bl.pack_workspace_bytes(100, 7) == 800
+    # 30 layers of the ~2B shapes: 388 MB of packed weights
+    tot = 30 * sum(bl.packed_bytes(n, k) for n, k in
+                   ((3840, 2560), (2560, 2560), (6912, 2560), (2560, 6912)))
+    assert tot == 388_300_800
+
+
+def test_workspace_plan(lib):
+    import w1_a8_bitlinear_02_b300 as bl
+    # decode (M <= 4) runs without workspace
+    for M in (1, 2, 3, 4):
+        assert bl.workspace_bytes(M, 2560, 6912) == 0
+    # larger M needs the bf16 code buffer and scales at least
+    for M, N, K in ((5, 256, 512), (64, 2560, 2560), (2048, 6912, 2560)):
+        need = bl.workspace_bytes(M, N, K)
+        assert need >= M * bl.packed_row_bytes(K) * 4 * 2 + 4 * M
+    # M = 1 with a K too large to hold in registers also takes the tensor-core path
+    assert bl.workspace_bytes(1, 128, 131072) > 0
+
+
+def test_invalid_arguments_return_status(lib):
+    from w1_a8_bitlinear_02_b300 import capi
+    sz = ctypes.c_size_t()
+    i64 = ctypes.c_int64()
+    assert lib.bitlinear_packed_bytes(1, 1, None) == capi.BL_ERR_NULL
+    assert lib.bitlinear_packed_row_bytes(0, ctypes.byref(i64)) == capi.BL_ERR_SHAPE
+    assert lib.bitlinear_packed_row_bytes(131073, ctypes.byref(i64)) == capi.BL_ERR_SHAPE
+    assert lib.bitlinear_workspace_bytes(0, 4, 4, ctypes.byref(sz)) == capi.BL_ERR_SHAPE
+    fake = ctypes.c_void_p(0x10000)  # never dereferenced: checks run first
+    odd = ctypes.c_void_p(0x10008)
+    # forward: NULL, shape, dtype, alignment
+    assert lib.bitlinear_forward(None, fake, 4, 4, fake, 0, 1, fake, None, 0, None) == capi.BL_ERR_NULL
+    assert lib.bitlinear_forward(fake, fake, 4, 4, fake, 7, 1, fake, None, 0, None) == capi.BL_ERR_DTYPE
+    assert lib.bitlinear_forward(fake, fake, 4, 0, fake, 0, 1, fake, None, 0, None) == capi.BL_ERR_SHAPE
+    assert lib.bitlinear_forward(fake, fake, 4, 4, fake, 0, 0, fake, None, 0, None) == capi.BL_ERR_SHAPE
+    assert lib.bitlinear_forward(odd, fake, 4, 4, fake, 0, 1, fake, None, 0, None) == capi.BL_ERR_ALIGN
+    assert lib.bitlinear_forward_q(fake, fake, 4, 4, fake, None, 1, fake, None, 0, None) == capi.BL_ERR_NULL
+    assert lib.bitlinear_matmul_i32(fake, 4, 4, fake, 1, None, None, 0, None) == capi.BL_ERR_NULL
+    assert lib.bitlinear_quant_act(fake, 2, 1, 4, fake, fake, None) == capi.BL_ERR_DTYPE
+    assert lib.bitlinear_rmsnorm_quant_act(fake, 0, None, ctypes.c_float(-1.0), 1, 4, fake, fake,
+                                           None) == capi.BL_ERR_SHAPE
+    assert lib.bitlinear_pack_weights(fake, 0, 4, 4, fake, fake, None, 0, None) == capi.BL_ERR_WORKSPACE
+    assert lib.bitlinear_pack_weights(fake, 0, 4, 4, odd, fake, fake, 32, None) == capi.BL_ERR_ALIGN
+
+
+def test_no_device_is_reported_not_crashed(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    from w1_a8_bitlinear_02_b300 import capi
+    fake = ctypes.c_void_p(0x10000)
+    st = lib.bitlinear_forward(fake, fake, 4, 4, fake, 0, 1, fake, None, 0, None)
+    assert st in (capi.BL_ERR_CUDA, capi.BL_ERR_UNSUPPORTED)
+
+
+def test_launch_overlap_switch(lib):
+    import w1_a8_bitlinear_02_b300 as bl
+    before = bl.get_launch_overlap()
+    bl.set_launch_overlap(True)
+    assert bl.get_launch_overlap()
+    bl.set_launch_overlap(False)
+    assert not bl.get_launch_overlap()
+    bl.set_launch_overlap(before)

@@ -1,0 +1,505 @@
+// C ABI of the BitLinear W1.58A8 forward (see include/bitlinear.h).
+// Host side: argument checks, path planning, TMA descriptors, launches.
+#include "bitlinear.h"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <set>
+#include <utility>
+
+#include "bl_gemm_tc.cuh"
+#include "bl_gemv.cuh"
+#include "bl_pack_quant.cuh"
+#include "bl_ptx.cuh"
+#include "bl_plan.h"
+
+namespace {
+
+using namespace bl;
+
+std::atomic<int> g_overlap{0};
+
+constexpr int64_t kMaxK = 131072;
+constexpr int64_t kMaxDim = 2147483647;
+
+// ------------------------------------------------------------ device checks
+struct DevState {
+  bool probed = false;
+  bool supported = false;
+  int sms = 0;
+  std::set<const void *> smem_set;  // kernels whose dynamic-smem limit was raised
+};
+std::mutex g_mu;
+DevState g_dev[64];
+
+bl_status current_device(int *dev, int *sms) {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess) {
+    cudaGetLastError();
+    return BL_ERR_CUDA;
+  }
+  if (d < 0 || d >= 64) return BL_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DevState &st = g_dev[d];
+  if (!st.probed) {
+    int major = 0, minor = 0, n = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, d) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, d) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d) != cudaSuccess) {
+      cudaGetLastError();
+      return BL_ERR_CUDA;
+    }
+    st.probed = true;
+    st.supported = (major == 10 && minor == 3);
+    st.sms = n;
+  }
+  if (!st.supported) return BL_ERR_UNSUPPORTED;
+  *dev = d;
+  if (sms) *sms = st.sms;
+  return BL_OK;
+}
+
+bl_status ensure_smem(int dev, const void *func, int bytes) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  DevState &st = g_dev[dev];
+  if (st.smem_set.count(func)) return BL_OK;
+  if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) {
+    cudaGetLastError();
+    return BL_ERR_CUDA;
+  }
+  st.smem_set.insert(func);
+  return BL_OK;
+}
+
+template <typename... KArgs, typename... Args>
+bl_status launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                 bool overlap, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  if (overlap) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  if (cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...) != cudaSuccess) {
+    cudaGetLastError();
+    return BL_ERR_CUDA;
+  }
+  return BL_OK;
+}
+
+// ------------------------------------------------------------ TMA descriptors
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+// bf16 activations [rows, ld] (k innermost), box 64 x box_rows, 128-byte swizzle.
+bool make_map_x(CUtensorMap *m, const void *ptr, int64_t rows, int64_t ld, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(ld), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * 2)};
+  cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t es[2] = {1u, 1u};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// packed weights [N, row_bytes] bytes, box 16 bytes x 128 rows, no swizzle.
+bool make_map_w(CUtensorMap *m, const void *ptr, int64_t N, int64_t row_bytes) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(N)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
+  cuuint32_t box[2] = {16u, static_cast<cuuint32_t>(tc::kBM)};
+  cuuint32_t es[2] = {1u, 1u};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+bl_status check_dims(int64_t M, int64_t N, int64_t K) {
+  if (M < 1 || M > kMaxDim || N < 1 || N > kMaxDim || K < 1 || K > kMaxK) return BL_ERR_SHAPE;
+  return BL_OK;
+}
+
+// ------------------------------------------------------------ GEMV dispatch
+template <int MT, int XM, bool OUT_I32>
+void *gemv_func(int wpt) {
+  switch (wpt) {
+    case 1: return reinterpret_cast<void *>(&gemv::gemv_kernel<MT, 1, XM, OUT_I32>);
+    case 2: return reinterpret_cast<void *>(&gemv::gemv_kernel<MT, 2, XM, OUT_I32>);
+    default: break;
+  }
+  if constexpr (MT <= 2) {
+    switch (wpt) {
+      case 3: return reinterpret_cast<void *>(&gemv::gemv_kernel<MT, 3, XM, OUT_I32>);
+      case 4: return reinterpret_cast<void *>(&gemv::gemv_kernel<MT, 4, XM, OUT_I32>);
+      default: break;
+    }
+  }
+  if constexpr (MT == 1) {
+    switch (wpt) {
+      case 5: return reinterpret_cast<void *>(&gemv::gemv_kernel<MT, 5, XM, OUT_I32>);
+      case 6: return reinterpret_cast<void *>(&gemv::gemv_kernel<MT, 6, XM, OUT_I32>);
+      case 7: return reinterpret_cast<void *>(&gemv::gemv_kernel<MT, 7, XM, OUT_I32>);
+      case 8: return reinterpret_cast<void *>(&gemv::gemv_kernel<MT, 8, XM, OUT_I32>);
+      default: break;
+    }
+  }
+  return nullptr;
+}
+
+template <int XM, bool OUT_I32>
+void *gemv_func_m(int mt, int wpt) {
+  if (mt == 1) return gemv_func<1, XM, OUT_I32>(wpt);
+  if (mt == 2) return gemv_func<2, XM, OUT_I32>(wpt);
+  return gemv_func<4, XM, OUT_I32>(wpt);
+}
+
+bl_status run_gemv(const plan::Plan &pl, int dev, int sms, int xm, bool out_i32, const uint8_t *packed,
+                   const float *gamma, const void *x, const int8_t *xq, const float *scale, float *y,
+                   int32_t *acc, cudaStream_t st) {
+  void *f = nullptr;
+  if (out_i32)
+    f = gemv_func_m<gemv::kXInt8, true>(pl.mt, pl.wpt);
+  else if (xm == gemv::kXF32)
+    f = gemv_func_m<gemv::kXF32, false>(pl.mt, pl.wpt);
+  else if (xm == gemv::kXBF16)
+    f = gemv_func_m<gemv::kXBF16, false>(pl.mt, pl.wpt);
+  else
+    f = gemv_func_m<gemv::kXInt8, false>(pl.mt, pl.wpt);
+  if (!f) return BL_ERR_UNSUPPORTED;
+  bl_status s = ensure_smem(dev, f, gemv::kSmemBytes);
+  if (s != BL_OK) return s;
+  gemv::Params p{};
+  p.packed = packed;
+  p.gamma = gamma;
+  p.x = x;
+  p.xq = xq;
+  p.scale = scale;
+  p.y = y;
+  p.acc = acc;
+  p.N = pl.N;
+  p.K = static_cast<int>(pl.K);
+  p.words = static_cast<int>(pl.row_bytes / 4);
+  p.row_bytes = static_cast<int>(pl.row_bytes);
+  p.M = static_cast<int>(pl.M);
+  const plan::GemvGrid g = plan::gemv_grid(pl, sms);
+  p.rows_per_cta = g.rows_per_cta;
+  p.stage_rows = g.stage_rows;
+  p.tpr_log2 = pl.tpr_log2;
+  return launch(reinterpret_cast<void (*)(gemv::Params)>(f), dim3(g.grid), dim3(gemv::kThreads),
+                gemv::kSmemBytes, st, g_overlap.load() != 0, p);
+}
+
+// ------------------------------------------------------------ tensor-core dispatch
+template <int BN, bool OUT_I32>
+bl_status run_tc_bn(const plan::Plan &pl, int dev, const CUtensorMap &mx, const CUtensorMap &mw,
+                    const tc::Params &p, cudaStream_t st) {
+  auto *f = &tc::tc_gemm_kernel<BN, OUT_I32>;
+  constexpr int smem = tc::Cfg<BN>::kSmemBytes;
+  bl_status s = ensure_smem(dev, reinterpret_cast<const void *>(f), smem);
+  if (s != BL_OK) return s;
+  dim3 grid(static_cast<unsigned>(pl.tiles_n), static_cast<unsigned>(pl.tiles_m),
+            static_cast<unsigned>(pl.splits));
+  return launch(f, grid, dim3(tc::kThreads), smem, st, g_overlap.load() != 0, mx, mw, p);
+}
+
+template <bool OUT_I32>
+bl_status run_tc(const plan::Plan &pl, int dev, const CUtensorMap &mx, const CUtensorMap &mw,
+                 const tc::Params &p, cudaStream_t st) {
+  switch (pl.bn) {
+    case 16: return run_tc_bn<16, OUT_I32>(pl, dev, mx, mw, p, st);
+    case 32: return run_tc_bn<32, OUT_I32>(pl, dev, mx, mw, p, st);
+    case 64: return run_tc_bn<64, OUT_I32>(pl, dev, mx, mw, p, st);
+    case 128: return run_tc_bn<128, OUT_I32>(pl, dev, mx, mw, p, st);
+    case 256: return run_tc_bn<256, OUT_I32>(pl, dev, mx, mw, p, st);
+    default: return BL_ERR_UNSUPPORTED;
+  }
+}
+
+// Shared body of forward / forward_q / matmul_i32 on the tensor-core path.
+// xm: activation source (f32 / bf16 to be quantised, or int8 codes).
+bl_status forward_tc(const plan::Plan &pl, int dev, int xm, bool out_i32, const uint8_t *packed,
+                     const float *gamma, const void *x, const int8_t *xq, const float *scale, float *y,
+                     int32_t *acc, void *ws, size_t ws_bytes, cudaStream_t st) {
+  if (ws == nullptr || ws_bytes < pl.ws_bytes) return BL_ERR_WORKSPACE;
+  if (!aligned(ws, 256)) return BL_ERR_ALIGN;
+  uint8_t *w = static_cast<uint8_t *>(ws);
+  auto *xb = reinterpret_cast<__nv_bfloat16 *>(w + pl.off_xb);
+  float *sc = reinterpret_cast<float *>(w + pl.off_sc);
+  int32_t *wacc = reinterpret_cast<int32_t *>(w + pl.off_acc);
+  unsigned *wcnt = reinterpret_cast<unsigned *>(w + pl.off_cnt);
+  const bool overlap = g_overlap.load() != 0;
+
+  CUtensorMap mx, mw;
+  if (!make_map_x(&mx, xb, pl.M, pl.Kp, pl.bn) || !make_map_w(&mw, packed, pl.N, pl.row_bytes))
+    return BL_ERR_CUDA;
+
+  // 1) activations -> bf16 codes (+ scales), zeroing the split-K accumulators
+  const bool zero_acc = pl.splits > 1;
+  int32_t *zrows = zero_acc ? (out_i32 ? acc : wacc) : nullptr;
+  unsigned *zcnt = (zero_acc && !out_i32) ? wcnt : nullptr;
+  bl_status s;
+  const dim3 qgrid(static_cast<unsigned>(pl.M));
+  const float *use_scale = scale;
+  if (xm == gemv::kXInt8) {
+    s = launch(&codes_to_bf16_kernel, qgrid, dim3(256), 0, st, overlap, xq, pl.K, pl.Kp, xb, zrows,
+               pl.N, zcnt, pl.tiles_total);
+  } else {
+    use_scale = sc;
+    if (xm == gemv::kXF32)
+      s = launch(&quant_act_kernel<float, true, false>, qgrid, dim3(256), 0, st, overlap,
+                 static_cast<const float *>(x), pl.K, pl.Kp, static_cast<const float *>(nullptr), 0.0f,
+                 static_cast<int8_t *>(nullptr), xb, sc, zrows, pl.N, zcnt, pl.tiles_total);
+    else
+      s = launch(&quant_act_kernel<__nv_bfloat16, true, false>, qgrid, dim3(256), 0, st, overlap,
+                 static_cast<const __nv_bfloat16 *>(x), pl.K, pl.Kp, static_cast<const float *>(nullptr),
+                 0.0f, static_cast<int8_t *>(nullptr), xb, sc, zrows, pl.N, zcnt, pl.tiles_total);
+  }
+  if (s != BL_OK) return s;
+
+  // 2) the contraction
+  tc::Params p{};
+  p.N = static_cast<int>(pl.N);
+  p.M = static_cast<int>(pl.M);
+  p.num_kt = static_cast<int>(pl.Kp / tc::kBK);
+  p.kt_per_split = pl.kt_per_split;
+  p.splits = pl.splits;
+  p.gamma = gamma;
+  p.scale = use_scale;
+  p.y = y;
+  p.acc_out = acc;
+  p.ws_acc = wacc;
+  p.ws_cnt = wcnt;
+  if (out_i32) return run_tc<true>(pl, dev, mx, mw, p, st);
+  return run_tc<false>(pl, dev, mx, mw, p, st);
+}
+
+bl_status forward_common(const uint8_t *packed, const float *gamma, int64_t N, int64_t K, int xm,
+                         const void *x, const int8_t *xq, const float *scale, int64_t M, float *y,
+                         int32_t *acc, void *ws, size_t ws_bytes, void *stream) {
+  const bool out_i32 = acc != nullptr;
+  if (packed == nullptr || (!out_i32 && (gamma == nullptr || y == nullptr)))
+    return BL_ERR_NULL;
+  if (xm == gemv::kXInt8 ? xq == nullptr : x == nullptr) return BL_ERR_NULL;
+  if (xm == gemv::kXInt8 && !out_i32 && scale == nullptr) return BL_ERR_NULL;
+  bl_status s = check_dims(M, N, K);
+  if (s != BL_OK) return s;
+  if (!aligned(packed, 16)) return BL_ERR_ALIGN;
+  if (N > 0x7fffffffLL / 1 || static_cast<double>(M) * static_cast<double>(N) > 9.0e15)
+    return BL_ERR_SHAPE;
+  const plan::Plan pl = plan::make(M, N, K);
+  if (pl.path == plan::kTc && (M > 0x7fffffff || N > 0x7fffffff)) return BL_ERR_SHAPE;
+  int dev = 0, sms = 0;
+  s = current_device(&dev, &sms);
+  if (s != BL_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (pl.path == plan::kGemv)
+    return run_gemv(pl, dev, sms, xm, out_i32, packed, gamma, x, xq, scale, y, acc, st);
+  return forward_tc(pl, dev, xm, out_i32, packed, gamma, x, xq, scale, y, acc, ws, ws_bytes, st);
+}
+
+}  // namespace
+
+// ====================================================================== C ABI
+extern "C" {
+
+int bitlinear_version(void) { return 100; }
+
+const char *bitlinear_status_string(int status) {
+  switch (status) {
+    case BL_OK: return "ok";
+    case BL_ERR_NULL: return "a required pointer is NULL";
+    case BL_ERR_SHAPE: return "a size is outside the supported range";
+    case BL_ERR_DTYPE: return "unknown dtype code";
+    case BL_ERR_ALIGN: return "a pointer is not suitably aligned";
+    case BL_ERR_WORKSPACE: return "workspace missing or too small";
+    case BL_ERR_CUDA: return "a CUDA call or kernel launch failed";
+    case BL_ERR_UNSUPPORTED: return "the current device is not an sm_103 GPU";
+    case BL_ERR_DEVICE: return "a kernel gave up a bounded wait";
+    default: return "unknown status";
+  }
+}
+
+bl_status bitlinear_packed_row_bytes(int64_t K, int64_t *bytes) {
+  if (bytes == nullptr) return BL_ERR_NULL;
+  if (K < 1 || K > kMaxK) return BL_ERR_SHAPE;
+  *bytes = plan::row_bytes(K);
+  return BL_OK;
+}
+
+bl_status bitlinear_packed_bytes(int64_t N, int64_t K, size_t *bytes) {
+  if (bytes == nullptr) return BL_ERR_NULL;
+  if (N < 1 || N > kMaxDim || K < 1 || K > kMaxK) return BL_ERR_SHAPE;
+  *bytes = static_cast<size_t>(N) * static_cast<size_t>(plan::row_bytes(K));
+  return BL_OK;
+}
+
+bl_status bitlinear_pack_workspace_bytes(int64_t N, int64_t K, size_t *bytes) {
+  if (bytes == nullptr) return BL_ERR_NULL;
+  if (N < 1 || N > kMaxDim || K < 1 || K > kMaxK) return BL_ERR_SHAPE;
+  *bytes = static_cast<size_t>(N) * sizeof(double);
+  return BL_OK;
+}
+
+bl_status bitlinear_pack_weights(const void *W, int dtype, int64_t N, int64_t K, uint8_t *packed,
+                                 float *gamma, void *ws, size_t ws_bytes, void *stream) {
+  if (W == nullptr || packed == nullptr || gamma == nullptr) return BL_ERR_NULL;
+  if (dtype != BL_F32 && dtype != BL_BF16) return BL_ERR_DTYPE;
+  if (N < 1 || N > kMaxDim || K < 1 || K > kMaxK) return BL_ERR_SHAPE;
+  if (ws == nullptr || ws_bytes < static_cast<size_t>(N) * sizeof(double)) return BL_ERR_WORKSPACE;
+  if (!aligned(packed, 16) || !aligned(ws, 8) || !aligned(gamma, 4)) return BL_ERR_ALIGN;
+  int dev = 0;
+  bl_status s = current_device(&dev, nullptr);
+  if (s != BL_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  double *rowsum = static_cast<double *>(ws);
+  const int64_t wpr = plan::row_bytes(K) / 4;
+  const unsigned gsum = static_cast<unsigned>((N + 255) / 256);
+  const unsigned gcode = static_cast<unsigned>((N * wpr + 255) / 256);
+  uint32_t *pw = reinterpret_cast<uint32_t *>(packed);
+  if (dtype == BL_F32) {
+    const float *w = static_cast<const float *>(W);
+    if ((s = launch(&pack_rowsum_kernel<float>, dim3(gsum), dim3(256), 0, st, false, w, N, K, rowsum)))
+      return s;
+    if ((s = launch(&pack_gamma_kernel, dim3(1), dim3(32), 0, st, false,
+                    static_cast<const double *>(rowsum), N, K, gamma)))
+      return s;
+    return launch(&pack_codes_kernel<float>, dim3(gcode), dim3(256), 0, st, false, w, N, K, wpr,
+                  static_cast<const float *>(gamma), pw);
+  }
+  const __nv_bfloat16 *w = static_cast<const __nv_bfloat16 *>(W);
+  if ((s = launch(&pack_rowsum_kernel<__nv_bfloat16>, dim3(gsum), dim3(256), 0, st, false, w, N, K,
+                  rowsum)))
+    return s;
+  if ((s = launch(&pack_gamma_kernel, dim3(1), dim3(32), 0, st, false, static_cast<const double *>(rowsum),
+                  N, K, gamma)))
+    return s;
+  return launch(&pack_codes_kernel<__nv_bfloat16>, dim3(gcode), dim3(256), 0, st, false, w, N, K, wpr,
+                static_cast<const float *>(gamma), pw);
+}
+
+static bl_status quant_common(const void *x, int dtype, const float *g, float eps, bool norm, int64_t M,
+                              int64_t K, int8_t *xq, float *scale, void *stream) {
+  if (x == nullptr || xq == nullptr || scale == nullptr) return BL_ERR_NULL;
+  if (dtype != BL_F32 && dtype != BL_BF16) return BL_ERR_DTYPE;
+  if (M < 1 || M > kMaxDim || K < 1 || K > kMaxK) return BL_ERR_SHAPE;
+  if (norm && !(eps >= 0.0f)) return BL_ERR_SHAPE;
+  int dev = 0;
+  bl_status s = current_device(&dev, nullptr);
+  if (s != BL_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool ov = g_overlap.load() != 0;
+  const dim3 grid(static_cast<unsigned>(M));
+  __nv_bfloat16 *nob = nullptr;
+  int32_t *noz = nullptr;
+  unsigned *noc = nullptr;
+  if (dtype == BL_F32) {
+    const float *xx = static_cast<const float *>(x);
+    if (norm)
+      return launch(&quant_act_kernel<float, false, true>, grid, dim3(256), 0, st, ov, xx, K, K, g, eps, xq,
+                    nob, scale, noz, int64_t(0), noc, 0);
+    return launch(&quant_act_kernel<float, false, false>, grid, dim3(256), 0, st, ov, xx, K, K, g, eps, xq,
+                  nob, scale, noz, int64_t(0), noc, 0);
+  }
+  const __nv_bfloat16 *xx = static_cast<const __nv_bfloat16 *>(x);
+  if (norm)
+    return launch(&quant_act_kernel<__nv_bfloat16, false, true>, grid, dim3(256), 0, st, ov, xx, K, K, g,
+                  eps, xq, nob, scale, noz, int64_t(0), noc, 0);
+  return launch(&quant_act_kernel<__nv_bfloat16, false, false>, grid, dim3(256), 0, st, ov, xx, K, K, g,
+                eps, xq, nob, scale, noz, int64_t(0), noc, 0);
+}
+
+bl_status bitlinear_quant_act(const void *x, int dtype, int64_t M, int64_t K, int8_t *xq, float *scale,
+                              void *stream) {
+  return quant_common(x, dtype, nullptr, 0.0f, false, M, K, xq, scale, stream);
+}
+
+bl_status bitlinear_rmsnorm_quant_act(const void *x, int dtype, const float *g, float eps, int64_t M,
+                                      int64_t K, int8_t *xq, float *scale, void *stream) {
+  return quant_common(x, dtype, g, eps, true, M, K, xq, scale, stream);
+}
+
+bl_status bitlinear_workspace_bytes(int64_t M, int64_t N, int64_t K, size_t *bytes) {
+  if (bytes == nullptr) return BL_ERR_NULL;
+  bl_status s = check_dims(M, N, K);
+  if (s != BL_OK) return s;
+  *bytes = plan::make(M, N, K).ws_bytes;
+  return BL_OK;
+}
+
+bl_status bitlinear_forward(const uint8_t *packed, const float *gamma, int64_t N, int64_t K, const void *x,
+                            int dtype, int64_t M, float *y, void *ws, size_t ws_bytes, void *stream) {
+  if (dtype != BL_F32 && dtype != BL_BF16) return BL_ERR_DTYPE;
+  const int xm = dtype == BL_F32 ? gemv::kXF32 : gemv::kXBF16;
+  if (y == nullptr) return BL_ERR_NULL;
+  return forward_common(packed, gamma, N, K, xm, x, nullptr, nullptr, M, y, nullptr, ws, ws_bytes, stream);
+}
+
+bl_status bitlinear_forward_q(const uint8_t *packed, const float *gamma, int64_t N, int64_t K,
+                              const int8_t *xq, const float *scale, int64_t M, float *y, void *ws,
+                              size_t ws_bytes, void *stream) {
+  if (y == nullptr) return BL_ERR_NULL;
+  return forward_common(packed, gamma, N, K, gemv::kXInt8, nullptr, xq, scale, M, y, nullptr, ws, ws_bytes,
+                        stream);
+}
+
+bl_status bitlinear_matmul_i32(const uint8_t *packed, int64_t N, int64_t K, const int8_t *xq, int64_t M,
+                               int32_t *acc, void *ws, size_t ws_bytes, void *stream) {
+  if (acc == nullptr) return BL_ERR_NULL;
+  return forward_common(packed, nullptr, N, K, gemv::kXInt8, nullptr, xq, nullptr, M, nullptr, acc, ws,
+                        ws_bytes, stream);
+}
+
+void bitlinear_set_launch_overlap(int on) { g_overlap.store(on ? 1 : 0); }
+
+int bitlinear_get_launch_overlap(void) { return g_overlap.load(); }
+
+bl_status bitlinear_device_error(unsigned int *flags, int clear) {
+  if (flags == nullptr) return BL_ERR_NULL;
+  unsigned v = 0;
+  if (cudaMemcpyFromSymbol(&v, bl::g_dev_error, sizeof(v)) != cudaSuccess) {
+    cudaGetLastError();
+    return BL_ERR_CUDA;
+  }
+  if (clear && v != 0) {
+    const unsigned z = 0;
+    if (cudaMemcpyToSymbol(bl::g_dev_error, &z, sizeof(z)) != cudaSuccess) {
+      cudaGetLastError();
+      return BL_ERR_CUDA;
+    }
+  }
+  *flags = v;
+  return v ? BL_ERR_DEVICE : BL_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,293 @@
+// Tensor-core BitLinear contraction for M > 4 tokens (batched decode and
+// prefill), tcgen05 on sm_103a.
+//
+// sm_103a has no integer MMA (ptxas rejects tcgen05.mma kind::i8 for this
+// target), so the int8 x ternary product runs as kind::f16 with bf16
+// operands: every code (-1, 0, +1) and every activation code (-128..127) is
+// an exact bf16, each product is exact and every partial sum is an integer
+// below 127 * K <= 2^24, which fp32 accumulation represents exactly.  The
+// accumulator is therefore the exact int32 dot product.
+//
+// Tile: 128 weight rows (the MMA's M) x BN tokens (the MMA's N) x 64 k per
+// pipeline stage.  Roles (192 threads):
+//   warp 0      TMA producer: the packed 2-bit weight tile (128 rows x 16 B)
+//               and the bf16 activation tile (BN rows x 128 B, 128-byte
+//               swizzle) of each stage, completion on one mbarrier.
+//   warp 1      allocates TMEM; one lane issues the MMAs (4 x K=16 per stage)
+//               and commits each stage back to the producer.
+//   warps 2..5  unpack: each thread expands one weight row of the packed tile
+//               (16 bytes = 64 codes) into 64 bf16 values, written straight
+//               into the 128-byte-swizzled K-major layout the MMA reads
+//               ("pack-store-load-unpack-compute": packed in HBM, unpacked in
+//               shared memory -- "微软AI大模型炸场：0.4GB，CPU就能跑",
+//               blog.csdn.net/2401_84494441, section 3, GPU bullet).  Then
+//               the epilogue: TMEM -> registers -> y = fl32(fl32(acc*gamma)/s).
+// Split-K (for small tile counts): partial int32 sums are added atomically
+// into a workspace zeroed by the preceding activation kernel; the last CTA
+// of each tile (an atomic ticket, no spinning) applies the rescale.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "bl_pack_quant.cuh"
+#include "bl_ptx.cuh"
+
+namespace bl {
+namespace tc {
+
+constexpr int kThreads = 192;
+constexpr int kBM = 128;                 // weight rows per tile
+constexpr int kBK = 64;                  // k per stage
+constexpr int kABytes = kBM * kBK * 2;   // unpacked weights, bf16
+constexpr int kPBytes = kBM * kBK / 4;   // packed weights
+constexpr int kSmemBudget = 200 * 1024;
+
+template <int BN>
+struct Cfg {
+  static constexpr int kBBytes = BN * kBK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes + kPBytes;
+  static constexpr int kStages = (kSmemBudget / kStageBytes) > 8 ? 8 : (kSmemBudget / kStageBytes);
+  static constexpr int kTmemCols = BN < 32 ? 32 : BN;
+  static constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 1024;
+  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
+  static_assert(kStages >= 2, "pipeline depth");
+};
+
+struct Params {
+  int N, M;
+  int num_kt;        // k tiles in the padded K (Kp / 64)
+  int kt_per_split;
+  int splits;
+  const float *gamma;
+  const float *scale;  // [M] activation scales (float output only)
+  float *y;            // [M, N]
+  int32_t *acc_out;    // [M, N] (int32 output)
+  int32_t *ws_acc;     // [M, N] split-K partial sums (float output, splits > 1)
+  unsigned *ws_cnt;    // per output tile tickets (float output, splits > 1)
+};
+
+struct Bars {
+  uint64_t full[8];
+  uint64_t afull[8];
+  uint64_t empty[8];
+  uint64_t accfull;
+  uint32_t tmem_base;
+  int abort_flag;
+  int last_flag;
+};
+
+// bf16 bytes of (code - 1) for code 0, 1, 2: -1.0 = 0xBF80, 0, +1.0 = 0x3F80.
+constexpr uint32_t kTabHi = 0x003F00BFu;
+constexpr uint32_t kTabLo = 0x00800080u;
+
+// Four 2-bit codes, one per byte, -> two 32-bit words of bf16 pairs.
+__device__ __forceinline__ void codes4_to_bf16(uint32_t codes, uint32_t &w01, uint32_t &w23) {
+  const uint32_t t = codes * 0x11u + 0x04040404u;  // selector nibbles [c+4, c] per code
+  w01 = __byte_perm(kTabHi, kTabLo, t);
+  w23 = __byte_perm(kTabHi, kTabLo, t >> 16);
+}
+
+template <int BN, bool OUT_I32>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
+                   const Params p) {
+  using C = Cfg<BN>;
+  constexpr int S = C::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  const uint32_t a_base = base;
+  const uint32_t b_base = base + S * kABytes;
+  const uint32_t p_base = b_base + S * C::kBBytes;
+  Bars &bars = *reinterpret_cast<Bars *>(smem_raw + (base - raw) + S * C::kStageBytes);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n0 = blockIdx.x * kBM;
+  const int m0 = blockIdx.y * BN;
+  const int kt0 = blockIdx.z * p.kt_per_split;
+  int nkt = p.num_kt - kt0;
+  if (nkt > p.kt_per_split) nkt = p.kt_per_split;
+
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_u32(&bars.full[s]), 1);
+      mbar_init(smem_u32(&bars.afull[s]), 128);
+      mbar_init(smem_u32(&bars.empty[s]), 1);
+    }
+    mbar_init(smem_u32(&bars.accfull), 1);
+    bars.abort_flag = 0;
+    bars.last_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&map_x);
+    prefetch_tensormap(&map_w);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&bars.tmem_base), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars.tmem_base;
+  pdl_launch_dependents();
+  volatile int *abort_flag = &bars.abort_flag;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_x = policy_evict_last();
+      constexpr uint32_t kTx = kPBytes + C::kBBytes;
+      const int pre = nkt < S ? nkt : S;
+      // Weights are static inputs: start on them before the previous kernel ends.
+      for (int i = 0; i < pre; ++i) {
+        const uint32_t fb = smem_u32(&bars.full[i]);
+        mbar_arrive_expect_tx(fb, kTx);
+        tma_load_2d(p_base + i * kPBytes, &map_w, (kt0 + i) * 16, n0, fb, pol_w);
+      }
+      pdl_wait_primary();
+      for (int i = 0; i < pre; ++i)
+        tma_load_2d(b_base + i * C::kBBytes, &map_x, (kt0 + i) * kBK, m0, smem_u32(&bars.full[i]),
+                    pol_x);
+      int issued = pre;
+      for (int i = pre; i < nkt; ++i) {
+        const int s = i % S;
+        if (!mbar_wait(smem_u32(&bars.empty[s]), ((i / S) - 1) & 1) || *abort_flag) {
+          *abort_flag = 1;
+          break;
+        }
+        const uint32_t fb = smem_u32(&bars.full[s]);
+        mbar_arrive_expect_tx(fb, kTx);
+        tma_load_2d(p_base + s * kPBytes, &map_w, (kt0 + i) * 16, n0, fb, pol_w);
+        tma_load_2d(b_base + s * C::kBBytes, &map_x, (kt0 + i) * kBK, m0, fb, pol_x);
+        issued = i + 1;
+      }
+      for (int i = issued - S < 0 ? 0 : issued - S; i < issued; ++i)
+        mbar_wait(smem_u32(&bars.full[i % S]), (i / S) & 1);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN);
+      for (int i = 0; i < nkt; ++i) {
+        const int s = i % S;
+        const uint32_t ph = (i / S) & 1;
+        if (!mbar_wait(smem_u32(&bars.afull[s]), ph) || !mbar_wait(smem_u32(&bars.full[s]), ph) ||
+            *abort_flag) {
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint64_t ad = smem_desc_sw128(a_base + s * kABytes);
+        const uint64_t bd = smem_desc_sw128(b_base + s * C::kBBytes);
+#pragma unroll
+        for (int j = 0; j < kBK / 16; ++j)
+          mma_bf16_ss(tmem, ad + 2u * j, bd + 2u * j, idesc, (i | j) != 0 ? 1u : 0u);
+        mma_commit(smem_u32(&bars.empty[s]));
+      }
+      mma_commit(smem_u32(&bars.accfull));  // fires once every issued MMA is done
+    }
+  } else {
+    // ------------------------------------------------------------ unpack
+    const int u = tid - 64;  // weight row of the tile
+    const uint32_t swz = static_cast<uint32_t>(u & 7);
+    for (int i = 0; i < nkt; ++i) {
+      const int s = i % S;
+      if (!mbar_wait(smem_u32(&bars.full[s]), (i / S) & 1) || *abort_flag) {
+        *abort_flag = 1;
+        break;
+      }
+      const uint4 pk = lds_u128(p_base + s * kPBytes + u * 16);
+      const uint32_t words[4] = {pk.x, pk.y, pk.z, pk.w};
+      const uint32_t arow = a_base + s * kABytes + u * 128;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {  // 16-byte chunk c holds k = 8c .. 8c+7
+        const uint32_t word = words[c >> 1];
+        // k = 8c .. 8c+3 sit at i = 2(c&1) (bit shift 2i), k = 8c+4 .. 8c+7 at i + 1
+        const int sh = 4 * (c & 1);
+        uint32_t v0, v1, v2, v3;
+        codes4_to_bf16((word >> sh) & 0x03030303u, v0, v1);
+        codes4_to_bf16((word >> (sh + 2)) & 0x03030303u, v2, v3);
+        sts_u128(arow + ((static_cast<uint32_t>(c) ^ swz) << 4), v0, v1, v2, v3);
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(smem_u32(&bars.afull[s]));
+    }
+
+    // ------------------------------------------------------------ epilogue
+    // scale / split-K workspace come from the previous kernel on the stream
+    pdl_wait_primary();
+    bool ok = mbar_wait(smem_u32(&bars.accfull), 0);
+    // One decision for all four epilogue warps (they share named barriers and
+    // warp-collective TMEM loads below).
+    ok = !named_bar_or(4, 128, !ok || *abort_flag);
+    tc_fence_after();
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int row = 32 * q + lane;
+    const int n = n0 + row;
+    const float gamma = OUT_I32 ? 1.0f : *p.gamma;
+    if (ok) {
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + c0, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int m = m0 + c0 + j;
+          if (c0 + j < BN && m < p.M && n < p.N) {
+            const int v = static_cast<int>(__uint_as_float(r[j]));
+            const int64_t o = static_cast<int64_t>(m) * p.N + n;
+            if constexpr (OUT_I32) {
+              if (p.splits == 1)
+                p.acc_out[o] = v;
+              else
+                atomicAdd(&p.acc_out[o], v);
+            } else {
+              if (p.splits == 1)
+                p.y[o] = __fdiv_rn(__fmul_rn(static_cast<float>(v), gamma), p.scale[m]);
+              else
+                atomicAdd(&p.ws_acc[o], v);
+            }
+          }
+        }
+      }
+      if constexpr (!OUT_I32) {
+        if (p.splits > 1) {
+          __threadfence();
+          named_bar(3, 128);
+          if (tid == 64) {
+            const unsigned t = atomicAdd(&p.ws_cnt[blockIdx.y * gridDim.x + blockIdx.x], 1u);
+            bars.last_flag = (t == static_cast<unsigned>(p.splits - 1)) ? 1 : 0;
+          }
+          named_bar(3, 128);
+          if (bars.last_flag) {
+            __threadfence();
+            if (n < p.N) {
+              for (int j = 0; j < BN; ++j) {
+                const int m = m0 + j;
+                if (m >= p.M) break;
+                const int64_t o = static_cast<int64_t>(m) * p.N + n;
+                const int v = __ldcg(&p.ws_acc[o]);
+                p.y[o] = __fdiv_rn(__fmul_rn(static_cast<float>(v), gamma), p.scale[m]);
+              }
+            }
+          }
+        }
+      }
+    }
+    tc_fence_before();
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+}  // namespace tc
+}  // namespace bl

@@ -1,0 +1,225 @@
+// Weight ternarisation + packing, and activation quantisation kernels.
+//
+// Weights: absmean ternarisation, one fp32 scale per tensor ("20亿参数仅0.4GB…
+// 「原生1.58bit」大模型", blog.csdn.net/soaring_casia, section 2 "BitLinear层",
+// item 1).  Activations: per-token absmax to int8 (same section, item 2).
+// The fused variant applies the subln RMSNorm first (item 3).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "bl_ptx.cuh"
+
+namespace bl {
+
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+// ------------------------------------------------------------------ pack
+// Row sums of |W| in fp64, each row added sequentially over k.  A block
+// owns 256 rows; 32-column slabs are staged through shared memory so the
+// global reads are coalesced while every row keeps its k order.
+template <typename WT>
+__global__ void __launch_bounds__(256) pack_rowsum_kernel(const WT *__restrict__ W, int64_t N,
+                                                          int64_t K, double *__restrict__ rowsum) {
+  __shared__ float tile[256][33];
+  const int64_t n0 = static_cast<int64_t>(blockIdx.x) * 256;
+  const int t = threadIdx.x;
+  double acc = 0.0;
+  for (int64_t k0 = 0; k0 < K; k0 += 32) {
+#pragma unroll 4
+    for (int i = 0; i < 32; ++i) {
+      const int r = (t >> 5) + 8 * i;
+      const int c = t & 31;
+      const int64_t n = n0 + r, k = k0 + c;
+      tile[r][c] = (n < N && k < K) ? to_f32(W[n * K + k]) : 0.0f;
+    }
+    __syncthreads();
+    const int kmax = static_cast<int>(K - k0 < 32 ? K - k0 : 32);
+    for (int c = 0; c < kmax; ++c) acc += fabs(static_cast<double>(tile[t][c]));
+    __syncthreads();
+  }
+  if (n0 + t < N) rowsum[n0 + t] = acc;
+}
+
+// gamma = fl32( fl32(S / (N*K)) + 1e-5f ), S = row sums added in row order.
+__global__ void pack_gamma_kernel(const double *__restrict__ rowsum, int64_t N, int64_t K,
+                                  float *__restrict__ gamma) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  double S = 0.0;
+  for (int64_t n = 0; n < N; ++n) S = __dadd_rn(S, rowsum[n]);
+  const float mean = __double2float_rn(__ddiv_rn(S, static_cast<double>(N) * static_cast<double>(K)));
+  *gamma = __fadd_rn(mean, 1e-5f);
+}
+
+// One thread per 32-bit packed word (16 weights).  Code = clip(rint(W/gamma))+1;
+// weight k = 16w + 4i + j goes to bit 8j + 2i; k >= K gets code 1.
+template <typename WT>
+__global__ void __launch_bounds__(256) pack_codes_kernel(const WT *__restrict__ W, int64_t N,
+                                                         int64_t K, int64_t words_per_row,
+                                                         const float *__restrict__ gamma,
+                                                         uint32_t *__restrict__ packed) {
+  const int64_t id = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (id >= N * words_per_row) return;
+  const int64_t n = id / words_per_row;
+  const int64_t w = id - n * words_per_row;
+  const float g = *gamma;
+  const WT *row = W + n * K;
+  uint32_t word = 0;
+#pragma unroll
+  for (int t = 0; t < 16; ++t) {
+    const int64_t k = 16 * w + t;
+    uint32_t code = 1u;
+    if (k < K) {
+      float q = rintf(__fdiv_rn(to_f32(row[k]), g));
+      q = fminf(fmaxf(q, -1.0f), 1.0f);
+      code = static_cast<uint32_t>(static_cast<int>(q) + 1);
+    }
+    word |= code << (8 * (t & 3) + 2 * (t >> 2));
+  }
+  packed[id] = word;
+}
+
+// ------------------------------------------------------------------ quant
+// Block-wide reductions over the first `nthreads` threads of a block
+// (a multiple of 32), using named barrier `bar_id`.
+__device__ __forceinline__ void named_bar(int bar_id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "r"(nthreads) : "memory");
+}
+
+// Barrier over the first `nthreads` threads that also ORs a predicate.
+__device__ __forceinline__ bool named_bar_or(int bar_id, int nthreads, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "barrier.cta.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "r"(bar_id), "r"(nthreads)
+      : "memory");
+  return r != 0u;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ double warp_sum_f64(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// xq = clip(rint(fl32(v * s)), -128, 127)
+__device__ __forceinline__ int quant_one(float v, float s) {
+  float r = rintf(__fmul_rn(v, s));
+  r = fminf(fmaxf(r, -128.0f), 127.0f);
+  return static_cast<int>(r);
+}
+
+__device__ __forceinline__ float act_scale(float amax) {
+  return __fdiv_rn(127.0f, fmaxf(amax, 1e-5f));
+}
+
+// Zero row m of an int32 [M, zn] accumulator and (block 0) ncnt tickets: the
+// split-K contraction that follows on the stream adds into them.
+__device__ __forceinline__ void zero_fill(int64_t m, int32_t *zrows, int64_t zn, unsigned *zcnt,
+                                          int ncnt) {
+  if (zrows != nullptr)
+    for (int64_t k = threadIdx.x; k < zn; k += blockDim.x) zrows[m * zn + k] = 0;
+  if (zcnt != nullptr && m == 0)
+    for (int i = threadIdx.x; i < ncnt; i += blockDim.x) zcnt[i] = 0u;
+}
+
+// One block (256 threads) per token row.
+//   OUT_BF16 = false: xq int8 [M, K] dense.
+//   OUT_BF16 = true : integer codes as bf16 [M, ld] (exact), zero for k in [K, ld);
+//                     the tensor-core path reads this layout.
+//   NORM: fused subln RMSNorm (gain g may be NULL).
+template <typename XT, bool OUT_BF16, bool NORM>
+__global__ void __launch_bounds__(256) quant_act_kernel(const XT *__restrict__ x, int64_t K,
+                                                        int64_t ld, const float *__restrict__ g,
+                                                        float eps, int8_t *__restrict__ xq,
+                                                        __nv_bfloat16 *__restrict__ xb,
+                                                        float *__restrict__ scale,
+                                                        int32_t *__restrict__ zrows, int64_t zn,
+                                                        unsigned *__restrict__ zcnt, int ncnt) {
+  __shared__ float red_f[8];
+  __shared__ double red_d[8];
+  pdl_wait_primary();
+  pdl_launch_dependents();
+  const int64_t m = blockIdx.x;
+  const XT *xr = x + m * K;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+
+  float r_norm = 1.0f;
+  if (NORM) {
+    // sum of squares: compensated fp32 per thread, fp64 across threads
+    float s1 = 0.0f, c1 = 0.0f;
+    for (int64_t k = t; k < K; k += 256) {
+      const float v = to_f32(xr[k]);
+      const float y = __fsub_rn(__fmul_rn(v, v), c1);
+      const float tt = __fadd_rn(s1, y);
+      c1 = __fsub_rn(__fsub_rn(tt, s1), y);
+      s1 = tt;
+    }
+    double part = static_cast<double>(s1) - static_cast<double>(c1);
+    part = warp_sum_f64(part);
+    if (lane == 0) red_d[warp] = part;
+    __syncthreads();
+    double S = 0.0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) S += red_d[i];
+    const float ms = __double2float_rn(S / static_cast<double>(K));
+    const float d = __fsqrt_rn(__fadd_rn(ms, eps));
+    r_norm = __fdiv_rn(1.0f, d);
+  }
+
+  float amax = 0.0f;
+  for (int64_t k = t; k < K; k += 256) {
+    float v = to_f32(xr[k]);
+    if (NORM && g != nullptr) v = __fmul_rn(v, g[k]);
+    amax = fmaxf(amax, fabsf(v));
+  }
+  amax = warp_max(amax);
+  if (lane == 0) red_f[warp] = amax;
+  __syncthreads();
+  amax = red_f[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red_f[i]);
+  const float s = act_scale(amax);
+  if (t == 0) scale[m] = NORM ? __fdiv_rn(s, r_norm) : s;
+
+  for (int64_t k = t; k < K; k += 256) {
+    float v = to_f32(xr[k]);
+    if (NORM && g != nullptr) v = __fmul_rn(v, g[k]);
+    const int q = quant_one(v, s);
+    if (OUT_BF16)
+      xb[m * ld + k] = __float2bfloat16_rn(static_cast<float>(q));
+    else
+      xq[m * K + k] = static_cast<int8_t>(q);
+  }
+  if (OUT_BF16)
+    for (int64_t k = K + t; k < ld; k += 256) xb[m * ld + k] = __float2bfloat16_rn(0.0f);
+  zero_fill(m, zrows, zn, zcnt, ncnt);
+}
+
+// int8 codes [M, K] -> bf16 [M, ld] (exact), zero padded; one block per row.
+__global__ void __launch_bounds__(256) codes_to_bf16_kernel(const int8_t *__restrict__ xq,
+                                                            int64_t K, int64_t ld,
+                                                            __nv_bfloat16 *__restrict__ xb,
+                                                            int32_t *__restrict__ zrows, int64_t zn,
+                                                            unsigned *__restrict__ zcnt, int ncnt) {
+  pdl_wait_primary();
+  pdl_launch_dependents();
+  const int64_t m = blockIdx.x;
+  for (int64_t k = threadIdx.x; k < ld; k += 256)
+    xb[m * ld + k] = __float2bfloat16_rn(k < K ? static_cast<float>(xq[m * K + k]) : 0.0f);
+  zero_fill(m, zrows, zn, zcnt, ncnt);
+}
+
+}  // namespace bl
