@@ -168,7 +168,7 @@ def matmul_i32(q, xq) -> np.ndarray:
 
 
 def rescale(acc, g, s) -> np.ndarray:
-    """y = fl32(fl32(float(acc) * gamma) / s_m)."""
+    """y = fl32(float(acc) * fl32(gamma / s_m))."""
     acc = np.ascontiguousarray(acc, dtype=np.int32)
     s = np.ascontiguousarray(s, dtype=np.float32)
     M, N = acc.shape

@@ -168,16 +168,18 @@ void bl_oracle_matmul_i32(const int8_t *q, const int8_t *xq, int64_t M,
   }
 }
 
-/* y[m, n] = fl32( fl32( float(acc) * gamma ) / s_m )  ([DeepDive 2.3(2)]:
- * y = (W_quant @ x_quant) * scale; the weight scale multiplies, the
- * activation scale 127/amax divides).  float(acc) is exact (|acc| < 2^24). */
+/* y[m, n] = fl32( float(acc) * c_m ),  c_m = fl32( gamma / s_m ).
+ * [DeepDive 2.3(2)]: y = (W_quant @ x_quant) * scale -- one scale applied to
+ * the integer product.  Here that scale is the weight scale gamma divided by
+ * the token's activation scale s_m = 127/amax (which quantised x by
+ * multiplication).  float(acc) is exact (|acc| < 2^24). */
 void bl_oracle_rescale(const int32_t *acc, float gamma, const float *s,
                        int64_t M, int64_t N, float *y) {
   for (int64_t m = 0; m < M; ++m) {
+    float c = gamma / s[m];
     for (int64_t n = 0; n < N; ++n) {
       float a = (float)acc[m * N + n];
-      float t = a * gamma;
-      y[m * N + n] = t / s[m];
+      y[m * N + n] = a * c;
     }
   }
 }
