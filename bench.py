@@ -47,79 +47,83 @@ def load_peaks() -> dict:
 
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
-    """Samples SM clock and throttle reasons through NVML while running."""
+    """Samples SM clocks and throttle reasons during the timed region.
 
-    REASONS = {  # NVML clocks-event reason bits
-        0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
-        0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
-        0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
-        0x100: "display_clock_setting"}
+    Uses the nvidia-smi query loop (the GPU picked by UUID, since nvidia-smi
+    numbers every GPU of the machine), or NVML when nvidia-smi is missing."""
 
-    def __init__(self, index: int, period_s: float = 0.002):
-        self.index, self.period = index, period_s
-        self.samples: list[tuple[int, int]] = []
-        self.max_mhz = None
-        self._stop = threading.Event()
-        self._t = None
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, index: int, period_ms: int = 50):
+        self.index, self.period_ms = index, period_ms
+        self.rows: list[list[str]] = []
         self.error = None
+        self._proc = None
+        self._t = None
 
-    def __enter__(self):
-        try:
-            import pynvml
-            pynvml.nvmlInit()
-            self._nv = pynvml
-            self._h = self._handle(pynvml)
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
-        except Exception as e:  # NVML missing: report, do not fail the bench
-            self.error = repr(e)
-            return self
-        self._t = threading.Thread(target=self._run, daemon=True)
-        self._t.start()
-        return self
-
-    def _handle(self, nv):
-        # NVML numbers every GPU of the machine; match the CUDA device by UUID.
+    def _uuid(self):
         import torch
         try:
-            want = str(torch.cuda.get_device_properties(self.index).uuid).lower()
-            for i in range(nv.nvmlDeviceGetCount()):
-                h = nv.nvmlDeviceGetHandleByIndex(i)
-                u = nv.nvmlDeviceGetUUID(h)
-                u = (u.decode() if isinstance(u, bytes) else u).lower()
-                if want and want in u:
-                    return h
+            u = str(torch.cuda.get_device_properties(self.index).uuid)
+            return u if u.startswith("GPU-") else "GPU-" + u
         except Exception:
-            pass
-        return nv.nvmlDeviceGetHandleByIndex(self.index)
+            return None
 
-    def _run(self):
-        nv = self._nv
-        while not self._stop.is_set():
-            try:
-                mhz = nv.nvmlDeviceGetClockInfo(self._h, nv.NVML_CLOCK_SM)
-                rs = nv.nvmlDeviceGetCurrentClocksEventReasons(self._h)
-                self.samples.append((mhz, rs))
-            except Exception as e:
-                self.error = repr(e)
-                return
-            time.sleep(self.period)
+    def __enter__(self):
+        import shutil
+        import subprocess
+        exe = shutil.which("nvidia-smi")
+        if exe is None:
+            self.error = "nvidia-smi not found"
+            return self
+        sel = self._uuid() or str(self.index)
+        cmd = [exe, "-i", sel, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", str(self.period_ms)]
+        try:
+            self._proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                          text=True)
+        except Exception as e:
+            self.error = repr(e)
+            return self
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+        time.sleep(0.3)  # let the first sample land before the timed region
+        return self
+
+    def _read(self):
+        for line in self._proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 8:
+                self.rows.append(parts)
 
     def __exit__(self, *a):
-        self._stop.set()
+        time.sleep(0.1)
+        if self._proc is not None:
+            self._proc.terminate()
+            try:
+                self._proc.wait(timeout=5)
+            except Exception:
+                self._proc.kill()
         if self._t is not None:
-            self._t.join()
+            self._t.join(timeout=5)
 
     def summary(self) -> dict:
-        if not self.samples:
-            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [],
-                    "samples": 0, "error": self.error}
-        mhz = [m for m, _ in self.samples]
-        bits = 0
-        for _, r in self.samples:
-            bits |= r
-        reasons = [n for b, n in self.REASONS.items() if bits & b and n != "gpu_idle"]
-        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": self.max_mhz,
-                "reasons": reasons, "samples": len(mhz)}
+        mhz, mx, reasons = [], None, set()
+        for r in self.rows:
+            try:
+                mhz.append(float(r[0]))
+                mx = float(r[1])
+            except ValueError:
+                continue
+            for name, v in zip(self.NAMES, r[4:8]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(mhz),
+                **({"error": self.error} if self.error else {})}
 
 
 # ------------------------------------------------------------------ helpers
@@ -389,6 +393,19 @@ def run_extras(bl, wl, torch, device, stream, peaks, items2b, args):
         return e0.elapsed_time(e1) / 1e3 / n
 
     with torch.cuda.stream(stream):
+        # the same M=1 sweep as independent calls (launch overlap mode 2: no
+        # call waits for the previous one; valid because every call has its own
+        # input and output buffers)
+        bl.set_launch_overlap(2)
+        g = capture(bl, items2b, stream)
+        s = timed(g.replay, max(3, min(args.steps, 200)))
+        bl.set_launch_overlap(0 if args.no_overlap else 1)
+        nb = sum(algorithmic_bytes(1, it["mt"].N, it["mt"].K) for it in items2b)
+        out["decode_2b_independent_calls"] = {
+            "GB/s": nb / s / 1e9, "frac_hbm": nb / s / 1e9 / peaks["hbm_gbs"], "ms_per_sweep": s * 1e3,
+            "how": "same 120 calls, launch overlap mode 2 (calls do not wait for each other)"}
+        del g
+
         # batched decode on the same weights
         mats = [it["mt"] for it in items2b]
         bd = {}
@@ -460,8 +477,8 @@ def run_extras(bl, wl, torch, device, stream, peaks, items2b, args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=500)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--layers", type=int, default=30)
     ap.add_argument("--no-overlap", action="store_true")

@@ -186,13 +186,20 @@ BL_API bl_status bitlinear_matmul_i32(const uint8_t *packed, int64_t N, int64_t 
                                void *ws, size_t ws_bytes, void *stream);
 
 /* Launch overlap (programmatic dependent launch) for the forward kernels.
- * When on (default off), forward / forward_q / matmul_i32 kernels are
- * launched so that they may start while the previous kernel on the stream
- * is still running; they prefetch `packed` and `gamma` before waiting for
- * it and read everything else only after it has completed.  Precondition
- * while on: `packed` and `gamma` are not written by the kernel launched
- * immediately before on the same stream.  Process-wide; host only. */
-BL_API void bitlinear_set_launch_overlap(int on);
+ * Process-wide; host only.  Modes:
+ *   0 (default)  ordinary stream order.
+ *   1            kernels may start while the previous kernel on the stream is
+ *                still running: they prefetch `packed` and `gamma`, then wait
+ *                for it before touching anything else.  Precondition:
+ *                `packed` and `gamma` are not written by the kernel launched
+ *                immediately before on the same stream.
+ *   2            as 1, and the decode kernel (M <= 8) does not wait at all:
+ *                for batches of independent calls.  Precondition: no buffer
+ *                of the call (inputs or output) is written or read by the
+ *                kernel launched immediately before it on the same stream.
+ *                Calls on the tensor-core path (larger M) behave as in 1.
+ * Out-of-range values are clamped to 0..2. */
+BL_API void bitlinear_set_launch_overlap(int mode);
 BL_API int bitlinear_get_launch_overlap(void);
 
 /* Failure detection.  Every wait inside a kernel is bounded (about 2 s);

@@ -78,11 +78,11 @@ def test_row_bytes_and_sizes(lib):
 
 def test_workspace_plan(lib):
     import w1_a8_bitlinear_02_b300 as bl
-    # decode (M <= 4) runs without workspace
-    for M in (1, 2, 3, 4):
+    # decode (M <= 8) runs without workspace on the GEMV path
+    for M in range(1, 9):
         assert bl.workspace_bytes(M, 2560, 6912) == 0
-    # larger M needs the bf16 code buffer and scales at least
-    for M, N, K in ((5, 256, 512), (64, 2560, 2560), (2048, 6912, 2560)):
+    # larger M (tensor cores) needs the bf16 code buffer and scales at least
+    for M, N, K in ((9, 256, 512), (64, 2560, 2560), (2048, 6912, 2560), (8, 128, 16384)):
         need = bl.workspace_bytes(M, N, K)
         assert need >= M * bl.packed_row_bytes(K) * 4 * 2 + 4 * M
     # M = 1 with a K too large to hold in registers also takes the tensor-core path

@@ -121,7 +121,7 @@ def test_rmsnorm_quant_act(bl, M, K, gain, dtype):
 
 # ------------------------------------------------------------------ forward
 SHAPES = [(256, 512), (300, 100), (130, 2560), (513, 1000)]
-MS = [1, 2, 3, 4, 5, 8, 16, 33, 64, 65, 130, 257]
+MS = [1, 2, 3, 4, 5, 7, 8, 9, 16, 33, 64, 65, 130, 257]
 
 
 @pytest.mark.parametrize("N,K", SHAPES)
@@ -189,6 +189,35 @@ def test_launch_overlap_gives_same_results(bl):
     for x, y in zip(xs, ys):
         assert_bits_equal(y.cpu().numpy(), oracle.forward_packed(p_ref, g_ref, N, K,
                                                                   x.float().numpy()), "overlap")
+
+
+def test_independent_calls_overlap_mode(bl):
+    """Mode 2: a batch of independent calls (distinct inputs and outputs) may run
+    concurrently; each result must still equal the oracle's."""
+    shapes = [(384, 2560), (640, 512), (256, 6912)]
+    mats = [pack_both(bl, N, K, 0.02, 40 + i) for i, (N, K) in enumerate(shapes)]
+    xs = [wl.activations(M, K, "normal", 60 + M + K, "cpu", torch.bfloat16)
+          for (N, K) in shapes for M in (1, 3, 8)]
+    bl.set_launch_overlap(2)
+    try:
+        ys = []
+        i = 0
+        for j, (N, K) in enumerate(shapes):
+            for M in (1, 3, 8):
+                packed, gamma, _, _ = mats[j]
+                ys.append(bl.bitlinear_forward(packed, gamma, N, K, xs[i].to(DEV)))
+                i += 1
+        torch.cuda.synchronize()
+    finally:
+        bl.set_launch_overlap(0)
+    i = 0
+    for j, (N, K) in enumerate(shapes):
+        _, _, p_ref, g_ref = mats[j]
+        for M in (1, 3, 8):
+            assert_bits_equal(ys[i].cpu().numpy(),
+                              oracle.forward_packed(p_ref, g_ref, N, K, xs[i].float().numpy()),
+                              f"mode 2 N={N} K={K} M={M}")
+            i += 1
 
 
 # ------------------------------------------------------------------ full workload shapes

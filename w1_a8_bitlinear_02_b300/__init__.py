@@ -190,13 +190,14 @@ def bitlinear_matmul_i32(packed: torch.Tensor, N: int, K: int, xq: torch.Tensor,
     return acc
 
 
-def set_launch_overlap(on: bool) -> None:
-    """Programmatic dependent launch for forward kernels (see the C header)."""
-    _lib().bitlinear_set_launch_overlap(1 if on else 0)
+def set_launch_overlap(mode) -> None:
+    """Launch overlap for forward kernels: 0 off, 1 (or True) prefetch weights
+    while the previous kernel runs, 2 independent calls (see the C header)."""
+    _lib().bitlinear_set_launch_overlap(int(mode))
 
 
-def get_launch_overlap() -> bool:
-    return bool(_lib().bitlinear_get_launch_overlap())
+def get_launch_overlap() -> int:
+    return int(_lib().bitlinear_get_launch_overlap())
 
 
 def device_error(clear: bool = True) -> int:

@@ -151,53 +151,54 @@ bl_status check_dims(int64_t M, int64_t N, int64_t K) {
 }
 
 // ------------------------------------------------------------ GEMV dispatch
-template <int MT, int XM, bool OUT_I32>
-void *gemv_func(int wpt) {
-  switch (wpt) {
-    case 1: return reinterpret_cast<void *>(&gemv::gemv_kernel<MT, 1, XM, OUT_I32>);
-    case 2: return reinterpret_cast<void *>(&gemv::gemv_kernel<MT, 2, XM, OUT_I32>);
-    default: break;
+template <int MT, int XM, bool OUT_I32, int CW>
+void *gemv_func_upt(int upt) {
+#define BL_G(U) reinterpret_cast<void *>(&gemv::gemv_kernel<MT, U, XM, OUT_I32, CW>)
+  if (upt == 1) return BL_G(1);
+  if constexpr (MT <= 4) {
+    if (upt == 2) return BL_G(2);
   }
   if constexpr (MT <= 2) {
-    switch (wpt) {
-      case 3: return reinterpret_cast<void *>(&gemv::gemv_kernel<MT, 3, XM, OUT_I32>);
-      case 4: return reinterpret_cast<void *>(&gemv::gemv_kernel<MT, 4, XM, OUT_I32>);
-      default: break;
-    }
+    if (upt == 3) return BL_G(3);
+    if (upt == 4) return BL_G(4);
   }
   if constexpr (MT == 1) {
-    switch (wpt) {
-      case 5: return reinterpret_cast<void *>(&gemv::gemv_kernel<MT, 5, XM, OUT_I32>);
-      case 6: return reinterpret_cast<void *>(&gemv::gemv_kernel<MT, 6, XM, OUT_I32>);
-      case 7: return reinterpret_cast<void *>(&gemv::gemv_kernel<MT, 7, XM, OUT_I32>);
-      case 8: return reinterpret_cast<void *>(&gemv::gemv_kernel<MT, 8, XM, OUT_I32>);
-      default: break;
-    }
+    if (upt == 5) return BL_G(5);
+    if (upt == 6) return BL_G(6);
+    if (upt == 7) return BL_G(7);
+    if (upt == 8) return BL_G(8);
   }
+#undef BL_G
   return nullptr;
 }
 
-template <int XM, bool OUT_I32>
-void *gemv_func_m(int mt, int wpt) {
-  if (mt == 1) return gemv_func<1, XM, OUT_I32>(wpt);
-  if (mt == 2) return gemv_func<2, XM, OUT_I32>(wpt);
-  return gemv_func<4, XM, OUT_I32>(wpt);
+template <int XM, bool OUT_I32, int CW>
+void *gemv_func_m(int mt, int upt) {
+  if (mt == 1) return gemv_func_upt<1, XM, OUT_I32, CW>(upt);
+  if constexpr (CW == 16) {
+    return nullptr;  // 16 consumer warps only for one token
+  } else {
+    if (mt == 2) return gemv_func_upt<2, XM, OUT_I32, CW>(upt);
+    if (mt == 4) return gemv_func_upt<4, XM, OUT_I32, CW>(upt);
+    return gemv_func_upt<8, XM, OUT_I32, CW>(upt);
+  }
+}
+
+template <int CW>
+void *gemv_func(int xm, bool out_i32, int mt, int upt) {
+  if (out_i32) return gemv_func_m<gemv::kXInt8, true, CW>(mt, upt);
+  if (xm == gemv::kXF32) return gemv_func_m<gemv::kXF32, false, CW>(mt, upt);
+  if (xm == gemv::kXBF16) return gemv_func_m<gemv::kXBF16, false, CW>(mt, upt);
+  return gemv_func_m<gemv::kXInt8, false, CW>(mt, upt);
 }
 
 bl_status run_gemv(const plan::Plan &pl, int dev, int sms, int xm, bool out_i32, const uint8_t *packed,
                    const float *gamma, const void *x, const int8_t *xq, const float *scale, float *y,
                    int32_t *acc, cudaStream_t st) {
-  void *f = nullptr;
-  if (out_i32)
-    f = gemv_func_m<gemv::kXInt8, true>(pl.mt, pl.wpt);
-  else if (xm == gemv::kXF32)
-    f = gemv_func_m<gemv::kXF32, false>(pl.mt, pl.wpt);
-  else if (xm == gemv::kXBF16)
-    f = gemv_func_m<gemv::kXBF16, false>(pl.mt, pl.wpt);
-  else
-    f = gemv_func_m<gemv::kXInt8, false>(pl.mt, pl.wpt);
+  const plan::GemvGrid g = plan::gemv_grid(pl, sms);
+  void *f = g.cw == 16 ? gemv_func<16>(xm, out_i32, pl.mt, pl.upt) : gemv_func<8>(xm, out_i32, pl.mt, pl.upt);
   if (!f) return BL_ERR_UNSUPPORTED;
-  bl_status s = ensure_smem(dev, f, gemv::kSmemBytes);
+  bl_status s = ensure_smem(dev, f, plan::kSmemMax);
   if (s != BL_OK) return s;
   gemv::Params p{};
   p.packed = packed;
@@ -209,15 +210,20 @@ bl_status run_gemv(const plan::Plan &pl, int dev, int sms, int xm, bool out_i32,
   p.acc = acc;
   p.N = pl.N;
   p.K = static_cast<int>(pl.K);
-  p.words = static_cast<int>(pl.row_bytes / 4);
+  p.kp = static_cast<int>(pl.Kp);
+  p.units = static_cast<int>(pl.row_bytes / 8);
   p.row_bytes = static_cast<int>(pl.row_bytes);
   p.M = static_cast<int>(pl.M);
-  const plan::GemvGrid g = plan::gemv_grid(pl, sms);
   p.rows_per_cta = g.rows_per_cta;
   p.stage_rows = g.stage_rows;
-  p.tpr_log2 = pl.tpr_log2;
-  return launch(reinterpret_cast<void (*)(gemv::Params)>(f), dim3(g.grid), dim3(gemv::kThreads),
-                gemv::kSmemBytes, st, g_overlap.load() != 0, p);
+  p.stage_bytes = g.stage_bytes;
+  p.nstages = g.nstages;
+  p.split_log2 = pl.split_log2;
+  p.chunk = pl.chunk;
+  const int ov = g_overlap.load();
+  p.wait_prior = ov == 2 ? 0 : 1;
+  return launch(reinterpret_cast<void (*)(gemv::Params)>(f), dim3(g.grid), dim3((g.cw + 1) * 32), g.smem,
+                st, ov != 0, p);
 }
 
 // ------------------------------------------------------------ tensor-core dispatch
@@ -480,7 +486,7 @@ bl_status bitlinear_matmul_i32(const uint8_t *packed, int64_t N, int64_t K, cons
                         ws_bytes, stream);
 }
 
-void bitlinear_set_launch_overlap(int on) { g_overlap.store(on ? 1 : 0); }
+void bitlinear_set_launch_overlap(int mode) { g_overlap.store(mode < 0 ? 0 : (mode > 2 ? 2 : mode)); }
 
 int bitlinear_get_launch_overlap(void) { return g_overlap.load(); }
 

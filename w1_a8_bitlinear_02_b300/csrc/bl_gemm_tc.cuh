@@ -50,7 +50,8 @@ struct Cfg {
   static constexpr int kStageBytes = kABytes + kBBytes + kPBytes;
   static constexpr int kStages = (kSmemBudget / kStageBytes) > 8 ? 8 : (kSmemBudget / kStageBytes);
   static constexpr int kTmemCols = BN < 32 ? 32 : BN;
-  static constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 1024;
+  // stages + up to 1023 bytes of alignment slack + the barrier block
+  static constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 2048;
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
   static_assert(kStages >= 2, "pipeline depth");
 };
@@ -76,6 +77,7 @@ struct Bars {
   uint32_t tmem_base;
   int abort_flag;
   int last_flag;
+  float cscale[256];  // per-token output scale gamma / s_m of this tile
 };
 
 // bf16 bytes of (code - 1) for code 0, 1, 2: -1.0 = 0xBF80, 0, +1.0 = 0x3F80.
@@ -221,6 +223,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue
     // scale / split-K workspace come from the previous kernel on the stream
     pdl_wait_primary();
+    if constexpr (!OUT_I32) {
+      const float g = *p.gamma;
+      for (int j = u; j < BN; j += 128)
+        bars.cscale[j] = (m0 + j < p.M) ? __fdiv_rn(g, p.scale[m0 + j]) : 0.0f;
+    }
     bool ok = mbar_wait(smem_u32(&bars.accfull), 0);
     // One decision for all four epilogue warps (they share named barriers and
     // warp-collective TMEM loads below).
@@ -229,7 +236,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row = 32 * q + lane;
     const int n = n0 + row;
-    const float gamma = OUT_I32 ? 1.0f : *p.gamma;
     if (ok) {
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 32) {
@@ -249,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 atomicAdd(&p.acc_out[o], v);
             } else {
               if (p.splits == 1)
-                p.y[o] = __fdiv_rn(__fmul_rn(static_cast<float>(v), gamma), p.scale[m]);
+                p.y[o] = __fmul_rn(static_cast<float>(v), bars.cscale[c0 + j]);
               else
                 atomicAdd(&p.ws_acc[o], v);
             }
@@ -273,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (m >= p.M) break;
                 const int64_t o = static_cast<int64_t>(m) * p.N + n;
                 const int v = __ldcg(&p.ws_acc[o]);
-                p.y[o] = __fdiv_rn(__fmul_rn(static_cast<float>(v), gamma), p.scale[m]);
+                p.y[o] = __fmul_rn(static_cast<float>(v), bars.cscale[j]);
               }
             }
           }

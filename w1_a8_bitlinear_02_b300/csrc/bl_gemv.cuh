@@ -1,27 +1,30 @@
-// Decode GEMV for M <= 4 tokens: y[m, n] = sum_k Wq[n, k] * xq[m, k], rescaled.
+// Decode GEMV for M <= 8 tokens: y[m, n] = sum_k Wq[n, k] * xq[m, k], rescaled.
 //
 // The pages place the GPU cost of BitLinear in memory traffic: ternary
 // weights are packed several per byte in HBM, loaded on chip and unpacked
 // there ("微软AI大模型炸场：0.4GB，CPU就能跑", blog.csdn.net/2401_84494441,
-// section 3 "软硬协同", GPU bullet).  This kernel is that idea on sm_103a:
+// section 3 "软硬协同", GPU bullet).  On sm_103a:
 //
-//  * A producer warp streams contiguous blocks of packed rows into a ring of
-//    shared-memory stages with 1-D bulk copies (cp.async.bulk, mbarrier
-//    completion), so each SM keeps ~96 KB of HBM reads in flight without
-//    tying up registers.
-//  * Each consumer thread owns a fixed set of packed 32-bit words (16
-//    weights each) of every row, so its slice of the quantised activations
-//    stays in registers for the whole kernel; rows stream past it.
-//  * Unpacking costs one AND per 4 weights: for mask i, the bytes of
-//    (word & (0x03030303 << 2i)) are the codes c = q + 1 of four weights
-//    times 4^i, fed straight to dp4a (unsigned codes x signed activations)
-//    into accumulator i; the 4^i factor is removed exactly at the end
-//    (each accumulator is a multiple of 4^i).  sum c*x - sum x = sum q*x.
-//  * Per-row partial sums are reduced across the threads that share a row
-//    with warp shuffles (and shared memory when a row spans warps).
-//
-// With launch overlap on, the producer starts streaming weights before the
-// previous kernel on the stream has finished; everything else waits.
+//  * One elected thread streams each block's contiguous run of packed rows
+//    into a ring of shared-memory stages with 1-D bulk copies (cp.async.bulk,
+//    mbarrier completion): up to ~190 KB in flight per SM without any
+//    per-thread copy instructions or registers.  With launch overlap on, it
+//    starts before the previous kernel on the stream has finished.
+//  * A warp owns whole rows.  Lane l holds the activation codes of the 8-byte
+//    units (32 weights) l, l + 32, ... of its chunk of K in registers, so a
+//    row costs each lane a few 8-byte shared loads and the row's sum is one
+//    warp reduction.  Very long rows are split over G warps whose partial
+//    sums meet in shared memory (a per-row counter picks the last arriver,
+//    which writes the output; no block barriers).
+//  * Unpacking: for M <= 2, one AND per 4 weights -- the bytes of
+//    (word & (0x03030303 << 2i)) are the codes c = q + 1 of four weights times
+//    4^i, fed to dp4a (unsigned codes x signed activations) into accumulator
+//    i; the 4^i factor is removed exactly at the end (each accumulator is a
+//    multiple of 4^i).  For more tokens the codes are shifted down once per
+//    word and shared by all tokens.  sum c*x - X = sum q*x, with
+//    X = sum_k xq[m, k] from the quantisation pass.
+//  * The activation rows are quantised once per block into shared memory
+//    (per-token absmax, block reduction), then each warp pulls its chunk.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -33,12 +36,10 @@
 namespace bl {
 namespace gemv {
 
-constexpr int kConsumerWarps = 8;
-constexpr int kConsumers = kConsumerWarps * 32;
-constexpr int kThreads = kConsumers + 32;  // + one producer warp
-constexpr int kStages = 3;
-constexpr int kStageBytes = 32 * 1024;
-constexpr int kSmemBytes = kStages * kStageBytes + 1024;
+constexpr int kMaxStages = 6;
+constexpr int kStageBytes = 32 * 1024;  // upper bound of one stage
+constexpr int kMaxSplitRows = 32;       // rows per stage when rows are split over warps
+constexpr int kSmemFixed = 8 * 1024;    // barriers, reductions, split-row partials
 
 enum XMode { kXF32 = 0, kXBF16 = 1, kXInt8 = 2 };
 
@@ -52,21 +53,29 @@ struct Params {
   int32_t *acc;         // [M, N] (int32 output)
   int64_t N;
   int K;
-  int words;            // packed 32-bit words per row (= row_bytes / 4)
+  int kp;               // K padded to 64: activation code row length in smem
+  int units;            // 8-byte units per packed row (= row_bytes / 8)
   int row_bytes;
   int M;
   int rows_per_cta;
-  int stage_rows;       // rows per shared-memory stage (multiple of rows/iter)
-  int tpr_log2;         // threads per row = 1 << tpr_log2
+  int stage_rows;       // rows per stage (<= kMaxSplitRows when split > 1)
+  int stage_bytes;      // stage_rows * row_bytes rounded up to 128
+  int nstages;          // ring depth (<= kMaxStages)
+  int split_log2;       // G = warps per row
+  int chunk;            // units per warp's chunk of a row (ceil(units / G))
+  int wait_prior;       // 1: inputs may come from the previous kernel (wait for it)
 };
 
 struct Smem {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
-  int32_t part[kConsumerWarps][4];
-  float fred[kConsumerWarps][4];
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
+  float fred[16][8];
+  int32_t xsum[16][8];
+  int32_t part[kMaxStages][kMaxSplitRows][8];
+  uint32_t cnt[kMaxStages][kMaxSplitRows];
   int abort_flag;
 };
+static_assert(sizeof(Smem) <= kSmemFixed, "fixed shared-memory region");
 
 template <int XM>
 __device__ __forceinline__ float load_x(const void *x, int64_t idx) {
@@ -76,231 +85,316 @@ __device__ __forceinline__ float load_x(const void *x, int64_t idx) {
     return __bfloat162float(static_cast<const __nv_bfloat16 *>(x)[idx]);
 }
 
-// MT: tokens held (M <= MT); WPT: packed words per thread per row.
-template <int MT, int WPT, int XM, bool OUT_I32>
-__global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const Params p) {
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t *stages = smem_raw;
-  Smem &sm = *reinterpret_cast<Smem *>(smem_raw + kStages * kStageBytes);
+template <int XM>
+__device__ __forceinline__ void load8x(const void *x, int64_t idx, float (&v)[8]) {
+  if constexpr (XM == kXF32)
+    load8(static_cast<const float *>(x) + idx, v);
+  else
+    load8(static_cast<const __nv_bfloat16 *>(x) + idx, v);
+}
 
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5, lane = tid & 31;
+__device__ __forceinline__ uint2 lds_u64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+
+// MT: tokens held (M <= MT); UPT: 8-byte units per lane; CW: consumer warps.
+template <int MT, int UPT, int XM, bool OUT_I32, int CW>
+__global__ void __launch_bounds__((CW + 1) * 32, 1) gemv_kernel(const Params p) {
+  constexpr int kConsumers = CW * 32;
+  constexpr bool kMasked = MT <= 2;
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  Smem &sm = *reinterpret_cast<Smem *>(smem_raw);
+  const uint32_t ring = smem_u32(smem_raw + kSmemFixed);
+  const uint32_t xs = ring + static_cast<uint32_t>(p.nstages * p.stage_bytes);  // [M][kp] codes
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t row0 = static_cast<int64_t>(blockIdx.x) * p.rows_per_cta;
-  int64_t nrows = p.N - row0;
-  if (nrows > p.rows_per_cta) nrows = p.rows_per_cta;
-  if (nrows <= 0) return;  // whole block exits together
-  const int n_stages = static_cast<int>((nrows + p.stage_rows - 1) / p.stage_rows);
+  int64_t nrows64 = p.N - row0;
+  if (nrows64 > p.rows_per_cta) nrows64 = p.rows_per_cta;
+  const int nrows = static_cast<int>(nrows64);
+  const int n_iters = (nrows + p.stage_rows - 1) / p.stage_rows;
+  const int S = p.nstages;
 
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(smem_u32(&sm.full[s]), 1);
-      mbar_init(smem_u32(&sm.empty[s]), kConsumerWarps);
+      mbar_init(smem_u32(&sm.empty[s]), CW);
     }
     sm.abort_flag = 0;
     fence_barrier_init();
   }
+  for (int i = tid; i < kMaxStages * kMaxSplitRows; i += blockDim.x) {
+    (&sm.cnt[0][0])[i] = 0u;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) (&sm.part[0][0][0])[i * 8 + m] = 0;
+  }
   __syncthreads();
-  pdl_launch_dependents();
 
-  if (warp == kConsumerWarps) {
+  if (warp == CW) {
     // ------------------------------------------------ producer warp
+    pdl_launch_dependents();
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
       int issued = 0;
-      for (int it = 0; it < n_stages; ++it) {
-        const int s = it % kStages;
-        if (it >= kStages) {
-          if (!mbar_wait(smem_u32(&sm.empty[s]), ((it / kStages) - 1) & 1)) {
+      for (int it = 0; it < n_iters; ++it) {
+        const int s = it % S;
+        if (it >= S) {
+          if (!mbar_wait(smem_u32(&sm.empty[s]), ((it / S) - 1) & 1)) {
             sm.abort_flag = 1;
             break;
           }
           if (*reinterpret_cast<volatile int *>(&sm.abort_flag)) break;
         }
-        int64_t rows = nrows - static_cast<int64_t>(it) * p.stage_rows;
+        int rows = nrows - it * p.stage_rows;
         if (rows > p.stage_rows) rows = p.stage_rows;
         const uint32_t bytes = static_cast<uint32_t>(rows) * static_cast<uint32_t>(p.row_bytes);
         const uint32_t fb = smem_u32(&sm.full[s]);
         mbar_arrive_expect_tx(fb, bytes);
-        bulk_g2s(smem_u32(stages + s * kStageBytes),
-                 p.packed + (row0 + static_cast<int64_t>(it) * p.stage_rows) * p.row_bytes, bytes, fb,
-                 pol);
+        bulk_g2s(ring + s * p.stage_bytes,
+                 p.packed + (row0 + static_cast<int64_t>(it) * p.stage_rows) * p.row_bytes, bytes, fb, pol);
         issued = it + 1;
       }
       // Do not leave while copies into this block's shared memory are in flight.
-      for (int it = issued - kStages < 0 ? 0 : issued - kStages; it < issued; ++it)
-        mbar_wait(smem_u32(&sm.full[it % kStages]), (it / kStages) & 1);
+      for (int it = issued - S < 0 ? 0 : issued - S; it < issued; ++it)
+        mbar_wait(smem_u32(&sm.full[it % S]), (it / S) & 1);
     }
     return;
   }
 
   // -------------------------------------------------- consumer warps
-  pdl_wait_primary();
-  const float gamma = *p.gamma;
-  const int tpr = 1 << p.tpr_log2;
-  const int lr = tid & (tpr - 1);       // word slot inside the row
-  const int rslot = tid >> p.tpr_log2;  // row slot inside an iteration
-  const int rpi = kConsumers >> p.tpr_log2;
+  // gamma is a static input like the packed weights: read it before waiting.
+  const float gamma = OUT_I32 ? 1.0f : __ldg(p.gamma);
+  pdl_launch_dependents();
+  if (p.wait_prior) pdl_wait_primary();
 
-  // ---- activations of this thread's words, quantised, in registers
-  uint32_t xw[MT][WPT][4];
-  int xsum[MT];
+  // ---- activation codes of the M tokens into shared memory, with
+  // X_m = sum_k xq[m, k] (turns sum c*x into sum q*x at the end)
   float sc[MT];
 #pragma unroll
-  for (int m = 0; m < MT; ++m) {
-    xsum[m] = 0;
-    sc[m] = 1.0f;
-  }
-
+  for (int m = 0; m < MT; ++m) sc[m] = 1.0f;
   if constexpr (XM == kXInt8) {
+    const bool vec = (reinterpret_cast<uintptr_t>(p.xq) & 15u) == 0u && (p.K % 16) == 0;
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
-      if (m < p.M) sc[m] = p.scale[m];
-#pragma unroll
-      for (int w = 0; w < WPT; ++w) {
-        const int kw = lr + w * tpr;
-        uint32_t v[4] = {0u, 0u, 0u, 0u};
-        if (m < p.M && kw < p.words) {
-          const int64_t base = static_cast<int64_t>(m) * p.K + 16 * kw;
-          const int8_t *src = p.xq + base;
-          if (16 * kw + 16 <= p.K && ((reinterpret_cast<uintptr_t>(src) & 15u) == 0u)) {
-            const uint4 u = *reinterpret_cast<const uint4 *>(src);
-            v[0] = u.x; v[1] = u.y; v[2] = u.z; v[3] = u.w;
-          } else {
-#pragma unroll
-            for (int b = 0; b < 16; ++b)
-              if (16 * kw + b < p.K)
-                v[b >> 2] |= (static_cast<uint32_t>(static_cast<uint8_t>(src[b]))) << (8 * (b & 3));
-          }
+      int part = 0;
+      if (m < p.M) {
+        const int8_t *src = p.xq + static_cast<int64_t>(m) * p.K;
+        const uint32_t xrow = xs + static_cast<uint32_t>(m * p.kp);
+        const int nv = vec ? p.K / 16 : 0;
+        for (int c = tid; c < nv; c += kConsumers) {
+          const uint4 v = __ldg(reinterpret_cast<const uint4 *>(src) + c);
+          sts_u128(xrow + 16 * c, v.x, v.y, v.z, v.w);
+          part = dp4a_us(0x01010101u, v.x, part);
+          part = dp4a_us(0x01010101u, v.y, part);
+          part = dp4a_us(0x01010101u, v.z, part);
+          part = dp4a_us(0x01010101u, v.w, part);
         }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          xw[m][w][i] = v[i];
-          xsum[m] = dp4a_us(0x01010101u, v[i], xsum[m]);
+        for (int k = 16 * nv + tid; k < p.kp; k += kConsumers) {
+          const int q = k < p.K ? static_cast<int>(src[k]) : 0;
+          sts_u8(xrow + k, static_cast<uint32_t>(q) & 0xFFu);
+          part += q;
         }
+        if constexpr (!OUT_I32) sc[m] = __ldg(p.scale + m);
       }
+      part = __reduce_add_sync(0xffffffffu, part);
+      if (lane == 0) sm.xsum[warp][m] = part;
     }
   } else {
-    // per-token absmax over the whole row, reduced over the consumer warps
-    float amax[MT];
+    // per-token absmax: 8-element vectors strided over K, block reduction;
+    // then the codes from a second pass over the same vectors (L1 hits)
+    const bool vec = (reinterpret_cast<uintptr_t>(p.x) & 15u) == 0u && (p.K % 8) == 0;
+    const int nv = vec ? p.K / 8 : 0;
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
-      amax[m] = 0.0f;
-      if (m < p.M)
-        for (int k = tid; k < p.K; k += kConsumers)
-          amax[m] = fmaxf(amax[m], fabsf(load_x<XM>(p.x, static_cast<int64_t>(m) * p.K + k)));
-      amax[m] = warp_max(amax[m]);
-      if (lane == 0) sm.fred[warp][m] = amax[m];
+      float a = 0.0f;
+      if (m < p.M) {
+        const int64_t row = static_cast<int64_t>(m) * p.K;
+#pragma unroll 2
+        for (int c = tid; c < nv; c += kConsumers) {
+          float v[8];
+          load8x<XM>(p.x, row + 8 * c, v);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) a = fmaxf(a, fabsf(v[j]));
+        }
+        for (int k = 8 * nv + tid; k < p.K; k += kConsumers) a = fmaxf(a, fabsf(load_x<XM>(p.x, row + k)));
+      }
+      a = warp_max_nonneg(a);
+      if (lane == 0) sm.fred[warp][m] = a;
     }
     named_bar(1, kConsumers);
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
       float a = sm.fred[0][m];
 #pragma unroll
-      for (int i = 1; i < kConsumerWarps; ++i) a = fmaxf(a, sm.fred[i][m]);
+      for (int i = 1; i < CW; ++i) a = fmaxf(a, sm.fred[i][m]);
       sc[m] = act_scale(a);
     }
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
+      int part = 0;
+      if (m < p.M) {
+        const int64_t row = static_cast<int64_t>(m) * p.K;
+        const uint32_t xrow = xs + static_cast<uint32_t>(m * p.kp);
+#pragma unroll 2
+        for (int c = tid; c < nv; c += kConsumers) {
+          float v[8];
+          load8x<XM>(p.x, row + 8 * c, v);
+          uint32_t lo = 0, hi = 0;
 #pragma unroll
-      for (int w = 0; w < WPT; ++w) {
-        const int kw = lr + w * tpr;
-        uint32_t v[4] = {0u, 0u, 0u, 0u};
-        if (m < p.M && kw < p.words) {
-#pragma unroll
-          for (int b = 0; b < 16; ++b) {
-            const int k = 16 * kw + b;
-            if (k < p.K) {
-              const int q = quant_one(load_x<XM>(p.x, static_cast<int64_t>(m) * p.K + k), sc[m]);
-              v[b >> 2] |= (static_cast<uint32_t>(q) & 0xFFu) << (8 * (b & 3));
-            }
+          for (int j = 0; j < 4; ++j) {
+            const int q0 = quant_one(v[j], sc[m]), q1 = quant_one(v[j + 4], sc[m]);
+            part += q0 + q1;
+            lo |= (static_cast<uint32_t>(q0) & 0xFFu) << (8 * j);
+            hi |= (static_cast<uint32_t>(q1) & 0xFFu) << (8 * j);
           }
+          sts_u64(xrow + 8 * c, lo, hi);
         }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          xw[m][w][i] = v[i];
-          xsum[m] = dp4a_us(0x01010101u, v[i], xsum[m]);
+        for (int k = 8 * nv + tid; k < p.kp; k += kConsumers) {
+          const int q = k < p.K ? quant_one(load_x<XM>(p.x, row + k), sc[m]) : 0;
+          part += q;
+          sts_u8(xrow + k, static_cast<uint32_t>(q) & 0xFFu);
         }
       }
+      part = __reduce_add_sync(0xffffffffu, part);
+      if (lane == 0) sm.xsum[warp][m] = part;
+    }
+  }
+  named_bar(1, kConsumers);
+
+  // the token's output scale c_m = gamma / s_m (one true division per token)
+  float cm[MT];
+  int xtot[MT];
+#pragma unroll
+  for (int m = 0; m < MT; ++m) {
+    cm[m] = __fdiv_rn(gamma, sc[m]);
+    int v = 0;
+#pragma unroll
+    for (int i = 0; i < CW; ++i) v += sm.xsum[i][m];
+    xtot[m] = v;
+  }
+
+  // ---- this lane's activation codes: 32 per 8-byte weight unit of its chunk
+  const int G = 1 << p.split_log2;
+  const int chunk_id = warp & (G - 1);
+  const int row_slot = warp >> p.split_log2;
+  const int row_step = CW >> p.split_log2;
+  const int ubase = chunk_id * p.chunk;
+  int uend = ubase + p.chunk;
+  if (uend > p.units) uend = p.units;
+  uint32_t xa[MT][UPT][8];
+#pragma unroll
+  for (int m = 0; m < MT; ++m) {
+#pragma unroll
+    for (int u = 0; u < UPT; ++u) {
+      const int unit = ubase + lane + 32 * u;
+      uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;
+      if (m < p.M && unit < uend) {
+        const uint32_t at = xs + static_cast<uint32_t>(m * p.kp + 32 * unit);
+        a = lds_u128(at);
+        b = lds_u128(at + 16);
+      }
+      xa[m][u][0] = a.x; xa[m][u][1] = a.y; xa[m][u][2] = a.z; xa[m][u][3] = a.w;
+      xa[m][u][4] = b.x; xa[m][u][5] = b.y; xa[m][u][6] = b.z; xa[m][u][7] = b.w;
     }
   }
 
   // ---- stream the rows
-  const uint32_t stage0 = smem_u32(stages);
-  for (int it = 0; it < n_stages; ++it) {
-    const int s = it % kStages;
-    bool failed = !mbar_wait(smem_u32(&sm.full[s]), (it / kStages) & 1);
-    // Warps that share rows meet at named barriers below: decide together.
-    if (tpr > 32) failed = named_bar_or(2, kConsumers, failed);
-    if (failed) {
+  for (int it = 0; it < n_iters; ++it) {
+    const int s = it % S;
+    if (!mbar_wait(smem_u32(&sm.full[s]), (it / S) & 1)) {
       sm.abort_flag = 1;
       break;
     }
-    int64_t rows_here = nrows - static_cast<int64_t>(it) * p.stage_rows;
+    int rows_here = nrows - it * p.stage_rows;
     if (rows_here > p.stage_rows) rows_here = p.stage_rows;
-    const uint32_t sbase = stage0 + s * kStageBytes;
-    for (int rr = 0; rr < rows_here; rr += rpi) {
-      const int r = rr + rslot;
-      const bool valid = r < rows_here;
+    const uint32_t sbase = ring + s * p.stage_bytes;
+    for (int r = row_slot; r < rows_here; r += row_step) {
+      const uint32_t rbase = sbase + static_cast<uint32_t>(r) * p.row_bytes;
       int tot[MT];
-#pragma unroll
-      for (int m = 0; m < MT; ++m) tot[m] = 0;
-      if (valid) {
+      if constexpr (kMasked) {
         int a0[MT], a1[MT], a2[MT], a3[MT];
 #pragma unroll
         for (int m = 0; m < MT; ++m) a0[m] = a1[m] = a2[m] = a3[m] = 0;
-        const uint32_t rbase = sbase + static_cast<uint32_t>(r) * p.row_bytes;
 #pragma unroll
-        for (int w = 0; w < WPT; ++w) {
-          const int kw = lr + w * tpr;
-          if (kw < p.words) {
-            const uint32_t word = lds_u32(rbase + 4u * kw);
-            const uint32_t c0 = word & 0x03030303u, c1 = word & 0x0C0C0C0Cu;
-            const uint32_t c2 = word & 0x30303030u, c3 = word & 0xC0C0C0C0u;
+        for (int u = 0; u < UPT; ++u) {
+          const int unit = ubase + lane + 32 * u;
+          if (unit < uend) {
+            const uint2 wv = lds_u64(rbase + 8u * unit);
 #pragma unroll
-            for (int m = 0; m < MT; ++m) {
-              a0[m] = dp4a_us(c0, xw[m][w][0], a0[m]);
-              a1[m] = dp4a_us(c1, xw[m][w][1], a1[m]);
-              a2[m] = dp4a_us(c2, xw[m][w][2], a2[m]);
-              a3[m] = dp4a_us(c3, xw[m][w][3], a3[m]);
+            for (int h = 0; h < 2; ++h) {
+              const uint32_t word = h ? wv.y : wv.x;
+              const uint32_t c0 = word & 0x03030303u, c1 = word & 0x0C0C0C0Cu;
+              const uint32_t c2 = word & 0x30303030u, c3 = word & 0xC0C0C0C0u;
+#pragma unroll
+              for (int m = 0; m < MT; ++m) {
+                a0[m] = dp4a_us(c0, xa[m][u][4 * h + 0], a0[m]);
+                a1[m] = dp4a_us(c1, xa[m][u][4 * h + 1], a1[m]);
+                a2[m] = dp4a_us(c2, xa[m][u][4 * h + 2], a2[m]);
+                a3[m] = dp4a_us(c3, xa[m][u][4 * h + 3], a3[m]);
+              }
             }
           }
         }
 #pragma unroll
-        for (int m = 0; m < MT; ++m)
-          tot[m] = a0[m] + (a1[m] >> 2) + (a2[m] >> 4) + (a3[m] >> 6) - xsum[m];
-      }
-      // reduce over the tpr threads of the row
-      const int width = tpr < 32 ? tpr : 32;
+        for (int m = 0; m < MT; ++m) tot[m] = a0[m] + (a1[m] >> 2) + (a2[m] >> 4) + (a3[m] >> 6);
+      } else {
+        int a[MT];
 #pragma unroll
-      for (int m = 0; m < MT; ++m)
-        for (int o = width >> 1; o > 0; o >>= 1) tot[m] += __shfl_xor_sync(0xffffffffu, tot[m], o);
-      if (tpr > 32) {
-        if (lane == 0) {
+        for (int m = 0; m < MT; ++m) a[m] = 0;
 #pragma unroll
-          for (int m = 0; m < MT; ++m) sm.part[warp][m] = tot[m];
-        }
-        named_bar(1, kConsumers);
-        if (lr == 0) {
-          const int w0 = warp, nw = tpr >> 5;
+        for (int u = 0; u < UPT; ++u) {
+          const int unit = ubase + lane + 32 * u;
+          if (unit < uend) {
+            const uint2 wv = lds_u64(rbase + 8u * unit);
 #pragma unroll
-          for (int m = 0; m < MT; ++m) {
-            int v = 0;
-            for (int i = 0; i < nw; ++i) v += sm.part[w0 + i][m];
-            tot[m] = v;
+            for (int h = 0; h < 2; ++h) {
+              const uint32_t word = h ? wv.y : wv.x;
+              const uint32_t c0 = word & 0x03030303u, c1 = (word >> 2) & 0x03030303u;
+              const uint32_t c2 = (word >> 4) & 0x03030303u, c3 = (word >> 6) & 0x03030303u;
+#pragma unroll
+              for (int m = 0; m < MT; ++m) {
+                a[m] = dp4a_us(c0, xa[m][u][4 * h + 0], a[m]);
+                a[m] = dp4a_us(c1, xa[m][u][4 * h + 1], a[m]);
+                a[m] = dp4a_us(c2, xa[m][u][4 * h + 2], a[m]);
+                a[m] = dp4a_us(c3, xa[m][u][4 * h + 3], a[m]);
+              }
+            }
           }
         }
-        named_bar(1, kConsumers);
-      }
-      if (valid && lr == 0) {
-        const int64_t n = row0 + static_cast<int64_t>(it) * p.stage_rows + r;
 #pragma unroll
-        for (int m = 0; m < MT; ++m) {
-          if (m < p.M) {
-            if constexpr (OUT_I32)
-              p.acc[static_cast<int64_t>(m) * p.N + n] = tot[m];
-            else
-              p.y[static_cast<int64_t>(m) * p.N + n] =
-                  __fdiv_rn(__fmul_rn(static_cast<float>(tot[m]), gamma), sc[m]);
+        for (int m = 0; m < MT; ++m) tot[m] = a[m];
+      }
+#pragma unroll
+      for (int m = 0; m < MT; ++m) tot[m] = __reduce_add_sync(0xffffffffu, tot[m]);
+      if (lane == 0) {
+        bool write = true;
+        if (G > 1) {  // meet the row's other chunks in shared memory
+#pragma unroll
+          for (int m = 0; m < MT; ++m)
+            if (m < p.M) atomicAdd(&sm.part[s][r][m], tot[m]);
+          __threadfence_block();
+          write = atomicAdd(&sm.cnt[s][r], 1u) == static_cast<uint32_t>(G - 1);
+          if (write) {
+            __threadfence_block();
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+              if (m < p.M) tot[m] = atomicExch(&sm.part[s][r][m], 0);
+            sm.cnt[s][r] = 0u;
+          }
+        }
+        if (write) {
+          const int64_t n = row0 + static_cast<int64_t>(it) * p.stage_rows + r;
+#pragma unroll
+          for (int m = 0; m < MT; ++m) {
+            if (m < p.M) {
+              const int q = tot[m] - xtot[m];  // sum (c - 1) x = sum q x
+              if constexpr (OUT_I32)
+                p.acc[static_cast<int64_t>(m) * p.N + n] = q;
+              else
+                p.y[static_cast<int64_t>(m) * p.N + n] = __fmul_rn(static_cast<float>(q), cm[m]);
+            }
           }
         }
       }

@@ -108,6 +108,12 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
+// Max over a warp of non-negative floats: their bit patterns order like
+// unsigned integers, so one redux instruction does it.
+__device__ __forceinline__ float warp_max_nonneg(float v) {
+  return __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(v)));
+}
+
 __device__ __forceinline__ double warp_sum_f64(double v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -135,11 +141,42 @@ __device__ __forceinline__ void zero_fill(int64_t m, int32_t *zrows, int64_t zn,
     for (int i = threadIdx.x; i < ncnt; i += blockDim.x) zcnt[i] = 0u;
 }
 
+// 8 consecutive activations as floats (16- or 32-byte vector loads).
+__device__ __forceinline__ void load8(const float *p, float (&v)[8]) {
+  const float4 a = __ldg(reinterpret_cast<const float4 *>(p));
+  const float4 b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+__device__ __forceinline__ void load8(const __nv_bfloat16 *p, float (&v)[8]) {
+  const uint4 u = __ldg(reinterpret_cast<const uint4 *>(p));
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    v[2 * j] = __uint_as_float(w[j] << 16);
+    v[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ bool al16(const void *p) {
+  return (reinterpret_cast<uintptr_t>(p) & 15u) == 0u;
+}
+
+// Kahan step: (s, c) += y  (compensated fp32 sum of squares)
+__device__ __forceinline__ void kahan_add(float &s, float &c, float y) {
+  const float yy = __fsub_rn(y, c);
+  const float t = __fadd_rn(s, yy);
+  c = __fsub_rn(__fsub_rn(t, s), yy);
+  s = t;
+}
+
 // One block (256 threads) per token row.
 //   OUT_BF16 = false: xq int8 [M, K] dense.
 //   OUT_BF16 = true : integer codes as bf16 [M, ld] (exact), zero for k in [K, ld);
 //                     the tensor-core path reads this layout.
 //   NORM: fused subln RMSNorm (gain g may be NULL).
+// Rows are read in 8-element vectors (two passes: max, then codes; the second
+// pass hits L1) when K and the pointers allow, else element by element.
 template <typename XT, bool OUT_BF16, bool NORM>
 __global__ void __launch_bounds__(256) quant_act_kernel(const XT *__restrict__ x, int64_t K,
                                                         int64_t ld, const float *__restrict__ g,
@@ -155,22 +192,45 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const XT *__restrict__ x
   const int64_t m = blockIdx.x;
   const XT *xr = x + m * K;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const bool use_g = NORM && g != nullptr;
+  const bool vec = (K % 8) == 0 && al16(x) && (!use_g || al16(g)) &&
+                   (OUT_BF16 ? (al16(xb) && ld % 8 == 0) : (reinterpret_cast<uintptr_t>(xq) & 7u) == 0u);
+  const int64_t nvec = vec ? K / 8 : 0;
 
+  // ---- pass 1: max |x * g| (and sum of x^2)
+  float amax = 0.0f, s1 = 0.0f, c1 = 0.0f;
+#pragma unroll 4
+  for (int64_t c = t; c < nvec; c += 256) {
+    float v[8];
+    load8(xr + 8 * c, v);
+    float gg[8];
+    if (use_g) load8(g + 8 * c, gg);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (NORM) kahan_add(s1, c1, __fmul_rn(v[j], v[j]));
+      const float u = use_g ? __fmul_rn(v[j], gg[j]) : v[j];
+      amax = fmaxf(amax, fabsf(u));
+    }
+  }
+  for (int64_t k = 8 * nvec + t; k < K; k += 256) {
+    const float v = to_f32(xr[k]);
+    if (NORM) kahan_add(s1, c1, __fmul_rn(v, v));
+    amax = fmaxf(amax, fabsf(use_g ? __fmul_rn(v, g[k]) : v));
+  }
+  amax = warp_max_nonneg(amax);
+  if (lane == 0) red_f[warp] = amax;
   float r_norm = 1.0f;
   if (NORM) {
-    // sum of squares: compensated fp32 per thread, fp64 across threads
-    float s1 = 0.0f, c1 = 0.0f;
-    for (int64_t k = t; k < K; k += 256) {
-      const float v = to_f32(xr[k]);
-      const float y = __fsub_rn(__fmul_rn(v, v), c1);
-      const float tt = __fadd_rn(s1, y);
-      c1 = __fsub_rn(__fsub_rn(tt, s1), y);
-      s1 = tt;
-    }
     double part = static_cast<double>(s1) - static_cast<double>(c1);
     part = warp_sum_f64(part);
     if (lane == 0) red_d[warp] = part;
-    __syncthreads();
+  }
+  __syncthreads();
+  amax = red_f[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red_f[i]);
+  const float s = act_scale(amax);
+  if (NORM) {
     double S = 0.0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) S += red_d[i];
@@ -178,26 +238,38 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const XT *__restrict__ x
     const float d = __fsqrt_rn(__fadd_rn(ms, eps));
     r_norm = __fdiv_rn(1.0f, d);
   }
-
-  float amax = 0.0f;
-  for (int64_t k = t; k < K; k += 256) {
-    float v = to_f32(xr[k]);
-    if (NORM && g != nullptr) v = __fmul_rn(v, g[k]);
-    amax = fmaxf(amax, fabsf(v));
-  }
-  amax = warp_max(amax);
-  if (lane == 0) red_f[warp] = amax;
-  __syncthreads();
-  amax = red_f[0];
-#pragma unroll
-  for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red_f[i]);
-  const float s = act_scale(amax);
   if (t == 0) scale[m] = NORM ? __fdiv_rn(s, r_norm) : s;
 
-  for (int64_t k = t; k < K; k += 256) {
-    float v = to_f32(xr[k]);
-    if (NORM && g != nullptr) v = __fmul_rn(v, g[k]);
-    const int q = quant_one(v, s);
+  // ---- pass 2: codes
+#pragma unroll 4
+  for (int64_t c = t; c < nvec; c += 256) {
+    float v[8];
+    load8(xr + 8 * c, v);
+    float gg[8];
+    if (use_g) load8(g + 8 * c, gg);
+    int q[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) q[j] = quant_one(use_g ? __fmul_rn(v[j], gg[j]) : v[j], s);
+    if (OUT_BF16) {
+      uint32_t w[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        w[j] = (__float_as_uint(static_cast<float>(q[2 * j])) >> 16) |
+               (__float_as_uint(static_cast<float>(q[2 * j + 1])) & 0xFFFF0000u);
+      *reinterpret_cast<uint4 *>(xb + m * ld + 8 * c) = make_uint4(w[0], w[1], w[2], w[3]);
+    } else {
+      uint32_t lo = 0, hi = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        lo |= (static_cast<uint32_t>(q[j]) & 0xFFu) << (8 * j);
+        hi |= (static_cast<uint32_t>(q[j + 4]) & 0xFFu) << (8 * j);
+      }
+      *reinterpret_cast<uint2 *>(xq + m * K + 8 * c) = make_uint2(lo, hi);
+    }
+  }
+  for (int64_t k = 8 * nvec + t; k < K; k += 256) {
+    const float v = to_f32(xr[k]);
+    const int q = quant_one(use_g ? __fmul_rn(v, g[k]) : v, s);
     if (OUT_BF16)
       xb[m * ld + k] = __float2bfloat16_rn(static_cast<float>(q));
     else

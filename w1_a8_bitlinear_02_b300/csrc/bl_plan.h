@@ -14,8 +14,11 @@ enum Path { kGemv = 0, kTc = 1 };
 // Reference SM count used for split-K decisions (B300: 148 SMs).  A fixed
 // value keeps workspace sizes independent of the device.
 constexpr int kRefSms = 148;
-constexpr int kGemvThreads = 256;        // consumer threads of the GEMV kernel
-constexpr int kGemvStageBytes = 32 * 1024;
+constexpr int kGemvStageBytes = 32 * 1024;   // upper bound of one GEMV ring stage
+constexpr int kGemvMaxStages = 6;
+constexpr int kGemvMaxSplitRows = 32;
+constexpr int kGemvSmemFixed = 8 * 1024;
+constexpr int kSmemMax = 227 * 1024;
 
 inline int64_t row_bytes(int64_t K) { return ((K + 63) / 64) * 16; }
 
@@ -24,8 +27,9 @@ inline size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255);
 struct Plan {
   int path = kGemv;
   int64_t M = 0, N = 0, K = 0, Kp = 0, row_bytes = 0;
-  // GEMV: tokens per thread (1, 2 or 4), words per thread, log2 threads per row
-  int mt = 1, wpt = 1, tpr_log2 = 0;
+  // GEMV: tokens held (1, 2, 4 or 8), 8-byte units per lane, log2 warps per
+  // row, units per warp chunk, consumer warps
+  int mt = 1, upt = 1, split_log2 = 0, chunk = 0, cw = 8;
   // tensor-core GEMM
   int bn = 0;
   int64_t tiles_n = 0, tiles_m = 0;
@@ -35,7 +39,9 @@ struct Plan {
   size_t off_xb = 0, off_sc = 0, off_acc = 0, off_cnt = 0, ws_bytes = 0;
 };
 
-inline int wpt_max(int mt) { return mt == 1 ? 8 : (mt == 2 ? 4 : 2); }
+// Units per lane so the activation slice stays within 64 registers
+// (8 registers per unit and token).
+inline int upt_max(int mt) { return mt == 1 ? 8 : (mt == 2 ? 4 : (mt == 4 ? 2 : 1)); }
 
 inline Plan make(int64_t M, int64_t N, int64_t K) {
   Plan p;
@@ -44,26 +50,20 @@ inline Plan make(int64_t M, int64_t N, int64_t K) {
   p.K = K;
   p.row_bytes = row_bytes(K);
   p.Kp = p.row_bytes * 4;
-  const int64_t words = p.row_bytes / 4;
-  if (M <= 4) {
-    p.mt = M == 1 ? 1 : (M == 2 ? 2 : 4);
-    const int wm = wpt_max(p.mt);
-    int best = -1;
-    int64_t best_waste = 0;
-    for (int lg = 0; lg <= 8; ++lg) {
-      const int64_t tpr = int64_t(1) << lg;
-      const int64_t w = (words + tpr - 1) / tpr;
-      if (w > wm) continue;
-      const int64_t waste = tpr * w - words;
-      if (best < 0 || waste < best_waste) {
-        best = lg;
-        best_waste = waste;
-      }
-    }
-    if (best >= 0) {
+  const int64_t units = p.row_bytes / 8;
+  if (M <= 8) {
+    p.mt = M == 1 ? 1 : (M == 2 ? 2 : (M <= 4 ? 4 : 8));
+    const int64_t per_warp = 32 * static_cast<int64_t>(upt_max(p.mt));
+    // warps per row: the fewest (a power of two, at most 8) whose chunks fit
+    int lg = 0;
+    while (lg < 3 && (units + (int64_t(1) << lg) - 1) / (int64_t(1) << lg) > per_warp) ++lg;
+    const int64_t chunk = (units + (int64_t(1) << lg) - 1) >> lg;
+    const int64_t kp_bytes = M * p.Kp;
+    if (chunk <= per_warp && kp_bytes <= 64 * 1024) {
       p.path = kGemv;
-      p.tpr_log2 = best;
-      p.wpt = static_cast<int>((words + (int64_t(1) << best) - 1) >> best);
+      p.split_log2 = lg;
+      p.chunk = static_cast<int>(chunk);
+      p.upt = static_cast<int>((chunk + 31) / 32);
       p.ws_bytes = 0;
       return p;
     }
@@ -103,23 +103,31 @@ inline Plan make(int64_t M, int64_t N, int64_t K) {
 }
 
 struct GemvGrid {
-  int grid = 1, rows_per_cta = 1, stage_rows = 1;
+  int grid = 1, rows_per_cta = 1, stage_rows = 1, stage_bytes = 128, nstages = 1, cw = 8;
+  int smem = 0;
 };
 
+// One block per SM, each a contiguous run of rows.  Single-token blocks with
+// much work get 16 consumer warps; the others 8, which leaves room for a
+// block of the next kernel to start alongside under launch overlap.
 inline GemvGrid gemv_grid(const Plan &p, int sms) {
   GemvGrid g;
-  const int64_t rpi = kGemvThreads >> p.tpr_log2;
-  int64_t want = (p.N + rpi - 1) / rpi;
-  if (want > sms) want = sms;
-  if (want < 1) want = 1;
-  const int64_t rpc = (p.N + want - 1) / want;
+  const int64_t rpc = (p.N + sms - 1) / sms;
   g.rows_per_cta = static_cast<int>(rpc);
   g.grid = static_cast<int>((p.N + rpc - 1) / rpc);
   int64_t sr = kGemvStageBytes / p.row_bytes;
+  if (p.split_log2 > 0 && sr > kGemvMaxSplitRows) sr = kGemvMaxSplitRows;
   if (sr < 1) sr = 1;
-  if (sr >= rpi) sr -= sr % rpi;
   if (sr > rpc) sr = rpc;
   g.stage_rows = static_cast<int>(sr);
+  g.stage_bytes = static_cast<int>(((sr * p.row_bytes) + 127) / 128 * 128);
+  const int64_t iters = (rpc + sr - 1) / sr;
+  const int64_t codes = p.M * p.Kp;
+  int64_t S = iters < kGemvMaxStages ? iters : kGemvMaxStages;
+  while (S > 1 && kGemvSmemFixed + S * g.stage_bytes + codes > kSmemMax) --S;
+  g.nstages = static_cast<int>(S);
+  g.smem = static_cast<int>(kGemvSmemFixed + S * g.stage_bytes + codes);
+  g.cw = (p.mt == 1 && rpc * p.row_bytes >= 64 * 1024) ? 16 : 8;
   return g;
 }
 

@@ -13,14 +13,9 @@ namespace bl {
 // Bit 0: a bounded wait gave up.  Read and cleared through the C ABI.
 __device__ unsigned int g_dev_error = 0u;
 constexpr unsigned kDevErrTimeout = 1u;
-// A wait that has not completed after this long is treated as a failure.
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;
-
-__device__ __forceinline__ unsigned long long globaltimer_ns() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
+// A wait that has not completed after this many SM cycles (about 2 s at the
+// B300's 2.03 GHz maximum clock, longer at lower clocks) is a failure.
+constexpr long long kWaitLimitCycles = 4000000000ll;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -59,12 +54,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Bounded wait for the phase with the given parity to complete.  Returns
-// false (and raises the device error flag) after kWaitLimitNs.
+// false (and raises the device error flag) after kWaitLimitCycles.
 __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity) {
-  const unsigned long long t0 = globaltimer_ns();
-  for (uint32_t i = 1;; ++i) {
+  const long long t0 = clock64();
+  while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63u) == 0u && globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (clock64() - t0 > kWaitLimitCycles) {
       atomicOr(&g_dev_error, kDevErrTimeout);
       return false;
     }
@@ -239,6 +234,14 @@ __device__ __forceinline__ uint4 lds_u128(uint32_t addr) {
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "r"(addr));
   return v;
+}
+
+__device__ __forceinline__ void sts_u64(uint32_t addr, uint32_t a, uint32_t b) {
+  asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
+}
+
+__device__ __forceinline__ void sts_u8(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.u8 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ void sts_u128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
