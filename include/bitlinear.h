@@ -185,6 +185,34 @@ BL_API bl_status bitlinear_matmul_i32(const uint8_t *packed, int64_t N, int64_t 
                                const int8_t *xq, int64_t M, int32_t *acc,
                                void *ws, size_t ws_bytes, void *stream);
 
+/* bitlinear_forward without a workspace argument, for callers that cannot
+ * allocate device memory when they call it: code that may only use memory
+ * it was handed (a serving engine's fixed memory pool, a plugin interface
+ * that passes in only its own tensors), or code that must not call
+ * cudaMalloc/cudaFree because those can synchronise the device or are not
+ * allowed where it runs.  The pages describe no such variant; it is an
+ * addition of this library.
+ *   Arguments and result as bitlinear_forward.  The call allocates nothing:
+ *   the scratch that larger M needs lives in one fixed 8 MiB array inside
+ *   the library's device memory, held by every GPU that loads the library
+ *   until the process exits.  Sizes whose scratch
+ *   (bitlinear_workspace_bytes(M, N, K)) exceeds 8 MiB return
+ *   BL_ERR_WORKSPACE before anything is enqueued: use bitlinear_forward with
+ *   a workspace for those (e.g. prefill with M in the thousands).
+ *   The first call on a device that needs the scratch looks up the array's
+ *   device address on that device (current device); make that first call
+ *   before any stream capture.  All calls share the one array: calls that can
+ *   run at the same time on the GPU (different streams with no ordering,
+ *   several host threads) race on it and give wrong results -- order them.
+ *   Each call writes everything it later reads from the array (its split-K
+ *   accumulators and tickets are zeroed by its own first kernel), so what an
+ *   earlier call left there does not matter.
+ * Errors: as bitlinear_forward, with BL_ERR_WORKSPACE meaning "larger than
+ * the fixed scratch". */
+BL_API bl_status bitlinear_forward_noalloc(const uint8_t *packed, const float *gamma,
+                                           int64_t N, int64_t K, const void *x, int dtype,
+                                           int64_t M, float *y, void *stream);
+
 /* Launch overlap (programmatic dependent launch) for the forward kernels.
  * Process-wide; host only.  Modes:
  *   0 (default)  ordinary stream order.

@@ -26,7 +26,8 @@ __all__ = [
     "BitLinearError", "BitLinear", "packed_row_bytes", "packed_bytes",
     "pack_workspace_bytes", "workspace_bytes", "bitlinear_pack_weights",
     "bitlinear_quant_act", "bitlinear_rmsnorm_quant_act", "bitlinear_forward",
-    "bitlinear_forward_q", "bitlinear_matmul_i32", "set_launch_overlap",
+    "bitlinear_forward_q", "bitlinear_matmul_i32", "bitlinear_forward_noalloc",
+    "set_launch_overlap",
     "get_launch_overlap", "device_error", "library_path",
 ]
 
@@ -188,6 +189,24 @@ def bitlinear_matmul_i32(packed: torch.Tensor, N: int, K: int, xq: torch.Tensor,
         _ptr(packed), N, K, _ptr(xq), M, _ptr(acc), _ptr(ws),
         0 if ws is None else ws.numel(), _stream(xq)), "bitlinear_matmul_i32")
     return acc
+
+
+def bitlinear_forward_noalloc(packed: torch.Tensor, gamma: torch.Tensor, N: int, K: int,
+                              x: torch.Tensor, y: torch.Tensor | None = None) -> torch.Tensor:
+    """bitlinear_forward without a workspace: the library's fixed 8 MiB device
+    scratch stands in for it (for callers that cannot allocate at call time).
+    Calls share that scratch, so calls that may overlap on the GPU must be
+    ordered.  Only y is allocated here, and only when not given."""
+    _need_cuda("packed", packed, torch.uint8)
+    _need_cuda("x", x, (torch.float32, torch.bfloat16), 2)
+    M = x.shape[0]
+    if x.shape[1] != K:
+        raise ValueError("x.shape[1] != K")
+    y = torch.empty((M, N), dtype=torch.float32, device=x.device) if y is None else y
+    capi.check(_lib().bitlinear_forward_noalloc(
+        _ptr(packed), _ptr(gamma), N, K, _ptr(x), _DTYPES[x.dtype], M, _ptr(y), _stream(x)),
+        "bitlinear_forward_noalloc")
+    return y
 
 
 def set_launch_overlap(mode) -> None:

@@ -20,6 +20,12 @@
 #include "bl_ptx.cuh"
 #include "bl_plan.h"
 
+// Scratch memory for bitlinear_forward_noalloc: a fixed array in the
+// library's own device memory, so that entry point never allocates.  Every GPU
+// that loads the library holds these bytes until the process exits.
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
 namespace {
 
 using namespace bl;
@@ -334,6 +340,26 @@ bl_status forward_common(const uint8_t *packed, const float *gamma, int64_t N, i
   return forward_tc(pl, dev, xm, out_i32, packed, gamma, x, xq, scale, y, acc, ws, ws_bytes, st);
 }
 
+// Device address of g_noalloc_scratch on device `dev` (which must be current).
+// In host code the array's name only stands for it; the address is looked up
+// once per device and kept.
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[64] = {};
+
+bl_status noalloc_scratch(int dev, void **out) {
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) {
+      cudaGetLastError();
+      return BL_ERR_CUDA;
+    }
+    g_noalloc_ptr[dev] = ptr;
+  }
+  *out = g_noalloc_ptr[dev];
+  return BL_OK;
+}
+
 }  // namespace
 
 // ====================================================================== C ABI
@@ -484,6 +510,26 @@ bl_status bitlinear_matmul_i32(const uint8_t *packed, int64_t N, int64_t K, cons
   if (acc == nullptr) return BL_ERR_NULL;
   return forward_common(packed, nullptr, N, K, gemv::kXInt8, nullptr, xq, nullptr, M, nullptr, acc, ws,
                         ws_bytes, stream);
+}
+
+bl_status bitlinear_forward_noalloc(const uint8_t *packed, const float *gamma, int64_t N, int64_t K,
+                                    const void *x, int dtype, int64_t M, float *y, void *stream) {
+  if (dtype != BL_F32 && dtype != BL_BF16) return BL_ERR_DTYPE;
+  if (packed == nullptr || gamma == nullptr || x == nullptr || y == nullptr) return BL_ERR_NULL;
+  bl_status s = check_dims(M, N, K);
+  if (s != BL_OK) return s;
+  const size_t need = plan::make(M, N, K).ws_bytes;
+  if (need > kNoAllocScratchBytes) return BL_ERR_WORKSPACE;
+  void *ws = nullptr;
+  if (need > 0) {
+    int dev = 0;
+    s = current_device(&dev, nullptr);
+    if (s != BL_OK) return s;
+    s = noalloc_scratch(dev, &ws);
+    if (s != BL_OK) return s;
+  }
+  return bitlinear_forward(packed, gamma, N, K, x, dtype, M, y, ws, need > 0 ? kNoAllocScratchBytes : 0,
+                           stream);
 }
 
 void bitlinear_set_launch_overlap(int mode) { g_overlap.store(mode < 0 ? 0 : (mode > 2 ? 2 : mode)); }
