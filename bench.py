@@ -33,6 +33,22 @@ sys.path.insert(0, ROOT)
 METRIC = "BitLinear GB/s (decode, % HBM peak) and int8 TOPS (prefill, % INT8 peak)"
 WORKLOAD = "decode_2b"
 
+# DRAM bytes (read + write) per decode-GEMV launch, mean over the four ~2B
+# shapes, from one ncu capture (profiles/gemv_decode_2b_m1.md).  Valid only for
+# the kernel source whose sha256 starts with `src`; otherwise reported as null.
+GEMV_TRAFFIC = {"bytes_per_launch": 3270720.0, "src": "219efa783253491c",
+                "file": "w1_a8_bitlinear_02_b300/csrc/bl_gemv.cuh"}
+
+
+def measured_traffic():
+    import hashlib
+    path = os.path.join(ROOT, GEMV_TRAFFIC["file"])
+    try:
+        h = hashlib.sha256(open(path, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    return GEMV_TRAFFIC["bytes_per_launch"] if h.startswith(GEMV_TRAFFIC["src"]) else None
+
 
 def load_peaks() -> dict:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -299,7 +315,9 @@ def run_ours(args, rank: int, world: int, local: int):
     per_launch_bytes = step_bytes / len(items)
     achieved = per_launch_bytes / per_launch_s / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                "frac": achieved / peaks["hbm_gbs"], "traffic": measured_traffic(),
+                "traffic_unit": "bytes per launch (dram read + write, ncu)",
+                "algorithmic_bytes_per_launch": per_launch_bytes,
                 "kernel": "bl::gemv::gemv_kernel<1,*,bf16>",
                 "peak_source": f"{peaks['source']} (copy bandwidth)"}
 
@@ -354,12 +372,14 @@ def run_ours(args, rank: int, world: int, local: int):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "int8", "data": "synthetic",
-            "config": {"workload": "decode_2b: M=1 over 30 layers x {qkv 3840x2560, o 2560x2560, "
-                                   "up 6912x2560, down 2560x6912}, x bf16, fused act-quant",
+            "config": {"workload": f"decode_2b: M=1 over {args.layers} layers x {{qkv 3840x2560, "
+                                   "o 2560x2560, up 6912x2560, down 2560x6912}, x bf16, fused act-quant",
                        "M": 1, "layers": args.layers, "matrices": len(items),
                        "packed_weight_bytes_per_step": packed_bytes,
                        "algorithmic_bytes_per_step": step_bytes,
-                       "l2": "inputs larger than L2 (packed weights 388 MB vs 126 MB L2); no flush",
+                       "l2": (f"inputs larger than L2 (packed weights {packed_bytes / 1e6:.0f} MB vs "
+                              "126 MB L2); no flush") if packed_bytes > 126e6 else
+                             f"packed weights {packed_bytes / 1e6:.0f} MB fit in L2 (reduced run)",
                        "launch": "CUDA graph of one bitlinear_forward per matrix, launch overlap "
                                  + ("off" if args.no_overlap else "on"),
                        "parallelism": f"{world} independent replica(s), weak scaling"},
