@@ -235,7 +235,8 @@ BL_API int bitlinear_get_launch_overlap(void);
  * returns early (its outputs are then invalid).  This reads (and, if
  * `clear`, resets) the flag of the current device.  Synchronous: it waits
  * for the device.  flags: host out, 0 = no error; bit 0 = pipeline wait
- * timed out.  Returns BL_ERR_DEVICE when a flag was set, BL_OK otherwise,
+ * timed out; bit 1 = a kernel received a launch configuration it cannot run
+ * (it skipped its work).  Returns BL_ERR_DEVICE when a flag was set, BL_OK otherwise,
  * BL_ERR_CUDA if the device could not be read. */
 BL_API bl_status bitlinear_device_error(unsigned int *flags, int clear);
 

@@ -1,0 +1,49 @@
+// Launch-plan invariants of the BitLinear library, checked on the host over
+// a grid of shapes: every GEMV plan covers each row with at most the block's
+// warps, its stages fit their buffers and shared memory, its grid covers N
+// exactly once; every tensor-core plan covers M, N and all k tiles.
+#include <cstdio>
+#include <cstdlib>
+#include <initializer_list>
+#include "bl_plan.h"
+using namespace bl::plan;
+int main() {
+  long checked = 0, gemv = 0, tc = 0;
+  const int sms = 148;
+  for (long M = 1; M <= 300; M += (M < 16 ? 1 : 37))
+    for (long K : {1L, 15L, 16L, 63L, 64L, 65L, 100L, 333L, 512L, 1000L, 2560L, 4096L, 6912L, 8192L, 9000L, 16384L, 28672L, 32768L, 65536L, 131072L})
+      for (long N : {1L, 7L, 128L, 129L, 256L, 300L, 513L, 2560L, 3840L, 6912L, 8192L, 28672L}) {
+        Plan p = make(M, N, K);
+        ++checked;
+        if (p.path == kGemv) {
+          ++gemv;
+          const int G = 1 << p.split_log2;
+          const long units = p.row_bytes / 8;
+          GemvGrid g = gemv_grid(p, sms);
+          bool ok = M <= 8 && G <= g.cw && (g.cw >> p.split_log2) >= 1 &&
+                    (long)p.chunk * G >= units && p.upt * 32 >= p.chunk && p.upt >= 1 &&
+                    p.upt <= upt_max(p.mt) && (g.cw == 8 || (g.cw == 16 && p.mt == 1));
+          ok = ok && g.grid >= 1 && (long)g.grid * g.rows_per_cta >= N && (long)(g.grid - 1) * g.rows_per_cta < N;
+          ok = ok && g.stage_rows >= 1 && g.stage_rows <= g.rows_per_cta && g.nstages >= 1 && g.nstages <= kGemvMaxStages;
+          ok = ok && (long)g.stage_rows * p.row_bytes <= g.stage_bytes && g.stage_bytes % 128 == 0;
+          ok = ok && ((long)g.stage_rows * p.row_bytes <= kGemvStageBytes || g.stage_rows == 1);
+          ok = ok && (p.split_log2 == 0 || g.stage_rows <= kGemvMaxSplitRows);
+          ok = ok && g.smem <= kSmemMax &&
+               g.smem == kGemvSmemFixed + g.nstages * g.stage_bytes + (int)(M * p.Kp);
+          if (!ok) { printf("BAD gemv M=%ld N=%ld K=%ld G=%d upt=%d chunk=%d\n", M, N, K, G, p.upt, p.chunk); return 1; }
+        } else {
+          ++tc;
+          bool ok = p.bn >= 16 && p.bn <= 256 && p.splits >= 1 && p.kt_per_split >= 1 &&
+                    (long)p.splits * p.kt_per_split >= p.Kp / 64 && (long)(p.splits - 1) * p.kt_per_split < p.Kp / 64 &&
+                    p.tiles_n * 128 >= N && p.tiles_m * p.bn >= M;
+          if (!ok) { printf("BAD tc M=%ld N=%ld K=%ld\n", M, N, K); return 1; }
+        }
+      }
+  printf("ok: %ld plans (%ld gemv, %ld tensor-core)\n", checked, gemv, tc);
+  // the specific shapes of the tests and bench
+  for (long M : {1L, 3L, 8L}) for (long K : {2560L, 6912L, 8192L, 28672L}) {
+    Plan p = make(M, 2560, K);
+    printf("M=%ld K=%ld path=%s G=%d upt=%d chunk=%d\n", M, K, p.path == kGemv ? "gemv" : "tc", 1 << p.split_log2, p.upt, p.chunk);
+  }
+  return 0;
+}

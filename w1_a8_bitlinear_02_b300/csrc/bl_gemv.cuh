@@ -279,7 +279,11 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) gemv_kernel(const Params p) 
   const int G = 1 << p.split_log2;
   const int chunk_id = warp & (G - 1);
   const int row_slot = warp >> p.split_log2;
-  const int row_step = CW >> p.split_log2;
+  // A row split over more warps than the block has cannot be covered: report
+  // it and do no row work (the launch plan guarantees G <= CW).
+  const bool split_ok = G <= CW;
+  if (!split_ok && tid == 0) atomicOr(&g_dev_error, kDevErrConfig);
+  const int row_step = split_ok ? (CW >> p.split_log2) : 1;
   const int ubase = chunk_id * p.chunk;
   int uend = ubase + p.chunk;
   if (uend > p.units) uend = p.units;
@@ -310,7 +314,7 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) gemv_kernel(const Params p) 
     int rows_here = nrows - it * p.stage_rows;
     if (rows_here > p.stage_rows) rows_here = p.stage_rows;
     const uint32_t sbase = ring + s * p.stage_bytes;
-    for (int r = row_slot; r < rows_here; r += row_step) {
+    for (int r = split_ok ? row_slot : rows_here; r < rows_here; r += row_step) {
       const uint32_t rbase = sbase + static_cast<uint32_t>(r) * p.row_bytes;
       int tot[MT];
       if constexpr (kMasked) {

@@ -10,9 +10,11 @@
 namespace bl {
 
 // ------------------------------------------------------------ error flag
-// Bit 0: a bounded wait gave up.  Read and cleared through the C ABI.
+// Bit 0: a bounded wait gave up; bit 1: an impossible launch configuration.
+// Read and cleared through the C ABI.
 __device__ unsigned int g_dev_error = 0u;
 constexpr unsigned kDevErrTimeout = 1u;
+constexpr unsigned kDevErrConfig = 2u;  // a kernel was given a configuration it cannot run
 // A wait that has not completed after this many SM cycles (about 2 s at the
 // B300's 2.03 GHz maximum clock, longer at lower clocks) is a failure.
 constexpr long long kWaitLimitCycles = 4000000000ll;
