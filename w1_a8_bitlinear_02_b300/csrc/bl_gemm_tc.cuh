@@ -1,4 +1,4 @@
-// Tensor-core BitLinear contraction for M > 4 tokens (batched decode and
+// Tensor-core BitLinear contraction for M > 8 tokens (batched decode and
 // prefill), tcgen05 on sm_103a.
 //
 // sm_103a has no integer MMA (ptxas rejects tcgen05.mma kind::i8 for this
@@ -9,19 +9,25 @@
 // accumulator is therefore the exact int32 dot product.
 //
 // Tile: 128 weight rows (the MMA's M) x BN tokens (the MMA's N) x 64 k per
-// pipeline stage.  Roles (192 threads):
+// pipeline stage.  Roles (320 threads):
 //   warp 0      TMA producer: the packed 2-bit weight tile (128 rows x 16 B)
 //               and the bf16 activation tile (BN rows x 128 B, 128-byte
 //               swizzle) of each stage, completion on one mbarrier.
-//   warp 1      allocates TMEM; one lane issues the MMAs (4 x K=16 per stage)
-//               and commits each stage back to the producer.
-//   warps 2..5  unpack: each thread expands one weight row of the packed tile
-//               (16 bytes = 64 codes) into 64 bf16 values, written straight
-//               into the 128-byte-swizzled K-major layout the MMA reads
-//               ("pack-store-load-unpack-compute": packed in HBM, unpacked in
-//               shared memory -- "微软AI大模型炸场：0.4GB，CPU就能跑",
-//               blog.csdn.net/2401_84494441, section 3, GPU bullet).  Then
-//               the epilogue: TMEM -> registers -> y = fl32(fl32(acc*gamma)/s).
+//   warp 1      allocates TMEM; one lane issues the MMAs (4 x K=16 per stage,
+//               A from tensor memory, B from shared memory) and commits each
+//               stage back to the producer.
+//   warps 2..9  unpack: warp w expands, for the 32 weight rows of TMEM lane
+//               quarter w % 4, one half (32 weights) of each row's 16 packed
+//               bytes into bf16 and stores them straight into the stage's A
+//               buffer in tensor memory ("pack-store-load-unpack-compute":
+//               packed in HBM, unpacked on chip -- "微软AI大模型炸场：0.4GB，
+//               CPU就能跑", blog.csdn.net/2401_84494441, section 3, GPU
+//               bullet).  Shared memory then only holds the activation and
+//               packed tiles, so more stages fit and the A operand costs no
+//               shared-memory bandwidth.  Then the epilogue:
+//               TMEM -> registers -> y = fl32(acc * c_m), c_m = gamma / s_m.
+// Tensor memory: D (accumulator) in columns [0, max(32, BN)), then one
+// 32-column A buffer (128 rows x 64 bf16) per stage.
 // Split-K (for small tile counts): partial int32 sums are added atomically
 // into a workspace zeroed by the preceding activation kernel; the last CTA
 // of each tile (an atomic ticket, no spinning) applies the rescale.
@@ -37,23 +43,29 @@
 namespace bl {
 namespace tc {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr int kUnpackWarps = 8;
+constexpr int kUnpackThreads = kUnpackWarps * 32;
 constexpr int kBM = 128;                 // weight rows per tile
 constexpr int kBK = 64;                  // k per stage
-constexpr int kABytes = kBM * kBK * 2;   // unpacked weights, bf16
-constexpr int kPBytes = kBM * kBK / 4;   // packed weights
-constexpr int kSmemBudget = 200 * 1024;
+constexpr int kPBytes = kBM * kBK / 4;   // packed weights per stage
+constexpr int kSmemBudget = 210 * 1024;
+constexpr int kTmemCols = 512;
 
 template <int BN>
 struct Cfg {
   static constexpr int kBBytes = BN * kBK * 2;
-  static constexpr int kStageBytes = kABytes + kBBytes + kPBytes;
-  static constexpr int kStages = (kSmemBudget / kStageBytes) > 8 ? 8 : (kSmemBudget / kStageBytes);
-  static constexpr int kTmemCols = BN < 32 ? 32 : BN;
+  static constexpr int kStageBytes = kBBytes + kPBytes;
+  static constexpr int kDCols = BN < 32 ? 32 : BN;
+  static constexpr int kBySmem = kSmemBudget / kStageBytes;
+  static constexpr int kByTmem = (kTmemCols - kDCols) / 32;
+  static constexpr int kMin = kBySmem < kByTmem ? kBySmem : kByTmem;
+  static constexpr int kStages = kMin < 8 ? kMin : 8;
   // stages + up to 1023 bytes of alignment slack + the barrier block
-  static constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 2048;
+  static constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 3072;
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
   static_assert(kStages >= 2, "pipeline depth");
+  static_assert(kDCols + 32 * kStages <= kTmemCols, "tensor memory columns");
 };
 
 struct Params {
@@ -100,8 +112,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
-  const uint32_t a_base = base;
-  const uint32_t b_base = base + S * kABytes;
+  const uint32_t b_base = base;
   const uint32_t p_base = b_base + S * C::kBBytes;
   Bars &bars = *reinterpret_cast<Bars *>(smem_raw + (base - raw) + S * C::kStageBytes);
 
@@ -115,7 +126,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(smem_u32(&bars.full[s]), 1);
-      mbar_init(smem_u32(&bars.afull[s]), 128);
+      mbar_init(smem_u32(&bars.afull[s]), kUnpackThreads);
       mbar_init(smem_u32(&bars.empty[s]), 1);
     }
     mbar_init(smem_u32(&bars.accfull), 1);
@@ -128,7 +139,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tensormap(&map_w);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(&bars.tmem_base), C::kTmemCols);
+    tmem_alloc(smem_u32(&bars.tmem_base), kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -184,39 +195,44 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint64_t ad = smem_desc_sw128(a_base + s * kABytes);
+        const uint32_t at = tmem + C::kDCols + 32u * s;
         const uint64_t bd = smem_desc_sw128(b_base + s * C::kBBytes);
 #pragma unroll
         for (int j = 0; j < kBK / 16; ++j)
-          mma_bf16_ss(tmem, ad + 2u * j, bd + 2u * j, idesc, (i | j) != 0 ? 1u : 0u);
+          mma_bf16_ts(tmem, at + 8u * j, bd + 2u * j, idesc, (i | j) != 0 ? 1u : 0u);
         mma_commit(smem_u32(&bars.empty[s]));
       }
       mma_commit(smem_u32(&bars.accfull));  // fires once every issued MMA is done
     }
   } else {
     // ------------------------------------------------------------ unpack
-    const int u = tid - 64;  // weight row of the tile
-    const uint32_t swz = static_cast<uint32_t>(u & 7);
+    const int u = tid - 64;            // 0 .. 255
+    const int q = warp & 3;            // TMEM lane quarter this warp may access
+    const int h = (warp - 2) >> 2;     // which 32 of the row's 64 weights
+    const int row = 32 * q + lane;     // weight row of the tile
+    const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
     for (int i = 0; i < nkt; ++i) {
       const int s = i % S;
       if (!mbar_wait(smem_u32(&bars.full[s]), (i / S) & 1) || *abort_flag) {
         *abort_flag = 1;
         break;
       }
-      const uint4 pk = lds_u128(p_base + s * kPBytes + u * 16);
-      const uint32_t words[4] = {pk.x, pk.y, pk.z, pk.w};
-      const uint32_t arow = a_base + s * kABytes + u * 128;
+      // words 2h, 2h+1 of the row's 16 packed bytes: k = 32h .. 32h+31
+      uint32_t w0, w1;
+      asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
+                   : "=r"(w0), "=r"(w1)
+                   : "r"(p_base + s * kPBytes + row * 16 + 8 * h));
+      uint32_t v[16];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {  // 16-byte chunk c holds k = 8c .. 8c+7
-        const uint32_t word = words[c >> 1];
-        // k = 8c .. 8c+3 sit at i = 2(c&1) (bit shift 2i), k = 8c+4 .. 8c+7 at i + 1
-        const int sh = 4 * (c & 1);
-        uint32_t v0, v1, v2, v3;
-        codes4_to_bf16((word >> sh) & 0x03030303u, v0, v1);
-        codes4_to_bf16((word >> (sh + 2)) & 0x03030303u, v2, v3);
-        sts_u128(arow + ((static_cast<uint32_t>(c) ^ swz) << 4), v0, v1, v2, v3);
+      for (int wi = 0; wi < 2; ++wi) {
+        const uint32_t word = wi ? w1 : w0;
+#pragma unroll
+        for (int i4 = 0; i4 < 4; ++i4)  // k = 16 wi + 4 i4 .. +3
+          codes4_to_bf16((word >> (2 * i4)) & 0x03030303u, v[8 * wi + 2 * i4], v[8 * wi + 2 * i4 + 1]);
       }
-      fence_proxy_async_smem();
+      tmem_st_32x32b_x16(tmem + lane_off + C::kDCols + 32u * s + 16u * h, v);
+      tmem_st_wait();
+      tc_fence_before();
       mbar_arrive(smem_u32(&bars.afull[s]));
     }
 
@@ -225,22 +241,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_wait_primary();
     if constexpr (!OUT_I32) {
       const float g = *p.gamma;
-      for (int j = u; j < BN; j += 128)
+      for (int j = u; j < BN; j += kUnpackThreads)
         bars.cscale[j] = (m0 + j < p.M) ? __fdiv_rn(g, p.scale[m0 + j]) : 0.0f;
     }
     bool ok = mbar_wait(smem_u32(&bars.accfull), 0);
-    // One decision for all four epilogue warps (they share named barriers and
+    // One decision for all epilogue warps (they share named barriers and
     // warp-collective TMEM loads below).
-    ok = !named_bar_or(4, 128, !ok || *abort_flag);
+    ok = !named_bar_or(4, kUnpackThreads, !ok || *abort_flag);
     tc_fence_after();
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
-    const int row = 32 * q + lane;
     const int n = n0 + row;
     if (ok) {
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 32) {
+      for (int c0 = 32 * h; c0 < BN; c0 += 64) {
         uint32_t r[32];
-        tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + c0, r);
+        tmem_ld_32x32b_x32(tmem + lane_off + c0, r);
         tmem_ld_wait();
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
@@ -265,16 +279,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       if constexpr (!OUT_I32) {
         if (p.splits > 1) {
           __threadfence();
-          named_bar(3, 128);
-          if (tid == 64) {
+          named_bar(3, kUnpackThreads);
+          if (u == 0) {
             const unsigned t = atomicAdd(&p.ws_cnt[blockIdx.y * gridDim.x + blockIdx.x], 1u);
             bars.last_flag = (t == static_cast<unsigned>(p.splits - 1)) ? 1 : 0;
           }
-          named_bar(3, 128);
+          named_bar(3, kUnpackThreads);
           if (bars.last_flag) {
             __threadfence();
             if (n < p.N) {
-              for (int j = 0; j < BN; ++j) {
+              for (int j = h; j < BN; j += 2) {
                 const int m = m0 + j;
                 if (m >= p.M) break;
                 const int64_t o = static_cast<int64_t>(m) * p.N + n;
@@ -291,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, C::kTmemCols);
+    tmem_dealloc(tmem, kTmemCols);
   }
 }
 
