@@ -78,11 +78,16 @@ def test_row_bytes_and_sizes(lib):
 
 def test_workspace_plan(lib):
     import w1_a8_bitlinear_02_b300 as bl
-    # decode (M <= 8) runs without workspace on the GEMV path
-    for M in range(1, 9):
-        assert bl.workspace_bytes(M, 2560, 6912) == 0
-    # larger M (tensor cores) needs the bf16 code buffer and scales at least
-    for M, N, K in ((9, 256, 512), (64, 2560, 2560), (2048, 6912, 2560), (8, 128, 16384)):
+    # decode (M = 1, GEMV) and batched decode (2 <= M <= 64, the few-token
+    # tensor-core kernel, which quantises in shared memory) need no workspace
+    for M in (1, 2, 3, 8, 9, 16, 33, 64):
+        for N, K in ((2560, 6912), (3840, 2560), (6912, 2560), (2560, 2560)):
+            assert bl.workspace_bytes(M, N, K) == 0, (M, N, K)
+    for M in (1, 2, 8):
+        for N, K in ((28672, 8192), (8192, 28672)):
+            assert bl.workspace_bytes(M, N, K) == 0, (M, N, K)
+    # prefill (tensor-core GEMM) needs the bf16 code buffer and scales at least
+    for M, N, K in ((65, 256, 512), (130, 2560, 2560), (2048, 6912, 2560), (2048, 2560, 6912)):
         need = bl.workspace_bytes(M, N, K)
         assert need >= M * bl.packed_row_bytes(K) * 4 * 2 + 4 * M
     # M = 1 with a K too large to hold in registers also takes the tensor-core path

@@ -234,6 +234,24 @@ def test_decode_2b_shapes_full(bl, name, N, K, kind):
                           f"{name} M={M}")
 
 
+@pytest.mark.parametrize("name,N,K,kind", [(n, N, K, k) for n, N, K, k in wl.PROJ_2B])
+def test_batched_decode_2b_shapes_full(bl, name, N, K, kind):
+    """Batched decode on one layer of the ~2B model: M = 16, 33 and 64 tokens with
+    1 % outlier channels, whole outputs, through forward and forward_q."""
+    packed, gamma, p_ref, g_ref = pack_both(bl, N, K, 0.02, wl.weight_seed("decode_2b", 1, 0) + N)
+    for M in (16, 33, 64):
+        x = wl.activations(M, K, "outliers1pct", 91 + M, "cpu", torch.bfloat16)
+        y = bl.bitlinear_forward(packed, gamma, N, K, x.to(DEV))
+        xq_ref, s_ref = oracle.quant_act(x.float().numpy())
+        y_q = bl.bitlinear_forward_q(packed, gamma, N, K, torch.from_numpy(xq_ref).to(DEV),
+                                     torch.from_numpy(s_ref).to(DEV))
+        torch.cuda.synchronize()
+        assert bl.device_error() == 0
+        y_ref = oracle.forward_packed(p_ref, g_ref, N, K, x.float().numpy())
+        assert_bits_equal(y.cpu().numpy(), y_ref, f"{name} M={M}")
+        assert_bits_equal(y_q.cpu().numpy(), y_ref, f"{name} M={M} forward_q")
+
+
 @pytest.mark.parametrize("N,K,kind", [(6912, 2560, "normal"), (2560, 6912, "relu2")])
 def test_prefill_2048_sampled_tokens(bl, N, K, kind):
     """M = 2048 on the tensor-core path; 12 sampled tokens checked in full

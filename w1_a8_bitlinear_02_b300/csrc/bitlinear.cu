@@ -10,15 +10,18 @@
 #include <atomic>
 #include <cstdint>
 #include <cstring>
+#include <map>
 #include <mutex>
 #include <set>
+#include <tuple>
 #include <utility>
 
 #include "bl_gemm_tc.cuh"
 #include "bl_gemv.cuh"
 #include "bl_pack_quant.cuh"
-#include "bl_ptx.cuh"
 #include "bl_plan.h"
+#include "bl_ptx.cuh"
+#include "bl_skinny.cuh"
 
 // Scratch memory for bitlinear_forward_noalloc: a fixed array in the
 // library's own device memory, so that entry point never allocates.  Every GPU
@@ -258,6 +261,132 @@ bl_status run_tc(const plan::Plan &pl, int dev, const CUtensorMap &mx, const CUt
   }
 }
 
+// ------------------------------------------------------------ few-token dispatch
+template <int XM, bool OUT_I32>
+void *sk_func_bn(int bn) {
+  if (bn == 16) return reinterpret_cast<void *>(&sk::skinny_kernel<16, XM, OUT_I32>);
+  if (bn == 32) return reinterpret_cast<void *>(&sk::skinny_kernel<32, XM, OUT_I32>);
+  if (bn == 64) return reinterpret_cast<void *>(&sk::skinny_kernel<64, XM, OUT_I32>);
+  return nullptr;
+}
+
+void *sk_func(int bn, int xm, bool out_i32) {
+  if (out_i32) return sk_func_bn<sk::kXInt8, true>(bn);
+  if (xm == gemv::kXF32) return sk_func_bn<sk::kXF32, false>(bn);
+  if (xm == gemv::kXBF16) return sk_func_bn<sk::kXBF16, false>(bn);
+  return sk_func_bn<sk::kXInt8, false>(bn);
+}
+
+// Clusters of `cs` blocks of kernel f (with `smem` bytes each) that the device
+// can hold at once; cached.
+std::map<std::tuple<int, const void *, int, int>, int> g_cluster_cap;
+
+int sk_threads(int bn) { return 32 * (1 + 5 * sk::lanes_for(bn)); }
+
+int cluster_capacity(int dev, const void *f, int cs, int smem, int threads) {
+  const auto key = std::make_tuple(dev, f, cs, smem);
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_cluster_cap.find(key);
+    if (it != g_cluster_cap.end()) return it->second;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(cs), 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(threads));
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(cs);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, f, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_cluster_cap[key] = n;
+  return n;
+}
+
+bl_status run_skinny(const plan::Plan &pl, int dev, int xm, bool out_i32, const uint8_t *packed,
+                     const float *gamma, const void *x, const int8_t *xq, const float *scale, float *y,
+                     int32_t *acc, cudaStream_t st) {
+  void *f = sk_func(pl.bn, xm, out_i32);
+  if (!f) return BL_ERR_UNSUPPORTED;
+  bl_status s = ensure_smem(dev, f, plan::kSmemMax);
+  if (s != BL_OK) return s;
+  const int num_kt = static_cast<int>(pl.Kp / 64);
+  // The plan's cluster size assumes every SM can host a block of a cluster;
+  // a smaller cluster wins when fewer clusters of the planned size fit at
+  // once.  Cost of a choice: waves x (k tiles per block + fixed cost).
+  int best_cs = pl.sk_cs, best_kp = pl.sk_kt_per;
+  double best_cost = 0.0;
+  for (int c = pl.sk_cs; c >= 1; --c) {
+    const int kp = (num_kt + c - 1) / c;
+    const int cc = (num_kt + kp - 1) / kp;
+    if (plan::sk_ring(pl.bn, kp, cc) == 0) continue;
+    const int cap = cluster_capacity(dev, f, cc, plan::sk_launch_smem(pl.bn, kp, cc), sk_threads(pl.bn));
+    if (cap <= 0) continue;
+    const double waves = static_cast<double>((pl.tiles_n + cap - 1) / cap);
+    const double cost = waves * (kp + 24.0);
+    if (best_cost == 0.0 || cost < best_cost) {
+      best_cost = cost;
+      best_cs = cc;
+      best_kp = kp;
+    }
+  }
+  CUtensorMap mw, mx;
+  std::memset(&mx, 0, sizeof(mx));
+  if (!make_map_w(&mw, packed, pl.N, pl.row_bytes)) return BL_ERR_CUDA;
+  // bf16 rows with 16-byte aligned starts come by TMA into the B operand
+  const bool x_tma = !out_i32 && xm == gemv::kXBF16 && pl.K % 8 == 0 && aligned(x, 16);
+  if (x_tma && !make_map_x(&mx, x, pl.M, pl.K, pl.bn)) return BL_ERR_CUDA;
+  sk::Params p{};
+  p.x = out_i32 || xm == gemv::kXInt8 ? static_cast<const void *>(xq) : x;
+  p.scale = scale;
+  p.gamma = gamma;
+  p.y = y;
+  p.acc = acc;
+  p.M = static_cast<int>(pl.M);
+  p.N = static_cast<int>(pl.N);
+  p.K = static_cast<int>(pl.K);
+  p.num_kt = num_kt;
+  p.kt_per = best_kp;
+  p.cs = best_cs;
+  p.ws = plan::sk_ring(pl.bn, best_kp, best_cs);
+  p.x_tma = x_tma ? 1 : 0;
+  const int smem = plan::sk_launch_smem(pl.bn, best_kp, best_cs);
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(best_cs), static_cast<unsigned>(pl.tiles_n), 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(sk_threads(pl.bn)));
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(best_cs);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  int na = 1;
+  if (g_overlap.load() != 0) {
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    na = 2;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  if (cudaLaunchKernelEx(&cfg, reinterpret_cast<void (*)(CUtensorMap, CUtensorMap, sk::Params)>(f), mw, mx,
+                         p) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return BL_ERR_CUDA;
+  }
+  return BL_OK;
+}
+
 // Shared body of forward / forward_q / matmul_i32 on the tensor-core path.
 // xm: activation source (f32 / bf16 to be quantised, or int8 codes).
 bl_status forward_tc(const plan::Plan &pl, int dev, int xm, bool out_i32, const uint8_t *packed,
@@ -337,6 +466,8 @@ bl_status forward_common(const uint8_t *packed, const float *gamma, int64_t N, i
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (pl.path == plan::kGemv)
     return run_gemv(pl, dev, sms, xm, out_i32, packed, gamma, x, xq, scale, y, acc, st);
+  if (pl.path == plan::kSkinny)
+    return run_skinny(pl, dev, xm, out_i32, packed, gamma, x, xq, scale, y, acc, st);
   return forward_tc(pl, dev, xm, out_i32, packed, gamma, x, xq, scale, y, acc, ws, ws_bytes, st);
 }
 

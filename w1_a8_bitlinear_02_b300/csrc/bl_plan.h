@@ -9,7 +9,7 @@
 namespace bl {
 namespace plan {
 
-enum Path { kGemv = 0, kTc = 1 };
+enum Path { kGemv = 0, kTc = 1, kSkinny = 2 };
 
 // Reference SM count used for split-K decisions (B300: 148 SMs).  A fixed
 // value keeps workspace sizes independent of the device.
@@ -19,6 +19,15 @@ constexpr int kGemvMaxStages = 6;
 constexpr int kGemvMaxSplitRows = 32;
 constexpr int kGemvSmemFixed = 8 * 1024;
 constexpr int kSmemMax = 227 * 1024;
+// Few-token tensor-core kernel: cluster size bound, weight ring stages, the
+// barrier block, and a shared-memory floor that keeps one block per SM (each
+// block takes all 512 tensor-memory columns).
+constexpr int kSkMaxCs = 8;
+constexpr int kSkStageBytes = 8192;  // four 64-k tiles of 128 packed rows
+constexpr int kSkMaxWs = 16;
+constexpr int kSkBarsBytes = 4096;
+constexpr int kSkSmemFloor = 120 * 1024;
+constexpr int kSkMaxM = 64;
 
 inline int64_t row_bytes(int64_t K) { return ((K + 63) / 64) * 16; }
 
@@ -35,6 +44,8 @@ struct Plan {
   int64_t tiles_n = 0, tiles_m = 0;
   int tiles_total = 0;
   int splits = 1, kt_per_split = 0;
+  // few-token kernel: blocks per cluster (K split) and k tiles per block
+  int sk_cs = 1, sk_kt_per = 0;
   // workspace (bytes, 256-aligned offsets)
   size_t off_xb = 0, off_sc = 0, off_acc = 0, off_cnt = 0, ws_bytes = 0;
 };
@@ -42,6 +53,52 @@ struct Plan {
 // Units per lane so the activation slice stays within 64 registers
 // (8 registers per unit and token).
 inline int upt_max(int mt) { return mt == 1 ? 8 : (mt == 2 ? 4 : (mt == 4 ? 2 : 1)); }
+
+// Few-token kernel: shared memory of a launch (alignment slack, the B operand
+// resident for the block's k tiles, a ring of ws weight stages, the split-K
+// partial sums a block receives -- cs x ceil(bn / cs) token rows of 128 int32
+// -- and the barrier block) and the ring depth that fits.
+inline int64_t sk_red_bytes(int bn, int cs) {
+  return cs > 1 ? static_cast<int64_t>(cs) * ((bn + cs - 1) / cs) * 128 * 4 : 0;
+}
+inline int64_t sk_smem(int bn, int64_t kt_per, int ws, int cs) {
+  return 1024 + static_cast<int64_t>(bn) * 128 * kt_per + static_cast<int64_t>(ws) * kSkStageBytes +
+         sk_red_bytes(bn, cs) + kSkBarsBytes;
+}
+// Lanes (issuer, unpack group, tensor-memory A slot) of the few-token kernel:
+// the ring depth is a multiple of them, at least two stages per lane.
+inline int sk_lanes(int bn) { return bn <= 32 ? 3 : 2; }
+inline int sk_ring(int bn, int64_t kt_per, int cs) {
+  const int64_t room = kSmemMax - sk_smem(bn, kt_per, 0, cs);
+  const int ni = sk_lanes(bn);
+  int64_t ws = room / kSkStageBytes;
+  if (ws > kSkMaxWs) ws = kSkMaxWs;
+  ws -= ws % ni;
+  return ws < 2 * ni ? 0 : static_cast<int>(ws);
+}
+inline int sk_launch_smem(int bn, int64_t kt_per, int cs) {
+  const int64_t b = sk_smem(bn, kt_per, sk_ring(bn, kt_per, cs), cs);
+  return static_cast<int>(b < kSkSmemFloor ? kSkSmemFloor : b);
+}
+
+// Few-token kernel: blocks per cluster and k tiles per block for a given
+// cluster size bound; false if the B operand does not fit.
+inline bool sk_split(int bn, int64_t tiles_n, int num_kt, int cs_max, int *cs, int *kt_per) {
+  int c0 = tiles_n >= kRefSms ? 1 : static_cast<int>(kRefSms / tiles_n);
+  if (c0 > cs_max) c0 = cs_max;
+  if (c0 > num_kt) c0 = num_kt;
+  if (c0 < 1) c0 = 1;
+  for (int c = c0; c <= cs_max && c <= num_kt; ++c) {
+    const int kp = (num_kt + c - 1) / c;
+    const int cc = (num_kt + kp - 1) / kp;
+    if (sk_ring(bn, kp, cc) > 0) {
+      *kt_per = kp;
+      *cs = cc;
+      return true;
+    }
+  }
+  return false;
+}
 
 inline Plan make(int64_t M, int64_t N, int64_t K) {
   Plan p;
@@ -51,6 +108,22 @@ inline Plan make(int64_t M, int64_t N, int64_t K) {
   p.row_bytes = row_bytes(K);
   p.Kp = p.row_bytes * 4;
   const int64_t units = p.row_bytes / 8;
+  if (M >= 2 && M <= kSkMaxM) {
+    const int bn = M <= 16 ? 16 : (M <= 32 ? 32 : 64);
+    const int64_t tiles_n = (N + 127) / 128;
+    const int num_kt = static_cast<int>(p.Kp / 64);
+    int cs = 1, kp = 0;
+    if (tiles_n <= 65535 && sk_split(bn, tiles_n, num_kt, kSkMaxCs, &cs, &kp)) {
+      p.path = kSkinny;
+      p.bn = bn;
+      p.tiles_n = tiles_n;
+      p.tiles_m = 1;
+      p.sk_cs = cs;
+      p.sk_kt_per = kp;
+      p.ws_bytes = 0;
+      return p;
+    }
+  }
   if (M <= 8) {
     p.mt = M == 1 ? 1 : (M == 2 ? 2 : (M <= 4 ? 4 : 8));
     const int64_t per_warp = 32 * static_cast<int64_t>(upt_max(p.mt));
