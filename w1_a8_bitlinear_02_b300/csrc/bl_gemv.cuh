@@ -37,7 +37,7 @@ namespace bl {
 namespace gemv {
 
 constexpr int kMaxStages = 6;
-constexpr int kStageBytes = 32 * 1024;  // upper bound of one stage
+constexpr int kStageBytes = 64 * 1024;  // upper bound of one stage
 constexpr int kMaxSplitRows = 32;       // rows per stage when rows are split over warps
 constexpr int kSmemFixed = 8 * 1024;    // barriers, reductions, split-row partials
 
@@ -99,11 +99,71 @@ __device__ __forceinline__ uint2 lds_u64(uint32_t addr) {
   return v;
 }
 
+// One row's sum over this lane's units (lbase: the lane's first unit; unit u
+// at + 256 u).  FULL: every unit exists; otherwise umask bit u says so.
+//   MT <= 2: the bytes of (word & (3 << 2i)) are codes x 4^i; dp4a into
+//   accumulator i and divide by 4^i exactly at the end.
+//   MT > 2: the codes are shifted down once per word and shared by the tokens.
+template <int MT, int UPT, bool FULL>
+__device__ __forceinline__ void row_dot(uint32_t lbase, uint32_t umask, const uint32_t (&xa)[MT][UPT][8],
+                                        int (&tot)[MT]) {
+  if constexpr (MT <= 2) {
+    int a0[MT], a1[MT], a2[MT], a3[MT];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) a0[m] = a1[m] = a2[m] = a3[m] = 0;
+#pragma unroll
+    for (int u = 0; u < UPT; ++u) {
+      if (FULL || ((umask >> u) & 1u)) {
+        const uint2 wv = lds_u64(lbase + 256u * u);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t word = h ? wv.y : wv.x;
+          const uint32_t c0 = word & 0x03030303u, c1 = word & 0x0C0C0C0Cu;
+          const uint32_t c2 = word & 0x30303030u, c3 = word & 0xC0C0C0C0u;
+#pragma unroll
+          for (int m = 0; m < MT; ++m) {
+            a0[m] = dp4a_us(c0, xa[m][u][4 * h + 0], a0[m]);
+            a1[m] = dp4a_us(c1, xa[m][u][4 * h + 1], a1[m]);
+            a2[m] = dp4a_us(c2, xa[m][u][4 * h + 2], a2[m]);
+            a3[m] = dp4a_us(c3, xa[m][u][4 * h + 3], a3[m]);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < MT; ++m) tot[m] = a0[m] + (a1[m] >> 2) + (a2[m] >> 4) + (a3[m] >> 6);
+  } else {
+    int a[MT];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) a[m] = 0;
+#pragma unroll
+    for (int u = 0; u < UPT; ++u) {
+      if (FULL || ((umask >> u) & 1u)) {
+        const uint2 wv = lds_u64(lbase + 256u * u);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t word = h ? wv.y : wv.x;
+          const uint32_t c0 = word & 0x03030303u, c1 = (word >> 2) & 0x03030303u;
+          const uint32_t c2 = (word >> 4) & 0x03030303u, c3 = (word >> 6) & 0x03030303u;
+#pragma unroll
+          for (int m = 0; m < MT; ++m) {
+            a[m] = dp4a_us(c0, xa[m][u][4 * h + 0], a[m]);
+            a[m] = dp4a_us(c1, xa[m][u][4 * h + 1], a[m]);
+            a[m] = dp4a_us(c2, xa[m][u][4 * h + 2], a[m]);
+            a[m] = dp4a_us(c3, xa[m][u][4 * h + 3], a[m]);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < MT; ++m) tot[m] = a[m];
+  }
+}
+
 // MT: tokens held (M <= MT); UPT: 8-byte units per lane; CW: consumer warps.
 template <int MT, int UPT, int XM, bool OUT_I32, int CW>
 __global__ void __launch_bounds__((CW + 1) * 32, 1) gemv_kernel(const Params p) {
   constexpr int kConsumers = CW * 32;
-  constexpr bool kMasked = MT <= 2;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   Smem &sm = *reinterpret_cast<Smem *>(smem_raw);
   const uint32_t ring = smem_u32(smem_raw + kSmemFixed);
@@ -202,21 +262,50 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) gemv_kernel(const Params p) 
       if (lane == 0) sm.xsum[warp][m] = part;
     }
   } else {
-    // per-token absmax: 8-element vectors strided over K, block reduction;
-    // then the codes from a second pass over the same vectors (L1 hits)
+    // per-token absmax over 8-element vectors strided over K, block reduction,
+    // then the codes.  When a thread's vectors of all tokens fit in JM
+    // registers each they are all requested at once and kept for the second
+    // step: one round trip to memory; else a second pass over the same
+    // vectors (L1 hits).
     const bool vec = (reinterpret_cast<uintptr_t>(p.x) & 15u) == 0u && (p.K % 8) == 0;
     const int nv = vec ? p.K / 8 : 0;
+    // A row of units <= 32 UPT (one warp per row) has K / 8 <= 4 UPT vectors,
+    // at most (UPT + 1) / 2 per thread of 8 consumer warps.
+    constexpr int JM = (UPT + 1) / 2 / MT > 0 ? (UPT + 1) / 2 / MT : 1;  // vectors per token in registers
+    const bool in_regs = nv <= JM * kConsumers;
+    float xv[MT][JM][8];
+    if (in_regs) {
+#pragma unroll
+      for (int m = 0; m < MT; ++m)
+#pragma unroll
+        for (int j = 0; j < JM; ++j) {
+          const int c = tid + j * kConsumers;
+          if (m < p.M && c < nv) {
+            load8x<XM>(p.x, static_cast<int64_t>(m) * p.K + 8 * c, xv[m][j]);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) xv[m][j][e] = 0.0f;
+          }
+        }
+    }
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
       float a = 0.0f;
       if (m < p.M) {
         const int64_t row = static_cast<int64_t>(m) * p.K;
-#pragma unroll 2
-        for (int c = tid; c < nv; c += kConsumers) {
-          float v[8];
-          load8x<XM>(p.x, row + 8 * c, v);
+        if (in_regs) {
 #pragma unroll
-          for (int j = 0; j < 8; ++j) a = fmaxf(a, fabsf(v[j]));
+          for (int j = 0; j < JM; ++j)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) a = fmaxf(a, fabsf(xv[m][j][e]));
+        } else {
+#pragma unroll 2
+          for (int c = tid; c < nv; c += kConsumers) {
+            float v[8];
+            load8x<XM>(p.x, row + 8 * c, v);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) a = fmaxf(a, fabsf(v[j]));
+          }
         }
         for (int k = 8 * nv + tid; k < p.K; k += kConsumers) a = fmaxf(a, fabsf(load_x<XM>(p.x, row + k)));
       }
@@ -237,10 +326,7 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) gemv_kernel(const Params p) 
       if (m < p.M) {
         const int64_t row = static_cast<int64_t>(m) * p.K;
         const uint32_t xrow = xs + static_cast<uint32_t>(m * p.kp);
-#pragma unroll 2
-        for (int c = tid; c < nv; c += kConsumers) {
-          float v[8];
-          load8x<XM>(p.x, row + 8 * c, v);
+        auto put8 = [&](int c, const float (&v)[8]) {
           uint32_t lo = 0, hi = 0;
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
@@ -250,6 +336,20 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) gemv_kernel(const Params p) 
             hi |= (static_cast<uint32_t>(q1) & 0xFFu) << (8 * j);
           }
           sts_u64(xrow + 8 * c, lo, hi);
+        };
+        if (in_regs) {
+#pragma unroll
+          for (int j = 0; j < JM; ++j) {
+            const int c = tid + j * kConsumers;
+            if (c < nv) put8(c, xv[m][j]);
+          }
+        } else {
+#pragma unroll 2
+          for (int c = tid; c < nv; c += kConsumers) {
+            float v[8];
+            load8x<XM>(p.x, row + 8 * c, v);
+            put8(c, v);
+          }
         }
         for (int k = 8 * nv + tid; k < p.kp; k += kConsumers) {
           const int q = k < p.K ? quant_one(load_x<XM>(p.x, row + k), sc[m]) : 0;
@@ -304,6 +404,16 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) gemv_kernel(const Params p) 
     }
   }
 
+  // This lane's units are ubase + lane + 32 u.  When every lane's UPT units
+  // lie inside the chunk (the common case) the row loop runs without
+  // per-unit checks; otherwise a per-lane mask says which units exist.
+  const uint32_t lane_addr = 8u * static_cast<uint32_t>(ubase + lane);
+  const bool all_in = ubase + 32 * UPT <= uend;
+  uint32_t umask = 0u;
+#pragma unroll
+  for (int u = 0; u < UPT; ++u)
+    if (ubase + lane + 32 * u < uend) umask |= 1u << u;
+
   // ---- stream the rows
   for (int it = 0; it < n_iters; ++it) {
     const int s = it % S;
@@ -315,61 +425,13 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) gemv_kernel(const Params p) 
     if (rows_here > p.stage_rows) rows_here = p.stage_rows;
     const uint32_t sbase = ring + s * p.stage_bytes;
     for (int r = split_ok ? row_slot : rows_here; r < rows_here; r += row_step) {
-      const uint32_t rbase = sbase + static_cast<uint32_t>(r) * p.row_bytes;
+      // this lane's units: lane_base + 256 u; only the last can fall past the chunk
+      const uint32_t lbase = sbase + static_cast<uint32_t>(r) * p.row_bytes + lane_addr;
       int tot[MT];
-      if constexpr (kMasked) {
-        int a0[MT], a1[MT], a2[MT], a3[MT];
-#pragma unroll
-        for (int m = 0; m < MT; ++m) a0[m] = a1[m] = a2[m] = a3[m] = 0;
-#pragma unroll
-        for (int u = 0; u < UPT; ++u) {
-          const int unit = ubase + lane + 32 * u;
-          if (unit < uend) {
-            const uint2 wv = lds_u64(rbase + 8u * unit);
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const uint32_t word = h ? wv.y : wv.x;
-              const uint32_t c0 = word & 0x03030303u, c1 = word & 0x0C0C0C0Cu;
-              const uint32_t c2 = word & 0x30303030u, c3 = word & 0xC0C0C0C0u;
-#pragma unroll
-              for (int m = 0; m < MT; ++m) {
-                a0[m] = dp4a_us(c0, xa[m][u][4 * h + 0], a0[m]);
-                a1[m] = dp4a_us(c1, xa[m][u][4 * h + 1], a1[m]);
-                a2[m] = dp4a_us(c2, xa[m][u][4 * h + 2], a2[m]);
-                a3[m] = dp4a_us(c3, xa[m][u][4 * h + 3], a3[m]);
-              }
-            }
-          }
-        }
-#pragma unroll
-        for (int m = 0; m < MT; ++m) tot[m] = a0[m] + (a1[m] >> 2) + (a2[m] >> 4) + (a3[m] >> 6);
-      } else {
-        int a[MT];
-#pragma unroll
-        for (int m = 0; m < MT; ++m) a[m] = 0;
-#pragma unroll
-        for (int u = 0; u < UPT; ++u) {
-          const int unit = ubase + lane + 32 * u;
-          if (unit < uend) {
-            const uint2 wv = lds_u64(rbase + 8u * unit);
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const uint32_t word = h ? wv.y : wv.x;
-              const uint32_t c0 = word & 0x03030303u, c1 = (word >> 2) & 0x03030303u;
-              const uint32_t c2 = (word >> 4) & 0x03030303u, c3 = (word >> 6) & 0x03030303u;
-#pragma unroll
-              for (int m = 0; m < MT; ++m) {
-                a[m] = dp4a_us(c0, xa[m][u][4 * h + 0], a[m]);
-                a[m] = dp4a_us(c1, xa[m][u][4 * h + 1], a[m]);
-                a[m] = dp4a_us(c2, xa[m][u][4 * h + 2], a[m]);
-                a[m] = dp4a_us(c3, xa[m][u][4 * h + 3], a[m]);
-              }
-            }
-          }
-        }
-#pragma unroll
-        for (int m = 0; m < MT; ++m) tot[m] = a[m];
-      }
+      if (all_in)
+        row_dot<MT, UPT, true>(lbase, umask, xa, tot);
+      else
+        row_dot<MT, UPT, false>(lbase, umask, xa, tot);
 #pragma unroll
       for (int m = 0; m < MT; ++m) tot[m] = __reduce_add_sync(0xffffffffu, tot[m]);
       if (lane == 0) {

@@ -14,7 +14,7 @@ enum Path { kGemv = 0, kTc = 1, kSkinny = 2 };
 // Reference SM count used for split-K decisions (B300: 148 SMs).  A fixed
 // value keeps workspace sizes independent of the device.
 constexpr int kRefSms = 148;
-constexpr int kGemvStageBytes = 32 * 1024;   // upper bound of one GEMV ring stage
+constexpr int kGemvStageBytes = 64 * 1024;   // upper bound of one GEMV ring stage
 constexpr int kGemvMaxStages = 6;
 constexpr int kGemvMaxSplitRows = 32;
 constexpr int kGemvSmemFixed = 8 * 1024;
