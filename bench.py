@@ -16,6 +16,9 @@ the same weights, prefill M = 2048 (tensor-core path; dense-equivalent
 
 --impl reference times the CPU oracle instead (the repository's plain C
 restatement of the method) on a bounded sample of the same workload.
+
+--profile CASE runs one case of these workloads a few times, untimed, and
+exits: the command the kernel profiles under profiles/ are captured with.
 """
 from __future__ import annotations
 
@@ -36,7 +39,7 @@ WORKLOAD = "decode_2b"
 # DRAM bytes (read + write) per decode-GEMV launch, mean over the four ~2B
 # shapes, from one ncu capture (profiles/gemv_decode_2b_m1.md).  Valid only for
 # the kernel source whose sha256 starts with `src`; otherwise reported as null.
-GEMV_TRAFFIC = {"bytes_per_launch": 3270720.0, "src": "219efa783253491c",
+GEMV_TRAFFIC = {"bytes_per_launch": 3276992.0, "src": "c34abe758c10f6cc",
                 "file": "w1_a8_bitlinear_02_b300/csrc/bl_gemv.cuh"}
 
 
@@ -234,6 +237,41 @@ def host_items(items, limit: int):
         out.append((it["packed"].cpu().numpy(), float(it["gamma"].item()), mt.N, mt.K,
                     it["x"].float().cpu().numpy()))
     return out
+
+
+# ------------------------------------------------------------------ profiling cases
+PROFILE_CASES = {
+    # name: (M, N, K, activation kind, weight std, calls)
+    "decode_2b_qkv": (1, 3840, 2560, "normal", 0.02, 6),
+    "decode_100b_up": (1, 28672, 8192, "normal", 0.01, 6),
+    "decode_100b_down": (1, 8192, 28672, "normal", 0.01, 6),
+    "batch_m16_qkv": (16, 3840, 2560, "outliers1pct", 0.02, 6),
+    "batch_m64_up": (64, 6912, 2560, "outliers1pct", 0.02, 6),
+    "prefill_up": (2048, 6912, 2560, "normal", 0.02, 6),
+    "prefill_down": (2048, 2560, 6912, "relu2", 0.02, 6),
+}
+
+
+def run_profile_case(name: str):
+    """A few untimed forward calls of one case on cuda:0 (for ncu captures)."""
+    import torch
+    import w1_a8_bitlinear_02_b300 as bl
+    from w1_a8_bitlinear_02_b300 import workloads as wl
+    M, N, K, kind, std, calls = PROFILE_CASES[name]
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    W = wl.weight(N, K, std, wl.weight_seed("decode_2b", 0, 0) + N, dev)
+    packed, gamma = bl.bitlinear_pack_weights(W)
+    del W
+    x = wl.activations(M, K, kind, 4500 + K, dev, torch.bfloat16)
+    y = torch.empty((M, N), dtype=torch.float32, device=dev)
+    wsn = bl.workspace_bytes(M, N, K)
+    ws = torch.empty(wsn, dtype=torch.uint8, device=dev) if wsn else None
+    for _ in range(calls):
+        bl.bitlinear_forward(packed, gamma, N, K, x, y=y, workspace=ws)
+    torch.cuda.synchronize()
+    assert bl.device_error() == 0
+    print(json.dumps({"profile_case": name, "M": M, "N": N, "K": K, "calls": calls}), flush=True)
 
 
 # ------------------------------------------------------------------ reference arm
@@ -506,7 +544,12 @@ def main():
     ap.add_argument("--no-100b", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--profile", choices=sorted(PROFILE_CASES),
+                    help="run one case a few times untimed (for ncu) and exit")
     args = ap.parse_args()
+    if args.profile:
+        run_profile_case(args.profile)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 

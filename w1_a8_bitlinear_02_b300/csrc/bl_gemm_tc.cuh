@@ -16,10 +16,12 @@
 //   warp 1      allocates TMEM; one lane issues the MMAs (4 x K=16 per stage,
 //               A from tensor memory, B from shared memory) and commits each
 //               stage back to the producer.
-//   warps 2..9  unpack: warp w expands, for the 32 weight rows of TMEM lane
-//               quarter w % 4, one half (32 weights) of each row's 16 packed
-//               bytes into bf16 and stores them straight into the stage's A
-//               buffer in tensor memory ("pack-store-load-unpack-compute":
+//   warps 2..9  unpack, two groups of four taking alternate stages (so one
+//               stage's load-convert-store latency overlaps the next's): warp
+//               w expands, for the 32 weight rows of TMEM lane quarter w % 4,
+//               each row's 16 packed bytes (64 weights) into bf16 and stores
+//               them straight into the stage's A buffer in tensor memory
+//               ("pack-store-load-unpack-compute":
 //               packed in HBM, unpacked on chip -- "微软AI大模型炸场：0.4GB，
 //               CPU就能跑", blog.csdn.net/2401_84494441, section 3, GPU
 //               bullet).  Shared memory then only holds the activation and
@@ -60,7 +62,8 @@ struct Cfg {
   static constexpr int kBySmem = kSmemBudget / kStageBytes;
   static constexpr int kByTmem = (kTmemCols - kDCols) / 32;
   static constexpr int kMin = kBySmem < kByTmem ? kBySmem : kByTmem;
-  static constexpr int kStages = kMin < 8 ? kMin : 8;
+  // even, so each ring slot always serves the same unpack group
+  static constexpr int kStages = (kMin < 8 ? kMin : 8) & ~1;
   // stages + up to 1023 bytes of alignment slack + the barrier block
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 3072;
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
@@ -126,7 +129,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(smem_u32(&bars.full[s]), 1);
-      mbar_init(smem_u32(&bars.afull[s]), kUnpackThreads);
+      mbar_init(smem_u32(&bars.afull[s]), kUnpackThreads / 2);
       mbar_init(smem_u32(&bars.empty[s]), 1);
     }
     mbar_init(smem_u32(&bars.accfull), 1);
@@ -186,11 +189,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN);
+      // afull implies full: the unpack warps arrive only after waiting for a
+      // stage's TMA bytes (activation tile included), and mbarrier
+      // release/acquire chains are transitive.  (Moving this wait between a
+      // stage's MMAs, to overlap it with them, measured slower.)
       for (int i = 0; i < nkt; ++i) {
         const int s = i % S;
-        const uint32_t ph = (i / S) & 1;
-        if (!mbar_wait(smem_u32(&bars.afull[s]), ph) || !mbar_wait(smem_u32(&bars.full[s]), ph) ||
-            *abort_flag) {
+        if (!mbar_wait(smem_u32(&bars.afull[s]), (i / S) & 1)) {
           *abort_flag = 1;
           break;
         }
@@ -208,29 +213,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ unpack
     const int u = tid - 64;            // 0 .. 255
     const int q = warp & 3;            // TMEM lane quarter this warp may access
-    const int h = (warp - 2) >> 2;     // which 32 of the row's 64 weights
+    const int h = (warp - 2) >> 2;     // unpack group: stages i = h (mod 2)
     const int row = 32 * q + lane;     // weight row of the tile
     const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
-    for (int i = 0; i < nkt; ++i) {
+    for (int i = h; i < nkt; i += 2) {
       const int s = i % S;
       if (!mbar_wait(smem_u32(&bars.full[s]), (i / S) & 1) || *abort_flag) {
         *abort_flag = 1;
         break;
       }
-      // words 2h, 2h+1 of the row's 16 packed bytes: k = 32h .. 32h+31
-      uint32_t w0, w1;
-      asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
-                   : "=r"(w0), "=r"(w1)
-                   : "r"(p_base + s * kPBytes + row * 16 + 8 * h));
-      uint32_t v[16];
+      const uint4 wv = lds_u128(p_base + s * kPBytes + row * 16);
+      const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
+      uint32_t v[32];
 #pragma unroll
-      for (int wi = 0; wi < 2; ++wi) {
-        const uint32_t word = wi ? w1 : w0;
+      for (int wi = 0; wi < 4; ++wi) {
 #pragma unroll
         for (int i4 = 0; i4 < 4; ++i4)  // k = 16 wi + 4 i4 .. +3
-          codes4_to_bf16((word >> (2 * i4)) & 0x03030303u, v[8 * wi + 2 * i4], v[8 * wi + 2 * i4 + 1]);
+          codes4_to_bf16((words[wi] >> (2 * i4)) & 0x03030303u, v[8 * wi + 2 * i4], v[8 * wi + 2 * i4 + 1]);
       }
-      tmem_st_32x32b_x16(tmem + lane_off + C::kDCols + 32u * s + 16u * h, v);
+      tmem_st_32x32b_x32(tmem + lane_off + C::kDCols + 32u * s, v);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(smem_u32(&bars.afull[s]));

@@ -375,4 +375,23 @@ __device__ __noinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity) {
   }
 }
 
+// ------------------------------------------------------------ TMA stores
+// 2-D tiled store shared -> global (box of the map), tracked by the bulk
+// async-group of the issuing thread.  The box is clipped to the tensor.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t src, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(src), "r"(x), "r"(y)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Waits until every committed bulk store of this thread has read its shared
+// memory source (the writes to global memory complete asynchronously).
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 }  // namespace bl
