@@ -10,7 +10,7 @@
 #include "bl_plan.h"
 using namespace bl::plan;
 int main() {
-  long checked = 0, gemv = 0, tc = 0, sk = 0;
+  long checked = 0, gemv = 0, tc = 0, sk = 0, streamk = 0;
   const int sms = 148;
   for (long M = 1; M <= 300; M += (M < 16 ? 1 : 37))
     for (long K : {1L, 15L, 16L, 63L, 64L, 65L, 100L, 333L, 512L, 1000L, 2560L, 4096L, 6912L, 8192L, 9000L, 16384L, 28672L, 32768L, 65536L, 131072L})
@@ -53,13 +53,25 @@ int main() {
           if (!ok) { printf("BAD skinny M=%ld N=%ld K=%ld cs=%d kp=%d\n", M, N, K, p.sk_cs, p.sk_kt_per); return 1; }
         } else {
           ++tc;
+          streamk += p.streamk;
           bool ok = p.bn >= 16 && p.bn <= 256 && p.splits >= 1 && p.kt_per_split >= 1 &&
                     (long)p.splits * p.kt_per_split >= p.Kp / 64 && (long)(p.splits - 1) * p.kt_per_split < p.Kp / 64 &&
                     p.tiles_n * 128 >= N && p.tiles_m * p.bn >= M;
+          if (p.streamk) {
+            // every block's share spans at least one whole tile (so a tile is
+            // split between at most two neighbouring blocks) and the shares cover
+            // every unit once (trailing blocks may get none); the workspace holds
+            // one partial tile and one flag per block
+            const long nkt = p.Kp / 64;
+            ok = ok && p.splits == 1 && p.sk_grid == kRefSms && p.units == (long)p.tiles_total * nkt &&
+                 p.units_per >= nkt && (long)p.units_per * p.sk_grid >= p.units &&
+                 p.off_cnt >= p.off_part + (size_t)p.sk_grid * p.bn * 128 * 4 &&
+                 p.ws_bytes >= p.off_cnt + (size_t)p.sk_grid * 4;
+          }
           if (!ok) { printf("BAD tc M=%ld N=%ld K=%ld\n", M, N, K); return 1; }
         }
       }
-  printf("ok: %ld plans (%ld gemv, %ld tensor-core, %ld few-token)\n", checked, gemv, tc, sk);
+  printf("ok: %ld plans (%ld gemv, %ld tensor-core of which %ld stream-K, %ld few-token)\n", checked, gemv, tc, streamk, sk);
   // the specific shapes of the tests and bench
   for (long M : {1L, 3L, 8L}) for (long K : {2560L, 6912L, 8192L, 28672L}) {
     Plan p = make(M, 2560, K);

@@ -252,6 +252,24 @@ def test_batched_decode_2b_shapes_full(bl, name, N, K, kind):
         assert_bits_equal(y_q.cpu().numpy(), y_ref, f"{name} M={M} forward_q")
 
 
+@pytest.mark.parametrize("M,N,K", [(2048, 2560, 320), (1900, 2500, 300), (2048, 2560, 6912)])
+def test_streamk_tiles_full_output(bl, M, N, K):
+    """Tile counts that fill the last wave poorly (160 tiles on 148 SMs) run
+    stream-K: tiles are shared by two blocks whose int32 partials meet in the
+    workspace.  Whole outputs (forward and matmul_i32) against the oracle; the
+    last shape is the prefill down projection itself, checked in full."""
+    packed, gamma, p_ref, g_ref = pack_both(bl, N, K, 0.02, 17 * N + K)
+    x = wl.activations(M, K, "outliers1pct", 3 * M + K, "cpu", torch.bfloat16)
+    y = bl.bitlinear_forward(packed, gamma, N, K, x.to(DEV))
+    xq_ref, s_ref = oracle.quant_act(x.float().numpy())
+    acc = bl.bitlinear_matmul_i32(packed, N, K, torch.from_numpy(xq_ref).to(DEV))
+    torch.cuda.synchronize()
+    assert bl.device_error() == 0
+    acc_ref = oracle.matmul_i32(oracle.unpack(p_ref, K), xq_ref)
+    assert np.array_equal(acc.cpu().numpy(), acc_ref)
+    assert_bits_equal(y.cpu().numpy(), oracle.rescale(acc_ref, g_ref, s_ref), f"stream-K M={M} N={N} K={K}")
+
+
 @pytest.mark.parametrize("N,K,kind", [(6912, 2560, "normal"), (2560, 6912, "relu2")])
 def test_prefill_2048_sampled_tokens(bl, N, K, kind):
     """M = 2048 on the tensor-core path; 12 sampled tokens checked in full

@@ -243,6 +243,26 @@ bl_status run_tc_bn(const plan::Plan &pl, int dev, const CUtensorMap &mx, const 
   constexpr int smem = tc::Cfg<BN>::kSmemBytes;
   bl_status s = ensure_smem(dev, reinterpret_cast<const void *>(f), smem);
   if (s != BL_OK) return s;
+  if (p.streamk) {
+    // One block per SM, all resident at once (a block may wait for its
+    // neighbour's partial): a cooperative launch, ordered after the previous
+    // kernel (which zeroed the flags) without launch overlap.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(pl.sk_grid));
+    cfg.blockDim = dim3(tc::kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, f, mx, mw, p) != cudaSuccess) {
+      cudaGetLastError();
+      return BL_ERR_CUDA;
+    }
+    return BL_OK;
+  }
   dim3 grid(static_cast<unsigned>(pl.tiles_n), static_cast<unsigned>(pl.tiles_m),
             static_cast<unsigned>(pl.splits));
   return launch(f, grid, dim3(tc::kThreads), smem, st, g_overlap.load() != 0, mx, mw, p);
@@ -405,26 +425,37 @@ bl_status forward_tc(const plan::Plan &pl, int dev, int xm, bool out_i32, const 
   if (!make_map_x(&mx, xb, pl.M, pl.Kp, pl.bn) || !make_map_w(&mw, packed, pl.N, pl.row_bytes))
     return BL_ERR_CUDA;
 
+  // Stream-K needs every block resident at once: one block per SM of a
+  // device with at least the planned number of SMs; otherwise whole tiles.
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return BL_ERR_CUDA;
+  }
+  const bool streamk = pl.streamk && sms >= pl.sk_grid;
+
   // 1) activations -> bf16 codes (+ scales), zeroing the split-K accumulators
+  //    or the stream-K flags
   const bool zero_acc = pl.splits > 1;
   int32_t *zrows = zero_acc ? (out_i32 ? acc : wacc) : nullptr;
-  unsigned *zcnt = (zero_acc && !out_i32) ? wcnt : nullptr;
+  unsigned *zcnt = (zero_acc && !out_i32) || streamk ? wcnt : nullptr;
+  const int ncnt = streamk ? pl.sk_grid : pl.tiles_total;
   bl_status s;
   const dim3 qgrid(static_cast<unsigned>(pl.M));
   const float *use_scale = scale;
   if (xm == gemv::kXInt8) {
     s = launch(&codes_to_bf16_kernel, qgrid, dim3(256), 0, st, overlap, xq, pl.K, pl.Kp, xb, zrows,
-               pl.N, zcnt, pl.tiles_total);
+               pl.N, zcnt, ncnt);
   } else {
     use_scale = sc;
     if (xm == gemv::kXF32)
       s = launch(&quant_act_kernel<float, true, false>, qgrid, dim3(256), 0, st, overlap,
                  static_cast<const float *>(x), pl.K, pl.Kp, static_cast<const float *>(nullptr), 0.0f,
-                 static_cast<int8_t *>(nullptr), xb, sc, zrows, pl.N, zcnt, pl.tiles_total);
+                 static_cast<int8_t *>(nullptr), xb, sc, zrows, pl.N, zcnt, ncnt);
     else
       s = launch(&quant_act_kernel<__nv_bfloat16, true, false>, qgrid, dim3(256), 0, st, overlap,
                  static_cast<const __nv_bfloat16 *>(x), pl.K, pl.Kp, static_cast<const float *>(nullptr),
-                 0.0f, static_cast<int8_t *>(nullptr), xb, sc, zrows, pl.N, zcnt, pl.tiles_total);
+                 0.0f, static_cast<int8_t *>(nullptr), xb, sc, zrows, pl.N, zcnt, ncnt);
   }
   if (s != BL_OK) return s;
 
@@ -441,6 +472,12 @@ bl_status forward_tc(const plan::Plan &pl, int dev, int xm, bool out_i32, const 
   p.acc_out = acc;
   p.ws_acc = wacc;
   p.ws_cnt = wcnt;
+  p.streamk = streamk ? 1 : 0;
+  p.tiles_n = static_cast<int>(pl.tiles_n);
+  p.units = pl.units;
+  p.units_per = pl.units_per;
+  p.ws_part = reinterpret_cast<int32_t *>(w + pl.off_part);
+  p.ws_flag = wcnt;
   if (out_i32) return run_tc<true>(pl, dev, mx, mw, p, st);
   return run_tc<false>(pl, dev, mx, mw, p, st);
 }

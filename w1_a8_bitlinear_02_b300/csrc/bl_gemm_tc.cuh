@@ -76,19 +76,75 @@ struct Params {
   int num_kt;        // k tiles in the padded K (Kp / 64)
   int kt_per_split;
   int splits;
+  // Stream-K (one split, a persistent grid of one block per SM): block b takes
+  // the flattened (output tile, k tile) units [b * units_per, (b + 1) *
+  // units_per) ∩ [0, units); tile t is (m tile t / tiles_n, n tile t % tiles_n).
+  int streamk;
+  int tiles_n;
+  int units, units_per;
   const float *gamma;
   const float *scale;  // [M] activation scales (float output only)
   float *y;            // [M, N]
   int32_t *acc_out;    // [M, N] (int32 output)
   int32_t *ws_acc;     // [M, N] split-K partial sums (float output, splits > 1)
   unsigned *ws_cnt;    // per output tile tickets (float output, splits > 1)
+  int32_t *ws_part;    // stream-K: [grid][BN][128] int32 partial tile of each block's first segment
+  unsigned *ws_flag;   // stream-K: [grid] set to 1 once that partial is written (zeroed by the
+                       // previous kernel on the stream)
+};
+
+// A run of k tiles of one output tile and what its epilogue does with it.
+enum SegKind {
+  kSegFull = 0,   // the whole K: write y
+  kSegSplit = 1,  // split-K part: add int32 into ws_acc; the last of the tile's parts writes y
+  kSegTail = 2,   // stream-K, first segment of a block, k0 > 0: int32 partial to ws_part[block]
+  kSegHead = 3    // stream-K, last segment of a block, k from 0: add ws_part[block + 1], write y
+};
+struct Seg {
+  int n0, m0, k0, nk, kind;
+};
+
+// Walks this block's segments in order (one for the plain and split-K grids).
+template <int BN>
+struct SegWalk {
+  int u, u1;
+  __device__ __forceinline__ explicit SegWalk(const Params &p) {
+    if (p.streamk) {
+      u = blockIdx.x * p.units_per;
+      u1 = u + p.units_per < p.units ? u + p.units_per : p.units;
+    } else {
+      u = 0;
+      u1 = 1;
+    }
+  }
+  __device__ __forceinline__ bool next(const Params &p, Seg &sg) {
+    if (u >= u1) return false;
+    if (p.streamk) {
+      const int t = u / p.num_kt;
+      sg.k0 = u - t * p.num_kt;
+      sg.nk = p.num_kt - sg.k0 < u1 - u ? p.num_kt - sg.k0 : u1 - u;
+      sg.n0 = (t % p.tiles_n) * kBM;
+      sg.m0 = (t / p.tiles_n) * BN;
+      sg.kind = (sg.k0 == 0 && sg.nk == p.num_kt) ? kSegFull : (sg.k0 > 0 ? kSegTail : kSegHead);
+      u += sg.nk;
+    } else {
+      sg.n0 = blockIdx.x * kBM;
+      sg.m0 = blockIdx.y * BN;
+      sg.k0 = blockIdx.z * p.kt_per_split;
+      sg.nk = p.num_kt - sg.k0 < p.kt_per_split ? p.num_kt - sg.k0 : p.kt_per_split;
+      sg.kind = p.splits == 1 ? kSegFull : kSegSplit;
+      u = u1;
+    }
+    return true;
+  }
 };
 
 struct Bars {
   uint64_t full[8];
   uint64_t afull[8];
   uint64_t empty[8];
-  uint64_t accfull;
+  uint64_t dfull;   // a segment's MMAs are done (phase per segment)
+  uint64_t dempty;  // the epilogue has read the accumulator (phase per segment)
   uint32_t tmem_base;
   int abort_flag;
   int last_flag;
@@ -106,6 +162,15 @@ __device__ __forceinline__ void codes4_to_bf16(uint32_t codes, uint32_t &w01, ui
   w23 = __byte_perm(kTabHi, kTabLo, t >> 16);
 }
 
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_u32(unsigned *p, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 template <int BN, bool OUT_I32>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
@@ -120,11 +185,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   Bars &bars = *reinterpret_cast<Bars *>(smem_raw + (base - raw) + S * C::kStageBytes);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n0 = blockIdx.x * kBM;
-  const int m0 = blockIdx.y * BN;
-  const int kt0 = blockIdx.z * p.kt_per_split;
-  int nkt = p.num_kt - kt0;
-  if (nkt > p.kt_per_split) nkt = p.kt_per_split;
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
@@ -132,7 +192,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&bars.afull[s]), kUnpackThreads / 2);
       mbar_init(smem_u32(&bars.empty[s]), 1);
     }
-    mbar_init(smem_u32(&bars.accfull), 1);
+    mbar_init(smem_u32(&bars.dfull), 1);
+    mbar_init(smem_u32(&bars.dempty), kUnpackThreads);
     bars.abort_flag = 0;
     bars.last_flag = 0;
     fence_barrier_init();
@@ -158,32 +219,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_w = policy_evict_first();
       const uint64_t pol_x = policy_evict_last();
       constexpr uint32_t kTx = kPBytes + C::kBBytes;
-      const int pre = nkt < S ? nkt : S;
-      // Weights are static inputs: start on them before the previous kernel ends.
-      for (int i = 0; i < pre; ++i) {
-        const uint32_t fb = smem_u32(&bars.full[i]);
-        mbar_arrive_expect_tx(fb, kTx);
-        tma_load_2d(p_base + i * kPBytes, &map_w, (kt0 + i) * 16, n0, fb, pol_w);
+      // Weights are static inputs: request the first S stages' before the
+      // previous kernel ends, their activation tiles after.
+      {
+        SegWalk<BN> w(p);
+        Seg sg;
+        int i = 0;
+        while (i < S && w.next(p, sg))
+          for (int t = 0; t < sg.nk && i < S; ++t, ++i) {
+            const uint32_t fb = smem_u32(&bars.full[i]);
+            mbar_arrive_expect_tx(fb, kTx);
+            tma_load_2d(p_base + i * kPBytes, &map_w, (sg.k0 + t) * 16, sg.n0, fb, pol_w);
+          }
       }
       pdl_wait_primary();
-      for (int i = 0; i < pre; ++i)
-        tma_load_2d(b_base + i * C::kBBytes, &map_x, (kt0 + i) * kBK, m0, smem_u32(&bars.full[i]),
-                    pol_x);
-      int issued = pre;
-      for (int i = pre; i < nkt; ++i) {
-        const int s = i % S;
-        if (!mbar_wait(smem_u32(&bars.empty[s]), ((i / S) - 1) & 1) || *abort_flag) {
-          *abort_flag = 1;
-          break;
+      SegWalk<BN> w(p);
+      Seg sg;
+      int i = 0, issued = 0;
+      bool go = true;
+      while (go && w.next(p, sg)) {
+        for (int t = 0; t < sg.nk; ++t, ++i) {
+          const int s = i % S;
+          const uint32_t fb = smem_u32(&bars.full[s]);
+          if (i >= S) {
+            if (!mbar_wait(smem_u32(&bars.empty[s]), ((i / S) - 1) & 1) || *abort_flag) {
+              *abort_flag = 1;
+              go = false;
+              break;
+            }
+            mbar_arrive_expect_tx(fb, kTx);
+            tma_load_2d(p_base + s * kPBytes, &map_w, (sg.k0 + t) * 16, sg.n0, fb, pol_w);
+          }
+          tma_load_2d(b_base + s * C::kBBytes, &map_x, (sg.k0 + t) * kBK, sg.m0, fb, pol_x);
+          issued = i + 1;
         }
-        const uint32_t fb = smem_u32(&bars.full[s]);
-        mbar_arrive_expect_tx(fb, kTx);
-        tma_load_2d(p_base + s * kPBytes, &map_w, (kt0 + i) * 16, n0, fb, pol_w);
-        tma_load_2d(b_base + s * C::kBBytes, &map_x, (kt0 + i) * kBK, m0, fb, pol_x);
-        issued = i + 1;
       }
-      for (int i = issued - S < 0 ? 0 : issued - S; i < issued; ++i)
-        mbar_wait(smem_u32(&bars.full[i % S]), (i / S) & 1);
+      for (int j = issued - S < 0 ? 0 : issued - S; j < issued; ++j)
+        mbar_wait(smem_u32(&bars.full[j % S]), (j / S) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -193,115 +265,189 @@ __global__ void __launch_bounds__(kThreads, 1)
       // stage's TMA bytes (activation tile included), and mbarrier
       // release/acquire chains are transitive.  (Moving this wait between a
       // stage's MMAs, to overlap it with them, measured slower.)
-      for (int i = 0; i < nkt; ++i) {
-        const int s = i % S;
-        if (!mbar_wait(smem_u32(&bars.afull[s]), (i / S) & 1)) {
+      SegWalk<BN> w(p);
+      Seg sg;
+      int i = 0, j = 0;
+      bool go = true;
+      while (go && w.next(p, sg)) {
+        // the accumulator is reused: the previous segment's epilogue must have read it
+        if (j > 0 && !mbar_wait(smem_u32(&bars.dempty), (j - 1) & 1)) {
           *abort_flag = 1;
           break;
         }
         tc_fence_after();
-        const uint32_t at = tmem + C::kDCols + 32u * s;
-        const uint64_t bd = smem_desc_sw128(b_base + s * C::kBBytes);
+        for (int t = 0; t < sg.nk; ++t, ++i) {
+          const int s = i % S;
+          if (!mbar_wait(smem_u32(&bars.afull[s]), (i / S) & 1)) {
+            *abort_flag = 1;
+            go = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t at = tmem + C::kDCols + 32u * s;
+          const uint64_t bd = smem_desc_sw128(b_base + s * C::kBBytes);
 #pragma unroll
-        for (int j = 0; j < kBK / 16; ++j)
-          mma_bf16_ts(tmem, at + 8u * j, bd + 2u * j, idesc, (i | j) != 0 ? 1u : 0u);
-        mma_commit(smem_u32(&bars.empty[s]));
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            mma_bf16_ts(tmem, at + 8u * kk, bd + 2u * kk, idesc, (t | kk) != 0 ? 1u : 0u);
+          mma_commit(smem_u32(&bars.empty[s]));
+        }
+        mma_commit(smem_u32(&bars.dfull));  // fires once the segment's MMAs are done
+        ++j;
       }
-      mma_commit(smem_u32(&bars.accfull));  // fires once every issued MMA is done
     }
   } else {
-    // ------------------------------------------------------------ unpack
+    // ------------------------------------------------------------ unpack + epilogue
     const int u = tid - 64;            // 0 .. 255
     const int q = warp & 3;            // TMEM lane quarter this warp may access
     const int h = (warp - 2) >> 2;     // unpack group: stages i = h (mod 2)
     const int row = 32 * q + lane;     // weight row of the tile
     const uint32_t lane_off = static_cast<uint32_t>(32 * q) << 16;
-    for (int i = h; i < nkt; i += 2) {
-      const int s = i % S;
-      if (!mbar_wait(smem_u32(&bars.full[s]), (i / S) & 1) || *abort_flag) {
-        *abort_flag = 1;
-        break;
-      }
-      const uint4 wv = lds_u128(p_base + s * kPBytes + row * 16);
-      const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
-      uint32_t v[32];
+    SegWalk<BN> w(p);
+    Seg sg;
+    int i = 0, j = 0;
+    bool alive = true;
+    while (w.next(p, sg)) {
+      for (int t = 0; t < sg.nk; ++t, ++i) {
+        if ((i & 1) != h || !alive) continue;
+        const int s = i % S;
+        if (!mbar_wait(smem_u32(&bars.full[s]), (i / S) & 1) || *abort_flag) {
+          *abort_flag = 1;
+          alive = false;
+          continue;
+        }
+        const uint4 wv = lds_u128(p_base + s * kPBytes + row * 16);
+        const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
+        uint32_t v[32];
 #pragma unroll
-      for (int wi = 0; wi < 4; ++wi) {
+        for (int wi = 0; wi < 4; ++wi) {
 #pragma unroll
-        for (int i4 = 0; i4 < 4; ++i4)  // k = 16 wi + 4 i4 .. +3
-          codes4_to_bf16((words[wi] >> (2 * i4)) & 0x03030303u, v[8 * wi + 2 * i4], v[8 * wi + 2 * i4 + 1]);
+          for (int i4 = 0; i4 < 4; ++i4)  // k = 16 wi + 4 i4 .. +3
+            codes4_to_bf16((words[wi] >> (2 * i4)) & 0x03030303u, v[8 * wi + 2 * i4], v[8 * wi + 2 * i4 + 1]);
+        }
+        tmem_st_32x32b_x32(tmem + lane_off + C::kDCols + 32u * s, v);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bars.afull[s]));
       }
-      tmem_st_32x32b_x32(tmem + lane_off + C::kDCols + 32u * s, v);
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(smem_u32(&bars.afull[s]));
-    }
 
-    // ------------------------------------------------------------ epilogue
-    // scale / split-K workspace come from the previous kernel on the stream
-    pdl_wait_primary();
-    if constexpr (!OUT_I32) {
-      const float g = *p.gamma;
-      for (int j = u; j < BN; j += kUnpackThreads)
-        bars.cscale[j] = (m0 + j < p.M) ? __fdiv_rn(g, p.scale[m0 + j]) : 0.0f;
-    }
-    bool ok = mbar_wait(smem_u32(&bars.accfull), 0);
-    // One decision for all epilogue warps (they share named barriers and
-    // warp-collective TMEM loads below).
-    ok = !named_bar_or(4, kUnpackThreads, !ok || *abort_flag);
-    tc_fence_after();
-    const int n = n0 + row;
-    if (ok) {
-#pragma unroll 1
-      for (int c0 = 32 * h; c0 < BN; c0 += 64) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(tmem + lane_off + c0, r);
-        tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int m = m0 + c0 + j;
-          if (c0 + j < BN && m < p.M && n < p.N) {
-            const int v = static_cast<int>(__uint_as_float(r[j]));
-            const int64_t o = static_cast<int64_t>(m) * p.N + n;
-            if constexpr (OUT_I32) {
-              if (p.splits == 1)
-                p.acc_out[o] = v;
-              else
-                atomicAdd(&p.acc_out[o], v);
-            } else {
-              if (p.splits == 1)
-                p.y[o] = __fmul_rn(static_cast<float>(v), bars.cscale[c0 + j]);
-              else
-                atomicAdd(&p.ws_acc[o], v);
+      // -------------------------------------------------------- epilogue of this segment
+      // scale / workspaces come from the previous kernel on the stream
+      pdl_wait_primary();
+      // every epilogue thread is past the previous segment's epilogue (which
+      // reads cscale) before it is rewritten
+      named_bar(5, kUnpackThreads);
+      if constexpr (!OUT_I32) {
+        const float g = *p.gamma;
+        for (int c = u; c < BN; c += kUnpackThreads)
+          bars.cscale[c] = (sg.m0 + c < p.M) ? __fdiv_rn(g, p.scale[sg.m0 + c]) : 0.0f;
+      }
+      bool ok = alive && mbar_wait(smem_u32(&bars.dfull), j & 1);
+      // One decision for all epilogue warps (they share named barriers and
+      // warp-collective TMEM loads below); also orders the cscale writes.
+      ok = !named_bar_or(4, kUnpackThreads, !ok || *abort_flag);
+      tc_fence_after();
+      const int n = sg.n0 + row;
+      const int m0 = sg.m0;
+      if (ok && sg.kind == kSegHead) {
+        // the rest of this tile's K is the next block's first segment
+        bool late = false;
+        if (u == 0) {
+          const long long t0 = clock64();
+          while (ld_acquire_u32(p.ws_flag + blockIdx.x + 1) == 0u) {
+            if (clock64() - t0 > kWaitLimitCycles) {
+              atomicOr(&g_dev_error, kDevErrTimeout);
+              late = true;
+              break;
             }
           }
         }
+        ok = !named_bar_or(4, kUnpackThreads, late);
       }
-      if constexpr (!OUT_I32) {
-        if (p.splits > 1) {
+      if (ok) {
+        const int32_t *part_in = p.ws_part + static_cast<int64_t>(blockIdx.x + 1) * BN * kBM;
+        int32_t *part_out = p.ws_part + static_cast<int64_t>(blockIdx.x) * BN * kBM;
+        const int kind = sg.kind;
+        // one loop per kind: the accumulator columns c0 .. c0 + 31 of row n
+#pragma unroll 1
+        for (int c0 = 32 * h; c0 < BN; c0 += 64) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(tmem + lane_off + c0, r);
+          tmem_ld_wait();
+          if (kind == kSegTail) {
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj)
+              part_out[(c0 + jj) * kBM + row] = static_cast<int>(__uint_as_float(r[jj]));
+          } else if (kind == kSegSplit) {
+            if (n < p.N) {
+#pragma unroll
+              for (int jj = 0; jj < 32; ++jj) {
+                const int m = m0 + c0 + jj;
+                if (m < p.M) {
+                  const int64_t o = static_cast<int64_t>(m) * p.N + n;
+                  if constexpr (OUT_I32)
+                    atomicAdd(&p.acc_out[o], static_cast<int>(__uint_as_float(r[jj])));
+                  else
+                    atomicAdd(&p.ws_acc[o], static_cast<int>(__uint_as_float(r[jj])));
+                }
+              }
+            }
+          } else {
+            if (kind == kSegHead) {
+#pragma unroll
+              for (int jj = 0; jj < 32; ++jj)
+                r[jj] = __float_as_uint(static_cast<float>(static_cast<int>(__uint_as_float(r[jj])) +
+                                                           __ldcg(part_in + (c0 + jj) * kBM + row)));
+            }
+            if (n < p.N) {
+#pragma unroll
+              for (int jj = 0; jj < 32; ++jj) {
+                const int m = m0 + c0 + jj;
+                if (m < p.M) {
+                  const int64_t o = static_cast<int64_t>(m) * p.N + n;
+                  const int v = static_cast<int>(__uint_as_float(r[jj]));
+                  if constexpr (OUT_I32)
+                    p.acc_out[o] = v;
+                  else
+                    p.y[o] = __fmul_rn(static_cast<float>(v), bars.cscale[c0 + jj]);
+                }
+              }
+            }
+          }
+        }
+        if (sg.kind == kSegTail) {
+          // publish this block's partial for the block that owns the tile
           __threadfence();
           named_bar(3, kUnpackThreads);
-          if (u == 0) {
-            const unsigned t = atomicAdd(&p.ws_cnt[blockIdx.y * gridDim.x + blockIdx.x], 1u);
-            bars.last_flag = (t == static_cast<unsigned>(p.splits - 1)) ? 1 : 0;
-          }
-          named_bar(3, kUnpackThreads);
-          if (bars.last_flag) {
+          if (u == 0) st_release_u32(p.ws_flag + blockIdx.x, 1u);
+        }
+        if constexpr (!OUT_I32) {
+          if (sg.kind == kSegSplit) {
             __threadfence();
-            if (n < p.N) {
-              for (int j = h; j < BN; j += 2) {
-                const int m = m0 + j;
-                if (m >= p.M) break;
-                const int64_t o = static_cast<int64_t>(m) * p.N + n;
-                const int v = __ldcg(&p.ws_acc[o]);
-                p.y[o] = __fmul_rn(static_cast<float>(v), bars.cscale[j]);
+            named_bar(3, kUnpackThreads);
+            if (u == 0) {
+              const unsigned t = atomicAdd(&p.ws_cnt[blockIdx.y * gridDim.x + blockIdx.x], 1u);
+              bars.last_flag = (t == static_cast<unsigned>(p.splits - 1)) ? 1 : 0;
+            }
+            named_bar(3, kUnpackThreads);
+            if (bars.last_flag) {
+              __threadfence();
+              if (n < p.N) {
+                for (int c = h; c < BN; c += 2) {
+                  const int m = m0 + c;
+                  if (m >= p.M) break;
+                  const int64_t o = static_cast<int64_t>(m) * p.N + n;
+                  const int v = __ldcg(&p.ws_acc[o]);
+                  p.y[o] = __fmul_rn(static_cast<float>(v), bars.cscale[c]);
+                }
               }
             }
           }
         }
       }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bars.dempty));  // the accumulator may be overwritten
+      ++j;
     }
-    tc_fence_before();
   }
   __syncthreads();
   if (warp == 1) {

@@ -44,10 +44,14 @@ struct Plan {
   int64_t tiles_n = 0, tiles_m = 0;
   int tiles_total = 0;
   int splits = 1, kt_per_split = 0;
+  // stream-K: one block per SM (kRefSms) takes an equal share of the
+  // flattened (tile, k tile) units; used when whole tiles fill the last wave
+  // poorly (each tile is then shared by at most two neighbouring blocks)
+  int streamk = 0, sk_grid = 0, units = 0, units_per = 0;
   // few-token kernel: blocks per cluster (K split) and k tiles per block
   int sk_cs = 1, sk_kt_per = 0;
   // workspace (bytes, 256-aligned offsets)
-  size_t off_xb = 0, off_sc = 0, off_acc = 0, off_cnt = 0, ws_bytes = 0;
+  size_t off_xb = 0, off_sc = 0, off_acc = 0, off_cnt = 0, off_part = 0, ws_bytes = 0;
 };
 
 // Units per lane so the activation slice stays within 64 registers
@@ -159,6 +163,15 @@ inline Plan make(int64_t M, int64_t N, int64_t K) {
   p.kt_per_split = (num_kt + splits - 1) / splits;
   p.splits = (num_kt + p.kt_per_split - 1) / p.kt_per_split;
   p.tiles_total = static_cast<int>(tiles < 0x7fffffff ? tiles : 0x7fffffff);
+  if (p.splits == 1 && tiles >= kRefSms && tiles * num_kt < 0x7fffffff) {
+    const int64_t waves = (tiles + kRefSms - 1) / kRefSms;
+    if (tiles * 10 < waves * kRefSms * 9) {  // whole tiles would leave > 10 % of the SMs idle
+      p.streamk = 1;
+      p.sk_grid = kRefSms;
+      p.units = static_cast<int>(tiles * num_kt);
+      p.units_per = (p.units + kRefSms - 1) / kRefSms;  // >= num_kt since tiles >= kRefSms
+    }
+  }
   size_t off = 0;
   p.off_xb = off;
   off = align256(off + static_cast<size_t>(M) * static_cast<size_t>(p.Kp) * 2);
@@ -166,10 +179,18 @@ inline Plan make(int64_t M, int64_t N, int64_t K) {
   off = align256(off + static_cast<size_t>(M) * 4);
   p.off_acc = off;
   p.off_cnt = off;
+  p.off_part = off;
   if (p.splits > 1) {
     off = align256(off + static_cast<size_t>(M) * static_cast<size_t>(N) * 4);
     p.off_cnt = off;
     off = align256(off + static_cast<size_t>(tiles) * 4);
+    p.off_part = off;
+  }
+  if (p.streamk) {
+    // int32 partial tile [bn][128] per block, then one flag per block
+    off = align256(off + static_cast<size_t>(p.sk_grid) * p.bn * 128 * 4);
+    p.off_cnt = off;
+    off = align256(off + static_cast<size_t>(p.sk_grid) * 4);
   }
   p.ws_bytes = off;
   return p;
