@@ -62,6 +62,7 @@ def _load():
     lib.bl_oracle_pack.argtypes = [P, I64, I64, P]
     lib.bl_oracle_unpack.argtypes = [P, I64, I64, P]
     lib.bl_oracle_quant_act.argtypes = [P, I64, I64, P, P]
+    lib.bl_oracle_relu2.argtypes = [P, I64, P]
     lib.bl_oracle_matmul_i32.argtypes = [P, P, I64, I64, I64, P]
     lib.bl_oracle_rescale.argtypes = [P, F, P, I64, I64, P]
     lib.bl_oracle_forward_packed.argtypes = [P, F, I64, I64, P, I64, P, P, P, P]
@@ -152,6 +153,24 @@ def quant_act(x):
     s = np.empty((M,), np.float32)
     _load().bl_oracle_quant_act(_ptr(x), M, K, _ptr(xq), _ptr(s))
     return xq, s
+
+
+def relu2(x) -> np.ndarray:
+    """Squared ReLU, elementwise: u = fl32(max(x, 0)^2)."""
+    x = _f32(x)
+    u = np.empty_like(x)
+    _load().bl_oracle_relu2(_ptr(x), x.size, _ptr(u))
+    return u
+
+
+def relu2_quant_act(x):
+    """Per-token absmax quantisation of relu2(x) -> (xq, s)."""
+    return quant_act(relu2(x))
+
+
+def forward_packed_relu2(packed, gamma: float, N: int, K: int, x) -> np.ndarray:
+    """BitLinear forward of relu2(x) (the down projection of a ReLU^2 FFN)."""
+    return forward_packed(packed, gamma, N, K, relu2(x))
 
 
 def matmul_i32(q, xq) -> np.ndarray:

@@ -150,6 +150,18 @@ void bl_oracle_quant_act(const float *x, int64_t M, int64_t K, int8_t *xq,
   }
 }
 
+/* Squared ReLU, the FFN activation whose output feeds the down projection
+ * ([CSDN-0.4GB] section "特殊设计", bullet 激活函数: 平方ReLU instead of SwiGLU):
+ *   u = fl32( r * r ),  r = x if x > 0 else 0
+ * (one correctly rounded fp32 product).  Its BitLinear input is then
+ * quantised per token exactly as bl_oracle_quant_act does with x. */
+void bl_oracle_relu2(const float *x, int64_t n, float *u) {
+  for (int64_t i = 0; i < n; ++i) {
+    float r = x[i] > 0.0f ? x[i] : 0.0f;
+    u[i] = r * r;
+  }
+}
+
 /* acc[m, n] = sum_k q[n, k] * xq[m, k] in int32 ([DeepDive 2.3(2)]:
  * W_quant @ x_quant; [CSDN-0.4GB 1]: with ternary weights the product needs
  * only additions).  |acc| <= 127 * K, far inside int32. */

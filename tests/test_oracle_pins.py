@@ -351,3 +351,63 @@ def test_rmsnorm_constant_row_closed_form():
         assert abs(float(r[m]) - 1 / math.sqrt(c * c + 1e-5)) <= 2 ** -23 / abs(c)
         s_u = np.float32(127) / np.float32(abs(c))
         assert s[m] == np.float32(s_u / r[m])
+
+
+# ------------------------------------------------------------------ squared ReLU
+def test_relu2_closed_form_on_exact_values():
+    """relu2 of multiples of 1/8 is exact: max(x, 0)^2 = k^2 / 64 for x = k / 8 > 0,
+    and 0 for x <= 0 (including -0.0)."""
+    k = np.arange(-200, 201, dtype=np.int64)
+    x = (k / 8.0).astype(np.float32)
+    u = oracle.relu2(x)
+    want = np.where(k > 0, (k * k) / 64.0, 0.0).astype(np.float32)
+    assert np.array_equal(u, want)
+    assert oracle.relu2(np.array([-0.0], np.float32))[0] == 0.0
+
+
+def test_relu2_is_the_correctly_rounded_square():
+    """For x > 0, fl32(x * x) equals the fp64 product (exact for two binary32
+    factors) rounded once to binary32: an independent evaluation path."""
+    rng = np.random.default_rng(7)
+    x = (rng.standard_normal(20000) * rng.choice([1e-3, 1.0, 30.0], 20000)).astype(np.float32)
+    u = oracle.relu2(x)
+    exact = np.where(x > 0, x.astype(np.float64) * x.astype(np.float64), 0.0).astype(np.float32)
+    assert np.array_equal(u, exact)
+
+
+def test_relu2_quant_act_invariants():
+    """Codes of a squared-ReLU input are never negative; every token with a
+    positive entry has a code 127; all-negative tokens give all-zero codes."""
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((16, 700)).astype(np.float32)
+    x[5] = -np.abs(x[5])  # a token with no positive entry
+    xq, s = oracle.relu2_quant_act(x)
+    assert xq.min() >= 0
+    for m in range(16):
+        if m == 5:
+            assert (xq[m] == 0).all() and s[m] == np.float32(127.0) / np.float32(1e-5)
+        else:
+            assert xq[m].max() == 127
+    # it is the plain quantisation applied to the activation values
+    xq2, s2 = oracle.quant_act(oracle.relu2(x))
+    assert np.array_equal(xq, xq2) and np.array_equal(s, s2)
+
+
+def test_forward_relu2_equals_forward_of_squared_relu_values():
+    """On integer-valued inputs whose positive squares stay below 128 the
+    activation scale is 127 / amax and the exact integer dot product of the
+    squares is recovered: y = fl32(acc * fl32(gamma / s))."""
+    rng = np.random.default_rng(11)
+    N, K = 24, 96
+    W = rng.standard_normal((N, K)).astype(np.float32) * 0.02
+    packed, g = oracle.pack_weights(W)
+    x = rng.integers(-11, 12, size=(3, K)).astype(np.float32)
+    x[:, 0] = 11.0  # amax of the squares is 121 in every token
+    y = oracle.forward_packed_relu2(packed, g, N, K, x)
+    u = np.where(x > 0, x * x, 0.0)
+    s = np.float32(127.0) / np.float32(121.0)
+    xq = np.clip(np.rint((u.astype(np.float32) * s).astype(np.float32)), -128, 127).astype(np.int64)
+    q = oracle.unpack(packed, K).astype(np.int64)
+    acc = xq @ q.T
+    c = np.float32(np.float32(g) / s)
+    assert np.array_equal(y, (acc.astype(np.float32) * c).astype(np.float32))
