@@ -143,6 +143,18 @@ BL_API bl_status bitlinear_rmsnorm_quant_act(const void *x, int dtype, const flo
                                       float eps, int64_t M, int64_t K,
                                       int8_t *xq, float *scale, void *stream);
 
+/* Squared ReLU fused with the per-token quantisation: the input of a ReLU^2
+ * FFN's down projection, from the up projection's output in one pass.
+ * [0.4GB page, section "特殊设计", bullet 激活函数: squared ReLU in the FFN
+ * instead of SwiGLU; quantisation as bitlinear_quant_act.]
+ *   x      [M, K] of `dtype`, device (e.g. the up projection's y).
+ *   xq     [M, K] int8 out: the codes of u = fl32(max(x, 0)^2), as
+ *          bitlinear_quant_act computes them for u (all >= 0).
+ *   scale  [M] float out: the absmax scale of u.
+ * Errors: as bitlinear_quant_act. */
+BL_API bl_status bitlinear_relu2_quant_act(const void *x, int dtype, int64_t M, int64_t K,
+                                           int8_t *xq, float *scale, void *stream);
+
 /* Workspace (device bytes) needed by bitlinear_forward, bitlinear_forward_q
  * and bitlinear_matmul_i32 for these sizes; 0 when the chosen path needs
  * none (small M).  Host output.  Errors: BL_ERR_NULL, BL_ERR_SHAPE. */
@@ -166,6 +178,16 @@ BL_API bl_status bitlinear_workspace_bytes(int64_t M, int64_t N, int64_t K,
 BL_API bl_status bitlinear_forward(const uint8_t *packed, const float *gamma, int64_t N,
                             int64_t K, const void *x, int dtype, int64_t M,
                             float *y, void *ws, size_t ws_bytes, void *stream);
+
+/* BitLinear forward of relu2(x) = fl32(max(x, 0)^2): the down projection of a
+ * ReLU^2 FFN, with the activation, its quantisation and the contraction in
+ * one call (the squared ReLU is applied where the forward quantises x).
+ * Equal, bit for bit, to bitlinear_relu2_quant_act followed by
+ * bitlinear_forward_q.  [0.4GB page, section "特殊设计", bullet 激活函数.]
+ *   Arguments, workspace and errors as bitlinear_forward. */
+BL_API bl_status bitlinear_forward_relu2(const uint8_t *packed, const float *gamma, int64_t N,
+                                         int64_t K, const void *x, int dtype, int64_t M,
+                                         float *y, void *ws, size_t ws_bytes, void *stream);
 
 /* BitLinear forward on pre-quantised activations.
  *   xq     [M, K] int8 codes, device;  scale [M] float, device (s_m).

@@ -154,6 +154,37 @@ def test_forward_q_and_matmul_i32(bl, M, N, K):
     assert_bits_equal(y.cpu().numpy(), oracle.rescale(acc_ref, g_ref, s_ref), "forward_q")
 
 
+@pytest.mark.parametrize("M,K,dtype", [(1, 6912, torch.float32), (5, 1000, torch.bfloat16),
+                                       (64, 6912, torch.float32), (300, 100, torch.bfloat16)])
+def test_relu2_quant_act(bl, M, K, dtype):
+    x = wl.activations(M, K, "normal", 19 * M + K, "cpu", dtype)
+    xq, s = bl.bitlinear_relu2_quant_act(x.to(DEV))
+    torch.cuda.synchronize()
+    xq_ref, s_ref = oracle.relu2_quant_act(x.float().numpy())
+    assert np.array_equal(xq.cpu().numpy(), xq_ref)
+    assert_bits_equal(s.cpu().numpy(), s_ref, "relu2 scales")
+
+
+# M = 1 (GEMV), 3 / 16 / 64 (few-token kernel), 130 (tensor-core GEMM)
+@pytest.mark.parametrize("N,K", [(300, 100), (513, 1000), (2560, 6912)])
+@pytest.mark.parametrize("M", [1, 3, 16, 64, 130])
+def test_forward_relu2(bl, M, N, K):
+    """The down projection of a ReLU^2 FFN in one call: every path applies the
+    squared ReLU where it quantises x, bit-exact with the oracle and with
+    relu2_quant_act followed by forward_q."""
+    packed, gamma, p_ref, g_ref = pack_both(bl, N, K, 0.02, 23 * N + K)
+    dtype = torch.float32 if M % 2 else torch.bfloat16
+    x = wl.activations(M, K, "normal", 29 * M + K, "cpu", dtype).to(DEV)
+    y = bl.bitlinear_forward_relu2(packed, gamma, N, K, x)
+    xq, s = bl.bitlinear_relu2_quant_act(x)
+    y2 = bl.bitlinear_forward_q(packed, gamma, N, K, xq, s)
+    torch.cuda.synchronize()
+    assert bl.device_error() == 0
+    y_ref = oracle.forward_packed_relu2(p_ref, g_ref, N, K, x.float().cpu().numpy())
+    assert_bits_equal(y.cpu().numpy(), y_ref, f"forward_relu2 M={M} N={N} K={K}")
+    assert torch.equal(y.view(torch.int32), y2.view(torch.int32))
+
+
 def test_forward_equals_quant_then_forward_q(bl):
     N, K, M = 384, 768, 40
     packed, gamma, _, _ = pack_both(bl, N, K, 0.02, 5)

@@ -129,6 +129,18 @@ def bitlinear_quant_act(x: torch.Tensor, xq: torch.Tensor | None = None,
     return xq, scale
 
 
+def bitlinear_relu2_quant_act(x: torch.Tensor, xq: torch.Tensor | None = None,
+                              scale: torch.Tensor | None = None):
+    """Per-token absmax int8 codes of relu2(x) = max(x, 0)^2 -> (xq, s)."""
+    _need_cuda("x", x, (torch.float32, torch.bfloat16), 2)
+    M, K = x.shape
+    xq = torch.empty((M, K), dtype=torch.int8, device=x.device) if xq is None else xq
+    scale = torch.empty((M,), dtype=torch.float32, device=x.device) if scale is None else scale
+    capi.check(_lib().bitlinear_relu2_quant_act(_ptr(x), _DTYPES[x.dtype], M, K, _ptr(xq),
+                                                _ptr(scale), _stream(x)), "bitlinear_relu2_quant_act")
+    return xq, scale
+
+
 def bitlinear_rmsnorm_quant_act(x: torch.Tensor, g: torch.Tensor | None = None,
                                 eps: float = 1e-5, xq: torch.Tensor | None = None,
                                 scale: torch.Tensor | None = None):
@@ -159,6 +171,23 @@ def bitlinear_forward(packed: torch.Tensor, gamma: torch.Tensor, N: int, K: int,
     capi.check(_lib().bitlinear_forward(
         _ptr(packed), _ptr(gamma), N, K, _ptr(x), _DTYPES[x.dtype], M, _ptr(y), _ptr(ws),
         0 if ws is None else ws.numel(), _stream(x)), "bitlinear_forward")
+    return y
+
+
+def bitlinear_forward_relu2(packed: torch.Tensor, gamma: torch.Tensor, N: int, K: int,
+                            x: torch.Tensor, y: torch.Tensor | None = None,
+                            workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """y [M, N] fp32 = BitLinear(relu2(x)): a ReLU^2 FFN's down projection in one call."""
+    _need_cuda("packed", packed, torch.uint8)
+    _need_cuda("x", x, (torch.float32, torch.bfloat16), 2)
+    M = x.shape[0]
+    if x.shape[1] != K:
+        raise ValueError("x.shape[1] != K")
+    y = torch.empty((M, N), dtype=torch.float32, device=x.device) if y is None else y
+    ws = _workspace(workspace_bytes(M, N, K), x.device, workspace)
+    capi.check(_lib().bitlinear_forward_relu2(
+        _ptr(packed), _ptr(gamma), N, K, _ptr(x), _DTYPES[x.dtype], M, _ptr(y), _ptr(ws),
+        0 if ws is None else ws.numel(), _stream(x)), "bitlinear_forward_relu2")
     return y
 
 

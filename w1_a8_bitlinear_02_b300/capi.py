@@ -45,6 +45,8 @@ SIGNATURES = {
     "bitlinear_forward_q": (_INT, [_P, _P, _I64, _I64, _P, _P, _I64, _P, _P, _SZ, _P]),
     "bitlinear_matmul_i32": (_INT, [_P, _I64, _I64, _P, _I64, _P, _P, _SZ, _P]),
     "bitlinear_forward_noalloc": (_INT, [_P, _P, _I64, _I64, _P, _INT, _I64, _P, _P]),
+    "bitlinear_relu2_quant_act": (_INT, [_P, _INT, _I64, _I64, _P, _P, _P]),
+    "bitlinear_forward_relu2": (_INT, [_P, _P, _I64, _I64, _P, _INT, _I64, _P, _P, _SZ, _P]),
     "bitlinear_set_launch_overlap": (None, [_INT]),
     "bitlinear_get_launch_overlap": (_INT, []),
     "bitlinear_device_error": (_INT, [ctypes.POINTER(ctypes.c_uint), _INT]),

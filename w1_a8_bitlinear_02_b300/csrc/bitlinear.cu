@@ -201,7 +201,7 @@ void *gemv_func(int xm, bool out_i32, int mt, int upt) {
   return gemv_func_m<gemv::kXInt8, false, CW>(mt, upt);
 }
 
-bl_status run_gemv(const plan::Plan &pl, int dev, int sms, int xm, bool out_i32, const uint8_t *packed,
+bl_status run_gemv(const plan::Plan &pl, int dev, int sms, int xm, int act, bool out_i32, const uint8_t *packed,
                    const float *gamma, const void *x, const int8_t *xq, const float *scale, float *y,
                    int32_t *acc, cudaStream_t st) {
   const plan::GemvGrid g = plan::gemv_grid(pl, sms);
@@ -231,6 +231,7 @@ bl_status run_gemv(const plan::Plan &pl, int dev, int sms, int xm, bool out_i32,
   p.chunk = pl.chunk;
   const int ov = g_overlap.load();
   p.wait_prior = ov == 2 ? 0 : 1;
+  p.act = act;
   return launch(reinterpret_cast<void (*)(gemv::Params)>(f), dim3(g.grid), dim3((g.cw + 1) * 32), g.smem,
                 st, ov != 0, p);
 }
@@ -331,7 +332,7 @@ int cluster_capacity(int dev, const void *f, int cs, int smem, int threads) {
   return n;
 }
 
-bl_status run_skinny(const plan::Plan &pl, int dev, int xm, bool out_i32, const uint8_t *packed,
+bl_status run_skinny(const plan::Plan &pl, int dev, int xm, int act, bool out_i32, const uint8_t *packed,
                      const float *gamma, const void *x, const int8_t *xq, const float *scale, float *y,
                      int32_t *acc, cudaStream_t st) {
   void *f = sk_func(pl.bn, xm, out_i32);
@@ -378,6 +379,7 @@ bl_status run_skinny(const plan::Plan &pl, int dev, int xm, bool out_i32, const 
   p.cs = best_cs;
   p.ws = plan::sk_ring(pl.bn, best_kp, best_cs);
   p.x_tma = x_tma ? 1 : 0;
+  p.act = act;
   const int smem = plan::sk_launch_smem(pl.bn, best_kp, best_cs);
 
   cudaLaunchConfig_t cfg = {};
@@ -409,7 +411,7 @@ bl_status run_skinny(const plan::Plan &pl, int dev, int xm, bool out_i32, const 
 
 // Shared body of forward / forward_q / matmul_i32 on the tensor-core path.
 // xm: activation source (f32 / bf16 to be quantised, or int8 codes).
-bl_status forward_tc(const plan::Plan &pl, int dev, int xm, bool out_i32, const uint8_t *packed,
+bl_status forward_tc(const plan::Plan &pl, int dev, int xm, int act, bool out_i32, const uint8_t *packed,
                      const float *gamma, const void *x, const int8_t *xq, const float *scale, float *y,
                      int32_t *acc, void *ws, size_t ws_bytes, cudaStream_t st) {
   if (ws == nullptr || ws_bytes < pl.ws_bytes) return BL_ERR_WORKSPACE;
@@ -451,11 +453,11 @@ bl_status forward_tc(const plan::Plan &pl, int dev, int xm, bool out_i32, const 
     if (xm == gemv::kXF32)
       s = launch(&quant_act_kernel<float, true, false>, qgrid, dim3(256), 0, st, overlap,
                  static_cast<const float *>(x), pl.K, pl.Kp, static_cast<const float *>(nullptr), 0.0f,
-                 static_cast<int8_t *>(nullptr), xb, sc, zrows, pl.N, zcnt, ncnt);
+                 static_cast<int8_t *>(nullptr), xb, sc, zrows, pl.N, zcnt, ncnt, act);
     else
       s = launch(&quant_act_kernel<__nv_bfloat16, true, false>, qgrid, dim3(256), 0, st, overlap,
                  static_cast<const __nv_bfloat16 *>(x), pl.K, pl.Kp, static_cast<const float *>(nullptr),
-                 0.0f, static_cast<int8_t *>(nullptr), xb, sc, zrows, pl.N, zcnt, ncnt);
+                 0.0f, static_cast<int8_t *>(nullptr), xb, sc, zrows, pl.N, zcnt, ncnt, act);
   }
   if (s != BL_OK) return s;
 
@@ -482,7 +484,7 @@ bl_status forward_tc(const plan::Plan &pl, int dev, int xm, bool out_i32, const 
   return run_tc<false>(pl, dev, mx, mw, p, st);
 }
 
-bl_status forward_common(const uint8_t *packed, const float *gamma, int64_t N, int64_t K, int xm,
+bl_status forward_common(const uint8_t *packed, const float *gamma, int64_t N, int64_t K, int xm, int act,
                          const void *x, const int8_t *xq, const float *scale, int64_t M, float *y,
                          int32_t *acc, void *ws, size_t ws_bytes, void *stream) {
   const bool out_i32 = acc != nullptr;
@@ -502,10 +504,10 @@ bl_status forward_common(const uint8_t *packed, const float *gamma, int64_t N, i
   if (s != BL_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (pl.path == plan::kGemv)
-    return run_gemv(pl, dev, sms, xm, out_i32, packed, gamma, x, xq, scale, y, acc, st);
+    return run_gemv(pl, dev, sms, xm, act, out_i32, packed, gamma, x, xq, scale, y, acc, st);
   if (pl.path == plan::kSkinny)
-    return run_skinny(pl, dev, xm, out_i32, packed, gamma, x, xq, scale, y, acc, st);
-  return forward_tc(pl, dev, xm, out_i32, packed, gamma, x, xq, scale, y, acc, ws, ws_bytes, st);
+    return run_skinny(pl, dev, xm, act, out_i32, packed, gamma, x, xq, scale, y, acc, st);
+  return forward_tc(pl, dev, xm, act, out_i32, packed, gamma, x, xq, scale, y, acc, ws, ws_bytes, st);
 }
 
 // Device address of g_noalloc_scratch on device `dev` (which must be current).
@@ -609,7 +611,7 @@ bl_status bitlinear_pack_weights(const void *W, int dtype, int64_t N, int64_t K,
 }
 
 static bl_status quant_common(const void *x, int dtype, const float *g, float eps, bool norm, int64_t M,
-                              int64_t K, int8_t *xq, float *scale, void *stream) {
+                              int64_t K, int8_t *xq, float *scale, void *stream, int act = kActNone) {
   if (x == nullptr || xq == nullptr || scale == nullptr) return BL_ERR_NULL;
   if (dtype != BL_F32 && dtype != BL_BF16) return BL_ERR_DTYPE;
   if (M < 1 || M > kMaxDim || K < 1 || K > kMaxK) return BL_ERR_SHAPE;
@@ -627,16 +629,16 @@ static bl_status quant_common(const void *x, int dtype, const float *g, float ep
     const float *xx = static_cast<const float *>(x);
     if (norm)
       return launch(&quant_act_kernel<float, false, true>, grid, dim3(256), 0, st, ov, xx, K, K, g, eps, xq,
-                    nob, scale, noz, int64_t(0), noc, 0);
+                    nob, scale, noz, int64_t(0), noc, 0, kActNone);
     return launch(&quant_act_kernel<float, false, false>, grid, dim3(256), 0, st, ov, xx, K, K, g, eps, xq,
-                  nob, scale, noz, int64_t(0), noc, 0);
+                  nob, scale, noz, int64_t(0), noc, 0, act);
   }
   const __nv_bfloat16 *xx = static_cast<const __nv_bfloat16 *>(x);
   if (norm)
     return launch(&quant_act_kernel<__nv_bfloat16, false, true>, grid, dim3(256), 0, st, ov, xx, K, K, g,
-                  eps, xq, nob, scale, noz, int64_t(0), noc, 0);
+                  eps, xq, nob, scale, noz, int64_t(0), noc, 0, kActNone);
   return launch(&quant_act_kernel<__nv_bfloat16, false, false>, grid, dim3(256), 0, st, ov, xx, K, K, g,
-                eps, xq, nob, scale, noz, int64_t(0), noc, 0);
+                eps, xq, nob, scale, noz, int64_t(0), noc, 0, act);
 }
 
 bl_status bitlinear_quant_act(const void *x, int dtype, int64_t M, int64_t K, int8_t *xq, float *scale,
@@ -662,24 +664,40 @@ bl_status bitlinear_forward(const uint8_t *packed, const float *gamma, int64_t N
   if (dtype != BL_F32 && dtype != BL_BF16) return BL_ERR_DTYPE;
   const int xm = dtype == BL_F32 ? gemv::kXF32 : gemv::kXBF16;
   if (y == nullptr) return BL_ERR_NULL;
-  return forward_common(packed, gamma, N, K, xm, x, nullptr, nullptr, M, y, nullptr, ws, ws_bytes, stream);
+  return forward_common(packed, gamma, N, K, xm, kActNone, x, nullptr, nullptr, M, y, nullptr, ws, ws_bytes,
+                        stream);
 }
 
 bl_status bitlinear_forward_q(const uint8_t *packed, const float *gamma, int64_t N, int64_t K,
                               const int8_t *xq, const float *scale, int64_t M, float *y, void *ws,
                               size_t ws_bytes, void *stream) {
   if (y == nullptr) return BL_ERR_NULL;
-  return forward_common(packed, gamma, N, K, gemv::kXInt8, nullptr, xq, scale, M, y, nullptr, ws, ws_bytes,
+  return forward_common(packed, gamma, N, K, gemv::kXInt8, kActNone, nullptr, xq, scale, M, y, nullptr, ws,
+                        ws_bytes,
                         stream);
 }
 
 bl_status bitlinear_matmul_i32(const uint8_t *packed, int64_t N, int64_t K, const int8_t *xq, int64_t M,
                                int32_t *acc, void *ws, size_t ws_bytes, void *stream) {
   if (acc == nullptr) return BL_ERR_NULL;
-  return forward_common(packed, nullptr, N, K, gemv::kXInt8, nullptr, xq, nullptr, M, nullptr, acc, ws,
+  return forward_common(packed, nullptr, N, K, gemv::kXInt8, kActNone, nullptr, xq, nullptr, M, nullptr, acc,
+                        ws,
                         ws_bytes, stream);
 }
 
+bl_status bitlinear_forward_relu2(const uint8_t *packed, const float *gamma, int64_t N, int64_t K,
+                                  const void *x, int dtype, int64_t M, float *y, void *ws, size_t ws_bytes,
+                                  void *stream) {
+  if (dtype != BL_F32 && dtype != BL_BF16) return BL_ERR_DTYPE;
+  const int xm = dtype == BL_F32 ? gemv::kXF32 : gemv::kXBF16;
+  if (y == nullptr) return BL_ERR_NULL;
+  return forward_common(packed, gamma, N, K, xm, kActRelu2, x, nullptr, nullptr, M, y, nullptr, ws, ws_bytes,
+                        stream);
+}
+bl_status bitlinear_relu2_quant_act(const void *x, int dtype, int64_t M, int64_t K, int8_t *xq, float *scale,
+                                    void *stream) {
+  return quant_common(x, dtype, nullptr, 0.0f, false, M, K, xq, scale, stream, kActRelu2);
+}
 bl_status bitlinear_forward_noalloc(const uint8_t *packed, const float *gamma, int64_t N, int64_t K,
                                     const void *x, int dtype, int64_t M, float *y, void *stream) {
   if (dtype != BL_F32 && dtype != BL_BF16) return BL_ERR_DTYPE;

@@ -64,6 +64,7 @@ struct Params {
   int split_log2;       // G = warps per row
   int chunk;            // units per warp's chunk of a row (ceil(units / G))
   int wait_prior;       // 1: inputs may come from the previous kernel (wait for it)
+  int act;              // activation before quantisation (kActNone / kActRelu2)
 };
 
 struct Smem {
@@ -282,6 +283,9 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) gemv_kernel(const Params p) 
           const int c = tid + j * kConsumers;
           if (m < p.M && c < nv) {
             load8x<XM>(p.x, static_cast<int64_t>(m) * p.K + 8 * c, xv[m][j]);
+            if (p.act == kActRelu2)
+#pragma unroll
+              for (int e = 0; e < 8; ++e) xv[m][j][e] = relu2f(xv[m][j][e]);
           } else {
 #pragma unroll
             for (int e = 0; e < 8; ++e) xv[m][j][e] = 0.0f;
@@ -304,10 +308,13 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) gemv_kernel(const Params p) 
             float v[8];
             load8x<XM>(p.x, row + 8 * c, v);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) a = fmaxf(a, fabsf(v[j]));
+            for (int j = 0; j < 8; ++j) a = fmaxf(a, fabsf(p.act == kActRelu2 ? relu2f(v[j]) : v[j]));
           }
         }
-        for (int k = 8 * nv + tid; k < p.K; k += kConsumers) a = fmaxf(a, fabsf(load_x<XM>(p.x, row + k)));
+        for (int k = 8 * nv + tid; k < p.K; k += kConsumers) {
+          const float v = load_x<XM>(p.x, row + k);
+          a = fmaxf(a, fabsf(p.act == kActRelu2 ? relu2f(v) : v));
+        }
       }
       a = warp_max_nonneg(a);
       if (lane == 0) sm.fred[warp][m] = a;
@@ -348,11 +355,16 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) gemv_kernel(const Params p) 
           for (int c = tid; c < nv; c += kConsumers) {
             float v[8];
             load8x<XM>(p.x, row + 8 * c, v);
+            if (p.act == kActRelu2)
+#pragma unroll
+              for (int e = 0; e < 8; ++e) v[e] = relu2f(v[e]);
             put8(c, v);
           }
         }
         for (int k = 8 * nv + tid; k < p.kp; k += kConsumers) {
-          const int q = k < p.K ? quant_one(load_x<XM>(p.x, row + k), sc[m]) : 0;
+          float v = k < p.K ? load_x<XM>(p.x, row + k) : 0.0f;
+          if (p.act == kActRelu2) v = relu2f(v);
+          const int q = k < p.K ? quant_one(v, sc[m]) : 0;
           part += q;
           sts_u8(xrow + k, static_cast<uint32_t>(q) & 0xFFu);
         }

@@ -127,6 +127,15 @@ __device__ __forceinline__ int quant_one(float v, float s) {
   return static_cast<int>(r);
 }
 
+// Activation applied before quantisation: 0 none, 1 squared ReLU
+// fl32(max(x, 0)^2) (the FFN activation feeding the down projection).
+constexpr int kActNone = 0;
+constexpr int kActRelu2 = 1;
+__device__ __forceinline__ float relu2f(float v) {
+  const float r = fmaxf(v, 0.0f);
+  return __fmul_rn(r, r);
+}
+
 __device__ __forceinline__ float act_scale(float amax) {
   return __fdiv_rn(127.0f, fmaxf(amax, 1e-5f));
 }
@@ -175,6 +184,7 @@ __device__ __forceinline__ void kahan_add(float &s, float &c, float y) {
 //   OUT_BF16 = true : integer codes as bf16 [M, ld] (exact), zero for k in [K, ld);
 //                     the tensor-core path reads this layout.
 //   NORM: fused subln RMSNorm (gain g may be NULL).
+//   act: kActRelu2 squares the positive part of x first (not with NORM).
 // Rows are read in 8-element vectors (two passes: max, then codes; the second
 // pass hits L1) when K and the pointers allow, else element by element.
 template <typename XT, bool OUT_BF16, bool NORM>
@@ -184,7 +194,7 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const XT *__restrict__ x
                                                         __nv_bfloat16 *__restrict__ xb,
                                                         float *__restrict__ scale,
                                                         int32_t *__restrict__ zrows, int64_t zn,
-                                                        unsigned *__restrict__ zcnt, int ncnt) {
+                                                        unsigned *__restrict__ zcnt, int ncnt, int act) {
   __shared__ float red_f[8];
   __shared__ double red_d[8];
   pdl_wait_primary();
@@ -203,6 +213,9 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const XT *__restrict__ x
   for (int64_t c = t; c < nvec; c += 256) {
     float v[8];
     load8(xr + 8 * c, v);
+    if (act == kActRelu2)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = relu2f(v[j]);
     float gg[8];
     if (use_g) load8(g + 8 * c, gg);
 #pragma unroll
@@ -213,7 +226,8 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const XT *__restrict__ x
     }
   }
   for (int64_t k = 8 * nvec + t; k < K; k += 256) {
-    const float v = to_f32(xr[k]);
+    float v = to_f32(xr[k]);
+    if (act == kActRelu2) v = relu2f(v);
     if (NORM) kahan_add(s1, c1, __fmul_rn(v, v));
     amax = fmaxf(amax, fabsf(use_g ? __fmul_rn(v, g[k]) : v));
   }
@@ -245,6 +259,9 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const XT *__restrict__ x
   for (int64_t c = t; c < nvec; c += 256) {
     float v[8];
     load8(xr + 8 * c, v);
+    if (act == kActRelu2)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = relu2f(v[j]);
     float gg[8];
     if (use_g) load8(g + 8 * c, gg);
     int q[8];
@@ -268,7 +285,8 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const XT *__restrict__ x
     }
   }
   for (int64_t k = 8 * nvec + t; k < K; k += 256) {
-    const float v = to_f32(xr[k]);
+    float v = to_f32(xr[k]);
+    if (act == kActRelu2) v = relu2f(v);
     const int q = quant_one(use_g ? __fmul_rn(v, g[k]) : v, s);
     if (OUT_BF16)
       xb[m * ld + k] = __float2bfloat16_rn(static_cast<float>(q));

@@ -105,6 +105,7 @@ struct Params {
   int cs;               // blocks per cluster (K split)
   int ws;               // weight ring stages (a multiple of the lanes)
   int x_tma;            // bf16 rows come by TMA (map_x valid)
+  int act;              // activation before quantisation (kActNone / kActRelu2)
 };
 
 // Eight bf16 codes (integers in [-128, 127], exact) as four bf16 pairs.
@@ -263,7 +264,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
           float v[8];
           bf16x8_f32(lds_u128(b_chunk(m, r)), v);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(v[i]));
+          for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(p.act == kActRelu2 ? relu2f(v[i]) : v[i]));
         }
         a = warp_max_nonneg(a);
         if (lane == 0) bars.amax[m] = a;
@@ -283,11 +284,14 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
             float v[8];
             load8(xr + k, v);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(v[i]));
+            for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(p.act == kActRelu2 ? relu2f(v[i]) : v[i]));
           }
         } else {
 #pragma unroll 4
-          for (int k = kbeg + lane; k < kend; k += 32) a = fmaxf(a, fabsf(to_f32(xr[k])));
+          for (int k = kbeg + lane; k < kend; k += 32) {
+            const float v = to_f32(xr[k]);
+            a = fmaxf(a, fabsf(p.act == kActRelu2 ? relu2f(v) : v));
+          }
         }
         a = warp_max_nonneg(a);
         if (lane == 0) bars.amax[m] = a;
@@ -339,7 +343,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
         const float s = bars.sc[m];
         int qv[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) qv[i] = quant_one(v[i], s);
+        for (int i = 0; i < 8; ++i) qv[i] = quant_one(p.act == kActRelu2 ? relu2f(v[i]) : v[i], s);
         uint32_t w[4];
         codes8_bf16(qv, w);
         sts_u128(ad, w[0], w[1], w[2], w[3]);
@@ -381,7 +385,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
             }
             const float s = bars.sc[m];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) qv[i] = quant_one(v[i], s);
+            for (int i = 0; i < 8; ++i) qv[i] = quant_one(p.act == kActRelu2 ? relu2f(v[i]) : v[i], s);
           }
           codes8_bf16(qv, w);
         }
