@@ -464,6 +464,23 @@ def run_extras(bl, wl, torch, device, stream, peaks, items2b, args):
             "how": "same 120 calls, launch overlap mode 2 (calls do not wait for each other)"}
         del g
 
+        # the same 120 calls as one decode-chain launch (each call waits for the
+        # previous one at a grid barrier instead of a kernel boundary)
+        ws_chain = torch.empty(256, dtype=torch.uint8, device=device)
+        chain = [dict(packed=it["packed"], gamma=it["gamma"], x=it["x"], y=it["y"], N=it["mt"].N,
+                      K=it["mt"].K, wait_prev=1) for it in items2b]
+        gch = torch.cuda.CUDAGraph()
+        bl.bitlinear_forward_chain(chain, ws_chain)
+        stream.synchronize()
+        with torch.cuda.graph(gch, stream=stream):
+            bl.bitlinear_forward_chain(chain, ws_chain)
+        s = timed(gch.replay, max(3, min(args.steps, 200)))
+        out["decode_2b_chain"] = {
+            "GB/s": nb / s / 1e9, "frac_hbm": nb / s / 1e9 / peaks["hbm_gbs"], "ms_per_sweep": s * 1e3,
+            "how": "bitlinear_forward_chain: the 120 calls in one persistent launch, each call "
+                   "waiting for the previous at a grid barrier"}
+        del gch
+
         # batched decode on the same weights
         mats = [it["mt"] for it in items2b]
         bd = {}

@@ -235,6 +235,52 @@ BL_API bl_status bitlinear_forward_noalloc(const uint8_t *packed, const float *g
                                            int64_t N, int64_t K, const void *x, int dtype,
                                            int64_t M, float *y, void *stream);
 
+/* Activation applied to x before quantisation (bl_chain_call.act). */
+enum { BL_ACT_NONE = 0, BL_ACT_RELU2 = 1 };
+
+/* One call of a decode chain (bitlinear_forward_chain), M = 1.
+ *   packed, gamma  as bitlinear_forward (device).
+ *   x              [K] of x_dtype, device; may be the y of an earlier call.
+ *   y              [N] float out, device.
+ *   N, K           sizes; K <= 8192.
+ *   x_dtype        BL_F32 or BL_BF16.
+ *   act            BL_ACT_NONE, or BL_ACT_RELU2 for relu2(x) (as
+ *                  bitlinear_forward_relu2).
+ *   wait_prev      1 when x (or anything the call reads) is written by an
+ *                  earlier call of the chain; 0 lets the call start while
+ *                  earlier calls still run. */
+typedef struct bl_chain_call {
+  const uint8_t *packed;
+  const float *gamma;
+  const void *x;
+  float *y;
+  int64_t N, K;
+  int x_dtype;
+  int act;
+  int wait_prev;
+} bl_chain_call;
+
+/* A decode chain: up to 128 single-token BitLinear forwards run in order in
+ * one persistent launch (one block per SM, all resident).  Each call's
+ * result equals, bit for bit, bitlinear_forward (or bitlinear_forward_relu2)
+ * of its x, and a call with wait_prev = 1 reads its input only after every
+ * earlier call has written its output, so chained layers can pass y to x.
+ * The packed weights of later calls stream in while earlier calls compute
+ * (the "pack-store-load-unpack-compute" weight stream of the 0.4GB page,
+ * section 3, carried across calls); dependent calls meet at a grid-wide
+ * barrier instead of a kernel boundary.
+ *   calls    host array of n descriptors (copied at the call; 1 <= n <= 128).
+ *   ws       >= 256 bytes, device, 256-byte aligned: the barrier counter,
+ *            zeroed by the call on `stream`.  Chains that share ws must be
+ *            ordered.
+ * Errors: BL_ERR_NULL, BL_ERR_SHAPE (n, N, K or act out of range),
+ * BL_ERR_DTYPE, BL_ERR_ALIGN, BL_ERR_WORKSPACE, BL_ERR_UNSUPPORTED,
+ * BL_ERR_CUDA (including a launch the device cannot fit on all its SMs).
+ * [The layer structure: 0.4GB page, section 2 (ReLU^2 FFN, no bias);
+ * soaring_casia page, section 2 (BitLinear in every projection).] */
+BL_API bl_status bitlinear_forward_chain(const bl_chain_call *calls, int n, void *ws,
+                                         size_t ws_bytes, void *stream);
+
 /* Launch overlap (programmatic dependent launch) for the forward kernels.
  * Process-wide; host only.  Modes:
  *   0 (default)  ordinary stream order.

@@ -137,3 +137,31 @@ def test_launch_overlap_switch(lib):
     bl.set_launch_overlap(False)
     assert not bl.get_launch_overlap()
     bl.set_launch_overlap(before)
+
+
+def test_chain_invalid_arguments_return_status(lib):
+    """bitlinear_forward_chain checks every descriptor before touching the device."""
+    from w1_a8_bitlinear_02_b300 import capi
+    fake, odd = 0x10000, 0x10008  # never dereferenced
+    ws = ctypes.c_void_p(fake)
+
+    def chain(**kw):
+        d = dict(packed=fake, gamma=fake, x=fake, y=fake, N=64, K=64, x_dtype=capi.BL_BF16,
+                 act=capi.BL_ACT_NONE, wait_prev=1)
+        d.update(kw)
+        arr = (capi.ChainCall * 1)(capi.ChainCall(d["packed"], d["gamma"], d["x"], d["y"], d["N"],
+                                                  d["K"], d["x_dtype"], d["act"], d["wait_prev"]))
+        return ctypes.cast(arr, ctypes.c_void_p), arr
+
+    p, keep = chain()
+    assert lib.bitlinear_forward_chain(None, 1, ws, 256, None) == capi.BL_ERR_NULL
+    assert lib.bitlinear_forward_chain(p, 1, None, 256, None) == capi.BL_ERR_NULL
+    assert lib.bitlinear_forward_chain(p, 0, ws, 256, None) == capi.BL_ERR_SHAPE
+    assert lib.bitlinear_forward_chain(p, 129, ws, 256, None) == capi.BL_ERR_SHAPE
+    assert lib.bitlinear_forward_chain(p, 1, ws, 255, None) == capi.BL_ERR_WORKSPACE
+    assert lib.bitlinear_forward_chain(p, 1, ctypes.c_void_p(odd), 256, None) == capi.BL_ERR_ALIGN
+    for kw, want in ((dict(y=0), capi.BL_ERR_NULL), (dict(K=8193), capi.BL_ERR_SHAPE),
+                     (dict(N=0), capi.BL_ERR_SHAPE), (dict(x_dtype=7), capi.BL_ERR_DTYPE),
+                     (dict(act=5), capi.BL_ERR_SHAPE), (dict(packed=odd), capi.BL_ERR_ALIGN)):
+        p2, keep2 = chain(**kw)
+        assert lib.bitlinear_forward_chain(p2, 1, ws, 256, None) == want, kw

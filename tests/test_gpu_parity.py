@@ -251,6 +251,70 @@ def test_independent_calls_overlap_mode(bl):
             i += 1
 
 
+# ------------------------------------------------------------------ decode chain
+def test_chain_with_data_dependencies(bl):
+    """Layers passing y to x inside one chain launch: o 2560->2560 (bf16 x),
+    up 2560->6912 on o's fp32 output, down 6912->2560 on relu2(up's output),
+    qkv 2560->3840 on down's output, and a ragged 300 x 1000 call.  Each step is
+    checked against the oracle on the oracle's own previous output."""
+    shapes = [(2560, 2560, 0), (6912, 2560, 0), (2560, 6912, 1), (3840, 2560, 0), (1000, 3840, 0)]
+    mats = [pack_both(bl, N, K, 0.02, 300 + i) for i, (N, K, _) in enumerate(shapes)]
+    x0 = wl.activations(1, 2560, "normal", 310, "cpu", torch.bfloat16)
+    calls, ys = [], []
+    x = x0.to(DEV)
+    for (N, K, act), (packed, gamma, _, _) in zip(shapes, mats):
+        y = torch.full((1, N), float("nan"), dtype=torch.float32, device=DEV)
+        calls.append(dict(packed=packed, gamma=gamma, x=x, y=y, N=N, K=K, act=act))
+        ys.append(y)
+        x = y
+    bl.bitlinear_forward_chain(calls)
+    torch.cuda.synchronize()
+    assert bl.device_error() == 0
+    xr = x0.float().numpy()
+    for i, ((N, K, act), (_, _, p_ref, g_ref)) in enumerate(zip(shapes, mats)):
+        f = oracle.forward_packed_relu2 if act else oracle.forward_packed
+        y_ref = f(p_ref, g_ref, N, K, xr)
+        assert_bits_equal(ys[i].cpu().numpy(), y_ref, f"chain step {i}")
+        xr = y_ref
+
+
+@pytest.mark.parametrize("wait_prev", [1, 0])
+def test_chain_equals_separate_calls(bl, wait_prev):
+    """120 calls of the ~2B decode workload (independent inputs) in one chain:
+    each output equals, bit for bit, a separate bitlinear_forward of the same call."""
+    mats = wl.matrices("decode_2b", layers=3)
+    calls, refs = [], []
+    for mt in mats:
+        W = wl.weight(mt.N, mt.K, mt.std, mt.seed, DEV)
+        packed, gamma = bl.bitlinear_pack_weights(W)
+        del W
+        x = wl.activations(1, mt.K, mt.x_kind, mt.seed + 500, DEV, torch.bfloat16)
+        y = torch.empty((1, mt.N), dtype=torch.float32, device=DEV)
+        calls.append(dict(packed=packed, gamma=gamma, x=x, y=y, N=mt.N, K=mt.K, wait_prev=wait_prev))
+        refs.append(bl.bitlinear_forward(packed, gamma, mt.N, mt.K, x))
+    calls = calls * 10  # 120 calls (the same twelve matrices ten times)
+    bl.bitlinear_forward_chain(calls)
+    torch.cuda.synchronize()
+    assert bl.device_error() == 0
+    for c, r in zip(calls[:12], refs):
+        assert torch.equal(c["y"].view(torch.int32), r.view(torch.int32))
+
+
+def test_chain_unaligned_and_odd_k(bl):
+    """K not a multiple of 8 and an input that starts off a 16-byte boundary
+    take the element-by-element activation path."""
+    N, K = 333, 999
+    packed, gamma, p_ref, g_ref = pack_both(bl, N, K, 0.02, 77)
+    xb = wl.activations(1, K + 1, "normal", 78, "cpu", torch.float32)
+    xdev = xb.to(DEV)[:, 1:]  # 4-byte offset
+    y = torch.empty((1, N), dtype=torch.float32, device=DEV)
+    bl.bitlinear_forward_chain([dict(packed=packed, gamma=gamma, x=xdev, y=y, N=N, K=K)])
+    torch.cuda.synchronize()
+    assert bl.device_error() == 0
+    y_ref = oracle.forward_packed(p_ref, g_ref, N, K, xb.numpy()[:, 1:].copy())
+    assert_bits_equal(y.cpu().numpy(), y_ref, "chain odd K")
+
+
 # ------------------------------------------------------------------ full workload shapes
 @pytest.mark.parametrize("name,N,K,kind", [(n, N, K, k) for n, N, K, k in wl.PROJ_2B])
 def test_decode_2b_shapes_full(bl, name, N, K, kind):

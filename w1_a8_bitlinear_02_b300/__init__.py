@@ -238,6 +238,31 @@ def bitlinear_forward_noalloc(packed: torch.Tensor, gamma: torch.Tensor, N: int,
     return y
 
 
+def bitlinear_forward_chain(calls, workspace: torch.Tensor | None = None) -> None:
+    """A decode chain of single-token forwards in one launch.
+
+    calls: sequence of dicts with packed, gamma, x [1, K] (fp32 / bf16), y [1, N]
+    fp32 (written), N, K and optionally act (capi.BL_ACT_RELU2 for relu2(x))
+    and wait_prev (default 1: x may be an earlier call's y).  workspace: >= 256
+    device bytes (allocated when None)."""
+    calls = list(calls)
+    if not calls:
+        raise ValueError("empty chain")
+    dev = calls[0]["x"].device
+    arr = (capi.ChainCall * len(calls))()
+    for i, c in enumerate(calls):
+        _need_cuda("packed", c["packed"], torch.uint8)
+        _need_cuda("x", c["x"], (torch.float32, torch.bfloat16))
+        _need_cuda("y", c["y"], torch.float32)
+        arr[i] = capi.ChainCall(c["packed"].data_ptr(), c["gamma"].data_ptr(), c["x"].data_ptr(),
+                                c["y"].data_ptr(), int(c["N"]), int(c["K"]), _DTYPES[c["x"].dtype],
+                                int(c.get("act", capi.BL_ACT_NONE)), int(c.get("wait_prev", 1)))
+    ws = workspace if workspace is not None else torch.empty(256, dtype=torch.uint8, device=dev)
+    capi.check(_lib().bitlinear_forward_chain(ctypes.cast(arr, ctypes.c_void_p), len(calls), _ptr(ws),
+                                              ws.numel(),
+                                              _stream(calls[0]["x"])), "bitlinear_forward_chain")
+
+
 def set_launch_overlap(mode) -> None:
     """Launch overlap for forward kernels: 0 off, 1 (or True) prefetch weights
     while the previous kernel runs, 2 independent calls (see the C header)."""

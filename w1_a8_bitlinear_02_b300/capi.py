@@ -25,6 +25,17 @@ BL_ERR_DEVICE = 8
 BL_F32 = 0
 BL_BF16 = 1
 
+BL_ACT_NONE = 0
+BL_ACT_RELU2 = 1
+
+
+class ChainCall(ctypes.Structure):
+    """bl_chain_call (include/bitlinear.h)."""
+    _fields_ = [("packed", ctypes.c_void_p), ("gamma", ctypes.c_void_p), ("x", ctypes.c_void_p),
+                ("y", ctypes.c_void_p), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("x_dtype", ctypes.c_int), ("act", ctypes.c_int), ("wait_prev", ctypes.c_int)]
+
+
 # name -> (restype, argtypes)
 _P = ctypes.c_void_p
 _I64 = ctypes.c_int64
@@ -46,6 +57,7 @@ SIGNATURES = {
     "bitlinear_matmul_i32": (_INT, [_P, _I64, _I64, _P, _I64, _P, _P, _SZ, _P]),
     "bitlinear_forward_noalloc": (_INT, [_P, _P, _I64, _I64, _P, _INT, _I64, _P, _P]),
     "bitlinear_relu2_quant_act": (_INT, [_P, _INT, _I64, _I64, _P, _P, _P]),
+    "bitlinear_forward_chain": (_INT, [_P, _INT, _P, _SZ, _P]),
     "bitlinear_forward_relu2": (_INT, [_P, _P, _I64, _I64, _P, _INT, _I64, _P, _P, _SZ, _P]),
     "bitlinear_set_launch_overlap": (None, [_INT]),
     "bitlinear_get_launch_overlap": (_INT, []),

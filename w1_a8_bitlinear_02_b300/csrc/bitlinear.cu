@@ -16,6 +16,7 @@
 #include <tuple>
 #include <utility>
 
+#include "bl_chain.cuh"
 #include "bl_gemm_tc.cuh"
 #include "bl_gemv.cuh"
 #include "bl_pack_quant.cuh"
@@ -697,6 +698,59 @@ bl_status bitlinear_forward_relu2(const uint8_t *packed, const float *gamma, int
 bl_status bitlinear_relu2_quant_act(const void *x, int dtype, int64_t M, int64_t K, int8_t *xq, float *scale,
                                     void *stream) {
   return quant_common(x, dtype, nullptr, 0.0f, false, M, K, xq, scale, stream, kActRelu2);
+}
+bl_status bitlinear_forward_chain(const bl_chain_call *calls, int n, void *ws, size_t ws_bytes,
+                                  void *stream) {
+  if (calls == nullptr || ws == nullptr) return BL_ERR_NULL;
+  if (n < 1 || n > chain::kMaxCalls) return BL_ERR_SHAPE;
+  if (ws_bytes < 256) return BL_ERR_WORKSPACE;
+  if (!aligned(ws, 256)) return BL_ERR_ALIGN;
+  chain::Params p{};
+  p.n = n;
+  p.bar = static_cast<unsigned *>(ws);
+  for (int i = 0; i < n; ++i) {
+    const bl_chain_call &c = calls[i];
+    if (c.packed == nullptr || c.gamma == nullptr || c.x == nullptr || c.y == nullptr) return BL_ERR_NULL;
+    if (c.x_dtype != BL_F32 && c.x_dtype != BL_BF16) return BL_ERR_DTYPE;
+    if (c.N < 1 || c.N > kMaxDim || c.K < 1 || c.K > chain::kMaxK) return BL_ERR_SHAPE;
+    if (c.act != BL_ACT_NONE && c.act != BL_ACT_RELU2) return BL_ERR_SHAPE;
+    if (!aligned(c.packed, 16)) return BL_ERR_ALIGN;
+    p.c[i].packed = c.packed;
+    p.c[i].gamma = c.gamma;
+    p.c[i].x = c.x;
+    p.c[i].y = c.y;
+    p.c[i].N = static_cast<int>(c.N);
+    p.c[i].K = static_cast<int>(c.K);
+    p.c[i].xbf16 = c.x_dtype == BL_BF16 ? 1 : 0;
+    p.c[i].act = c.act;
+    p.c[i].wait_prev = c.wait_prev ? 1 : 0;
+  }
+  int dev = 0, sms = 0;
+  bl_status s = current_device(&dev, &sms);
+  if (s != BL_OK) return s;
+  s = ensure_smem(dev, reinterpret_cast<const void *>(&chain::chain_kernel), chain::kSmemBytes);
+  if (s != BL_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(ws, 0, 256, st) != cudaSuccess) {
+    cudaGetLastError();
+    return BL_ERR_CUDA;
+  }
+  // every block waits for the others at the grid barrier: all must be resident
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(sms));
+  cfg.blockDim = dim3(chain::kThreads);
+  cfg.dynamicSmemBytes = chain::kSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, &chain::chain_kernel, p) != cudaSuccess) {
+    cudaGetLastError();
+    return BL_ERR_CUDA;
+  }
+  return BL_OK;
 }
 bl_status bitlinear_forward_noalloc(const uint8_t *packed, const float *gamma, int64_t N, int64_t K,
                                     const void *x, int dtype, int64_t M, float *y, void *stream) {
