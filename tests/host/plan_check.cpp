@@ -36,7 +36,7 @@ int main() {
         } else if (p.path == kSkinny) {
           ++sk;
           const long nkt = p.Kp / 64;
-          bool ok = M >= 2 && M <= kSkMaxM && (p.bn == 16 || p.bn == 32 || p.bn == 64) && p.bn >= M &&
+          bool ok = M >= 3 && M <= kSkMaxM && (p.bn == 16 || p.bn == 32 || p.bn == 64) && p.bn >= M &&
                     p.tiles_n * 128 >= N && (p.tiles_n - 1) * 128 < N && p.ws_bytes == 0;
           ok = ok && p.sk_cs >= 1 && p.sk_cs <= kSkMaxCs && p.sk_kt_per >= 1 &&
                (long)p.sk_cs * p.sk_kt_per >= nkt && (long)(p.sk_cs - 1) * p.sk_kt_per < nkt;

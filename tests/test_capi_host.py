@@ -78,7 +78,7 @@ def test_row_bytes_and_sizes(lib):
 
 def test_workspace_plan(lib):
     import w1_a8_bitlinear_02_b300 as bl
-    # decode (M = 1, GEMV) and batched decode (2 <= M <= 64, the few-token
+    # decode (M <= 2, GEMV) and batched decode (3 <= M <= 64, the few-token
     # tensor-core kernel, which quantises in shared memory) need no workspace
     for M in (1, 2, 3, 8, 9, 16, 33, 64):
         for N, K in ((2560, 6912), (3840, 2560), (6912, 2560), (2560, 2560)):

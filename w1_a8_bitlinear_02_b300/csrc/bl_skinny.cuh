@@ -1,4 +1,4 @@
-// Tensor-core BitLinear forward for a few tokens (2 <= M <= 64, batched
+// Tensor-core BitLinear forward for a few tokens (3 <= M <= 64, batched
 // decode), tcgen05 on sm_103a: one launch per call, no workspace.
 //
 // At a few tokens one MMA instruction (128 weight rows x 16..64 tokens x 16 k)
