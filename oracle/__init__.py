@@ -63,6 +63,7 @@ def _load():
     lib.bl_oracle_unpack.argtypes = [P, I64, I64, P]
     lib.bl_oracle_quant_act.argtypes = [P, I64, I64, P, P]
     lib.bl_oracle_relu2.argtypes = [P, I64, P]
+    lib.bl_oracle_output.argtypes = [P, P, I64, ctypes.c_int, P, P]
     lib.bl_oracle_matmul_i32.argtypes = [P, P, I64, I64, I64, P]
     lib.bl_oracle_rescale.argtypes = [P, F, P, I64, I64, P]
     lib.bl_oracle_forward_packed.argtypes = [P, F, I64, I64, P, I64, P, P, P, P]
@@ -171,6 +172,19 @@ def relu2_quant_act(x):
 def forward_packed_relu2(packed, gamma: float, N: int, K: int, x) -> np.ndarray:
     """BitLinear forward of relu2(x) (the down projection of a ReLU^2 FFN)."""
     return forward_packed(packed, gamma, N, K, relu2(x))
+
+
+def output(y, residual=None, bf16: bool = False) -> np.ndarray:
+    """Forward output variants: fl32(y + residual) (residual fp32 values, e.g.
+    widened bf16), then one RNE rounding to bf16 when bf16 (returned as the
+    uint16 bit patterns); otherwise fp32."""
+    y = _f32(y)
+    r = None if residual is None else _f32(residual).reshape(y.shape)
+    out_f = np.empty_like(y)
+    out_b = np.empty(y.shape, np.uint16)
+    _load().bl_oracle_output(_ptr(y), None if r is None else _ptr(r), y.size, 1 if bf16 else 0,
+                             _ptr(out_f), _ptr(out_b))
+    return out_b if bf16 else out_f
 
 
 def matmul_i32(q, xq) -> np.ndarray:

@@ -162,6 +162,32 @@ void bl_oracle_relu2(const float *x, int64_t n, float *u) {
   }
 }
 
+/* Output variants of the forward's last step (this library's options; the
+ * pages give the residual stream of the architecture, 0.4GB page section 2,
+ * and the output precision is left open):
+ *   y_out = fl32( y + r )  when a residual r is given (r widened to fp32,
+ *           exact from bf16), else y;
+ *   then, for a bf16 output, one round-to-nearest-even to bf16. */
+static uint16_t f32_to_bf16_rne(float f) {
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  /* finite inputs only (a precondition of the forward) */
+  uint32_t lsb = (u >> 16) & 1u;
+  u += 0x7FFFu + lsb;
+  return (uint16_t)(u >> 16);
+}
+void bl_oracle_output(const float *y, const float *r, int64_t n, int bf16_out, float *out_f32,
+                      uint16_t *out_bf16) {
+  for (int64_t i = 0; i < n; ++i) {
+    float v = y[i];
+    if (r) v = v + r[i];
+    if (bf16_out)
+      out_bf16[i] = f32_to_bf16_rne(v);
+    else
+      out_f32[i] = v;
+  }
+}
+
 /* acc[m, n] = sum_k q[n, k] * xq[m, k] in int32 ([DeepDive 2.3(2)]:
  * W_quant @ x_quant; [CSDN-0.4GB 1]: with ternary weights the product needs
  * only additions).  |acc| <= 127 * K, far inside int32. */

@@ -411,3 +411,35 @@ def test_forward_relu2_equals_forward_of_squared_relu_values():
     acc = xq @ q.T
     c = np.float32(np.float32(g) / s)
     assert np.array_equal(y, (acc.astype(np.float32) * c).astype(np.float32))
+
+
+# ------------------------------------------------------------------ output variants
+def test_output_bf16_rounding_pins():
+    """bf16 output rounding against values whose bf16 neighbours are known:
+    exact values pass through, halfway cases go to the even neighbour, and the
+    result is the nearest bf16 (checked against an fp64 nearest search)."""
+    exact = np.array([1.0, -2.5, 0.0, 3.140625, 65280.0], np.float32)
+    assert np.array_equal(oracle.output(exact, bf16=True),
+                          (exact.view(np.uint32) >> 16).astype(np.uint16))
+    # 1 + 2^-8 is halfway between 1 and 1 + 2^-7: to even (1.0); 1 + 3 * 2^-8 -> 1 + 2^-6
+    half = np.array([1 + 2 ** -8, 1 + 3 * 2 ** -8, -(1 + 2 ** -8)], np.float32)
+    assert oracle.output(half, bf16=True).tolist() == [0x3F80, 0x3F82, 0xBF80]
+    rng = np.random.default_rng(5)
+    v = (rng.standard_normal(5000) * 100).astype(np.float32)
+    b = oracle.output(v, bf16=True)
+    up = (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    lo = ((b.astype(np.uint32) - 1) << 16).view(np.float32).astype(np.float64)
+    hi = ((b.astype(np.uint32) + 1) << 16).view(np.float32).astype(np.float64)
+    d = np.abs(up - v.astype(np.float64))
+    assert (d <= np.abs(lo - v) + 0).all() and (d <= np.abs(hi - v)).all()
+
+
+def test_output_residual_is_one_fp32_add():
+    """With a residual the output is the correctly rounded fp32 sum (the exact
+    fp64 sum of two binary32 values rounded once)."""
+    rng = np.random.default_rng(9)
+    y = (rng.standard_normal(4000) * 3).astype(np.float32)
+    r = (rng.standard_normal(4000) * 1000).astype(np.float32)
+    out = oracle.output(y, r)
+    assert np.array_equal(out, (y.astype(np.float64) + r.astype(np.float64)).astype(np.float32))
+    assert np.array_equal(oracle.output(y), y)
