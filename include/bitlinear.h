@@ -81,6 +81,10 @@ typedef enum bl_dtype {
   BL_BF16 = 1  /* bfloat16 (widened to fp32 exactly)   */
 } bl_dtype;
 
+/* Activation applied to x before quantisation (bitlinear_forward_ex,
+ * bl_chain_call.act). */
+enum { BL_ACT_NONE = 0, BL_ACT_RELU2 = 1 };
+
 /* Library version, e.g. 100 for 0.1.0.  Host only; never fails. */
 BL_API int bitlinear_version(void);
 
@@ -189,6 +193,27 @@ BL_API bl_status bitlinear_forward_relu2(const uint8_t *packed, const float *gam
                                          int64_t K, const void *x, int dtype, int64_t M,
                                          float *y, void *ws, size_t ws_bytes, void *stream);
 
+/* BitLinear forward with the options of a transformer block: an activation
+ * on x before quantisation, a bf16 or fp32 output, and a residual added to the
+ * output (the residual stream around every projection: 0.4GB page, section 2
+ * architecture; the pages leave the output precision open).
+ *   x, x_dtype, M, packed, gamma, N, K, ws   as bitlinear_forward.
+ *   act        BL_ACT_NONE, or BL_ACT_RELU2: the forward of relu2(x)
+ *              (as bitlinear_forward_relu2).
+ *   y          [M, N] of y_dtype (BL_F32 or BL_BF16), device, written:
+ *              v = fl32(float(acc) * c_m) as in bitlinear_forward, then
+ *              v = fl32(v + residual[m, n]) when residual is given, then one
+ *              round-to-nearest-even to bf16 for a bf16 y.
+ *   residual   [M, N] of y_dtype, device, or NULL; it may be y itself
+ *              (in-place residual update).
+ * With act = BL_ACT_NONE, y_dtype = BL_F32 and no residual it is
+ * bitlinear_forward.  Errors: as bitlinear_forward, plus BL_ERR_DTYPE for
+ * y_dtype and BL_ERR_SHAPE for act. */
+BL_API bl_status bitlinear_forward_ex(const uint8_t *packed, const float *gamma, int64_t N,
+                                      int64_t K, const void *x, int x_dtype, int64_t M, int act,
+                                      void *y, int y_dtype, const void *residual, void *ws,
+                                      size_t ws_bytes, void *stream);
+
 /* BitLinear forward on pre-quantised activations.
  *   xq     [M, K] int8 codes, device;  scale [M] float, device (s_m).
  *   Other arguments and the result as bitlinear_forward. */
@@ -234,9 +259,6 @@ BL_API bl_status bitlinear_matmul_i32(const uint8_t *packed, int64_t N, int64_t 
 BL_API bl_status bitlinear_forward_noalloc(const uint8_t *packed, const float *gamma,
                                            int64_t N, int64_t K, const void *x, int dtype,
                                            int64_t M, float *y, void *stream);
-
-/* Activation applied to x before quantisation (bl_chain_call.act). */
-enum { BL_ACT_NONE = 0, BL_ACT_RELU2 = 1 };
 
 /* One call of a decode chain (bitlinear_forward_chain), M = 1.
  *   packed, gamma  as bitlinear_forward (device).

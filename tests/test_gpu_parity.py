@@ -185,6 +185,39 @@ def test_forward_relu2(bl, M, N, K):
     assert torch.equal(y.view(torch.int32), y2.view(torch.int32))
 
 
+# M = 1, 2 (GEMV), 3, 33, 64 (few-token kernel), 130 (tensor-core GEMM);
+# the last shape also takes stream-K at M = 2048 (one case below)
+@pytest.mark.parametrize("M,N,K", [(1, 513, 1000), (2, 300, 100), (3, 513, 1000), (33, 2560, 2560),
+                                   (64, 384, 768), (130, 300, 100), (2048, 2560, 320)])
+@pytest.mark.parametrize("y_dtype,res,act", [(torch.float32, None, 0), (torch.bfloat16, None, 0),
+                                             (torch.float32, "sep", 1), (torch.bfloat16, "inplace", 0),
+                                             (torch.float32, "inplace", 1)])
+def test_forward_ex_output_variants(bl, M, N, K, y_dtype, res, act):
+    """bf16 / fp32 output, residual (separate or in place) and the squared-ReLU
+    input, on every path, bit-exact with the oracle's output step."""
+    packed, gamma, p_ref, g_ref = pack_both(bl, N, K, 0.02, 31 * N + K)
+    x = wl.activations(M, K, "outliers1pct", 37 * M + K, "cpu", torch.bfloat16)
+    r = (torch.randn((M, N), generator=torch.Generator().manual_seed(M + N)) * 2).to(y_dtype)
+    y = torch.empty((M, N), dtype=y_dtype, device=DEV)
+    residual = None
+    if res == "sep":
+        residual = r.to(DEV)
+    elif res == "inplace":
+        y.copy_(r.to(DEV))
+        residual = y
+    bl.bitlinear_forward_ex(packed, gamma, N, K, x.to(DEV), y=y, residual=residual, act=act)
+    torch.cuda.synchronize()
+    assert bl.device_error() == 0
+    f = oracle.forward_packed_relu2 if act else oracle.forward_packed
+    y32 = f(p_ref, g_ref, N, K, x.float().numpy())
+    want = oracle.output(y32, None if res is None else r.float().numpy(), bf16=y_dtype == torch.bfloat16)
+    got = y.cpu()
+    if y_dtype == torch.bfloat16:
+        assert np.array_equal(got.view(torch.int16).numpy().view(np.uint16), want)
+    else:
+        assert_bits_equal(got.numpy(), want, f"forward_ex M={M} N={N} K={K}")
+
+
 def test_forward_equals_quant_then_forward_q(bl):
     N, K, M = 384, 768, 40
     packed, gamma, _, _ = pack_both(bl, N, K, 0.02, 5)

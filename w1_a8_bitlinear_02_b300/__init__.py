@@ -174,6 +174,29 @@ def bitlinear_forward(packed: torch.Tensor, gamma: torch.Tensor, N: int, K: int,
     return y
 
 
+def bitlinear_forward_ex(packed: torch.Tensor, gamma: torch.Tensor, N: int, K: int,
+                         x: torch.Tensor, y: torch.Tensor | None = None,
+                         y_dtype: torch.dtype = torch.float32, residual: torch.Tensor | None = None,
+                         act: int = 0, workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """y [M, N] (fp32 or bf16) = BitLinear(act(x)) (+ residual, which may be y itself)."""
+    _need_cuda("packed", packed, torch.uint8)
+    _need_cuda("x", x, (torch.float32, torch.bfloat16), 2)
+    M = x.shape[0]
+    if x.shape[1] != K:
+        raise ValueError("x.shape[1] != K")
+    if y is None:
+        y = torch.empty((M, N), dtype=y_dtype, device=x.device)
+    _need_cuda("y", y, (torch.float32, torch.bfloat16), 2)
+    if residual is not None:
+        _need_cuda("residual", residual, y.dtype, 2)
+    ws = _workspace(workspace_bytes(M, N, K), x.device, workspace)
+    capi.check(_lib().bitlinear_forward_ex(
+        _ptr(packed), _ptr(gamma), N, K, _ptr(x), _DTYPES[x.dtype], M, int(act), _ptr(y),
+        _DTYPES[y.dtype], _ptr(residual), _ptr(ws), 0 if ws is None else ws.numel(), _stream(x)),
+        "bitlinear_forward_ex")
+    return y
+
+
 def bitlinear_forward_relu2(packed: torch.Tensor, gamma: torch.Tensor, N: int, K: int,
                             x: torch.Tensor, y: torch.Tensor | None = None,
                             workspace: torch.Tensor | None = None) -> torch.Tensor:

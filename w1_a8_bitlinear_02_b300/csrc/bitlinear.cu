@@ -203,7 +203,7 @@ void *gemv_func(int xm, bool out_i32, int mt, int upt) {
 }
 
 bl_status run_gemv(const plan::Plan &pl, int dev, int sms, int xm, int act, bool out_i32, const uint8_t *packed,
-                   const float *gamma, const void *x, const int8_t *xq, const float *scale, float *y,
+                   const float *gamma, const void *x, const int8_t *xq, const float *scale, const OutSpec &out,
                    int32_t *acc, cudaStream_t st) {
   const plan::GemvGrid g = plan::gemv_grid(pl, sms);
   void *f = g.cw == 16 ? gemv_func<16>(xm, out_i32, pl.mt, pl.upt) : gemv_func<8>(xm, out_i32, pl.mt, pl.upt);
@@ -216,7 +216,7 @@ bl_status run_gemv(const plan::Plan &pl, int dev, int sms, int xm, int act, bool
   p.x = x;
   p.xq = xq;
   p.scale = scale;
-  p.y = y;
+  p.out = out;
   p.acc = acc;
   p.N = pl.N;
   p.K = static_cast<int>(pl.K);
@@ -334,7 +334,7 @@ int cluster_capacity(int dev, const void *f, int cs, int smem, int threads) {
 }
 
 bl_status run_skinny(const plan::Plan &pl, int dev, int xm, int act, bool out_i32, const uint8_t *packed,
-                     const float *gamma, const void *x, const int8_t *xq, const float *scale, float *y,
+                     const float *gamma, const void *x, const int8_t *xq, const float *scale, const OutSpec &out,
                      int32_t *acc, cudaStream_t st) {
   void *f = sk_func(pl.bn, xm, out_i32);
   if (!f) return BL_ERR_UNSUPPORTED;
@@ -370,7 +370,7 @@ bl_status run_skinny(const plan::Plan &pl, int dev, int xm, int act, bool out_i3
   p.x = out_i32 || xm == gemv::kXInt8 ? static_cast<const void *>(xq) : x;
   p.scale = scale;
   p.gamma = gamma;
-  p.y = y;
+  p.out = out;
   p.acc = acc;
   p.M = static_cast<int>(pl.M);
   p.N = static_cast<int>(pl.N);
@@ -413,7 +413,7 @@ bl_status run_skinny(const plan::Plan &pl, int dev, int xm, int act, bool out_i3
 // Shared body of forward / forward_q / matmul_i32 on the tensor-core path.
 // xm: activation source (f32 / bf16 to be quantised, or int8 codes).
 bl_status forward_tc(const plan::Plan &pl, int dev, int xm, int act, bool out_i32, const uint8_t *packed,
-                     const float *gamma, const void *x, const int8_t *xq, const float *scale, float *y,
+                     const float *gamma, const void *x, const int8_t *xq, const float *scale, const OutSpec &out,
                      int32_t *acc, void *ws, size_t ws_bytes, cudaStream_t st) {
   if (ws == nullptr || ws_bytes < pl.ws_bytes) return BL_ERR_WORKSPACE;
   if (!aligned(ws, 256)) return BL_ERR_ALIGN;
@@ -471,7 +471,7 @@ bl_status forward_tc(const plan::Plan &pl, int dev, int xm, int act, bool out_i3
   p.splits = pl.splits;
   p.gamma = gamma;
   p.scale = use_scale;
-  p.y = y;
+  p.out = out;
   p.acc_out = acc;
   p.ws_acc = wacc;
   p.ws_cnt = wcnt;
@@ -485,11 +485,14 @@ bl_status forward_tc(const plan::Plan &pl, int dev, int xm, int act, bool out_i3
   return run_tc<false>(pl, dev, mx, mw, p, st);
 }
 
+OutSpec out_f32(float *y) { return OutSpec{y, nullptr, 0}; }
+
+// y: fp32 [M, N] unless out.bf16; out.res: optional residual of y's dtype.
 bl_status forward_common(const uint8_t *packed, const float *gamma, int64_t N, int64_t K, int xm, int act,
-                         const void *x, const int8_t *xq, const float *scale, int64_t M, float *y,
+                         const void *x, const int8_t *xq, const float *scale, int64_t M, OutSpec out,
                          int32_t *acc, void *ws, size_t ws_bytes, void *stream) {
   const bool out_i32 = acc != nullptr;
-  if (packed == nullptr || (!out_i32 && (gamma == nullptr || y == nullptr)))
+  if (packed == nullptr || (!out_i32 && (gamma == nullptr || out.y == nullptr)))
     return BL_ERR_NULL;
   if (xm == gemv::kXInt8 ? xq == nullptr : x == nullptr) return BL_ERR_NULL;
   if (xm == gemv::kXInt8 && !out_i32 && scale == nullptr) return BL_ERR_NULL;
@@ -505,10 +508,10 @@ bl_status forward_common(const uint8_t *packed, const float *gamma, int64_t N, i
   if (s != BL_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (pl.path == plan::kGemv)
-    return run_gemv(pl, dev, sms, xm, act, out_i32, packed, gamma, x, xq, scale, y, acc, st);
+    return run_gemv(pl, dev, sms, xm, act, out_i32, packed, gamma, x, xq, scale, out, acc, st);
   if (pl.path == plan::kSkinny)
-    return run_skinny(pl, dev, xm, act, out_i32, packed, gamma, x, xq, scale, y, acc, st);
-  return forward_tc(pl, dev, xm, act, out_i32, packed, gamma, x, xq, scale, y, acc, ws, ws_bytes, st);
+    return run_skinny(pl, dev, xm, act, out_i32, packed, gamma, x, xq, scale, out, acc, st);
+  return forward_tc(pl, dev, xm, act, out_i32, packed, gamma, x, xq, scale, out, acc, ws, ws_bytes, st);
 }
 
 // Device address of g_noalloc_scratch on device `dev` (which must be current).
@@ -665,35 +668,47 @@ bl_status bitlinear_forward(const uint8_t *packed, const float *gamma, int64_t N
   if (dtype != BL_F32 && dtype != BL_BF16) return BL_ERR_DTYPE;
   const int xm = dtype == BL_F32 ? gemv::kXF32 : gemv::kXBF16;
   if (y == nullptr) return BL_ERR_NULL;
-  return forward_common(packed, gamma, N, K, xm, kActNone, x, nullptr, nullptr, M, y, nullptr, ws, ws_bytes,
-                        stream);
+  return forward_common(packed, gamma, N, K, xm, kActNone, x, nullptr, nullptr, M, out_f32(y), nullptr, ws,
+                        ws_bytes, stream);
 }
 
 bl_status bitlinear_forward_q(const uint8_t *packed, const float *gamma, int64_t N, int64_t K,
                               const int8_t *xq, const float *scale, int64_t M, float *y, void *ws,
                               size_t ws_bytes, void *stream) {
   if (y == nullptr) return BL_ERR_NULL;
-  return forward_common(packed, gamma, N, K, gemv::kXInt8, kActNone, nullptr, xq, scale, M, y, nullptr, ws,
-                        ws_bytes,
+  return forward_common(packed, gamma, N, K, gemv::kXInt8, kActNone, nullptr, xq, scale, M, out_f32(y), nullptr,
+                        ws, ws_bytes,
                         stream);
 }
 
 bl_status bitlinear_matmul_i32(const uint8_t *packed, int64_t N, int64_t K, const int8_t *xq, int64_t M,
                                int32_t *acc, void *ws, size_t ws_bytes, void *stream) {
   if (acc == nullptr) return BL_ERR_NULL;
-  return forward_common(packed, nullptr, N, K, gemv::kXInt8, kActNone, nullptr, xq, nullptr, M, nullptr, acc,
-                        ws,
+  return forward_common(packed, nullptr, N, K, gemv::kXInt8, kActNone, nullptr, xq, nullptr, M,
+                        OutSpec{nullptr, nullptr, 0}, acc, ws,
                         ws_bytes, stream);
 }
 
+bl_status bitlinear_forward_ex(const uint8_t *packed, const float *gamma, int64_t N, int64_t K, const void *x,
+                               int x_dtype, int64_t M, int act, void *y, int y_dtype, const void *residual,
+                               void *ws, size_t ws_bytes, void *stream) {
+  if (x_dtype != BL_F32 && x_dtype != BL_BF16) return BL_ERR_DTYPE;
+  if (y_dtype != BL_F32 && y_dtype != BL_BF16) return BL_ERR_DTYPE;
+  if (act != BL_ACT_NONE && act != BL_ACT_RELU2) return BL_ERR_SHAPE;
+  if (y == nullptr) return BL_ERR_NULL;
+  const int xm = x_dtype == BL_F32 ? gemv::kXF32 : gemv::kXBF16;
+  const OutSpec out{y, residual, y_dtype == BL_BF16 ? 1 : 0};
+  return forward_common(packed, gamma, N, K, xm, act == BL_ACT_RELU2 ? kActRelu2 : kActNone, x, nullptr, nullptr,
+                        M, out, nullptr, ws, ws_bytes, stream);
+}
 bl_status bitlinear_forward_relu2(const uint8_t *packed, const float *gamma, int64_t N, int64_t K,
                                   const void *x, int dtype, int64_t M, float *y, void *ws, size_t ws_bytes,
                                   void *stream) {
   if (dtype != BL_F32 && dtype != BL_BF16) return BL_ERR_DTYPE;
   const int xm = dtype == BL_F32 ? gemv::kXF32 : gemv::kXBF16;
   if (y == nullptr) return BL_ERR_NULL;
-  return forward_common(packed, gamma, N, K, xm, kActRelu2, x, nullptr, nullptr, M, y, nullptr, ws, ws_bytes,
-                        stream);
+  return forward_common(packed, gamma, N, K, xm, kActRelu2, x, nullptr, nullptr, M, out_f32(y), nullptr, ws,
+                        ws_bytes, stream);
 }
 bl_status bitlinear_relu2_quant_act(const void *x, int dtype, int64_t M, int64_t K, int8_t *xq, float *scale,
                                     void *stream) {

@@ -84,7 +84,7 @@ struct Params {
   int units, units_per;
   const float *gamma;
   const float *scale;  // [M] activation scales (float output only)
-  float *y;            // [M, N]
+  OutSpec out;         // y [M, N]
   int32_t *acc_out;    // [M, N] (int32 output)
   int32_t *ws_acc;     // [M, N] split-K partial sums (float output, splits > 1)
   unsigned *ws_cnt;    // per output tile tickets (float output, splits > 1)
@@ -408,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   if constexpr (OUT_I32)
                     p.acc_out[o] = v;
                   else
-                    p.y[o] = __fmul_rn(static_cast<float>(v), bars.cscale[c0 + jj]);
+                    put_y(p.out, o, __fmul_rn(static_cast<float>(v), bars.cscale[c0 + jj]));
                 }
               }
             }
@@ -437,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   if (m >= p.M) break;
                   const int64_t o = static_cast<int64_t>(m) * p.N + n;
                   const int v = __ldcg(&p.ws_acc[o]);
-                  p.y[o] = __fmul_rn(static_cast<float>(v), bars.cscale[c]);
+                  put_y(p.out, o, __fmul_rn(static_cast<float>(v), bars.cscale[c]));
                 }
               }
             }

@@ -49,7 +49,7 @@ struct Params {
   const void *x;        // kXF32 / kXBF16: [M, K] activations
   const int8_t *xq;     // kXInt8: [M, K] codes
   const float *scale;   // kXInt8: [M] scales
-  float *y;             // [M, N] (float output)
+  OutSpec out;          // y [M, N] (float output)
   int32_t *acc;         // [M, N] (int32 output)
   int64_t N;
   int K;
@@ -283,14 +283,19 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) gemv_kernel(const Params p) 
           const int c = tid + j * kConsumers;
           if (m < p.M && c < nv) {
             load8x<XM>(p.x, static_cast<int64_t>(m) * p.K + 8 * c, xv[m][j]);
-            if (p.act == kActRelu2)
-#pragma unroll
-              for (int e = 0; e < 8; ++e) xv[m][j][e] = relu2f(xv[m][j][e]);
           } else {
 #pragma unroll
             for (int e = 0; e < 8; ++e) xv[m][j][e] = 0.0f;
           }
         }
+      // the activation after every load is in flight (relu2(0) = 0)
+      if (p.act == kActRelu2)
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+#pragma unroll
+          for (int j = 0; j < JM; ++j)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) xv[m][j][e] = relu2f(xv[m][j][e]);
     }
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
@@ -303,12 +308,22 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) gemv_kernel(const Params p) 
 #pragma unroll
             for (int e = 0; e < 8; ++e) a = fmaxf(a, fabsf(xv[m][j][e]));
         } else {
+          if (p.act == kActRelu2) {
 #pragma unroll 2
-          for (int c = tid; c < nv; c += kConsumers) {
-            float v[8];
-            load8x<XM>(p.x, row + 8 * c, v);
+            for (int c = tid; c < nv; c += kConsumers) {
+              float v[8];
+              load8x<XM>(p.x, row + 8 * c, v);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) a = fmaxf(a, fabsf(p.act == kActRelu2 ? relu2f(v[j]) : v[j]));
+              for (int j = 0; j < 8; ++j) a = fmaxf(a, relu2f(v[j]));
+            }
+          } else {
+#pragma unroll 2
+            for (int c = tid; c < nv; c += kConsumers) {
+              float v[8];
+              load8x<XM>(p.x, row + 8 * c, v);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) a = fmaxf(a, fabsf(v[j]));
+            }
           }
         }
         for (int k = 8 * nv + tid; k < p.K; k += kConsumers) {
@@ -471,7 +486,7 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) gemv_kernel(const Params p) 
               if constexpr (OUT_I32)
                 p.acc[static_cast<int64_t>(m) * p.N + n] = q;
               else
-                p.y[static_cast<int64_t>(m) * p.N + n] = __fmul_rn(static_cast<float>(q), cm[m]);
+                put_y(p.out, static_cast<int64_t>(m) * p.N + n, __fmul_rn(static_cast<float>(q), cm[m]));
             }
           }
         }

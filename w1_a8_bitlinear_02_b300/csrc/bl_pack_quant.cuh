@@ -136,6 +136,24 @@ __device__ __forceinline__ float relu2f(float v) {
   return __fmul_rn(r, r);
 }
 
+// Where a forward writes y[i] = v: fp32 or bf16 (one round to nearest even),
+// adding first, in fp32, a residual of the output's dtype when one is given
+// (it may be y itself: each element is read and then written by one thread).
+struct OutSpec {
+  void *y;          // [M, N] fp32 or bf16
+  const void *res;  // [M, N] of the same dtype, or null
+  int bf16;
+};
+__device__ __forceinline__ void put_y(const OutSpec &o, int64_t i, float v) {
+  if (o.res != nullptr)
+    v = __fadd_rn(v, o.bf16 ? __bfloat162float(static_cast<const __nv_bfloat16 *>(o.res)[i])
+                            : static_cast<const float *>(o.res)[i]);
+  if (o.bf16)
+    static_cast<__nv_bfloat16 *>(o.y)[i] = __float2bfloat16_rn(v);
+  else
+    static_cast<float *>(o.y)[i] = v;
+}
+
 __device__ __forceinline__ float act_scale(float amax) {
   return __fdiv_rn(127.0f, fmaxf(amax, 1e-5f));
 }

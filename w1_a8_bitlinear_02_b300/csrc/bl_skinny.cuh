@@ -97,7 +97,7 @@ struct Params {
   const void *x;        // [M, K]: f32 / bf16 activations, or int8 codes
   const float *scale;   // int8 codes with float output: their scales [M]
   const float *gamma;   // float output
-  float *y;             // [M, N]
+  OutSpec out;          // y [M, N]
   int32_t *acc;         // [M, N] (int32 output)
   int M, N, K;
   int num_kt;           // 64-k tiles in the padded K
@@ -477,7 +477,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
               if constexpr (OUT_I32)
                 p.acc[o] = sum[i];
               else
-                p.y[o] = __fmul_rn(static_cast<float>(sum[i]), bars.cscale[m]);
+                put_y(p.out, o, __fmul_rn(static_cast<float>(sum[i]), bars.cscale[m]));
             }
           } else {
             // to block m % cs, slot [this block][m / cs][row]
@@ -514,7 +514,7 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
           if constexpr (OUT_I32)
             p.acc[o] = sum;
           else
-            p.y[o] = __fmul_rn(static_cast<float>(sum), bars.cscale[m]);
+            put_y(p.out, o, __fmul_rn(static_cast<float>(sum), bars.cscale[m]));
         }
       }
     }
