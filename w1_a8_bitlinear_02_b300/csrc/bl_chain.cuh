@@ -40,7 +40,7 @@ constexpr int kMaxK = 32 * kUPT * 32;     // 8192
 constexpr int kStageBytes = 32 * 1024;
 constexpr int kStages = 6;
 constexpr int kJM = 4;                    // x vectors of 8 per consumer thread (8192 / 8 / 256)
-constexpr int kSmemFixed = 2048;
+constexpr int kSmemFixed = 8192;  // barriers, reductions and the call table
 constexpr int kSmemBytes = kSmemFixed + kStages * kStageBytes + kMaxK;  // + activation codes
 
 struct Call {
@@ -66,7 +66,10 @@ struct Smem {
   float fred[kCW];
   int xsum[kCW];
   int abort_flag;
+  Call calls[kMaxCalls];  // the parameters, copied once: indexed reads of the
+                          // parameter space go through the constant cache
 };
+static_assert(sizeof(Call) % 4 == 0, "call table copied in words");
 static_assert(sizeof(Smem) <= kSmemFixed, "fixed shared-memory region");
 
 __device__ __forceinline__ void red_release_add(unsigned *p, unsigned v) {
@@ -80,35 +83,36 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
 
 // One row's code-weighted sum over this lane's first U units (unit u at
 // lbase + 256 u), as the GEMV's masked dp4a loop; FULL: all U units exist,
-// otherwise umask bit u says so.  U is the call's ceil(units / 32), so short
-// rows do not pay for the longest row's loop.
+// otherwise unit u is read at lbase + uoff[u], an existing unit of the row
+// where unit u does not exist (its activation codes are zero: it adds
+// nothing, and the loop needs no per-unit branch).  U is the call's
+// ceil(units / 32), so short rows do not pay for the longest row's loop.
 template <int U, bool FULL>
-__device__ __forceinline__ int row_sum(uint32_t lbase, uint32_t umask, const uint32_t (&xa)[kUPT][8]) {
+__device__ __forceinline__ int row_sum(uint32_t lbase, const uint32_t (&uoff)[kUPT], const uint32_t (&xa)[kUPT][8]) {
   int a0 = 0, a1 = 0, a2 = 0, a3 = 0;
 #pragma unroll
   for (int u = 0; u < U; ++u) {
-    if (FULL || ((umask >> u) & 1u)) {
-      const uint2 wv = gemv::lds_u64(lbase + 256u * u);
+    const uint2 wv = gemv::lds_u64(lbase + (FULL ? 256u * u : uoff[u]));
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const uint32_t word = h ? wv.y : wv.x;
-        a0 = dp4a_us(word & 0x03030303u, xa[u][4 * h + 0], a0);
-        a1 = dp4a_us(word & 0x0C0C0C0Cu, xa[u][4 * h + 1], a1);
-        a2 = dp4a_us(word & 0x30303030u, xa[u][4 * h + 2], a2);
-        a3 = dp4a_us(word & 0xC0C0C0C0u, xa[u][4 * h + 3], a3);
-      }
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t word = h ? wv.y : wv.x;
+      a0 = dp4a_us(word & 0x03030303u, xa[u][4 * h + 0], a0);
+      a1 = dp4a_us(word & 0x0C0C0C0Cu, xa[u][4 * h + 1], a1);
+      a2 = dp4a_us(word & 0x30303030u, xa[u][4 * h + 2], a2);
+      a3 = dp4a_us(word & 0xC0C0C0C0u, xa[u][4 * h + 3], a3);
     }
   }
   return a0 + (a1 >> 2) + (a2 >> 4) + (a3 >> 6);
 }
 
 template <int U>
-__device__ __forceinline__ void stage_rows(uint32_t sbase, int nr, int rb, int lane, int warp, uint32_t umask,
-                                           bool full, const uint32_t (&xa)[kUPT][8], int xtot, float cm,
-                                           float *y) {
+__device__ __forceinline__ void stage_rows(uint32_t sbase, int nr, int rb, uint32_t laddr, int warp,
+                                           const uint32_t (&uoff)[kUPT], bool full,
+                                           const uint32_t (&xa)[kUPT][8], int xtot, float cm, float *y,
+                                           int lane) {
   for (int r = warp; r < nr; r += kCW) {
-    const uint32_t lbase = sbase + static_cast<uint32_t>(r * rb) + 8u * lane;
-    int t = full ? row_sum<U, true>(lbase, umask, xa) : row_sum<U, false>(lbase, umask, xa);
+    const uint32_t lbase = sbase + static_cast<uint32_t>(r * rb) + laddr;
+    int t = full ? row_sum<U, true>(lbase, uoff, xa) : row_sum<U, false>(lbase, uoff, xa);
     t = __reduce_add_sync(0xffffffffu, t);
     if (lane == 0) y[r] = __fmul_rn(static_cast<float>(t - xtot), cm);
   }
@@ -138,6 +142,12 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
     sm.abort_flag = 0;
     fence_barrier_init();
   }
+  {
+    const uint32_t *src = reinterpret_cast<const uint32_t *>(p.c);
+    uint32_t *dst = reinterpret_cast<uint32_t *>(sm.calls);
+    const int words = p.n * static_cast<int>(sizeof(Call) / 4);
+    for (int w = tid; w < words; w += kThreads) dst[w] = src[w];
+  }
   __syncthreads();
   volatile int *abort_flag = &sm.abort_flag;
 
@@ -148,7 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
       int i = 0, issued = 0;
       bool go = true;
       for (int ci = 0; ci < p.n && go; ++ci) {
-        const Call &c = p.c[ci];
+        const Call &c = sm.calls[ci];
         int r0, rows;
         block_rows(c, r0, rows);
         const int rb = row_bytes_of(c.K);
@@ -179,7 +189,8 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
   constexpr int kC = kCW * 32;
   int i = 0;  // ring stage counter, in the producer's order
   for (int ci = 0; ci < p.n; ++ci) {
-    const Call &c = p.c[ci];
+    const Call c = sm.calls[ci];
+    const float gam = __ldg(c.gamma);  // static input: fetched while the barrier is awaited
     int r0, rows;
     block_rows(c, r0, rows);
     const int rb = row_bytes_of(c.K);
@@ -281,19 +292,22 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
       int xtot = 0;
 #pragma unroll
       for (int w = 0; w < kCW; ++w) xtot += sm.xsum[w];
-      const float cm = __fdiv_rn(__ldg(c.gamma), s);
+      const float cm = __fdiv_rn(gam, s);
 
       // ---- this lane's activation codes: units lane + 32 u
       uint32_t xa[kUPT][8];
-      uint32_t umask = 0u;
+      uint32_t uoff[kUPT];
+      const bool lane_in = lane < units;  // otherwise every unit is read at unit 0
+      const uint32_t laddr = lane_in ? 8u * lane : 0u;
 #pragma unroll
       for (int u = 0; u < kUPT; ++u) {
         const int unit = lane + 32 * u;
         uint4 lo4 = make_uint4(0u, 0u, 0u, 0u), hi4 = lo4;
+        uoff[u] = 0u;
         if (unit < units) {
           lo4 = lds_u128(xs + 32 * unit);
           hi4 = lds_u128(xs + 32 * unit + 16);
-          umask |= 1u << u;
+          uoff[u] = 256u * u;
         }
         xa[u][0] = lo4.x; xa[u][1] = lo4.y; xa[u][2] = lo4.z; xa[u][3] = lo4.w;
         xa[u][4] = hi4.x; xa[u][5] = hi4.y; xa[u][6] = hi4.z; xa[u][7] = hi4.w;
@@ -313,14 +327,14 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
         const uint32_t sbase = ring + st * kStageBytes;
         float *yq = c.y + r0 + q;
         switch (upt) {
-          case 1: stage_rows<1>(sbase, nr, rb, lane, warp, umask, full, xa, xtot, cm, yq); break;
-          case 2: stage_rows<2>(sbase, nr, rb, lane, warp, umask, full, xa, xtot, cm, yq); break;
-          case 3: stage_rows<3>(sbase, nr, rb, lane, warp, umask, full, xa, xtot, cm, yq); break;
-          case 4: stage_rows<4>(sbase, nr, rb, lane, warp, umask, full, xa, xtot, cm, yq); break;
-          case 5: stage_rows<5>(sbase, nr, rb, lane, warp, umask, full, xa, xtot, cm, yq); break;
-          case 6: stage_rows<6>(sbase, nr, rb, lane, warp, umask, full, xa, xtot, cm, yq); break;
-          case 7: stage_rows<7>(sbase, nr, rb, lane, warp, umask, full, xa, xtot, cm, yq); break;
-          default: stage_rows<8>(sbase, nr, rb, lane, warp, umask, full, xa, xtot, cm, yq); break;
+          case 1: stage_rows<1>(sbase, nr, rb, laddr, warp, uoff, full, xa, xtot, cm, yq, lane); break;
+          case 2: stage_rows<2>(sbase, nr, rb, laddr, warp, uoff, full, xa, xtot, cm, yq, lane); break;
+          case 3: stage_rows<3>(sbase, nr, rb, laddr, warp, uoff, full, xa, xtot, cm, yq, lane); break;
+          case 4: stage_rows<4>(sbase, nr, rb, laddr, warp, uoff, full, xa, xtot, cm, yq, lane); break;
+          case 5: stage_rows<5>(sbase, nr, rb, laddr, warp, uoff, full, xa, xtot, cm, yq, lane); break;
+          case 6: stage_rows<6>(sbase, nr, rb, laddr, warp, uoff, full, xa, xtot, cm, yq, lane); break;
+          case 7: stage_rows<7>(sbase, nr, rb, laddr, warp, uoff, full, xa, xtot, cm, yq, lane); break;
+          default: stage_rows<8>(sbase, nr, rb, laddr, warp, uoff, full, xa, xtot, cm, yq, lane); break;
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&sm.empty[st]));

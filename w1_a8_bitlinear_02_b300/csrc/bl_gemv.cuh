@@ -101,12 +101,16 @@ __device__ __forceinline__ uint2 lds_u64(uint32_t addr) {
 }
 
 // One row's sum over this lane's units (lbase: the lane's first unit; unit u
-// at + 256 u).  FULL: every unit exists; otherwise umask bit u says so.
+// at + 256 u).  FULL: every unit exists; otherwise unit u is read at + uoff[u],
+// which points back at an existing unit of the row where unit u does not
+// exist: its activation codes are zero, so it adds nothing, and the loop has
+// no per-unit branch (a branch per unit serialises the loads and measured
+// more than twice as slow per row on B300).
 //   MT <= 2: the bytes of (word & (3 << 2i)) are codes x 4^i; dp4a into
 //   accumulator i and divide by 4^i exactly at the end.
 //   MT > 2: the codes are shifted down once per word and shared by the tokens.
 template <int MT, int UPT, bool FULL>
-__device__ __forceinline__ void row_dot(uint32_t lbase, uint32_t umask, const uint32_t (&xa)[MT][UPT][8],
+__device__ __forceinline__ void row_dot(uint32_t lbase, const uint32_t (&uoff)[UPT], const uint32_t (&xa)[MT][UPT][8],
                                         int (&tot)[MT]) {
   if constexpr (MT <= 2) {
     int a0[MT], a1[MT], a2[MT], a3[MT];
@@ -114,20 +118,18 @@ __device__ __forceinline__ void row_dot(uint32_t lbase, uint32_t umask, const ui
     for (int m = 0; m < MT; ++m) a0[m] = a1[m] = a2[m] = a3[m] = 0;
 #pragma unroll
     for (int u = 0; u < UPT; ++u) {
-      if (FULL || ((umask >> u) & 1u)) {
-        const uint2 wv = lds_u64(lbase + 256u * u);
+      const uint2 wv = lds_u64(lbase + (FULL ? 256u * u : uoff[u]));
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const uint32_t word = h ? wv.y : wv.x;
-          const uint32_t c0 = word & 0x03030303u, c1 = word & 0x0C0C0C0Cu;
-          const uint32_t c2 = word & 0x30303030u, c3 = word & 0xC0C0C0C0u;
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t word = h ? wv.y : wv.x;
+        const uint32_t c0 = word & 0x03030303u, c1 = word & 0x0C0C0C0Cu;
+        const uint32_t c2 = word & 0x30303030u, c3 = word & 0xC0C0C0C0u;
 #pragma unroll
-          for (int m = 0; m < MT; ++m) {
-            a0[m] = dp4a_us(c0, xa[m][u][4 * h + 0], a0[m]);
-            a1[m] = dp4a_us(c1, xa[m][u][4 * h + 1], a1[m]);
-            a2[m] = dp4a_us(c2, xa[m][u][4 * h + 2], a2[m]);
-            a3[m] = dp4a_us(c3, xa[m][u][4 * h + 3], a3[m]);
-          }
+        for (int m = 0; m < MT; ++m) {
+          a0[m] = dp4a_us(c0, xa[m][u][4 * h + 0], a0[m]);
+          a1[m] = dp4a_us(c1, xa[m][u][4 * h + 1], a1[m]);
+          a2[m] = dp4a_us(c2, xa[m][u][4 * h + 2], a2[m]);
+          a3[m] = dp4a_us(c3, xa[m][u][4 * h + 3], a3[m]);
         }
       }
     }
@@ -139,20 +141,18 @@ __device__ __forceinline__ void row_dot(uint32_t lbase, uint32_t umask, const ui
     for (int m = 0; m < MT; ++m) a[m] = 0;
 #pragma unroll
     for (int u = 0; u < UPT; ++u) {
-      if (FULL || ((umask >> u) & 1u)) {
-        const uint2 wv = lds_u64(lbase + 256u * u);
+      const uint2 wv = lds_u64(lbase + (FULL ? 256u * u : uoff[u]));
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const uint32_t word = h ? wv.y : wv.x;
-          const uint32_t c0 = word & 0x03030303u, c1 = (word >> 2) & 0x03030303u;
-          const uint32_t c2 = (word >> 4) & 0x03030303u, c3 = (word >> 6) & 0x03030303u;
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t word = h ? wv.y : wv.x;
+        const uint32_t c0 = word & 0x03030303u, c1 = (word >> 2) & 0x03030303u;
+        const uint32_t c2 = (word >> 4) & 0x03030303u, c3 = (word >> 6) & 0x03030303u;
 #pragma unroll
-          for (int m = 0; m < MT; ++m) {
-            a[m] = dp4a_us(c0, xa[m][u][4 * h + 0], a[m]);
-            a[m] = dp4a_us(c1, xa[m][u][4 * h + 1], a[m]);
-            a[m] = dp4a_us(c2, xa[m][u][4 * h + 2], a[m]);
-            a[m] = dp4a_us(c3, xa[m][u][4 * h + 3], a[m]);
-          }
+        for (int m = 0; m < MT; ++m) {
+          a[m] = dp4a_us(c0, xa[m][u][4 * h + 0], a[m]);
+          a[m] = dp4a_us(c1, xa[m][u][4 * h + 1], a[m]);
+          a[m] = dp4a_us(c2, xa[m][u][4 * h + 2], a[m]);
+          a[m] = dp4a_us(c3, xa[m][u][4 * h + 3], a[m]);
         }
       }
     }
@@ -432,14 +432,15 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) gemv_kernel(const Params p) 
   }
 
   // This lane's units are ubase + lane + 32 u.  When every lane's UPT units
-  // lie inside the chunk (the common case) the row loop runs without
-  // per-unit checks; otherwise a per-lane mask says which units exist.
-  const uint32_t lane_addr = 8u * static_cast<uint32_t>(ubase + lane);
+  // lie inside the chunk the row loop uses fixed offsets; otherwise a unit
+  // past the chunk is read at the chunk's first unit (codes zero, see row_dot),
+  // and so is every unit of a lane that starts past it.
+  const bool lane_in = ubase + lane < uend;
+  const uint32_t lane_addr = 8u * static_cast<uint32_t>(lane_in ? ubase + lane : ubase);
   const bool all_in = ubase + 32 * UPT <= uend;
-  uint32_t umask = 0u;
+  uint32_t uoff[UPT];
 #pragma unroll
-  for (int u = 0; u < UPT; ++u)
-    if (ubase + lane + 32 * u < uend) umask |= 1u << u;
+  for (int u = 0; u < UPT; ++u) uoff[u] = (lane_in && ubase + lane + 32 * u < uend) ? 256u * u : 0u;
 
   // ---- stream the rows
   for (int it = 0; it < n_iters; ++it) {
@@ -456,9 +457,9 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) gemv_kernel(const Params p) 
       const uint32_t lbase = sbase + static_cast<uint32_t>(r) * p.row_bytes + lane_addr;
       int tot[MT];
       if (all_in)
-        row_dot<MT, UPT, true>(lbase, umask, xa, tot);
+        row_dot<MT, UPT, true>(lbase, uoff, xa, tot);
       else
-        row_dot<MT, UPT, false>(lbase, umask, xa, tot);
+        row_dot<MT, UPT, false>(lbase, uoff, xa, tot);
 #pragma unroll
       for (int m = 0; m < MT; ++m) tot[m] = __reduce_add_sync(0xffffffffu, tot[m]);
       if (lane == 0) {
