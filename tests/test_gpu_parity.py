@@ -364,10 +364,11 @@ def test_decode_2b_shapes_full(bl, name, N, K, kind):
 
 @pytest.mark.parametrize("name,N,K,kind", [(n, N, K, k) for n, N, K, k in wl.PROJ_2B])
 def test_batched_decode_2b_shapes_full(bl, name, N, K, kind):
-    """Batched decode on one layer of the ~2B model: M = 16, 33 and 64 tokens with
-    1 % outlier channels, whole outputs, through forward and forward_q."""
+    """Batched decode on one layer of the ~2B model: M = 3 (GEMV), 5, 16, 33 and
+    64 tokens (the few-token kernel, or the GEMM where that needs more than one
+    wave) with 1 % outlier channels, whole outputs, through forward and forward_q."""
     packed, gamma, p_ref, g_ref = pack_both(bl, N, K, 0.02, wl.weight_seed("decode_2b", 1, 0) + N)
-    for M in (16, 33, 64):
+    for M in (3, 5, 16, 33, 64):
         x = wl.activations(M, K, "outliers1pct", 91 + M, "cpu", torch.bfloat16)
         y = bl.bitlinear_forward(packed, gamma, N, K, x.to(DEV))
         xq_ref, s_ref = oracle.quant_act(x.float().numpy())
@@ -380,12 +381,14 @@ def test_batched_decode_2b_shapes_full(bl, name, N, K, kind):
         assert_bits_equal(y_q.cpu().numpy(), y_ref, f"{name} M={M} forward_q")
 
 
-@pytest.mark.parametrize("M,N,K", [(2048, 2560, 320), (1900, 2500, 300), (2048, 2560, 6912)])
+@pytest.mark.parametrize("M,N,K", [(2048, 2560, 320), (1900, 2500, 300), (2048, 2560, 6912),
+                                   (8, 20480, 640), (24, 20480, 640), (40, 19000, 448)])
 def test_streamk_tiles_full_output(bl, M, N, K):
-    """Tile counts that fill the last wave poorly (160 tiles on 148 SMs) run
+    """Tile counts that fill the last wave poorly (149-160 tiles on 148 SMs) run
     stream-K: tiles are shared by two blocks whose int32 partials meet in the
     workspace.  Whole outputs (forward and matmul_i32) against the oracle; the
-    last shape is the prefill down projection itself, checked in full."""
+    third shape is the prefill down projection itself, checked in full; the
+    last three have token tiles of 16, 32 and 64 (a few tokens on many rows)."""
     packed, gamma, p_ref, g_ref = pack_both(bl, N, K, 0.02, 17 * N + K)
     x = wl.activations(M, K, "outliers1pct", 3 * M + K, "cpu", torch.bfloat16)
     y = bl.bitlinear_forward(packed, gamma, N, K, x.to(DEV))
@@ -415,10 +418,12 @@ def test_prefill_2048_sampled_tokens(bl, N, K, kind):
                       "prefill")
 
 
-def test_decode_100b_shape_full(bl):
-    """One 100B-class matrix (28672 x 8192), packed on the GPU, M = 1 and 8."""
-    N, K = 28672, 8192
-    W = wl.weight(N, K, 0.01, wl.weight_seed("decode_100b", 0, 0), DEV)
+@pytest.mark.parametrize("N,K,Ms", [(28672, 8192, (1, 3, 8)), (8192, 28672, (1, 4, 8))])
+def test_decode_100b_shape_full(bl, N, K, Ms):
+    """The 100B-class matrices (28672 x 8192 and 8192 x 28672), packed on the
+    GPU, whole outputs at one token, a few (GEMV or GEMM by fit) and eight
+    (the GEMM: the few-token kernel would need more than one wave)."""
+    W = wl.weight(N, K, 0.01, wl.weight_seed("decode_100b", 0, 0) + N, DEV)
     packed, gamma = bl.bitlinear_pack_weights(W)
     Wh = W.cpu().numpy()
     del W
@@ -426,10 +431,11 @@ def test_decode_100b_shape_full(bl):
     del Wh
     assert float(gamma.item()) == float(g_ref)
     assert np.array_equal(packed.cpu().numpy(), p_ref)
-    for M in (1, 8):
+    for M in Ms:
         x = wl.activations(M, K, "normal", 5000 + M, "cpu", torch.bfloat16)
         y = bl.bitlinear_forward(packed, gamma, N, K, x.to(DEV))
         torch.cuda.synchronize()
+        assert bl.device_error() == 0
         assert_bits_equal(y.cpu().numpy(), oracle.forward_packed(p_ref, g_ref, N, K,
                                                                   x.float().numpy()),
-                          f"100b M={M}")
+                          f"100b {N}x{K} M={M}")

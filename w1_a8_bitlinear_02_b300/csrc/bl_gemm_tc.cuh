@@ -373,14 +373,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t r[32];
           tmem_ld_32x32b_x32(tmem + lane_off + c0, r);
           tmem_ld_wait();
+          // below 32 tokens a tile has BN < 32 accumulator columns: the rest
+          // of the 32 loaded are not this tile's (and the partial tile in the
+          // workspace has BN rows)
+          constexpr int kCols = BN < 32 ? BN : 32;
           if (kind == kSegTail) {
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj)
+            for (int jj = 0; jj < kCols; ++jj)
               part_out[(c0 + jj) * kBM + row] = static_cast<int>(__uint_as_float(r[jj]));
           } else if (kind == kSegSplit) {
             if (n < p.N) {
 #pragma unroll
-              for (int jj = 0; jj < 32; ++jj) {
+              for (int jj = 0; jj < kCols; ++jj) {
                 const int m = m0 + c0 + jj;
                 if (m < p.M) {
                   const int64_t o = static_cast<int64_t>(m) * p.N + n;
@@ -394,13 +398,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             if (kind == kSegHead) {
 #pragma unroll
-              for (int jj = 0; jj < 32; ++jj)
+              for (int jj = 0; jj < kCols; ++jj)
                 r[jj] = __float_as_uint(static_cast<float>(static_cast<int>(__uint_as_float(r[jj])) +
                                                            __ldcg(part_in + (c0 + jj) * kBM + row)));
             }
             if (n < p.N) {
 #pragma unroll
-              for (int jj = 0; jj < 32; ++jj) {
+              for (int jj = 0; jj < kCols; ++jj) {
                 const int m = m0 + c0 + jj;
                 if (m < p.M) {
                   const int64_t o = static_cast<int64_t>(m) * p.N + n;

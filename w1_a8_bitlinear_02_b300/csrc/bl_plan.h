@@ -112,26 +112,11 @@ inline Plan make(int64_t M, int64_t N, int64_t K) {
   p.row_bytes = row_bytes(K);
   p.Kp = p.row_bytes * 4;
   const int64_t units = p.row_bytes / 8;
-  // Few tokens: the tensor-core kernel from three tokens (at two the GEMV's
-  // masked dp4a loop measured 1.5-2x faster on the ~2B shapes; at four they tie).
-  if (M >= 3 && M <= kSkMaxM) {
-    const int bn = M <= 16 ? 16 : (M <= 32 ? 32 : 64);
-    const int64_t tiles_n = (N + 127) / 128;
-    const int num_kt = static_cast<int>(p.Kp / 64);
-    int cs = 1, kp = 0;
-    if (tiles_n <= 65535 && sk_split(bn, tiles_n, num_kt, kSkMaxCs, &cs, &kp)) {
-      p.path = kSkinny;
-      p.bn = bn;
-      p.tiles_n = tiles_n;
-      p.tiles_m = 1;
-      p.sk_cs = cs;
-      p.sk_kt_per = kp;
-      p.ws_bytes = 0;
-      return p;
-    }
-  }
-  if (M <= 8) {
-    p.mt = M == 1 ? 1 : (M == 2 ? 2 : (M <= 4 ? 4 : 8));
+  // One or two tokens, and three or four where the codes fit: the GEMV (its
+  // dp4a loop measured faster than the few-token tensor-core kernel there,
+  // up to 1.8x on the 28672 x 8192 shape at three and four tokens).
+  if (M <= 4) {
+    p.mt = M == 1 ? 1 : (M == 2 ? 2 : 4);
     const int64_t per_warp = 32 * static_cast<int64_t>(upt_max(p.mt));
     // warps per row: the fewest (a power of two, at most 8) whose chunks fit
     int lg = 0;
@@ -143,6 +128,28 @@ inline Plan make(int64_t M, int64_t N, int64_t K) {
       p.split_log2 = lg;
       p.chunk = static_cast<int>(chunk);
       p.upt = static_cast<int>((chunk + 31) / 32);
+      p.ws_bytes = 0;
+      return p;
+    }
+  }
+  // A few tokens: the few-token tensor-core kernel when its clusters cover
+  // the weights in one wave of blocks (one per SM).  With more blocks than
+  // SMs its per-block latency repeats per wave, and the GEMM below (shared
+  // activation quantisation, stream-K or split-K over all SMs) measured
+  // faster: 1.3-1.8x on 6912 x 2560 at 64 tokens and on the 28672 x 8192 and
+  // 8192 x 28672 shapes at 8-64 tokens.
+  if (M >= 3 && M <= kSkMaxM) {
+    const int bn = M <= 16 ? 16 : (M <= 32 ? 32 : 64);
+    const int64_t tiles_n = (N + 127) / 128;
+    const int num_kt = static_cast<int>(p.Kp / 64);
+    int cs = 1, kp = 0;
+    if (tiles_n <= 65535 && sk_split(bn, tiles_n, num_kt, kSkMaxCs, &cs, &kp) && tiles_n * cs <= kRefSms) {
+      p.path = kSkinny;
+      p.bn = bn;
+      p.tiles_n = tiles_n;
+      p.tiles_m = 1;
+      p.sk_cs = cs;
+      p.sk_kt_per = kp;
       p.ws_bytes = 0;
       return p;
     }
