@@ -68,6 +68,9 @@ def _load():
     lib.bl_oracle_rescale.argtypes = [P, F, P, I64, I64, P]
     lib.bl_oracle_forward_packed.argtypes = [P, F, I64, I64, P, I64, P, P, P, P]
     lib.bl_oracle_rmsnorm_quant_act.argtypes = [P, P, F, I64, I64, P, P, P, P]
+    lib.bl_oracle_gamma_groups.argtypes = [P, I64, I64, I64, P]
+    lib.bl_oracle_ternarize_groups.argtypes = [P, I64, I64, I64, P, P]
+    lib.bl_oracle_rescale_groups.argtypes = [P, P, I64, P, I64, I64, P]
     _lib = lib
     return lib
 
@@ -233,6 +236,62 @@ def forward(W, x):
     packed, g = pack_weights(W)
     N, K = np.asarray(W).shape
     return forward_packed(packed, g, N, K, x), packed, g
+
+
+def _check_groups(N: int, G: int) -> None:
+    if G < 1 or N % G:
+        raise ValueError("group_rows must be >= 1 and divide N")
+
+
+def gamma_groups(W, G: int) -> np.ndarray:
+    """One absmean scale per group of G consecutive output rows:
+    gamma_g = fl32(fl32(S_g / (G*K)) + 1e-5), S_g the fp64 |W| sum of the
+    group's rows (row sums in row order), fp32 [N / G]."""
+    W = _f32(W)
+    N, K = W.shape
+    _check_groups(N, G)
+    g = np.empty((N // G,), np.float32)
+    _load().bl_oracle_gamma_groups(_ptr(W), N, K, G, _ptr(g))
+    return g
+
+
+def ternarize_groups(W, g, G: int) -> np.ndarray:
+    """clip(rne(fl32(W[n] / gamma_{n / G})), -1, 1) as int8 [N, K]."""
+    W = _f32(W)
+    N, K = W.shape
+    _check_groups(N, G)
+    g = np.ascontiguousarray(g, dtype=np.float32)
+    q = np.empty((N, K), np.int8)
+    _load().bl_oracle_ternarize_groups(_ptr(W), N, K, G, _ptr(g), _ptr(q))
+    return q
+
+
+def pack_weights_groups(W, G: int):
+    """W fp32 [N, K] -> (packed uint8 [N, row_bytes(K)], gamma fp32 [N / G])."""
+    g = gamma_groups(W, G)
+    return pack(ternarize_groups(W, g, G)), g
+
+
+def rescale_groups(acc, g, G: int, s) -> np.ndarray:
+    """y[m, n] = fl32(float(acc[m, n]) * fl32(gamma_{n / G} / s_m))."""
+    acc = np.ascontiguousarray(acc, dtype=np.int32)
+    s = np.ascontiguousarray(s, dtype=np.float32)
+    g = np.ascontiguousarray(g, dtype=np.float32)
+    M, N = acc.shape
+    _check_groups(N, G)
+    y = np.empty((M, N), np.float32)
+    _load().bl_oracle_rescale_groups(_ptr(acc), _ptr(g), G, _ptr(s), M, N, _ptr(y))
+    return y
+
+
+def forward_packed_groups(packed, g, G: int, N: int, K: int, x) -> np.ndarray:
+    """Forward with grouped weight scales: quant x, unpack, contract, rescale
+    each output row by its group's scale."""
+    packed = np.ascontiguousarray(packed, dtype=np.uint8)
+    if packed.shape != (N, row_bytes(K)):
+        raise ValueError("packed shape does not match (N, row_bytes(K))")
+    xq, s = quant_act(x)
+    return rescale_groups(matmul_i32(unpack(packed, K), xq), g, G, s)
 
 
 def rmsnorm_quant_act(x, gain=None, eps: float = 1e-5):

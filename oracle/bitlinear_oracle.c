@@ -250,6 +250,59 @@ void bl_oracle_forward_packed(const uint8_t *packed, float gamma, int64_t N,
   bl_oracle_rescale(acc, gamma, s, M, N, y);
 }
 
+/* Scale granularity: one weight scale per group of G consecutive output rows
+ * ([DeepDive 5.2]: the trainable BitLinear views W as (-1, group_size, K),
+ * i.e. groups of group_size output rows, group_size = 128; [DeepDive 2.2]:
+ * one scale per output row, i.e. G = 1).  The pages pair these groupings
+ * with a threshold-at-mean ternariser and learnt scales; this oracle keeps
+ * the absmean-round quantiser of the per-tensor case and only narrows the
+ * set the mean runs over: for group g = rows [gG, gG + G),
+ *   S_g     = sum over the group's rows, in row order, of the row sums of
+ *             |W| (fp64, sequential over k), as for the per-tensor S;
+ *   gamma_g = fl32( fl32(S_g / (G*K)) + 1e-5f );
+ *   Wq[n,k] = clip( rne( fl32(W[n,k] / gamma_{n/G}) ), -1, +1 );
+ *   y[m,n]  = fl32( float(acc[m,n]) * fl32(gamma_{n/G} / s_m) ).
+ * G must divide N (the pages' reshape needs it); G = N is the per-tensor
+ * scale. */
+void bl_oracle_gamma_groups(const float *W, int64_t N, int64_t K, int64_t G,
+                            float *gamma) {
+  for (int64_t g = 0; g < N / G; ++g) {
+    double S = 0.0;
+    for (int64_t n = g * G; n < (g + 1) * G; ++n) {
+      double row = 0.0;
+      for (int64_t k = 0; k < K; ++k) row += fabs((double)W[n * K + k]);
+      S += row;
+    }
+    float mean = (float)(S / ((double)G * (double)K));
+    gamma[g] = mean + 1e-5f;
+  }
+}
+
+void bl_oracle_ternarize_groups(const float *W, int64_t N, int64_t K, int64_t G,
+                                const float *gamma, int8_t *q) {
+  for (int64_t n = 0; n < N; ++n) {
+    float g = gamma[n / G];
+    for (int64_t k = 0; k < K; ++k) {
+      float r = W[n * K + k] / g;
+      float t = rintf(r);
+      if (t > 1.0f) t = 1.0f;
+      if (t < -1.0f) t = -1.0f;
+      q[n * K + k] = (int8_t)t;
+    }
+  }
+}
+
+void bl_oracle_rescale_groups(const int32_t *acc, const float *gamma, int64_t G,
+                              const float *s, int64_t M, int64_t N, float *y) {
+  for (int64_t m = 0; m < M; ++m) {
+    for (int64_t n = 0; n < N; ++n) {
+      float c = gamma[n / G] / s[m];
+      float a = (float)acc[m * N + n];
+      y[m * N + n] = a * c;
+    }
+  }
+}
+
 /* Fused subln RMSNorm + activation quantisation.
  * [CSDN-2B4T 2, item 3] and [CSDN-0.4GB 1] 归一化方法: subln normalisation
  * sits before the quantised projection; no bias anywhere.

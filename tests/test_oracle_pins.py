@@ -443,3 +443,93 @@ def test_output_residual_is_one_fp32_add():
     out = oracle.output(y, r)
     assert np.array_equal(out, (y.astype(np.float64) + r.astype(np.float64)).astype(np.float32))
     assert np.array_equal(oracle.output(y), y)
+
+
+# ------------------------------------------------- grouped weight scales
+# "BitNet b1.58 深度解析" (chenxutan.com) section 5.2 groups the weight's
+# output rows by 128 for its scales, section 2.2 keeps one scale per output
+# row; the absmean-round quantiser is kept, only the mean's support narrows.
+
+def test_groups_of_all_rows_are_the_per_tensor_scale():
+    """G = N is the per-tensor case: same scale, same codes, same outputs."""
+    rng = np.random.default_rng(11)
+    for N, K in ((256, 512), (96, 100), (1, 7)):
+        W = rng.normal(0, 0.02, (N, K)).astype(np.float32)
+        p1, g1 = oracle.pack_weights(W)
+        p2, g2 = oracle.pack_weights_groups(W, N)
+        assert g2.shape == (1,) and g2[0] == g1
+        assert np.array_equal(p1, p2)
+        x = rng.normal(0, 1, (3, K)).astype(np.float32)
+        y1 = oracle.forward_packed(p1, g1, N, K, x)
+        y2 = oracle.forward_packed_groups(p2, g2, N, N, K, x)
+        assert np.array_equal(y1.view(np.uint32), y2.view(np.uint32))
+
+
+def test_groups_hand_worked_per_row_example():
+    """Two rows, one scale each (G = 1), every value derived by hand.
+    Row 0 = [0.5, -0.5, 0.25, 0]: mean|w| = 1.25 / 4 = 0.3125, w / gamma =
+    [1.6, -1.6, 0.8, 0] -> rne, clip -> [1, -1, 1, 0].  Row 1 = [4, -2, 0, 1]:
+    mean 7 / 4 = 1.75, w / gamma = [2.29, -1.14, 0, 0.57] -> [1, -1, 0, 1].
+    (One scale for both rows, mean 8.25 / 8 = 1.03125, would zero row 0.)
+    Token [1, 2, 3, 4]: s = 127 / 4 = 31.75, x s = [31.75, 63.5, 95.25, 127]
+    -> [32, 64, 95, 127] (63.5 rounds to even); acc = [32 - 64 + 95,
+    32 - 64 + 127] = [63, 95]; y_n = acc_n * gamma_n / 31.75."""
+    W = np.array([[0.5, -0.5, 0.25, 0.0], [4.0, -2.0, 0.0, 1.0]], np.float32)
+    g = oracle.gamma_groups(W, 1)
+    assert g[0] == fl32(Fraction(5, 16) + Fraction(float(np.float32(1e-5))))
+    assert g[1] == fl32(Fraction(7, 4) + Fraction(float(np.float32(1e-5))))
+    q = oracle.ternarize_groups(W, g, 1)
+    assert q.tolist() == [[1, -1, 1, 0], [1, -1, 0, 1]]
+    assert oracle.ternarize(W, oracle.gamma(W)).tolist()[0] == [0, 0, 0, 0]
+    packed, g2 = oracle.pack_weights_groups(W, 1)
+    assert np.array_equal(g, g2)
+    x = np.array([[1.0, 2.0, 3.0, 4.0]], np.float32)
+    xq, s = oracle.quant_act(x)
+    assert xq.tolist() == [[32, 64, 95, 127]] and s[0] == np.float32(31.75)
+    y = oracle.forward_packed_groups(packed, g, 1, 2, 4, x)
+    for n, acc in enumerate((63, 95)):
+        exact = Fraction(acc) * Fraction(float(g[n])) / Fraction(127, 4)
+        assert abs(Fraction(float(y[0, n])) - exact) <= Y_REL * abs(exact)
+
+
+def test_groups_are_the_per_tensor_scale_of_each_row_block():
+    """G = 128 on three blocks of rows with magnitudes 1e-3, 1 and 30: each
+    block's codes and scale are the per-tensor ones of that block alone."""
+    rng = np.random.default_rng(12)
+    K = 200
+    W = np.concatenate([rng.normal(0, a, (128, K)) for a in (1e-3, 1.0, 30.0)]).astype(np.float32)
+    packed, g = oracle.pack_weights_groups(W, 128)
+    assert g.shape == (3,)
+    for b in range(3):
+        pb, gb = oracle.pack_weights(W[128 * b:128 * (b + 1)])
+        assert g[b] == gb
+        assert np.array_equal(packed[128 * b:128 * (b + 1)], pb)
+    # the small block survives its own scale (about a third zeros), and
+    # would not survive one scale for the whole tensor
+    q = oracle.unpack(packed, K)
+    assert 0.25 < np.mean(q[:128] == 0) < 0.45
+    assert np.all(oracle.ternarize(W, oracle.gamma(W))[:128] == 0)
+
+
+def test_groups_per_row_closed_form():
+    """W[n] = a_n t_n with t ternary and exactly a quarter zeros per row: the
+    row's absmean is 0.75 a_n, so W / gamma_n = +-1.33 or 0 and the codes are
+    t itself for scales a_n over five decades; y against exact rationals."""
+    rng = np.random.default_rng(13)
+    N, K, M = 40, 64, 3
+    t = np.zeros((N, K), np.int8)
+    for n in range(N):
+        nz = rng.permutation(K)[:48]
+        t[n, nz] = rng.choice(np.array([-1, 1], np.int8), 48)
+    a = (10.0 ** rng.uniform(-3, 2, N)).astype(np.float32)
+    W = (t.astype(np.float32) * a[:, None]).astype(np.float32)
+    packed, g = oracle.pack_weights_groups(W, 1)
+    assert np.array_equal(oracle.unpack(packed, K), t)
+    x = rng.normal(0, 1, (M, K)).astype(np.float32)
+    y = oracle.forward_packed_groups(packed, g, 1, N, K, x)
+    xq, s = oracle.quant_act(x)
+    for m in range(M):
+        for n in range(N):
+            acc = int(np.dot(t[n].astype(np.int64), xq[m].astype(np.int64)))
+            exact = Fraction(acc) * Fraction(float(g[n])) / Fraction(float(s[m]))
+            assert abs(Fraction(float(y[m, n])) - exact) <= Y_REL * abs(exact)
