@@ -117,6 +117,25 @@ BL_API bl_status bitlinear_pack_weights(const void *W, int dtype, int64_t N, int
                                  uint8_t *packed, float *gamma, void *ws,
                                  size_t ws_bytes, void *stream);
 
+/* bitlinear_pack_weights with one scale per group of group_rows consecutive
+ * output rows instead of one per tensor: group_rows = 1 gives a scale per
+ * output channel, 128 the groups of the trainable BitLinear.  [深度解析 page,
+ * section 5.2 (weight viewed as (-1, group_size, in_features), group_size 128)
+ * and section 2.2 (a scale per output feature); the absmean-round quantiser
+ * of the per-tensor case is kept, the mean runs over the group's rows.]
+ *   group_rows  a power of two that divides N.
+ *   gamma       [N / group_rows] floats out, device, 4-byte aligned:
+ *               gamma_g = fl32(fl32(S_g / (group_rows*K)) + 1e-5f), S_g the
+ *               fp64 sum of |W| over the group's rows (sequential over k in
+ *               each row, then over the group's rows in order).
+ * Codes: Wq[n,k] = clip(rint(fl32(W[n,k] / gamma_{n / group_rows})), -1, 1).
+ * Other arguments and workspace as bitlinear_pack_weights.
+ * Errors: as bitlinear_pack_weights; BL_ERR_SHAPE for a group_rows that is
+ * not a power of two dividing N. */
+BL_API bl_status bitlinear_pack_weights_grouped(const void *W, int dtype, int64_t N, int64_t K,
+                                                int64_t group_rows, uint8_t *packed, float *gamma,
+                                                void *ws, size_t ws_bytes, void *stream);
+
 /* Per-token absmax int8 quantisation of activations.
  * [soaring_casia page, section 2, item 2; 0.4GB page, section 1 "激活8位量化".]
  *   x      [M, K] of `dtype`, device.
@@ -172,8 +191,8 @@ BL_API bl_status bitlinear_workspace_bytes(int64_t M, int64_t N, int64_t K,
  *   packed [N, row_bytes(K)] packed codes, device, 16-byte aligned.
  *   gamma  1 float, device (as written by bitlinear_pack_weights).
  *   x      [M, K] of `dtype`, device.
- *   y      [M, N] float out, device: y = fl32(fl32(float(acc) * gamma) / s_m),
- *          acc = sum_k Wq[n,k] * xq[m,k] (exact int32).
+ *   y      [M, N] float out, device: y = fl32(float(acc) * c_m) with
+ *          c_m = fl32(gamma / s_m), acc = sum_k Wq[n,k] * xq[m,k] (exact int32).
  *   ws     >= bitlinear_workspace_bytes(M, N, K) bytes, device, 256-aligned
  *          (may be NULL when that size is 0).  Calls that share a workspace
  *          must be ordered (same stream or synchronised).
@@ -213,6 +232,20 @@ BL_API bl_status bitlinear_forward_ex(const uint8_t *packed, const float *gamma,
                                       int64_t K, const void *x, int x_dtype, int64_t M, int act,
                                       void *y, int y_dtype, const void *residual, void *ws,
                                       size_t ws_bytes, void *stream);
+
+/* bitlinear_forward_ex for weights packed by bitlinear_pack_weights_grouped:
+ * row n is rescaled by its group's scale, y[m,n] = fl32(float(acc) * c) with
+ * c = fl32(gamma_{n / group_rows} / s_m) (one division per output element),
+ * then the residual and output dtype as bitlinear_forward_ex.
+ *   gamma       [N / group_rows] floats, device, 4-byte aligned.
+ *   group_rows  the value the weights were packed with (a power of two
+ *               dividing N).
+ * Other arguments, workspace and errors as bitlinear_forward_ex; BL_ERR_SHAPE
+ * for a group_rows that is not a power of two dividing N. */
+BL_API bl_status bitlinear_forward_grouped(const uint8_t *packed, const float *gamma, int64_t group_rows,
+                                           int64_t N, int64_t K, const void *x, int x_dtype, int64_t M,
+                                           int act, void *y, int y_dtype, const void *residual, void *ws,
+                                           size_t ws_bytes, void *stream);
 
 /* BitLinear forward on pre-quantised activations.
  *   xq     [M, K] int8 codes, device;  scale [M] float, device (s_m).

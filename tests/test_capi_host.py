@@ -128,6 +128,18 @@ def test_invalid_arguments_return_status(lib):
                                            None) == capi.BL_ERR_SHAPE
     assert lib.bitlinear_pack_weights(fake, 0, 4, 4, fake, fake, None, 0, None) == capi.BL_ERR_WORKSPACE
     assert lib.bitlinear_pack_weights(fake, 0, 4, 4, odd, fake, fake, 32, None) == capi.BL_ERR_ALIGN
+    # grouped scales: group_rows must be a power of two dividing N
+    for G in (0, 3, 8, -4):
+        assert lib.bitlinear_pack_weights_grouped(fake, 0, 4, 4, G, fake, fake, fake, 32,
+                                                  None) == capi.BL_ERR_SHAPE, G
+        assert lib.bitlinear_forward_grouped(fake, fake, G, 4, 4, fake, 0, 1, 0, fake, 0, None, None, 0,
+                                             None) == capi.BL_ERR_SHAPE, G
+    assert lib.bitlinear_pack_weights_grouped(fake, 0, 4, 4, 2, fake, fake, None, 0,
+                                              None) == capi.BL_ERR_WORKSPACE
+    assert lib.bitlinear_forward_grouped(fake, None, 2, 4, 4, fake, 0, 1, 0, fake, 0, None, None, 0,
+                                         None) == capi.BL_ERR_NULL
+    assert lib.bitlinear_forward_grouped(fake, ctypes.c_void_p(0x10002), 2, 4, 4, fake, 0, 1, 0, fake, 0, None,
+                                         None, 0, None) == capi.BL_ERR_ALIGN
 
 
 def test_no_device_is_reported_not_crashed(lib):

@@ -439,3 +439,45 @@ def test_decode_100b_shape_full(bl, N, K, Ms):
         assert_bits_equal(y.cpu().numpy(), oracle.forward_packed(p_ref, g_ref, N, K,
                                                                   x.float().numpy()),
                           f"100b {N}x{K} M={M}")
+
+
+# ------------------------------------------------- grouped weight scales
+@pytest.mark.parametrize("N,K,G,dtype", [(256, 512, 1, torch.float32), (384, 1000, 128, torch.bfloat16),
+                                         (6912, 2560, 128, torch.float32), (300, 70, 4, torch.float32)])
+def test_pack_weights_grouped(bl, N, K, G, dtype):
+    """One absmean scale per group of G output rows: codes and scales bit-exact."""
+    W = wl.weight(N, K, 0.02, 41 * N + G, "cpu")
+    W[: N // 2] *= 0.05  # groups of very different magnitude
+    W = W.to(dtype)
+    packed, gamma = bl.bitlinear_pack_weights_grouped(W.to(DEV), G)
+    torch.cuda.synchronize()
+    p_ref, g_ref = oracle.pack_weights_groups(W.float().numpy(), G)
+    assert np.array_equal(gamma.cpu().numpy().view(np.uint32), g_ref.view(np.uint32))
+    assert np.array_equal(packed.cpu().numpy(), p_ref)
+
+
+# M = 1, 3 (GEMV), 16 / 64 (few-token kernel), 130 (GEMM), 2048 (stream-K)
+@pytest.mark.parametrize("M,N,K", [(1, 384, 1000), (3, 2560, 2560), (16, 384, 1000), (64, 2560, 2560),
+                                   (130, 384, 1000), (2048, 2560, 320)])
+@pytest.mark.parametrize("G", [1, 128])
+def test_forward_grouped(bl, M, N, K, G):
+    """Grouped-scale forward on every path, bit-exact with the oracle; the
+    last case also through the bf16 output with an in-place residual."""
+    W = wl.weight(N, K, 0.02, 43 * N + K, "cpu")
+    W[N // 4: N // 2] *= 20.0
+    packed, gamma = bl.bitlinear_pack_weights_grouped(W.to(DEV), G)
+    p_ref, g_ref = oracle.pack_weights_groups(W.numpy(), G)
+    x = wl.activations(M, K, "outliers1pct", 47 * M + K, "cpu", torch.bfloat16)
+    y = bl.bitlinear_forward_grouped(packed, gamma, G, N, K, x.to(DEV))
+    torch.cuda.synchronize()
+    assert bl.device_error() == 0
+    y_ref = oracle.forward_packed_groups(p_ref, g_ref, G, N, K, x.float().numpy())
+    assert_bits_equal(y.cpu().numpy(), y_ref, f"grouped G={G} M={M} N={N} K={K}")
+    if M == 2048:
+        r = (torch.randn((M, N), generator=torch.Generator().manual_seed(G)) * 2).to(torch.bfloat16)
+        yb = r.to(DEV)
+        bl.bitlinear_forward_grouped(packed, gamma, G, N, K, x.to(DEV), y=yb, residual=yb, act=1)
+        torch.cuda.synchronize()
+        y2 = oracle.forward_packed_groups(p_ref, g_ref, G, N, K, oracle.relu2(x.float().numpy()))
+        want = oracle.output(y2, r.float().numpy(), bf16=True)
+        assert np.array_equal(yb.cpu().view(torch.int16).numpy().view(np.uint16), want)

@@ -25,10 +25,11 @@ from .capi import BitLinearError
 __all__ = [
     "BitLinearError", "BitLinear", "packed_row_bytes", "packed_bytes",
     "pack_workspace_bytes", "workspace_bytes", "bitlinear_pack_weights",
-    "bitlinear_quant_act", "bitlinear_rmsnorm_quant_act", "bitlinear_forward",
-    "bitlinear_forward_q", "bitlinear_matmul_i32", "bitlinear_forward_noalloc",
-    "set_launch_overlap",
-    "get_launch_overlap", "device_error", "library_path",
+    "bitlinear_pack_weights_grouped", "bitlinear_quant_act", "bitlinear_relu2_quant_act",
+    "bitlinear_rmsnorm_quant_act", "bitlinear_forward", "bitlinear_forward_ex",
+    "bitlinear_forward_grouped", "bitlinear_forward_relu2", "bitlinear_forward_q",
+    "bitlinear_matmul_i32", "bitlinear_forward_noalloc", "bitlinear_forward_chain",
+    "set_launch_overlap", "get_launch_overlap", "device_error", "library_path",
 ]
 
 _DTYPES = {torch.float32: capi.BL_F32, torch.bfloat16: capi.BL_BF16}
@@ -117,6 +118,25 @@ def bitlinear_pack_weights(W: torch.Tensor, packed: torch.Tensor | None = None,
     return packed, gamma
 
 
+def bitlinear_pack_weights_grouped(W: torch.Tensor, group_rows: int, packed: torch.Tensor | None = None,
+                                   gamma: torch.Tensor | None = None):
+    """Absmean-ternarise W [N, K] with one scale per group of group_rows output
+    rows (a power of two dividing N; 1 = per output channel) ->
+    (packed uint8 [N, row_bytes], gamma fp32 [N / group_rows])."""
+    _need_cuda("W", W, (torch.float32, torch.bfloat16), 2)
+    N, K = W.shape
+    rb = packed_row_bytes(K)
+    if packed is None:
+        packed = torch.empty((N, rb), dtype=torch.uint8, device=W.device)
+    if gamma is None:
+        gamma = torch.empty((max(N // max(int(group_rows), 1), 1),), dtype=torch.float32, device=W.device)
+    ws = torch.empty(pack_workspace_bytes(N, K), dtype=torch.uint8, device=W.device)
+    capi.check(_lib().bitlinear_pack_weights_grouped(
+        _ptr(W), _DTYPES[W.dtype], N, K, int(group_rows), _ptr(packed), _ptr(gamma), _ptr(ws), ws.numel(),
+        _stream(W)), "bitlinear_pack_weights_grouped")
+    return packed, gamma
+
+
 def bitlinear_quant_act(x: torch.Tensor, xq: torch.Tensor | None = None,
                         scale: torch.Tensor | None = None):
     """Per-token absmax int8 codes of x [M, K] -> (xq int8 [M, K], s fp32 [M])."""
@@ -194,6 +214,31 @@ def bitlinear_forward_ex(packed: torch.Tensor, gamma: torch.Tensor, N: int, K: i
         _ptr(packed), _ptr(gamma), N, K, _ptr(x), _DTYPES[x.dtype], M, int(act), _ptr(y),
         _DTYPES[y.dtype], _ptr(residual), _ptr(ws), 0 if ws is None else ws.numel(), _stream(x)),
         "bitlinear_forward_ex")
+    return y
+
+
+def bitlinear_forward_grouped(packed: torch.Tensor, gamma: torch.Tensor, group_rows: int, N: int, K: int,
+                              x: torch.Tensor, y: torch.Tensor | None = None,
+                              y_dtype: torch.dtype = torch.float32, residual: torch.Tensor | None = None,
+                              act: int = 0, workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """bitlinear_forward_ex for weights packed with one scale per group of
+    group_rows output rows (gamma fp32 [N / group_rows])."""
+    _need_cuda("packed", packed, torch.uint8)
+    _need_cuda("gamma", gamma, torch.float32)
+    _need_cuda("x", x, (torch.float32, torch.bfloat16), 2)
+    M = x.shape[0]
+    if x.shape[1] != K:
+        raise ValueError("x.shape[1] != K")
+    if y is None:
+        y = torch.empty((M, N), dtype=y_dtype, device=x.device)
+    _need_cuda("y", y, (torch.float32, torch.bfloat16), 2)
+    if residual is not None:
+        _need_cuda("residual", residual, y.dtype, 2)
+    ws = _workspace(workspace_bytes(M, N, K), x.device, workspace)
+    capi.check(_lib().bitlinear_forward_grouped(
+        _ptr(packed), _ptr(gamma), int(group_rows), N, K, _ptr(x), _DTYPES[x.dtype], M, int(act), _ptr(y),
+        _DTYPES[y.dtype], _ptr(residual), _ptr(ws), 0 if ws is None else ws.numel(), _stream(x)),
+        "bitlinear_forward_grouped")
     return y
 
 

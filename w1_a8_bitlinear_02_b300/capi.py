@@ -59,6 +59,9 @@ SIGNATURES = {
     "bitlinear_relu2_quant_act": (_INT, [_P, _INT, _I64, _I64, _P, _P, _P]),
     "bitlinear_forward_chain": (_INT, [_P, _INT, _P, _SZ, _P]),
     "bitlinear_forward_ex": (_INT, [_P, _P, _I64, _I64, _P, _INT, _I64, _INT, _P, _INT, _P, _P, _SZ, _P]),
+    "bitlinear_pack_weights_grouped": (_INT, [_P, _INT, _I64, _I64, _I64, _P, _P, _P, _SZ, _P]),
+    "bitlinear_forward_grouped": (_INT, [_P, _P, _I64, _I64, _I64, _P, _INT, _I64, _INT, _P, _INT, _P, _P, _SZ,
+                                         _P]),
     "bitlinear_forward_relu2": (_INT, [_P, _P, _I64, _I64, _P, _INT, _I64, _P, _P, _SZ, _P]),
     "bitlinear_set_launch_overlap": (None, [_INT]),
     "bitlinear_get_launch_overlap": (_INT, []),

@@ -577,11 +577,22 @@ bl_status bitlinear_pack_workspace_bytes(int64_t N, int64_t K, size_t *bytes) {
   return BL_OK;
 }
 
-bl_status bitlinear_pack_weights(const void *W, int dtype, int64_t N, int64_t K, uint8_t *packed,
-                                 float *gamma, void *ws, size_t ws_bytes, void *stream) {
+// log2 of a power of two, else -1.
+static int log2_exact(int64_t v) {
+  if (v < 1 || (v & (v - 1)) != 0) return -1;
+  int l = 0;
+  while ((int64_t(1) << l) < v) ++l;
+  return l;
+}
+
+// group_rows 0: one per-tensor scale; otherwise one per group of group_rows rows.
+static bl_status pack_common(const void *W, int dtype, int64_t N, int64_t K, int64_t group_rows,
+                             uint8_t *packed, float *gamma, void *ws, size_t ws_bytes, void *stream) {
   if (W == nullptr || packed == nullptr || gamma == nullptr) return BL_ERR_NULL;
   if (dtype != BL_F32 && dtype != BL_BF16) return BL_ERR_DTYPE;
   if (N < 1 || N > kMaxDim || K < 1 || K > kMaxK) return BL_ERR_SHAPE;
+  const int glog2 = group_rows == 0 ? -1 : log2_exact(group_rows);
+  if (group_rows != 0 && (glog2 < 0 || N % group_rows != 0)) return BL_ERR_SHAPE;
   if (ws == nullptr || ws_bytes < static_cast<size_t>(N) * sizeof(double)) return BL_ERR_WORKSPACE;
   if (!aligned(packed, 16) || !aligned(ws, 8) || !aligned(gamma, 4)) return BL_ERR_ALIGN;
   int dev = 0;
@@ -593,25 +604,39 @@ bl_status bitlinear_pack_weights(const void *W, int dtype, int64_t N, int64_t K,
   const unsigned gsum = static_cast<unsigned>((N + 255) / 256);
   const unsigned gcode = static_cast<unsigned>((N * wpr + 255) / 256);
   uint32_t *pw = reinterpret_cast<uint32_t *>(packed);
-  if (dtype == BL_F32) {
-    const float *w = static_cast<const float *>(W);
-    if ((s = launch(&pack_rowsum_kernel<float>, dim3(gsum), dim3(256), 0, st, false, w, N, K, rowsum)))
-      return s;
-    if ((s = launch(&pack_gamma_kernel, dim3(1), dim3(32), 0, st, false,
-                    static_cast<const double *>(rowsum), N, K, gamma)))
-      return s;
-    return launch(&pack_codes_kernel<float>, dim3(gcode), dim3(256), 0, st, false, w, N, K, wpr,
-                  static_cast<const float *>(gamma), pw);
+  if (dtype == BL_F32)
+    s = launch(&pack_rowsum_kernel<float>, dim3(gsum), dim3(256), 0, st, false, static_cast<const float *>(W),
+               N, K, rowsum);
+  else
+    s = launch(&pack_rowsum_kernel<__nv_bfloat16>, dim3(gsum), dim3(256), 0, st, false,
+               static_cast<const __nv_bfloat16 *>(W), N, K, rowsum);
+  if (s != BL_OK) return s;
+  if (group_rows == 0) {
+    s = launch(&pack_gamma_kernel, dim3(1), dim3(32), 0, st, false, static_cast<const double *>(rowsum), N, K,
+               gamma);
+  } else {
+    const int64_t groups = N / group_rows;
+    s = launch(&pack_gamma_groups_kernel, dim3(static_cast<unsigned>((groups + 127) / 128)), dim3(128), 0, st,
+               false, static_cast<const double *>(rowsum), groups, group_rows, K, gamma);
   }
-  const __nv_bfloat16 *w = static_cast<const __nv_bfloat16 *>(W);
-  if ((s = launch(&pack_rowsum_kernel<__nv_bfloat16>, dim3(gsum), dim3(256), 0, st, false, w, N, K,
-                  rowsum)))
-    return s;
-  if ((s = launch(&pack_gamma_kernel, dim3(1), dim3(32), 0, st, false, static_cast<const double *>(rowsum),
-                  N, K, gamma)))
-    return s;
-  return launch(&pack_codes_kernel<__nv_bfloat16>, dim3(gcode), dim3(256), 0, st, false, w, N, K, wpr,
-                static_cast<const float *>(gamma), pw);
+  if (s != BL_OK) return s;
+  if (dtype == BL_F32)
+    return launch(&pack_codes_kernel<float>, dim3(gcode), dim3(256), 0, st, false, static_cast<const float *>(W),
+                  N, K, wpr, static_cast<const float *>(gamma), glog2, pw);
+  return launch(&pack_codes_kernel<__nv_bfloat16>, dim3(gcode), dim3(256), 0, st, false,
+                static_cast<const __nv_bfloat16 *>(W), N, K, wpr, static_cast<const float *>(gamma), glog2, pw);
+}
+
+bl_status bitlinear_pack_weights(const void *W, int dtype, int64_t N, int64_t K, uint8_t *packed,
+                                 float *gamma, void *ws, size_t ws_bytes, void *stream) {
+  return pack_common(W, dtype, N, K, 0, packed, gamma, ws, ws_bytes, stream);
+}
+
+bl_status bitlinear_pack_weights_grouped(const void *W, int dtype, int64_t N, int64_t K, int64_t group_rows,
+                                         uint8_t *packed, float *gamma, void *ws, size_t ws_bytes,
+                                         void *stream) {
+  if (group_rows < 1) return BL_ERR_SHAPE;
+  return pack_common(W, dtype, N, K, group_rows, packed, gamma, ws, ws_bytes, stream);
 }
 
 static bl_status quant_common(const void *x, int dtype, const float *g, float eps, bool norm, int64_t M,
@@ -698,6 +723,23 @@ bl_status bitlinear_forward_ex(const uint8_t *packed, const float *gamma, int64_
   if (y == nullptr) return BL_ERR_NULL;
   const int xm = x_dtype == BL_F32 ? gemv::kXF32 : gemv::kXBF16;
   const OutSpec out{y, residual, y_dtype == BL_BF16 ? 1 : 0};
+  return forward_common(packed, gamma, N, K, xm, act == BL_ACT_RELU2 ? kActRelu2 : kActNone, x, nullptr, nullptr,
+                        M, out, nullptr, ws, ws_bytes, stream);
+}
+bl_status bitlinear_forward_grouped(const uint8_t *packed, const float *gamma, int64_t group_rows, int64_t N,
+                                    int64_t K, const void *x, int x_dtype, int64_t M, int act, void *y,
+                                    int y_dtype, const void *residual, void *ws, size_t ws_bytes, void *stream) {
+  if (x_dtype != BL_F32 && x_dtype != BL_BF16) return BL_ERR_DTYPE;
+  if (y_dtype != BL_F32 && y_dtype != BL_BF16) return BL_ERR_DTYPE;
+  if (act != BL_ACT_NONE && act != BL_ACT_RELU2) return BL_ERR_SHAPE;
+  if (y == nullptr || gamma == nullptr) return BL_ERR_NULL;
+  const int glog2 = log2_exact(group_rows);
+  if (glog2 < 0 || N < 1 || N % group_rows != 0) return BL_ERR_SHAPE;
+  if (!aligned(gamma, 4)) return BL_ERR_ALIGN;
+  const int xm = x_dtype == BL_F32 ? gemv::kXF32 : gemv::kXBF16;
+  OutSpec out{y, residual, y_dtype == BL_BF16 ? 1 : 0};
+  out.gvec = gamma;
+  out.glog2 = glog2;
   return forward_common(packed, gamma, N, K, xm, act == BL_ACT_RELU2 ? kActRelu2 : kActNone, x, nullptr, nullptr,
                         M, out, nullptr, ws, ws_bytes, stream);
 }

@@ -412,7 +412,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                   if constexpr (OUT_I32)
                     p.acc_out[o] = v;
                   else
-                    put_y(p.out, o, __fmul_rn(static_cast<float>(v), bars.cscale[c0 + jj]));
+                    put_y(p.out, o, __fmul_rn(static_cast<float>(v), p.out.gvec ? group_scale(p.out, n, __ldg(p.scale + m))
+                                                                               : bars.cscale[c0 + jj]));
                 }
               }
             }
@@ -441,7 +442,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                   if (m >= p.M) break;
                   const int64_t o = static_cast<int64_t>(m) * p.N + n;
                   const int v = __ldcg(&p.ws_acc[o]);
-                  put_y(p.out, o, __fmul_rn(static_cast<float>(v), bars.cscale[c]));
+                  put_y(p.out, o, __fmul_rn(static_cast<float>(v), p.out.gvec ? group_scale(p.out, n, __ldg(p.scale + m))
+                                                                             : bars.cscale[c]));
                 }
               }
             }

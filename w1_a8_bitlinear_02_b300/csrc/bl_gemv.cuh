@@ -487,7 +487,8 @@ __global__ void __launch_bounds__((CW + 1) * 32, 1) gemv_kernel(const Params p) 
               if constexpr (OUT_I32)
                 p.acc[static_cast<int64_t>(m) * p.N + n] = q;
               else
-                put_y(p.out, static_cast<int64_t>(m) * p.N + n, __fmul_rn(static_cast<float>(q), cm[m]));
+                put_y(p.out, static_cast<int64_t>(m) * p.N + n,
+                      __fmul_rn(static_cast<float>(q), p.out.gvec ? group_scale(p.out, n, sc[m]) : cm[m]));
             }
           }
         }

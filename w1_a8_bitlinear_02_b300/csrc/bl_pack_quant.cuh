@@ -53,18 +53,32 @@ __global__ void pack_gamma_kernel(const double *__restrict__ rowsum, int64_t N, 
   *gamma = __fadd_rn(mean, 1e-5f);
 }
 
+// Grouped weights: gamma_g = fl32( fl32(S_g / (G*K)) + 1e-5f ) for each group
+// of G consecutive rows, S_g its row sums added in row order (one thread per
+// group, so the order is the same as the per-tensor scale's).
+__global__ void pack_gamma_groups_kernel(const double *__restrict__ rowsum, int64_t groups, int64_t G,
+                                         int64_t K, float *__restrict__ gamma) {
+  const int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (g >= groups) return;
+  double S = 0.0;
+  for (int64_t n = g * G; n < (g + 1) * G; ++n) S = __dadd_rn(S, rowsum[n]);
+  const float mean = __double2float_rn(__ddiv_rn(S, static_cast<double>(G) * static_cast<double>(K)));
+  gamma[g] = __fadd_rn(mean, 1e-5f);
+}
+
 // One thread per 32-bit packed word (16 weights).  Code = clip(rint(W/gamma))+1;
-// weight k = 16w + 4i + j goes to bit 8j + 2i; k >= K gets code 1.
+// weight k = 16w + 4i + j goes to bit 8j + 2i; k >= K gets code 1.  Row n
+// takes gamma[n >> glog2]; glog2 < 0: the one per-tensor scale gamma[0].
 template <typename WT>
 __global__ void __launch_bounds__(256) pack_codes_kernel(const WT *__restrict__ W, int64_t N,
                                                          int64_t K, int64_t words_per_row,
-                                                         const float *__restrict__ gamma,
+                                                         const float *__restrict__ gamma, int glog2,
                                                          uint32_t *__restrict__ packed) {
   const int64_t id = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (id >= N * words_per_row) return;
   const int64_t n = id / words_per_row;
   const int64_t w = id - n * words_per_row;
-  const float g = *gamma;
+  const float g = gamma[glog2 < 0 ? 0 : (n >> glog2)];
   const WT *row = W + n * K;
   uint32_t word = 0;
 #pragma unroll
@@ -140,10 +154,19 @@ __device__ __forceinline__ float relu2f(float v) {
 // adding first, in fp32, a residual of the output's dtype when one is given
 // (it may be y itself: each element is read and then written by one thread).
 struct OutSpec {
-  void *y;          // [M, N] fp32 or bf16
-  const void *res;  // [M, N] of the same dtype, or null
+  void *y;                      // [M, N] fp32 or bf16
+  const void *res;              // [M, N] of the same dtype, or null
   int bf16;
+  const float *gvec = nullptr;  // grouped weights: one scale per 2^glog2 output rows, else null
+  int glog2 = 0;
 };
+
+// Grouped weights: the output scale of token m at row n is fl32(gamma_g / s_m)
+// with g row n's group (per-tensor weights use c_m = fl32(gamma / s_m),
+// computed once per token).
+__device__ __forceinline__ float group_scale(const OutSpec &o, int64_t n, float s_m) {
+  return __fdiv_rn(__ldg(o.gvec + (n >> o.glog2)), s_m);
+}
 __device__ __forceinline__ void put_y(const OutSpec &o, int64_t i, float v) {
   if (o.res != nullptr)
     v = __fadd_rn(v, o.bf16 ? __bfloat162float(static_cast<const __nv_bfloat16 *>(o.res)[i])

@@ -477,7 +477,8 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
               if constexpr (OUT_I32)
                 p.acc[o] = sum[i];
               else
-                put_y(p.out, o, __fmul_rn(static_cast<float>(sum[i]), bars.cscale[m]));
+                put_y(p.out, o, __fmul_rn(static_cast<float>(sum[i]),
+                                          p.out.gvec ? group_scale(p.out, n, bars.sc[m]) : bars.cscale[m]));
             }
           } else {
             // to block m % cs, slot [this block][m / cs][row]
@@ -514,7 +515,8 @@ __global__ void __launch_bounds__(Cfg<BN>::kThreads, 1)
           if constexpr (OUT_I32)
             p.acc[o] = sum;
           else
-            put_y(p.out, o, __fmul_rn(static_cast<float>(sum), bars.cscale[m]));
+            put_y(p.out, o, __fmul_rn(static_cast<float>(sum),
+                                      p.out.gvec ? group_scale(p.out, n, bars.sc[m]) : bars.cscale[m]));
         }
       }
     }
