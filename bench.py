@@ -247,6 +247,7 @@ PROFILE_CASES = {
     "decode_100b_down": (1, 8192, 28672, "normal", 0.01, 6),
     "batch_m16_qkv": (16, 3840, 2560, "outliers1pct", 0.02, 6),
     "batch_m64_up": (64, 6912, 2560, "outliers1pct", 0.02, 6),
+    "batch_m8_100b_up": (8, 28672, 8192, "normal", 0.01, 6),
     "prefill_up": (2048, 6912, 2560, "normal", 0.02, 6),
     "prefill_down": (2048, 2560, 6912, "relu2", 0.02, 6),
 }
@@ -480,6 +481,37 @@ def run_extras(bl, wl, torch, device, stream, peaks, items2b, args):
             "how": "bitlinear_forward_chain: the 120 calls in one persistent launch, each call "
                    "waiting for the previous at a grid barrier"}
         del gch
+
+        # the same chained M=1 sweep with one weight scale per 128 output rows
+        # (grouped packing of the same seeded weights; the forward rescales
+        # each row by its group's scale)
+        G = 128
+        gits = []
+        for it in items2b:
+            mt = it["mt"]
+            W = wl.weight(mt.N, mt.K, mt.std, mt.seed, device)
+            pk, gv = bl.bitlinear_pack_weights_grouped(W, G)
+            del W
+            gits.append(dict(mt=mt, packed=pk, gamma=gv, x=it["x"], y=it["y"], ws=it["ws"]))
+        torch.cuda.synchronize()
+
+        def grouped_sweep():
+            for it in gits:
+                mt = it["mt"]
+                bl.bitlinear_forward_grouped(it["packed"], it["gamma"], G, mt.N, mt.K, it["x"], y=it["y"],
+                                             workspace=it["ws"])
+        gg = torch.cuda.CUDAGraph()
+        grouped_sweep()
+        stream.synchronize()
+        with torch.cuda.graph(gg, stream=stream):
+            grouped_sweep()
+        s = timed(gg.replay, max(3, min(args.steps, 200)))
+        nbg = nb + sum(4 * (it["mt"].N // G - 1) for it in items2b)  # the scale vectors
+        out["decode_2b_grouped128"] = {
+            "GB/s": nbg / s / 1e9, "frac_hbm": nbg / s / 1e9 / peaks["hbm_gbs"], "ms_per_sweep": s * 1e3,
+            "how": "bitlinear_forward_grouped, one weight scale per 128 output rows, the same "
+                   "120 chained calls (launch overlap on)"}
+        del gg, gits
 
         # batched decode on the same weights
         mats = [it["mt"] for it in items2b]
