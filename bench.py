@@ -39,7 +39,7 @@ WORKLOAD = "decode_2b"
 # DRAM bytes (read + write) per decode-GEMV launch, mean over the four ~2B
 # shapes, from one ncu capture (profiles/gemv_decode_2b_m1.md).  Valid only for
 # the kernel source whose sha256 starts with `src`; otherwise reported as null.
-GEMV_TRAFFIC = {"bytes_per_launch": 3281184.0, "src": "b3dc2b03b1740753",
+GEMV_TRAFFIC = {"bytes_per_launch": 3282560.0, "src": "d10bf5d2912effc9",
                 "file": "w1_a8_bitlinear_02_b300/csrc/bl_gemv.cuh"}
 
 

@@ -238,10 +238,10 @@ bl_status run_gemv(const plan::Plan &pl, int dev, int sms, int xm, int act, bool
 }
 
 // ------------------------------------------------------------ tensor-core dispatch
-template <int BN, bool OUT_I32>
+template <int BN, bool OUT_I32, bool GROUPED>
 bl_status run_tc_bn(const plan::Plan &pl, int dev, const CUtensorMap &mx, const CUtensorMap &mw,
                     const tc::Params &p, cudaStream_t st) {
-  auto *f = &tc::tc_gemm_kernel<BN, OUT_I32>;
+  auto *f = &tc::tc_gemm_kernel<BN, OUT_I32, GROUPED>;
   constexpr int smem = tc::Cfg<BN>::kSmemBytes;
   bl_status s = ensure_smem(dev, reinterpret_cast<const void *>(f), smem);
   if (s != BL_OK) return s;
@@ -270,17 +270,24 @@ bl_status run_tc_bn(const plan::Plan &pl, int dev, const CUtensorMap &mx, const 
   return launch(f, grid, dim3(tc::kThreads), smem, st, g_overlap.load() != 0, mx, mw, p);
 }
 
+template <bool OUT_I32, bool GROUPED>
+bl_status run_tc_g(const plan::Plan &pl, int dev, const CUtensorMap &mx, const CUtensorMap &mw,
+                   const tc::Params &p, cudaStream_t st) {
+  switch (pl.bn) {
+    case 16: return run_tc_bn<16, OUT_I32, GROUPED>(pl, dev, mx, mw, p, st);
+    case 32: return run_tc_bn<32, OUT_I32, GROUPED>(pl, dev, mx, mw, p, st);
+    case 64: return run_tc_bn<64, OUT_I32, GROUPED>(pl, dev, mx, mw, p, st);
+    case 128: return run_tc_bn<128, OUT_I32, GROUPED>(pl, dev, mx, mw, p, st);
+    case 256: return run_tc_bn<256, OUT_I32, GROUPED>(pl, dev, mx, mw, p, st);
+    default: return BL_ERR_UNSUPPORTED;
+  }
+}
+
 template <bool OUT_I32>
 bl_status run_tc(const plan::Plan &pl, int dev, const CUtensorMap &mx, const CUtensorMap &mw,
                  const tc::Params &p, cudaStream_t st) {
-  switch (pl.bn) {
-    case 16: return run_tc_bn<16, OUT_I32>(pl, dev, mx, mw, p, st);
-    case 32: return run_tc_bn<32, OUT_I32>(pl, dev, mx, mw, p, st);
-    case 64: return run_tc_bn<64, OUT_I32>(pl, dev, mx, mw, p, st);
-    case 128: return run_tc_bn<128, OUT_I32>(pl, dev, mx, mw, p, st);
-    case 256: return run_tc_bn<256, OUT_I32>(pl, dev, mx, mw, p, st);
-    default: return BL_ERR_UNSUPPORTED;
-  }
+  if (!OUT_I32 && p.out.gvec != nullptr) return run_tc_g<OUT_I32, true>(pl, dev, mx, mw, p, st);
+  return run_tc_g<OUT_I32, false>(pl, dev, mx, mw, p, st);
 }
 
 // ------------------------------------------------------------ few-token dispatch

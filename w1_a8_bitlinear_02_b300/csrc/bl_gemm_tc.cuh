@@ -171,7 +171,10 @@ __device__ __forceinline__ void st_release_u32(unsigned *p, unsigned v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-template <int BN, bool OUT_I32>
+// GROUPED: weights with one scale per group of output rows (the output scale
+// is fl32(gamma_g / s_m) per element); a separate instantiation so that the
+// per-tensor epilogue stays as tight as before.
+template <int BN, bool OUT_I32, bool GROUPED = false>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
                    const Params p) {
@@ -409,11 +412,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (m < p.M) {
                   const int64_t o = static_cast<int64_t>(m) * p.N + n;
                   const int v = static_cast<int>(__uint_as_float(r[jj]));
-                  if constexpr (OUT_I32)
+                  if constexpr (OUT_I32) {
                     p.acc_out[o] = v;
-                  else
-                    put_y(p.out, o, __fmul_rn(static_cast<float>(v), p.out.gvec ? group_scale(p.out, n, __ldg(p.scale + m))
-                                                                               : bars.cscale[c0 + jj]));
+                  } else {
+                    float cmn;
+                    if constexpr (GROUPED)
+                      cmn = group_scale(p.out, n, __ldg(p.scale + m));
+                    else
+                      cmn = bars.cscale[c0 + jj];
+                    put_y(p.out, o, __fmul_rn(static_cast<float>(v), cmn));
+                  }
                 }
               }
             }
@@ -442,8 +450,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                   if (m >= p.M) break;
                   const int64_t o = static_cast<int64_t>(m) * p.N + n;
                   const int v = __ldcg(&p.ws_acc[o]);
-                  put_y(p.out, o, __fmul_rn(static_cast<float>(v), p.out.gvec ? group_scale(p.out, n, __ldg(p.scale + m))
-                                                                             : bars.cscale[c]));
+                  float cmn;
+                  if constexpr (GROUPED)
+                    cmn = group_scale(p.out, n, __ldg(p.scale + m));
+                  else
+                    cmn = bars.cscale[c];
+                  put_y(p.out, o, __fmul_rn(static_cast<float>(v), cmn));
                 }
               }
             }
