@@ -442,7 +442,7 @@ bl_status forward_tc(const plan::Plan &pl, int dev, int xm, int act, bool out_i3
     cudaGetLastError();
     return BL_ERR_CUDA;
   }
-  const bool streamk = pl.streamk && sms >= pl.sk_grid;
+  const bool streamk = pl.streamk && sms * tc::blocks_per_sm(pl.bn) >= pl.sk_grid;
 
   // 1) activations -> bf16 codes (+ scales), zeroing the split-K accumulators
   //    or the stream-K flags

@@ -52,20 +52,26 @@ constexpr int kBM = 128;                 // weight rows per tile
 constexpr int kBK = 64;                  // k per stage
 constexpr int kPBytes = kBM * kBK / 4;   // packed weights per stage
 constexpr int kSmemBudget = 210 * 1024;
-constexpr int kTmemCols = 512;
+// Token tiles of up to 32 use half the tensor memory (256 columns) and at
+// least 80 KB of shared memory, so two blocks share an SM (never three): at a
+// few tokens one block's barrier round trips and single-thread MMA issue leave
+// the SM mostly idle, and a second block fills it.
+__host__ __device__ constexpr int blocks_per_sm(int bn) { return bn <= 32 ? 2 : 1; }
 
 template <int BN>
 struct Cfg {
   static constexpr int kBBytes = BN * kBK * 2;
   static constexpr int kStageBytes = kBBytes + kPBytes;
   static constexpr int kDCols = BN < 32 ? 32 : BN;
+  static constexpr int kTmemCols = blocks_per_sm(BN) == 2 ? 256 : 512;
   static constexpr int kBySmem = kSmemBudget / kStageBytes;
   static constexpr int kByTmem = (kTmemCols - kDCols) / 32;
   static constexpr int kMin = kBySmem < kByTmem ? kBySmem : kByTmem;
   // even, so each ring slot always serves the same unpack group
   static constexpr int kStages = (kMin < 8 ? kMin : 8) & ~1;
   // stages + up to 1023 bytes of alignment slack + the barrier block
-  static constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 3072;
+  static constexpr int kSmemRaw = kStages * kStageBytes + 1024 + 3072;
+  static constexpr int kSmemBytes = blocks_per_sm(BN) == 2 && kSmemRaw < 80 * 1024 ? 80 * 1024 : kSmemRaw;
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
   static_assert(kStages >= 2, "pipeline depth");
   static_assert(kDCols + 32 * kStages <= kTmemCols, "tensor memory columns");
@@ -175,7 +181,7 @@ __device__ __forceinline__ void st_release_u32(unsigned *p, unsigned v) {
 // is fl32(gamma_g / s_m) per element); a separate instantiation so that the
 // per-tensor epilogue stays as tight as before.
 template <int BN, bool OUT_I32, bool GROUPED = false>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, blocks_per_sm(BN))
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
                    const Params p) {
   using C = Cfg<BN>;
@@ -206,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tensormap(&map_w);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(&bars.tmem_base), kTmemCols);
+    tmem_alloc(smem_u32(&bars.tmem_base), C::kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -470,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc(tmem, C::kTmemCols);
   }
 }
 

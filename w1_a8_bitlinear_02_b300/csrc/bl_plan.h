@@ -162,9 +162,11 @@ inline Plan make(int64_t M, int64_t N, int64_t K) {
   p.tiles_m = (M + bn - 1) / bn;
   const int64_t tiles = p.tiles_n * p.tiles_m;
   const int num_kt = static_cast<int>(p.Kp / 64);
+  // block slots: token tiles of up to 32 run two blocks per SM
+  const int64_t slots = static_cast<int64_t>(kRefSms) * (bn <= 32 ? 2 : 1);
   int splits = 1;
-  if (tiles < kRefSms / 2) {
-    int by_sms = static_cast<int>(kRefSms / tiles);
+  if (tiles < slots / 2) {
+    int by_sms = static_cast<int>(slots / tiles);
     int by_k = num_kt / 2 > 0 ? num_kt / 2 : 1;
     splits = by_sms < by_k ? by_sms : by_k;
     if (splits < 1) splits = 1;
@@ -172,13 +174,13 @@ inline Plan make(int64_t M, int64_t N, int64_t K) {
   p.kt_per_split = (num_kt + splits - 1) / splits;
   p.splits = (num_kt + p.kt_per_split - 1) / p.kt_per_split;
   p.tiles_total = static_cast<int>(tiles < 0x7fffffff ? tiles : 0x7fffffff);
-  if (p.splits == 1 && tiles >= kRefSms && tiles * num_kt < 0x7fffffff) {
-    const int64_t waves = (tiles + kRefSms - 1) / kRefSms;
-    if (tiles * 10 < waves * kRefSms * 9) {  // whole tiles would leave > 10 % of the SMs idle
+  if (p.splits == 1 && tiles >= slots && tiles * num_kt < 0x7fffffff) {
+    const int64_t waves = (tiles + slots - 1) / slots;
+    if (tiles * 10 < waves * slots * 9) {  // whole tiles would leave > 10 % of the slots idle
       p.streamk = 1;
-      p.sk_grid = kRefSms;
+      p.sk_grid = static_cast<int>(slots);
       p.units = static_cast<int>(tiles * num_kt);
-      p.units_per = (p.units + kRefSms - 1) / kRefSms;  // >= num_kt since tiles >= kRefSms
+      p.units_per = static_cast<int>((p.units + slots - 1) / slots);  // >= num_kt since tiles >= slots
     }
   }
   size_t off = 0;
