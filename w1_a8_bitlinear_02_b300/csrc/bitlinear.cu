@@ -238,6 +238,11 @@ bl_status run_gemv(const plan::Plan &pl, int dev, int sms, int xm, int act, bool
 }
 
 // ------------------------------------------------------------ tensor-core dispatch
+static_assert(plan::tc_blocks_per_sm(16) == tc::blocks_per_sm(16) && plan::tc_blocks_per_sm(32) == tc::blocks_per_sm(32) &&
+                  plan::tc_blocks_per_sm(64) == tc::blocks_per_sm(64) &&
+                  plan::tc_blocks_per_sm(128) == tc::blocks_per_sm(128) &&
+                  plan::tc_blocks_per_sm(256) == tc::blocks_per_sm(256),
+              "planner and GEMM kernel agree on blocks per SM");
 template <int BN, bool OUT_I32, bool GROUPED>
 bl_status run_tc_bn(const plan::Plan &pl, int dev, const CUtensorMap &mx, const CUtensorMap &mw,
                     const tc::Params &p, cudaStream_t st) {

@@ -52,11 +52,11 @@ constexpr int kBM = 128;                 // weight rows per tile
 constexpr int kBK = 64;                  // k per stage
 constexpr int kPBytes = kBM * kBK / 4;   // packed weights per stage
 constexpr int kSmemBudget = 210 * 1024;
-// Token tiles of up to 32 use half the tensor memory (256 columns) and at
+// Token tiles of up to 64 use half the tensor memory (256 columns) and at
 // least 80 KB of shared memory, so two blocks share an SM (never three): at a
 // few tokens one block's barrier round trips and single-thread MMA issue leave
 // the SM mostly idle, and a second block fills it.
-__host__ __device__ constexpr int blocks_per_sm(int bn) { return bn <= 32 ? 2 : 1; }
+__host__ __device__ constexpr int blocks_per_sm(int bn) { return bn <= 64 ? 2 : 1; }
 
 template <int BN>
 struct Cfg {

@@ -104,6 +104,10 @@ inline bool sk_split(int bn, int64_t tiles_n, int num_kt, int cs_max, int *cs, i
   return false;
 }
 
+// GEMM blocks sharing one SM at token tile bn (the kernel's tensor-memory and
+// shared-memory sizes are chosen for it; bitlinear.cu checks that they agree).
+inline constexpr int tc_blocks_per_sm(int bn) { return bn <= 64 ? 2 : 1; }
+
 inline Plan make(int64_t M, int64_t N, int64_t K) {
   Plan p;
   p.M = M;
@@ -162,8 +166,8 @@ inline Plan make(int64_t M, int64_t N, int64_t K) {
   p.tiles_m = (M + bn - 1) / bn;
   const int64_t tiles = p.tiles_n * p.tiles_m;
   const int num_kt = static_cast<int>(p.Kp / 64);
-  // block slots: token tiles of up to 32 run two blocks per SM
-  const int64_t slots = static_cast<int64_t>(kRefSms) * (bn <= 32 ? 2 : 1);
+  // block slots: token tiles of up to 64 run two GEMM blocks per SM
+  const int64_t slots = static_cast<int64_t>(kRefSms) * tc_blocks_per_sm(bn);
   int splits = 1;
   if (tiles < slots / 2) {
     int by_sms = static_cast<int>(slots / tiles);
