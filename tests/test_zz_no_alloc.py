@@ -54,8 +54,8 @@ def test_noalloc_matches_forward_twice(lib, M, N, K):
     torch.cuda.set_device(dev)
     need = ctypes.c_size_t()
     assert lib.bitlinear_workspace_bytes(M, N, K, ctypes.byref(need)) == 0
-    # M > 64 (tensor-core GEMM) uses the scratch; 3 <= M <= 64 runs on the
-    # few-token kernel, which needs none
+    # M > 64 (tensor-core GEMM) uses the scratch; these few-token shapes run on
+    # the few-token kernel (one wave of clusters), which needs none
     assert need.value <= 8 << 20
     assert (need.value > 0) == (M > 64)
     W = wl.weight(N, K, 0.02, 7 * N + K, dev)
