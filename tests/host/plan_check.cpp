@@ -3,7 +3,9 @@
 // warps, its stages fit their buffers and shared memory, its grid covers N
 // exactly once; every tensor-core plan covers M, N and all k tiles; every
 // few-token plan gives each block of a cluster at least one k tile, fits its
-// operands in shared memory and holds the split-K sums it receives.
+// operands in shared memory and holds the split-K sums it receives, and its
+// clusters fit one wave of blocks; GEMM plans count two blocks per SM for
+// token tiles of up to 64.
 #include <cstdio>
 #include <cstdlib>
 #include <initializer_list>
@@ -14,7 +16,7 @@ int main() {
   const int sms = 148;
   for (long M = 1; M <= 300; M += (M < 16 ? 1 : 37))
     for (long K : {1L, 15L, 16L, 63L, 64L, 65L, 100L, 333L, 512L, 1000L, 2560L, 4096L, 6912L, 8192L, 9000L, 16384L, 28672L, 32768L, 65536L, 131072L})
-      for (long N : {1L, 7L, 128L, 129L, 256L, 300L, 513L, 2560L, 3840L, 6912L, 8192L, 28672L}) {
+      for (long N : {1L, 7L, 128L, 129L, 256L, 300L, 513L, 2560L, 3840L, 6912L, 8192L, 28672L, 40960L}) {
         Plan p = make(M, N, K);
         ++checked;
         if (p.path == kGemv) {
@@ -22,7 +24,7 @@ int main() {
           const int G = 1 << p.split_log2;
           const long units = p.row_bytes / 8;
           GemvGrid g = gemv_grid(p, sms);
-          bool ok = M <= 8 && G <= g.cw && (g.cw >> p.split_log2) >= 1 &&
+          bool ok = M <= 4 && G <= g.cw && (g.cw >> p.split_log2) >= 1 &&
                     (long)p.chunk * G >= units && p.upt * 32 >= p.chunk && p.upt >= 1 &&
                     p.upt <= upt_max(p.mt) && (g.cw == 8 || (g.cw == 16 && p.mt == 1));
           ok = ok && g.grid >= 1 && (long)g.grid * g.rows_per_cta >= N && (long)(g.grid - 1) * g.rows_per_cta < N;
@@ -37,7 +39,8 @@ int main() {
           ++sk;
           const long nkt = p.Kp / 64;
           bool ok = M >= 3 && M <= kSkMaxM && (p.bn == 16 || p.bn == 32 || p.bn == 64) && p.bn >= M &&
-                    p.tiles_n * 128 >= N && (p.tiles_n - 1) * 128 < N && p.ws_bytes == 0;
+                    p.tiles_n * 128 >= N && (p.tiles_n - 1) * 128 < N && p.ws_bytes == 0 &&
+                    p.tiles_n * p.sk_cs <= kRefSms;
           ok = ok && p.sk_cs >= 1 && p.sk_cs <= kSkMaxCs && p.sk_kt_per >= 1 &&
                (long)p.sk_cs * p.sk_kt_per >= nkt && (long)(p.sk_cs - 1) * p.sk_kt_per < nkt;
           // every smaller cluster the launch may pick instead keeps the same properties
@@ -63,7 +66,7 @@ int main() {
             // every unit once (trailing blocks may get none); the workspace holds
             // one partial tile and one flag per block
             const long nkt = p.Kp / 64;
-            ok = ok && p.splits == 1 && p.sk_grid == kRefSms && p.units == (long)p.tiles_total * nkt &&
+            ok = ok && p.splits == 1 && p.sk_grid == kRefSms * tc_blocks_per_sm(p.bn) && p.units == (long)p.tiles_total * nkt &&
                  p.units_per >= nkt && (long)p.units_per * p.sk_grid >= p.units &&
                  p.off_cnt >= p.off_part + (size_t)p.sk_grid * p.bn * 128 * 4 &&
                  p.ws_bytes >= p.off_cnt + (size_t)p.sk_grid * 4;
