@@ -5,7 +5,7 @@
 // few-token plan gives each block of a cluster at least one k tile, fits its
 // operands in shared memory and holds the split-K sums it receives, and its
 // clusters fit one wave of blocks; GEMM plans count two blocks per SM for
-// token tiles of up to 64.
+// token tiles of up to 64 and use stream-K only at one block per SM.
 #include <cstdio>
 #include <cstdlib>
 #include <initializer_list>
@@ -66,7 +66,7 @@ int main() {
             // every unit once (trailing blocks may get none); the workspace holds
             // one partial tile and one flag per block
             const long nkt = p.Kp / 64;
-            ok = ok && p.splits == 1 && p.sk_grid == kRefSms * tc_blocks_per_sm(p.bn) && p.units == (long)p.tiles_total * nkt &&
+            ok = ok && p.splits == 1 && tc_blocks_per_sm(p.bn) == 1 && p.sk_grid == kRefSms && p.units == (long)p.tiles_total * nkt &&
                  p.units_per >= nkt && (long)p.units_per * p.sk_grid >= p.units &&
                  p.off_cnt >= p.off_part + (size_t)p.sk_grid * p.bn * 128 * 4 &&
                  p.ws_bytes >= p.off_cnt + (size_t)p.sk_grid * 4;

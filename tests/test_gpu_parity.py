@@ -382,13 +382,16 @@ def test_batched_decode_2b_shapes_full(bl, name, N, K, kind):
 
 
 @pytest.mark.parametrize("M,N,K", [(2048, 2560, 320), (1900, 2500, 300), (2048, 2560, 6912),
-                                   (8, 20480, 640), (24, 20480, 640), (40, 19000, 448)])
+                                   (8, 20480, 640), (24, 20480, 640), (40, 19000, 448),
+                                   (8, 40960, 640), (24, 40960, 640), (40, 38000, 448)])
 def test_streamk_tiles_full_output(bl, M, N, K):
     """Tile counts that fill the last wave poorly (149-160 tiles on 148 SMs) run
     stream-K: tiles are shared by two blocks whose int32 partials meet in the
     workspace.  Whole outputs (forward and matmul_i32) against the oracle; the
     third shape is the prefill down projection itself, checked in full; the
-    last three have token tiles of 16, 32 and 64 (a few tokens on many rows)."""
+    rest have token tiles of 16, 32 and 64 (a few tokens on many rows), which
+    run as whole tiles two blocks per SM (149-160 tiles in one wave, 297-320 in
+    two) rather than stream-K."""
     packed, gamma, p_ref, g_ref = pack_both(bl, N, K, 0.02, 17 * N + K)
     x = wl.activations(M, K, "outliers1pct", 3 * M + K, "cpu", torch.bfloat16)
     y = bl.bitlinear_forward(packed, gamma, N, K, x.to(DEV))

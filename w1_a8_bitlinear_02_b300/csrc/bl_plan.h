@@ -178,13 +178,16 @@ inline Plan make(int64_t M, int64_t N, int64_t K) {
   p.kt_per_split = (num_kt + splits - 1) / splits;
   p.splits = (num_kt + p.kt_per_split - 1) / p.kt_per_split;
   p.tiles_total = static_cast<int>(tiles < 0x7fffffff ? tiles : 0x7fffffff);
-  if (p.splits == 1 && tiles >= slots && tiles * num_kt < 0x7fffffff) {
-    const int64_t waves = (tiles + slots - 1) / slots;
-    if (tiles * 10 < waves * slots * 9) {  // whole tiles would leave > 10 % of the slots idle
+  // Stream-K (a cooperative grid, one block per SM) only for token tiles that
+  // run one block per SM; smaller tiles take whole tiles over their 296 slots
+  // (a cooperative grid of two blocks per SM was refused at launch).
+  if (p.splits == 1 && tc_blocks_per_sm(bn) == 1 && tiles >= kRefSms && tiles * num_kt < 0x7fffffff) {
+    const int64_t waves = (tiles + kRefSms - 1) / kRefSms;
+    if (tiles * 10 < waves * kRefSms * 9) {  // whole tiles would leave > 10 % of the SMs idle
       p.streamk = 1;
-      p.sk_grid = static_cast<int>(slots);
+      p.sk_grid = kRefSms;
       p.units = static_cast<int>(tiles * num_kt);
-      p.units_per = static_cast<int>((p.units + slots - 1) / slots);  // >= num_kt since tiles >= slots
+      p.units_per = (p.units + kRefSms - 1) / kRefSms;  // >= num_kt since tiles >= kRefSms
     }
   }
   size_t off = 0;
