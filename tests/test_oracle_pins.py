@@ -533,3 +533,25 @@ def test_groups_per_row_closed_form():
             acc = int(np.dot(t[n].astype(np.int64), xq[m].astype(np.int64)))
             exact = Fraction(acc) * Fraction(float(g[n])) / Fraction(float(s[m]))
             assert abs(Fraction(float(y[m, n])) - exact) <= Y_REL * abs(exact)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_groups_random_shapes_match_per_tensor_of_each_group(seed):
+    """For random N, K and group sizes G dividing N, every group's scale and
+    codes equal the per-tensor oracle applied to that group's rows alone, and
+    the grouped rescale of each group's rows equals the per-tensor rescale."""
+    rng = np.random.default_rng(100 + seed)
+    G = int(rng.choice([1, 2, 4, 8, 16]))
+    N = G * int(rng.integers(1, 6))
+    K = int(rng.integers(1, 150))
+    W = (rng.normal(0, 1, (N, K)) * (10.0 ** rng.uniform(-3, 1, (N, 1)))).astype(np.float32)
+    packed, g = oracle.pack_weights_groups(W, G)
+    x = rng.normal(0, 1, (3, K)).astype(np.float32)
+    y = oracle.forward_packed_groups(packed, g, G, N, K, x)
+    for b in range(N // G):
+        rows = slice(b * G, (b + 1) * G)
+        pb, gb = oracle.pack_weights(W[rows])
+        assert g[b] == gb
+        assert np.array_equal(packed[rows], pb)
+        yb = oracle.forward_packed(pb, gb, G, K, x)
+        assert np.array_equal(y[:, rows].view(np.uint32), yb.view(np.uint32))
