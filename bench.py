@@ -37,8 +37,8 @@ METRIC = "BitLinear GB/s (decode, % HBM peak) and int8 TOPS (prefill, % INT8 pea
 WORKLOAD = "decode_2b"
 
 # DRAM bytes (read + write) per decode-GEMV launch, mean over the four ~2B
-# shapes, from one ncu capture (profiles/gemv_decode_2b_m1.md).  Valid only for
-# the kernel source whose sha256 starts with `src`; otherwise reported as null.
+# shapes, from one ncu capture of the kernel source whose sha256 starts with
+# `src`; reported as null once that source has changed.
 GEMV_TRAFFIC = {"bytes_per_launch": 3282560.0, "src": "d10bf5d2912effc9",
                 "file": "w1_a8_bitlinear_02_b300/csrc/bl_gemv.cuh"}
 
@@ -170,6 +170,24 @@ def prepare(bl, wl, mats, M: int, device, x_dtype):
     return out
 
 
+def to_slabs(items, torch):
+    """Move every call's x (and y) into one contiguous device buffer, so an
+    end-to-end step copies all inputs in with one transfer and all outputs out
+    with one.  Each call keeps a view; offsets stay 16-byte aligned."""
+    for key in ("x", "y"):
+        ts = [it[key] for it in items]
+        slab = torch.empty(sum(t.numel() for t in ts), dtype=ts[0].dtype, device=ts[0].device)
+        off = 0
+        for it, t in zip(items, ts):
+            v = slab[off:off + t.numel()].view(t.shape)
+            v.copy_(t)
+            it[key] = v
+            off += t.numel()
+            assert (v.data_ptr() % 16) == 0
+        items[0]["_" + key + "_slab"] = slab
+    return items[0]["_x_slab"], items[0]["_y_slab"]
+
+
 def sweep_calls(bl, items):
     for it in items:
         mt = it["mt"]
@@ -213,11 +231,31 @@ def launches_per_call(bl, M: int, N: int, K: int) -> int:
 
 
 # ------------------------------------------------------------------ CPU oracle timing
-def oracle_timing(items_host, budget_s: float, min_reps: int = 1):
-    """Time the CPU oracle's forward on host copies of (packed, gamma, x).
-    Returns (seconds, algorithmic bytes, calls, threads)."""
+ORACLE_WARM_S = 1.5  # thread pool up, caches warm, other CPU work settled
+
+
+def oracle_warm(items_host, seconds: float = ORACLE_WARM_S) -> float:
+    """Run the oracle's forward over the items for `seconds`; return the mean
+    seconds per call seen (used to size a bounded sample)."""
     import oracle
     oracle.set_threads(os.cpu_count() or 1)
+    t0 = time.perf_counter()
+    calls = 0
+    while True:
+        for (packed, g, N, K, x) in items_host:
+            oracle.forward_packed(packed, g, N, K, x)
+            calls += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            return el / calls
+
+
+def oracle_timing(items_host, budget_s: float):
+    """Time the CPU oracle's forward on host copies of (packed, gamma, x) for
+    about `budget_s` seconds after the same warm-up as the reference arm.
+    Returns (seconds, algorithmic bytes, calls, threads)."""
+    import oracle
+    oracle_warm(items_host)
     t0 = time.perf_counter()
     nbytes, calls = 0, 0
     while True:
@@ -226,7 +264,7 @@ def oracle_timing(items_host, budget_s: float, min_reps: int = 1):
             nbytes += algorithmic_bytes(x.shape[0], N, K)
             calls += 1
         el = time.perf_counter() - t0
-        if el >= budget_s and calls >= min_reps:
+        if el >= budget_s:
             return el, nbytes, calls, oracle.get_threads()
 
 
@@ -277,9 +315,13 @@ def run_profile_case(name: str):
 
 # ------------------------------------------------------------------ reference arm
 def run_reference(args, rank: int):
+    """The CPU oracle on a bounded sample of the headline workload: layer 0's
+    four projections at M = 1 (inputs drawn and packed on the host by the
+    oracle itself).  A step is R forward calls cycling through the four
+    projections, R sized from the warm-up so that the K timed steps take about
+    REF_TIMED_S seconds; value = algorithmic bytes / time."""
     if rank != 0:
         return
-    import numpy as np
     import oracle
     import torch
     from w1_a8_bitlinear_02_b300 import workloads as wl
@@ -290,35 +332,40 @@ def run_reference(args, rank: int):
         packed, g = oracle.pack_weights(W)
         x = wl.activations(1, mt.K, mt.x_kind, mt.seed + 500, "cpu", torch.bfloat16)
         items.append((packed, float(g), mt.N, mt.K, x.float().numpy()))
-    oracle.set_threads(os.cpu_count() or 1)
-    nb_step = [algorithmic_bytes(1, N, K) for (_, _, N, K, _) in items]
+    t_call = oracle_warm(items)
     for i in range(args.warmup):
         p, g, N, K, x = items[i % len(items)]
         oracle.forward_packed(p, g, N, K, x)
+    R = int(min(1000, max(len(items), -(-REF_TIMED_S // (args.steps * t_call)))))
     t0 = time.perf_counter()
-    nbytes = 0
-    for i in range(args.steps):
-        p, g, N, K, x = items[i % len(items)]
-        oracle.forward_packed(p, g, N, K, x)
-        nbytes += nb_step[i % len(items)]
+    nbytes, c = 0, 0
+    for _ in range(args.steps):
+        for _ in range(R):
+            p, g, N, K, x = items[c % len(items)]
+            oracle.forward_packed(p, g, N, K, x)
+            nbytes += algorithmic_bytes(1, N, K)
+            c += 1
     el = time.perf_counter() - t0
     gbs = nbytes / el / 1e9
     cores = oracle.get_threads()
-    sample = ("one BitLinear forward per step at M=1, cycling through layer 0's four "
-              "projections (QKV, O, up, down) of the ~2B decode workload")
+    sample = (f"{R} oracle forwards per step at M=1, cycling through layer 0's four projections "
+              f"(QKV, O, up, down) of the ~2B decode workload; {args.steps * R} calls, "
+              f"{el:.1f} s timed after {ORACLE_WARM_S} s of warm-up calls")
     line = {
         "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int8", "data": "synthetic",
-        "config": {"workload": "decode_2b M=1 (CPU oracle, bounded sample)",
-                   "sample": sample},
+        "config": {"workload": "decode_2b M=1 (CPU oracle, bounded sample)", "sample": sample},
         "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
     print(json.dumps(line), flush=True)
+
+
+REF_TIMED_S = 6.0
 
 
 # ------------------------------------------------------------------ our arm
@@ -337,6 +384,7 @@ def run_ours(args, rank: int, world: int, local: int):
 
     mats = wl.matrices(WORKLOAD, layers=args.layers)
     items = prepare(bl, wl, mats, 1, device, torch.bfloat16)
+    x_slab, y_slab = to_slabs(items, torch)
     step_bytes = sum(algorithmic_bytes(1, it["mt"].N, it["mt"].K) for it in items)
     packed_bytes = sum(it["packed"].numel() for it in items)
     g = capture(bl, items, stream)
@@ -349,7 +397,9 @@ def run_ours(args, rank: int, world: int, local: int):
     ms_step = secs_max / args.steps * 1e3
     assert bl.device_error() == 0, "a kernel reported a device-side failure"
 
-    # the dominant kernel: the M=1 GEMV, one launch per matrix
+    # the dominant kernel: the M=1 GEMV, the only kernel of the step (one
+    # launch per matrix); with launch overlap consecutive launches overlap, so
+    # the per-launch duration is the step time divided by the launches
     per_launch_s = secs / (args.steps * len(items))
     per_launch_bytes = step_bytes / len(items)
     achieved = per_launch_bytes / per_launch_s / 1e9
@@ -358,24 +408,25 @@ def run_ours(args, rank: int, world: int, local: int):
                 "traffic_unit": "bytes per launch (dram read + write, ncu)",
                 "algorithmic_bytes_per_launch": per_launch_bytes,
                 "kernel": "bl::gemv::gemv_kernel<1,*,bf16>",
+                "duration": "step time / launches per step (CUDA events on the launching stream; "
+                            "the GEMV is the only kernel in the step)",
                 "peak_source": f"{peaks['source']} (copy bandwidth)"}
 
     # end to end: pinned host x -> device, the sweep, device y -> pinned host
-    xs_host = [it["x"].cpu().pin_memory() for it in items]
-    ys_host = [torch.empty_like(it["y"], device="cpu").pin_memory() for it in items]
-    h2d = sum(x.numel() * x.element_size() for x in xs_host)
-    d2h = sum(y.numel() * y.element_size() for y in ys_host)
+    # (one copy each way per step: the calls' inputs and outputs are slabs)
+    x_host = x_slab.cpu().pin_memory()
+    y_host = torch.empty_like(y_slab, device="cpu").pin_memory()
+    h2d = x_host.numel() * x_host.element_size()
+    d2h = y_host.numel() * y_host.element_size()
 
     def e2e_step():
-        for xh, it in zip(xs_host, items):
-            it["x"].copy_(xh, non_blocking=True)
+        x_slab.copy_(x_host, non_blocking=True)
         g.replay()
-        for yh, it in zip(ys_host, items):
-            yh.copy_(it["y"], non_blocking=True)
+        y_host.copy_(y_slab, non_blocking=True)
 
     with torch.cuda.stream(stream):
-        e2e_steps = max(1, min(args.steps, 200))
-        for _ in range(min(args.warmup, 5)):
+        e2e_steps = max(1, min(args.steps, 1000))
+        for _ in range(max(3, min(args.warmup, 20))):
             e2e_step()
         stream.synchronize()
         D.barrier()
@@ -389,7 +440,8 @@ def run_ours(args, rank: int, world: int, local: int):
     e2e_s, e2e_bytes = D.aggregate(e0.elapsed_time(e1) / 1e3, step_bytes * e2e_steps, device)
     e2e = {"value": e2e_bytes / e2e_s / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": d2h,
-           "how": "per step: pinned-host x -> device, the 120-call graph, y -> pinned host"}
+           "how": "per step: one pinned-host -> device copy of every call's x (one slab), the "
+                  "120-call graph, one device -> pinned-host copy of every call's y (one slab)"}
 
     extras = {}
     if not args.no_extras:
@@ -534,7 +586,10 @@ def run_extras(bl, wl, torch, device, stream, peaks, items2b, args):
             del g, its
         out["decode_2b_batch"] = bd
 
-        # prefill M = 2048 on the tensor-core path (forward = quant + GEMM)
+        # prefill M = 2048 on the tensor-core path (forward = activation
+        # quantisation kernel + GEMM kernel).  The GEMM's own time is
+        # estimated as the forward's minus that of bitlinear_quant_act on the
+        # same x (the same one-pass quantisation, int8 instead of bf16 codes).
         pf = {}
         for name, N, K, kind in (("up", 6912, 2560, "normal"), ("down", 2560, 6912, "relu2")):
             W = wl.weight(N, K, 0.02, wl.weight_seed("prefill_2b", 0, 0) + N, device)
@@ -543,23 +598,35 @@ def run_extras(bl, wl, torch, device, stream, peaks, items2b, args):
             x = wl.activations(2048, K, kind, 4500 + K, device, torch.bfloat16)
             y = torch.empty((2048, N), dtype=torch.float32, device=device)
             ws = torch.empty(bl.workspace_bytes(2048, N, K), dtype=torch.uint8, device=device)
+            xq = torch.empty((2048, K), dtype=torch.int8, device=device)
+            sc = torch.empty((2048,), dtype=torch.float32, device=device)
             s = timed(lambda: bl.bitlinear_forward(packed, gamma, N, K, x, y=y, workspace=ws), reps)
+            sq = timed(lambda: bl.bitlinear_quant_act(x, xq=xq, scale=sc), reps)
             ops = 2 * 2048 * N * K
             tops = ops / s / 1e12
+            tops_g = ops / max(s - sq, 1e-9) / 1e12
             pf[name] = {"N": N, "K": K, "M": 2048, "ms": s * 1e3, "TOPS_dense_equiv": tops,
                         "frac_bf16_peak": tops / peaks["bf16_tflops"],
+                        "quant_ms": sq * 1e3, "gemm_ms_est": (s - sq) * 1e3,
+                        "gemm_roofline": {"bound": "tensor", "achieved": tops_g,
+                                          "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                                          "frac": tops_g / peaks["bf16_tflops"],
+                                          "duration": "forward time minus bitlinear_quant_act time "
+                                                      "(CUDA events, same stream)"},
                         "note": "sm_103a has no integer MMA; int8 x ternary runs exactly as "
                                 "bf16 x bf16 -> fp32 on tcgen05 (kind::f16); peak = measured "
                                 "dense bf16 (burst)"}
-            del packed, gamma, x, y, ws
+            del packed, gamma, x, y, ws, xq, sc
         out["prefill_2b"] = pf
 
-        # 100B-class decode: 80 layers x {28672x8192, 8192x28672}, 9.4 GB resident
+        # 100B-class decode: 80 layers x {28672x8192, 8192x28672}, 9.4 GB
+        # resident; M = 1 chained (launch overlap mode 1) and as independent
+        # calls (mode 2: the GEMV's own streaming rate), M = 8 chained
         if not args.no_100b:
             mats = wl.matrices("decode_100b")
             its = prepare(bl, wl, mats, 1, device, torch.bfloat16)
             res = {}
-            for M in (1, 8):
+            for M, mode in ((1, 1), (1, 2), (8, 1)):
                 if M == 8:
                     for it in its:
                         mt = it["mt"]
@@ -568,12 +635,17 @@ def run_extras(bl, wl, torch, device, stream, peaks, items2b, args):
                         it["y"] = torch.empty((8, mt.N), dtype=torch.float32, device=device)
                         wsn = bl.workspace_bytes(8, mt.N, mt.K)
                         it["ws"] = torch.empty(wsn, dtype=torch.uint8, device=device) if wsn else None
+                bl.set_launch_overlap(mode)
                 g = capture(bl, its, stream)
                 s = timed(g.replay, max(3, min(args.steps, 20)))
+                bl.set_launch_overlap(0 if args.no_overlap else 1)
                 nb = sum(algorithmic_bytes(M, it["mt"].N, it["mt"].K) for it in its)
-                res[f"M={M}"] = {"GB/s": nb / s / 1e9, "frac_hbm": nb / s / 1e9 / peaks["hbm_gbs"],
-                                 "ms_per_sweep": s * 1e3,
-                                 "resident_packed_GB": sum(it["packed"].numel() for it in its) / 1e9}
+                res[f"M={M}" + ("" if mode == 1 else " independent")] = {
+                    "GB/s": nb / s / 1e9, "frac_hbm": nb / s / 1e9 / peaks["hbm_gbs"],
+                    "ms_per_sweep": s * 1e3, "us_per_call": s * 1e6 / len(its),
+                    "resident_packed_GB": sum(it["packed"].numel() for it in its) / 1e9,
+                    "how": ("chained calls (launch overlap mode 1)" if mode == 1 else
+                            "independent calls (launch overlap mode 2)")}
                 del g
             del its
             out["decode_100b"] = res

@@ -180,7 +180,9 @@ BL_API bl_status bitlinear_relu2_quant_act(const void *x, int dtype, int64_t M, 
 
 /* Workspace (device bytes) needed by bitlinear_forward, bitlinear_forward_q
  * and bitlinear_matmul_i32 for these sizes; 0 when the chosen path needs
- * none (small M).  Host output.  Errors: BL_ERR_NULL, BL_ERR_SHAPE. */
+ * none (small M).  Host output.  Errors: BL_ERR_NULL, BL_ERR_SHAPE (also for
+ * sizes whose launch grid would exceed the device's limits, e.g. more than
+ * 65535 token tiles: M beyond about 16.7 million). */
 BL_API bl_status bitlinear_workspace_bytes(int64_t M, int64_t N, int64_t K,
                                     size_t *bytes);
 
@@ -344,11 +346,13 @@ BL_API bl_status bitlinear_forward_chain(const bl_chain_call *calls, int n, void
  *                for it before touching anything else.  Precondition:
  *                `packed` and `gamma` are not written by the kernel launched
  *                immediately before on the same stream.
- *   2            as 1, and the decode kernel (M <= 8) does not wait at all:
- *                for batches of independent calls.  Precondition: no buffer
- *                of the call (inputs or output) is written or read by the
- *                kernel launched immediately before it on the same stream.
- *                Calls on the tensor-core path (larger M) behave as in 1.
+ *   2            as 1, and a call that runs on the GEMV path (M = 1 with
+ *                K <= 65536, M = 2 with K <= 32768, or M = 3..4 with
+ *                K <= 16384) does not wait at all: for batches of independent
+ *                calls.  Precondition: no
+ *                buffer of the call (inputs or output) is written or read by
+ *                the kernel launched immediately before it on the same
+ *                stream.  Calls on the tensor-core paths behave as in 1.
  * Out-of-range values are clamped to 0..2. */
 BL_API void bitlinear_set_launch_overlap(int mode);
 BL_API int bitlinear_get_launch_overlap(void);

@@ -19,6 +19,10 @@ int main() {
       for (long N : {1L, 7L, 128L, 129L, 256L, 300L, 513L, 2560L, 3840L, 6912L, 8192L, 28672L, 40960L}) {
         Plan p = make(M, N, K);
         ++checked;
+        // the GEMV takes exactly the calls the header documents for launch
+        // overlap mode 2
+        const bool want_gemv = (M == 1 && K <= 65536) || (M == 2 && K <= 32768) || ((M == 3 || M == 4) && K <= 16384);
+        if ((p.path == kGemv) != want_gemv) { printf("BAD route M=%ld N=%ld K=%ld\n", M, N, K); return 1; }
         if (p.path == kGemv) {
           ++gemv;
           const int G = 1 << p.split_log2;

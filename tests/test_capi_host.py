@@ -142,6 +142,23 @@ def test_invalid_arguments_return_status(lib):
                                          None, 0, None) == capi.BL_ERR_ALIGN
 
 
+def test_grid_limits_are_checked_before_launch(lib):
+    """A token count whose GEMM grid would need more than 65535 token tiles is
+    refused as a shape error, by the size query and by the forward, before
+    anything is enqueued (fake pointers, never dereferenced)."""
+    from w1_a8_bitlinear_02_b300 import capi
+    sz = ctypes.c_size_t()
+    fake = ctypes.c_void_p(0x10000)
+    M = 20_000_000  # 78125 tiles of 256 tokens
+    assert lib.bitlinear_workspace_bytes(M, 64, 64, ctypes.byref(sz)) == capi.BL_ERR_SHAPE
+    assert lib.bitlinear_forward(fake, fake, 64, 64, fake, capi.BL_BF16, M, fake, fake, 1 << 40,
+                                 None) == capi.BL_ERR_SHAPE
+    assert lib.bitlinear_forward_noalloc(fake, fake, 64, 64, fake, capi.BL_BF16, M, fake,
+                                         None) == capi.BL_ERR_SHAPE
+    # 65535 tiles of 256 tokens still plan
+    assert lib.bitlinear_workspace_bytes(65535 * 256, 64, 64, ctypes.byref(sz)) == capi.BL_OK
+
+
 def test_no_device_is_reported_not_crashed(lib):
     import torch
     if torch.cuda.is_available():

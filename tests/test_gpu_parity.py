@@ -9,7 +9,7 @@ squares is summed in a different order (documented in the header): it is held
 to the 1e-6 relative tolerance while its codes stay bit-exact.
 
 Sizes span several tiles and ragged tails and run in seconds on the oracle;
-the last tests use the full workload shapes with per-token sampling.
+the last tests use the full workload shapes, whole outputs.
 """
 from __future__ import annotations
 
@@ -121,7 +121,8 @@ def test_rmsnorm_quant_act(bl, M, K, gain, dtype):
 
 # ------------------------------------------------------------------ forward
 SHAPES = [(256, 512), (300, 100), (130, 2560), (513, 1000)]
-MS = [1, 2, 3, 4, 5, 7, 8, 9, 16, 33, 64, 65, 130, 257]
+# 17-32 tokens take the few-token kernel's 32-token tile (bn = 32)
+MS = [1, 2, 3, 4, 5, 7, 8, 9, 16, 17, 24, 32, 33, 64, 65, 130, 257]
 
 
 @pytest.mark.parametrize("N,K", SHAPES)
@@ -138,7 +139,7 @@ def test_forward(bl, M, N, K):
 
 
 @pytest.mark.parametrize("N,K", [(256, 512), (300, 100), (513, 1000)])
-@pytest.mark.parametrize("M", [1, 3, 4, 7, 64, 200])
+@pytest.mark.parametrize("M", [1, 3, 4, 7, 17, 32, 64, 200])
 def test_forward_q_and_matmul_i32(bl, M, N, K):
     packed, gamma, p_ref, g_ref = pack_both(bl, N, K, 0.02, 13 * N + K)
     x = wl.activations(M, K, "normal", 7 * M + K, "cpu", torch.float32)
@@ -165,9 +166,9 @@ def test_relu2_quant_act(bl, M, K, dtype):
     assert_bits_equal(s.cpu().numpy(), s_ref, "relu2 scales")
 
 
-# M = 1 (GEMV), 3 / 16 / 64 (few-token kernel), 130 (tensor-core GEMM)
+# M = 1 (GEMV), 3 / 16 / 32 / 64 (few-token kernel), 130 (tensor-core GEMM)
 @pytest.mark.parametrize("N,K", [(300, 100), (513, 1000), (2560, 6912)])
-@pytest.mark.parametrize("M", [1, 3, 16, 64, 130])
+@pytest.mark.parametrize("M", [1, 3, 16, 32, 64, 130])
 def test_forward_relu2(bl, M, N, K):
     """The down projection of a ReLU^2 FFN in one call: every path applies the
     squared ReLU where it quantises x, bit-exact with the oracle and with
@@ -185,9 +186,10 @@ def test_forward_relu2(bl, M, N, K):
     assert torch.equal(y.view(torch.int32), y2.view(torch.int32))
 
 
-# M = 1, 2 (GEMV), 3, 33, 64 (few-token kernel), 130 (tensor-core GEMM);
+# M = 1, 2 (GEMV), 3, 24, 33, 64 (few-token kernel), 130 (tensor-core GEMM);
 # the last shape also takes stream-K at M = 2048 (one case below)
-@pytest.mark.parametrize("M,N,K", [(1, 513, 1000), (2, 300, 100), (3, 513, 1000), (33, 2560, 2560),
+@pytest.mark.parametrize("M,N,K", [(1, 513, 1000), (2, 300, 100), (3, 513, 1000), (24, 2560, 2560),
+                                   (33, 2560, 2560),
                                    (64, 384, 768), (130, 300, 100), (2048, 2560, 320)])
 @pytest.mark.parametrize("y_dtype,res,act", [(torch.float32, None, 0), (torch.bfloat16, None, 0),
                                              (torch.float32, "sep", 1), (torch.bfloat16, "inplace", 0),
@@ -364,11 +366,12 @@ def test_decode_2b_shapes_full(bl, name, N, K, kind):
 
 @pytest.mark.parametrize("name,N,K,kind", [(n, N, K, k) for n, N, K, k in wl.PROJ_2B])
 def test_batched_decode_2b_shapes_full(bl, name, N, K, kind):
-    """Batched decode on one layer of the ~2B model: M = 3 (GEMV), 5, 16, 33 and
-    64 tokens (the few-token kernel, or the GEMM where that needs more than one
-    wave) with 1 % outlier channels, whole outputs, through forward and forward_q."""
+    """Batched decode on one layer of the ~2B model: M = 3 (GEMV), 5, 8, 16, 17,
+    24, 32, 33 and 64 tokens (the few-token kernel at its 16-, 32- and 64-token
+    tiles, or the GEMM where that needs more than one wave) with 1 % outlier
+    channels, whole outputs, through forward and forward_q."""
     packed, gamma, p_ref, g_ref = pack_both(bl, N, K, 0.02, wl.weight_seed("decode_2b", 1, 0) + N)
-    for M in (3, 5, 16, 33, 64):
+    for M in (3, 5, 8, 16, 17, 24, 32, 33, 64):
         x = wl.activations(M, K, "outliers1pct", 91 + M, "cpu", torch.bfloat16)
         y = bl.bitlinear_forward(packed, gamma, N, K, x.to(DEV))
         xq_ref, s_ref = oracle.quant_act(x.float().numpy())
@@ -405,20 +408,17 @@ def test_streamk_tiles_full_output(bl, M, N, K):
 
 
 @pytest.mark.parametrize("N,K,kind", [(6912, 2560, "normal"), (2560, 6912, "relu2")])
-def test_prefill_2048_sampled_tokens(bl, N, K, kind):
-    """M = 2048 on the tensor-core path; 12 sampled tokens checked in full
-    (tokens are independent, so a sampled row is exactly the full result's)."""
+def test_prefill_2048_full(bl, N, K, kind):
+    """M = 2048 on the tensor-core path (up projection: whole 256-token tiles;
+    down projection: stream-K), the whole output against the oracle."""
     M = 2048
     packed, gamma, p_ref, g_ref = pack_both(bl, N, K, 0.02, 4000 + N)
     x = wl.activations(M, K, kind, 4500 + K, "cpu", torch.bfloat16)
     y = bl.bitlinear_forward(packed, gamma, N, K, x.to(DEV))
     torch.cuda.synchronize()
     assert bl.device_error() == 0
-    rows = np.random.default_rng(0).choice(M, 12, replace=False)
-    rows[:2] = (0, M - 1)
-    xs = x.float().numpy()[rows]
-    assert_bits_equal(y.cpu().numpy()[rows], oracle.forward_packed(p_ref, g_ref, N, K, xs),
-                      "prefill")
+    assert_bits_equal(y.cpu().numpy(), oracle.forward_packed(p_ref, g_ref, N, K, x.float().numpy()),
+                      f"prefill {N}x{K}")
 
 
 @pytest.mark.parametrize("N,K,Ms", [(28672, 8192, (1, 3, 8)), (8192, 28672, (1, 4, 8))])
@@ -459,8 +459,9 @@ def test_pack_weights_grouped(bl, N, K, G, dtype):
     assert np.array_equal(packed.cpu().numpy(), p_ref)
 
 
-# M = 1, 3 (GEMV), 16 / 64 (few-token kernel), 130 (GEMM), 2048 (stream-K)
-@pytest.mark.parametrize("M,N,K", [(1, 384, 1000), (3, 2560, 2560), (16, 384, 1000), (64, 2560, 2560),
+# M = 1, 3 (GEMV), 16 / 32 / 64 (few-token kernel), 130 (GEMM), 2048 (stream-K)
+@pytest.mark.parametrize("M,N,K", [(1, 384, 1000), (3, 2560, 2560), (16, 384, 1000), (32, 2560, 2560),
+                                   (64, 2560, 2560),
                                    (130, 384, 1000), (2048, 2560, 320)])
 @pytest.mark.parametrize("G", [1, 128])
 def test_forward_grouped(bl, M, N, K, G):

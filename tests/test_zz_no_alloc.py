@@ -42,11 +42,15 @@ def test_noalloc_rejects_sizes_beyond_its_scratch(lib):
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("M,N,K", [(65, 2560, 2560), (130, 384, 1000), (200, 640, 512),
-                                   (33, 384, 1000), (64, 2560, 2560)])
+                                   (17, 384, 1000), (32, 2560, 2560), (33, 384, 1000),
+                                   (64, 2560, 2560)])
 def test_noalloc_matches_forward_twice(lib, M, N, K):
+    """Two calls in a row through the C ABI: each result equals bitlinear_forward's
+    (with a caller workspace) bit for bit, and the CPU oracle's."""
     import torch
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
+    import oracle
     import w1_a8_bitlinear_02_b300 as bl
     from w1_a8_bitlinear_02_b300 import capi
     from w1_a8_bitlinear_02_b300 import workloads as wl
@@ -58,12 +62,16 @@ def test_noalloc_matches_forward_twice(lib, M, N, K):
     # the few-token kernel (one wave of clusters), which needs none
     assert need.value <= 8 << 20
     assert (need.value > 0) == (M > 64)
-    W = wl.weight(N, K, 0.02, 7 * N + K, dev)
-    packed, gamma = bl.bitlinear_pack_weights(W)
+    W = wl.weight(N, K, 0.02, 7 * N + K, "cpu")
+    packed, gamma = bl.bitlinear_pack_weights(W.to(dev))
+    p_ref, g_ref = oracle.pack_weights(W.numpy())
+    torch.cuda.synchronize()
+    assert np.array_equal(packed.cpu().numpy(), p_ref)
     stream = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
     ws = torch.empty(max(need.value, 1), dtype=torch.uint8, device=dev)
     for call in range(2):  # two calls in a row share (and reuse) the fixed scratch
-        x = wl.activations(M, K, "outliers1pct", 100 * call + M, dev, torch.bfloat16)
+        xh = wl.activations(M, K, "outliers1pct", 100 * call + M, "cpu", torch.bfloat16)
+        x = xh.to(dev)
         y_ref = torch.empty((M, N), dtype=torch.float32, device=dev)
         y = torch.full((M, N), float("nan"), dtype=torch.float32, device=dev)
         assert lib.bitlinear_forward(_ptr(packed), _ptr(gamma), N, K, _ptr(x), capi.BL_BF16, M,
@@ -76,3 +84,5 @@ def test_noalloc_matches_forward_twice(lib, M, N, K):
         assert np.isfinite(got).all()
         assert (np.abs(got - ref) <= REL_TOL * np.abs(ref)).all(), f"call {call}"
         assert np.array_equal(got.view(np.uint32), ref.view(np.uint32)), f"call {call}"
+        want = oracle.forward_packed(p_ref, g_ref, N, K, xh.float().numpy())
+        assert np.array_equal(got.view(np.uint32), want.view(np.uint32)), f"call {call} vs oracle"

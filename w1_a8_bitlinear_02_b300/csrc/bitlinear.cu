@@ -46,8 +46,9 @@ struct DevState {
   int sms = 0;
   std::set<const void *> smem_set;  // kernels whose dynamic-smem limit was raised
 };
+constexpr int kMaxDevices = 64;  // device ordinals this library keeps state for
 std::mutex g_mu;
-DevState g_dev[64];
+DevState g_dev[kMaxDevices];
 
 bl_status current_device(int *dev, int *sms) {
   int d = 0;
@@ -55,7 +56,7 @@ bl_status current_device(int *dev, int *sms) {
     cudaGetLastError();
     return BL_ERR_CUDA;
   }
-  if (d < 0 || d >= 64) return BL_ERR_UNSUPPORTED;
+  if (d < 0 || d >= kMaxDevices) return BL_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lk(g_mu);
   DevState &st = g_dev[d];
   if (!st.probed) {
@@ -157,6 +158,16 @@ bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 bl_status check_dims(int64_t M, int64_t N, int64_t K) {
   if (M < 1 || M > kMaxDim || N < 1 || N > kMaxDim || K < 1 || K > kMaxK) return BL_ERR_SHAPE;
+  return BL_OK;
+}
+
+// The launch grids a plan needs must exist: the tensor-core GEMM puts token
+// tiles and K splits on grid dimensions y and z (at most 65535 each), the
+// few-token kernel its row tiles on y.  Checked before anything is enqueued.
+bl_status check_grid(const plan::Plan &pl) {
+  if (pl.path == plan::kTc && (pl.tiles_m > 65535 || pl.splits > 65535 || pl.tiles_n > 0x7fffffff))
+    return BL_ERR_SHAPE;
+  if (pl.path == plan::kSkinny && pl.tiles_n > 65535) return BL_ERR_SHAPE;
   return BL_OK;
 }
 
@@ -515,6 +526,8 @@ bl_status forward_common(const uint8_t *packed, const float *gamma, int64_t N, i
     return BL_ERR_SHAPE;
   const plan::Plan pl = plan::make(M, N, K);
   if (pl.path == plan::kTc && (M > 0x7fffffff || N > 0x7fffffff)) return BL_ERR_SHAPE;
+  s = check_grid(pl);
+  if (s != BL_OK) return s;
   int dev = 0, sms = 0;
   s = current_device(&dev, &sms);
   if (s != BL_OK) return s;
@@ -530,9 +543,10 @@ bl_status forward_common(const uint8_t *packed, const float *gamma, int64_t N, i
 // In host code the array's name only stands for it; the address is looked up
 // once per device and kept.
 std::mutex g_noalloc_mu;
-void *g_noalloc_ptr[64] = {};
+void *g_noalloc_ptr[kMaxDevices] = {};
 
 bl_status noalloc_scratch(int dev, void **out) {
+  if (dev < 0 || dev >= kMaxDevices) return BL_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lk(g_noalloc_mu);
   if (g_noalloc_ptr[dev] == nullptr) {
     void *ptr = nullptr;
@@ -696,7 +710,10 @@ bl_status bitlinear_workspace_bytes(int64_t M, int64_t N, int64_t K, size_t *byt
   if (bytes == nullptr) return BL_ERR_NULL;
   bl_status s = check_dims(M, N, K);
   if (s != BL_OK) return s;
-  *bytes = plan::make(M, N, K).ws_bytes;
+  const plan::Plan pl = plan::make(M, N, K);
+  s = check_grid(pl);
+  if (s != BL_OK) return s;
+  *bytes = pl.ws_bytes;
   return BL_OK;
 }
 
@@ -827,7 +844,10 @@ bl_status bitlinear_forward_noalloc(const uint8_t *packed, const float *gamma, i
   if (packed == nullptr || gamma == nullptr || x == nullptr || y == nullptr) return BL_ERR_NULL;
   bl_status s = check_dims(M, N, K);
   if (s != BL_OK) return s;
-  const size_t need = plan::make(M, N, K).ws_bytes;
+  const plan::Plan pl = plan::make(M, N, K);
+  s = check_grid(pl);
+  if (s != BL_OK) return s;
+  const size_t need = pl.ws_bytes;
   if (need > kNoAllocScratchBytes) return BL_ERR_WORKSPACE;
   void *ws = nullptr;
   if (need > 0) {
