@@ -297,15 +297,17 @@ BL_API bl_status bitlinear_forward_noalloc(const uint8_t *packed, const float *g
 
 /* One call of a decode chain (bitlinear_forward_chain), M = 1.
  *   packed, gamma  as bitlinear_forward (device).
- *   x              [K] of x_dtype, device; may be the y of an earlier call.
- *   y              [N] float out, device.
- *   N, K           sizes; K <= 8192.
+ *   x              [K] of x_dtype, device; may lie inside an earlier call's y.
+ *   y              [N] float out, device, 4-byte aligned; must not overlap
+ *                  this call's x, packed or gamma.
+ *   N, K           sizes; N <= 2^30, K <= 32768.
  *   x_dtype        BL_F32 or BL_BF16.
  *   act            BL_ACT_NONE, or BL_ACT_RELU2 for relu2(x) (as
  *                  bitlinear_forward_relu2).
- *   wait_prev      1 when x (or anything the call reads) is written by an
- *                  earlier call of the chain; 0 lets the call start while
- *                  earlier calls still run. */
+ *   wait_prev      1 forces every earlier call of the chain to finish before
+ *                  this one starts.  The library finds the dependencies
+ *                  between calls from their buffers and orders them itself,
+ *                  so 0 is always safe; 1 only costs a grid-wide barrier. */
 typedef struct bl_chain_call {
   const uint8_t *packed;
   const float *gamma;
@@ -317,22 +319,38 @@ typedef struct bl_chain_call {
   int wait_prev;
 } bl_chain_call;
 
-/* A decode chain: up to 128 single-token BitLinear forwards run in order in
+/* Workspace (device bytes) that bitlinear_forward_chain needs for these
+ * calls: 256 bytes of control words, plus 8 * N bytes for every call whose
+ * output a later call reads.  Host only; the calls' pointers are compared, not
+ * dereferenced.  Errors: as bitlinear_forward_chain's argument checks. */
+BL_API bl_status bitlinear_chain_workspace_bytes(const bl_chain_call *calls, int n, size_t *bytes);
+
+/* A decode chain: up to 256 single-token BitLinear forwards run in order in
  * one persistent launch (one block per SM, all resident).  Each call's
  * result equals, bit for bit, bitlinear_forward (or bitlinear_forward_relu2)
- * of its x, and a call with wait_prev = 1 reads its input only after every
- * earlier call has written its output, so chained layers can pass y to x.
+ * of its x as it stands when the call runs in sequence.
  * The packed weights of later calls stream in while earlier calls compute
  * (the "pack-store-load-unpack-compute" weight stream of the 0.4GB page,
- * section 3, carried across calls); dependent calls meet at a grid-wide
- * barrier instead of a kernel boundary.
- *   calls    host array of n descriptors (copied at the call; 1 <= n <= 128).
- *   ws       >= 256 bytes, device, 256-byte aligned: the barrier counter,
- *            zeroed by the call on `stream`.  Chains that share ws must be
- *            ordered.
- * Errors: BL_ERR_NULL, BL_ERR_SHAPE (n, N, K or act out of range),
- * BL_ERR_DTYPE, BL_ERR_ALIGN, BL_ERR_WORKSPACE, BL_ERR_UNSUPPORTED,
- * BL_ERR_CUDA (including a launch the device cannot fit on all its SMs).
+ * section 3, carried across calls).  Dependencies are taken from the buffers:
+ *   - x inside an earlier call's fp32 y (that call being the last to write
+ *     any of x's bytes): the earlier call also writes its outputs as 8-byte
+ *     {value, tag} words into ws and this call reads x from them as soon as
+ *     they carry the earlier call's tag -- no barrier;
+ *   - any other overlap between a call's inputs and an earlier call's output,
+ *     or between its output and an earlier call's inputs or output, and
+ *     wait_prev = 1: every block first finishes all earlier calls (a
+ *     grid-wide barrier).
+ *   calls    host array of n descriptors (copied at the call; 1 <= n <= 256).
+ *   ws       >= bitlinear_chain_workspace_bytes(calls, n) bytes, device,
+ *            256-byte aligned, ZERO-FILLED before its first use; the library
+ *            keeps its contents valid from launch to launch (a sequence
+ *            number in the control words makes each launch's tags new).
+ *            Chains that share ws must be ordered.  If bitlinear_device_error
+ *            reports a failure, zero ws again before reusing it.
+ * Errors: BL_ERR_NULL, BL_ERR_SHAPE (n, N, K or act out of range, or a call
+ * whose output overlaps its own inputs), BL_ERR_DTYPE, BL_ERR_ALIGN,
+ * BL_ERR_WORKSPACE, BL_ERR_UNSUPPORTED, BL_ERR_CUDA (including a launch the
+ * device cannot fit on all its SMs).
  * [The layer structure: 0.4GB page, section 2 (ReLU^2 FFN, no bias);
  * soaring_casia page, section 2 (BitLinear in every projection).] */
 BL_API bl_status bitlinear_forward_chain(const bl_chain_call *calls, int n, void *ws,

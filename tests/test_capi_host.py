@@ -193,15 +193,17 @@ def test_chain_invalid_arguments_return_status(lib):
                                                   d["K"], d["x_dtype"], d["act"], d["wait_prev"]))
         return ctypes.cast(arr, ctypes.c_void_p), arr
 
-    p, keep = chain()
+    p, keep = chain(y=0x900000)
     assert lib.bitlinear_forward_chain(None, 1, ws, 256, None) == capi.BL_ERR_NULL
     assert lib.bitlinear_forward_chain(p, 1, None, 256, None) == capi.BL_ERR_NULL
     assert lib.bitlinear_forward_chain(p, 0, ws, 256, None) == capi.BL_ERR_SHAPE
-    assert lib.bitlinear_forward_chain(p, 129, ws, 256, None) == capi.BL_ERR_SHAPE
+    assert lib.bitlinear_forward_chain(p, 257, ws, 256, None) == capi.BL_ERR_SHAPE
     assert lib.bitlinear_forward_chain(p, 1, ws, 255, None) == capi.BL_ERR_WORKSPACE
     assert lib.bitlinear_forward_chain(p, 1, ctypes.c_void_p(odd), 256, None) == capi.BL_ERR_ALIGN
-    for kw, want in ((dict(y=0), capi.BL_ERR_NULL), (dict(K=8193), capi.BL_ERR_SHAPE),
+    for kw, want in ((dict(y=0), capi.BL_ERR_NULL), (dict(K=32769), capi.BL_ERR_SHAPE),
                      (dict(N=0), capi.BL_ERR_SHAPE), (dict(x_dtype=7), capi.BL_ERR_DTYPE),
-                     (dict(act=5), capi.BL_ERR_SHAPE), (dict(packed=odd), capi.BL_ERR_ALIGN)):
+                     (dict(act=5), capi.BL_ERR_SHAPE), (dict(packed=odd), capi.BL_ERR_ALIGN),
+                     (dict(y=fake + 64), capi.BL_ERR_SHAPE)):  # y over its own x
+        kw.setdefault("y", 0x900000)
         p2, keep2 = chain(**kw)
         assert lib.bitlinear_forward_chain(p2, 1, ws, 256, None) == want, kw

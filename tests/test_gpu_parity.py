@@ -335,6 +335,70 @@ def test_chain_equals_separate_calls(bl, wait_prev):
         assert torch.equal(c["y"].view(torch.int32), r.view(torch.int32))
 
 
+def test_chain_subrange_inputs_and_long_rows(bl):
+    """Inputs that are part of an earlier output (a prefix, an offset that keeps
+    16-byte vectors, an odd offset read word by word), rows longer than one
+    warp's 8192 weights (split over 2 and 4 warps), ReLU^2 on a chained input;
+    the chain is launched three times on one workspace (each launch's tags are
+    new) and every output is checked against the oracle each time."""
+    # (N, K, src, offset into src's output, act)
+    specs = [(3840, 2560, -1, 0, 0),      # x0 (bf16)
+             (2560, 2560, 0, 0, 0),       # prefix of call 0's output
+             (9000, 2560, 1, 0, 0),
+             (2560, 9000, 2, 0, 1),       # K = 9000: rows over 2 warps; relu2
+             (700, 2000, 0, 1280, 0),     # offset 1280 floats: 16-byte aligned words
+             (333, 999, 0, 1, 0),         # odd offset, odd K: word by word
+             (512, 20000, -1, 0, 0)]      # K = 20000 from x0's row: 4 warps per row
+    mats = [pack_both(bl, N, K, 0.02, 700 + i) for i, (N, K, _, _, _) in enumerate(specs)]
+    x0 = wl.activations(1, 20000, "normal", 710, "cpu", torch.bfloat16)
+    xdev = x0.to(DEV)
+    ys = [torch.full((1, N), float("nan"), dtype=torch.float32, device=DEV) for (N, *_ ) in specs]
+    calls = []
+    for i, ((N, K, src, off, act), (packed, gamma, _, _)) in enumerate(zip(specs, mats)):
+        x = xdev[:, :K] if src < 0 else ys[src][:, off:off + K]
+        calls.append(dict(packed=packed, gamma=gamma, x=x, y=ys[i], N=N, K=K, act=act))
+    ws = bl.chain_workspace(calls, DEV)
+    outs = []
+    xr0 = x0.float().numpy()
+    for (N, K, src, off, act), (_, _, p_ref, g_ref) in zip(specs, mats):
+        xin = xr0[:, :K] if src < 0 else outs[src][:, off:off + K]
+        f = oracle.forward_packed_relu2 if act else oracle.forward_packed
+        outs.append(f(p_ref, g_ref, N, K, np.ascontiguousarray(xin, np.float32)))
+    for launch in range(3):
+        for y in ys:
+            y.fill_(float("nan"))
+        bl.bitlinear_forward_chain(calls, ws)
+        torch.cuda.synchronize()
+        assert bl.device_error() == 0
+        for i, y in enumerate(ys):
+            assert_bits_equal(y.cpu().numpy(), outs[i], f"launch {launch} call {i}")
+
+
+def test_chain_write_after_read_and_write_after_write(bl):
+    """Outputs that overwrite an earlier call's input buffer or output buffer:
+    the library puts a grid barrier before such calls, so the results are those
+    of running the calls one after another."""
+    N, K = 2560, 2560
+    mats = [pack_both(bl, N, K, 0.02, 800 + i) for i in range(4)]
+    a0 = wl.activations(1, K, "normal", 810, "cpu", torch.float32)
+    A = a0.to(DEV)
+    B = torch.empty((1, N), dtype=torch.float32, device=DEV)
+    C = torch.empty((1, N), dtype=torch.float32, device=DEV)
+    # 0: A -> B;  1: B -> A (overwrites call 0's input);  2: A -> C;  3: B -> C (C again)
+    plan = [(A, B), (B, A), (A, C), (B, C)]
+    calls = [dict(packed=m[0], gamma=m[1], x=x, y=y, N=N, K=K) for m, (x, y) in zip(mats, plan)]
+    bl.bitlinear_forward_chain(calls)
+    torch.cuda.synchronize()
+    assert bl.device_error() == 0
+    ref = {"A": a0.numpy()}
+    for i, (xn, yn) in enumerate((("A", "B"), ("B", "A"), ("A", "C"), ("B", "C"))):
+        _, _, p_ref, g_ref = mats[i]
+        ref[yn] = oracle.forward_packed(p_ref, g_ref, N, K, ref[xn])
+    assert_bits_equal(A.cpu().numpy(), ref["A"], "A")
+    assert_bits_equal(B.cpu().numpy(), ref["B"], "B")
+    assert_bits_equal(C.cpu().numpy(), ref["C"], "C")
+
+
 def test_chain_unaligned_and_odd_k(bl):
     """K not a multiple of 8 and an input that starts off a 16-byte boundary
     take the element-by-element activation path."""

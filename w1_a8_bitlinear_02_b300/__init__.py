@@ -306,17 +306,10 @@ def bitlinear_forward_noalloc(packed: torch.Tensor, gamma: torch.Tensor, N: int,
     return y
 
 
-def bitlinear_forward_chain(calls, workspace: torch.Tensor | None = None) -> None:
-    """A decode chain of single-token forwards in one launch.
-
-    calls: sequence of dicts with packed, gamma, x [1, K] (fp32 / bf16), y [1, N]
-    fp32 (written), N, K and optionally act (capi.BL_ACT_RELU2 for relu2(x))
-    and wait_prev (default 1: x may be an earlier call's y).  workspace: >= 256
-    device bytes (allocated when None)."""
+def _chain_array(calls):
     calls = list(calls)
     if not calls:
         raise ValueError("empty chain")
-    dev = calls[0]["x"].device
     arr = (capi.ChainCall * len(calls))()
     for i, c in enumerate(calls):
         _need_cuda("packed", c["packed"], torch.uint8)
@@ -324,8 +317,34 @@ def bitlinear_forward_chain(calls, workspace: torch.Tensor | None = None) -> Non
         _need_cuda("y", c["y"], torch.float32)
         arr[i] = capi.ChainCall(c["packed"].data_ptr(), c["gamma"].data_ptr(), c["x"].data_ptr(),
                                 c["y"].data_ptr(), int(c["N"]), int(c["K"]), _DTYPES[c["x"].dtype],
-                                int(c.get("act", capi.BL_ACT_NONE)), int(c.get("wait_prev", 1)))
-    ws = workspace if workspace is not None else torch.empty(256, dtype=torch.uint8, device=dev)
+                                int(c.get("act", capi.BL_ACT_NONE)), int(c.get("wait_prev", 0)))
+    return calls, arr
+
+
+def chain_workspace_bytes(calls) -> int:
+    """Device bytes bitlinear_forward_chain needs for these calls."""
+    calls, arr = _chain_array(calls)
+    n = ctypes.c_size_t()
+    capi.check(_lib().bitlinear_chain_workspace_bytes(ctypes.cast(arr, ctypes.c_void_p), len(calls),
+                                                      ctypes.byref(n)), "bitlinear_chain_workspace_bytes")
+    return int(n.value)
+
+
+def chain_workspace(calls, device) -> torch.Tensor:
+    """A zero-filled workspace for this chain (keep it for later launches)."""
+    return torch.zeros(chain_workspace_bytes(calls), dtype=torch.uint8, device=device)
+
+
+def bitlinear_forward_chain(calls, workspace: torch.Tensor | None = None) -> None:
+    """A decode chain of single-token forwards in one launch.
+
+    calls: sequence of dicts with packed, gamma, x [1, K] (fp32 / bf16), y [1, N]
+    fp32 (written), N, K and optionally act (capi.BL_ACT_RELU2 for relu2(x))
+    and wait_prev (default 0: the library orders dependent calls itself).
+    workspace: from chain_workspace (zero-filled before its first use; reuse it
+    across launches); allocated when None."""
+    calls, arr = _chain_array(calls)
+    ws = workspace if workspace is not None else chain_workspace(calls, calls[0]["x"].device)
     capi.check(_lib().bitlinear_forward_chain(ctypes.cast(arr, ctypes.c_void_p), len(calls), _ptr(ws),
                                               ws.numel(),
                                               _stream(calls[0]["x"])), "bitlinear_forward_chain")

@@ -58,6 +58,7 @@ SIGNATURES = {
     "bitlinear_forward_noalloc": (_INT, [_P, _P, _I64, _I64, _P, _INT, _I64, _P, _P]),
     "bitlinear_relu2_quant_act": (_INT, [_P, _INT, _I64, _I64, _P, _P, _P]),
     "bitlinear_forward_chain": (_INT, [_P, _INT, _P, _SZ, _P]),
+    "bitlinear_chain_workspace_bytes": (_INT, [_P, _INT, ctypes.POINTER(_SZ)]),
     "bitlinear_forward_ex": (_INT, [_P, _P, _I64, _I64, _P, _INT, _I64, _INT, _P, _INT, _P, _P, _SZ, _P]),
     "bitlinear_pack_weights_grouped": (_INT, [_P, _INT, _I64, _I64, _I64, _P, _P, _P, _SZ, _P]),
     "bitlinear_forward_grouped": (_INT, [_P, _P, _I64, _I64, _I64, _P, _INT, _I64, _INT, _P, _INT, _P, _P, _SZ,

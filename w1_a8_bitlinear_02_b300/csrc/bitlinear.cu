@@ -15,6 +15,7 @@
 #include <set>
 #include <tuple>
 #include <utility>
+#include <vector>
 
 #include "bl_chain.cuh"
 #include "bl_gemm_tc.cuh"
@@ -785,43 +786,138 @@ bl_status bitlinear_relu2_quant_act(const void *x, int dtype, int64_t M, int64_t
                                     void *stream) {
   return quant_common(x, dtype, nullptr, 0.0f, false, M, K, xq, scale, stream, kActRelu2);
 }
-bl_status bitlinear_forward_chain(const bl_chain_call *calls, int n, void *ws, size_t ws_bytes,
-                                  void *stream) {
-  if (calls == nullptr || ws == nullptr) return BL_ERR_NULL;
+// Plan of a decode chain (host): each call's rows per block, row split and
+// stage rows; where its input comes from (an earlier call's output words, or
+// memory); which calls need a grid barrier first; the workspace layout.
+// Dependencies are read off the calls' buffers:
+//   * x inside an earlier call's y (fp32, the latest earlier writer of any of
+//     x's bytes): read from that call's output words (it writes them);
+//   * any other input byte (x, packed, gamma) written by an earlier call, an
+//     output byte written or read (from memory) by an earlier call, or
+//     wait_prev: a grid barrier before the call.
+// A call's output may not overlap its own inputs.  p may be null (size only).
+static bl_status chain_plan(const bl_chain_call *calls, int n, int grid, chain::Params *p, size_t *ws_need,
+                            void *ws) {
+  if (calls == nullptr) return BL_ERR_NULL;
   if (n < 1 || n > chain::kMaxCalls) return BL_ERR_SHAPE;
-  if (ws_bytes < 256) return BL_ERR_WORKSPACE;
-  if (!aligned(ws, 256)) return BL_ERR_ALIGN;
-  chain::Params p{};
-  p.n = n;
-  p.bar = static_cast<unsigned *>(ws);
+  struct Rng {
+    uintptr_t lo, hi;
+  };
+  auto ovl = [](const Rng &a, const Rng &b) { return a.lo < b.hi && b.lo < a.hi; };
+  std::vector<Rng> xr(n), yr(n), pr(n), gr(n);
   for (int i = 0; i < n; ++i) {
     const bl_chain_call &c = calls[i];
     if (c.packed == nullptr || c.gamma == nullptr || c.x == nullptr || c.y == nullptr) return BL_ERR_NULL;
     if (c.x_dtype != BL_F32 && c.x_dtype != BL_BF16) return BL_ERR_DTYPE;
-    if (c.N < 1 || c.N > kMaxDim || c.K < 1 || c.K > chain::kMaxK) return BL_ERR_SHAPE;
+    if (c.N < 1 || c.N > chain::kMaxN || c.K < 1 || c.K > chain::kMaxK) return BL_ERR_SHAPE;
     if (c.act != BL_ACT_NONE && c.act != BL_ACT_RELU2) return BL_ERR_SHAPE;
-    if (!aligned(c.packed, 16)) return BL_ERR_ALIGN;
-    p.c[i].packed = c.packed;
-    p.c[i].gamma = c.gamma;
-    p.c[i].x = c.x;
-    p.c[i].y = c.y;
-    p.c[i].N = static_cast<int>(c.N);
-    p.c[i].K = static_cast<int>(c.K);
-    p.c[i].xbf16 = c.x_dtype == BL_BF16 ? 1 : 0;
-    p.c[i].act = c.act;
-    p.c[i].wait_prev = c.wait_prev ? 1 : 0;
+    if (!aligned(c.packed, 16) || !aligned(c.gamma, 4) || !aligned(c.y, 4)) return BL_ERR_ALIGN;
+    const uintptr_t es = c.x_dtype == BL_BF16 ? 2 : 4;
+    xr[i] = {reinterpret_cast<uintptr_t>(c.x), reinterpret_cast<uintptr_t>(c.x) + static_cast<uintptr_t>(c.K) * es};
+    yr[i] = {reinterpret_cast<uintptr_t>(c.y), reinterpret_cast<uintptr_t>(c.y) + static_cast<uintptr_t>(c.N) * 4};
+    pr[i] = {reinterpret_cast<uintptr_t>(c.packed),
+             reinterpret_cast<uintptr_t>(c.packed) + static_cast<uintptr_t>(c.N * plan::row_bytes(c.K))};
+    gr[i] = {reinterpret_cast<uintptr_t>(c.gamma), reinterpret_cast<uintptr_t>(c.gamma) + 4};
+    if (ovl(yr[i], xr[i]) || ovl(yr[i], pr[i]) || ovl(yr[i], gr[i])) return BL_ERR_SHAPE;
   }
+  std::vector<int> src(n, -1);
+  std::vector<char> produces(n, 0), barrier(n, 0);
+  for (int c = 0; c < n; ++c) {
+    bool bar = c > 0 && calls[c].wait_prev != 0;
+    int j = -1;
+    for (int i = c - 1; i >= 0; --i)
+      if (ovl(yr[i], xr[c])) {
+        j = i;
+        break;
+      }
+    if (j >= 0) {
+      if (calls[c].x_dtype == BL_F32 && xr[c].lo >= yr[j].lo && xr[c].hi <= yr[j].hi &&
+          (xr[c].lo - yr[j].lo) % 4 == 0) {
+        src[c] = j;
+        produces[j] = 1;
+      } else {
+        bar = true;
+      }
+    }
+    for (int i = 0; i < c && !bar; ++i) {
+      if (ovl(yr[i], pr[c]) || ovl(yr[i], gr[c]) || ovl(yr[c], yr[i]) || ovl(yr[c], pr[i]) ||
+          ovl(yr[c], gr[i]) || (src[i] < 0 && ovl(yr[c], xr[i])))
+        bar = true;
+    }
+    barrier[c] = bar ? 1 : 0;
+  }
+  std::vector<size_t> mb_off(n, 0);
+  size_t off = chain::kMailboxOffset;
+  for (int i = 0; i < n; ++i)
+    if (produces[i]) {
+      mb_off[i] = off;
+      off = plan::align256(off + static_cast<size_t>(calls[i].N) * 8);
+    }
+  *ws_need = off;
+  if (p == nullptr) return BL_OK;
+  p->n = n;
+  p->ctl = static_cast<unsigned *>(ws);
+  uint8_t *wsb = static_cast<uint8_t *>(ws);
+  for (int i = 0; i < n; ++i) {
+    const bl_chain_call &c = calls[i];
+    chain::Call &d = p->c[i];
+    const int64_t rb = plan::row_bytes(c.K);
+    const int64_t units = rb / 8;
+    int lg = 0;
+    while ((units + (int64_t(1) << lg) - 1) / (int64_t(1) << lg) > chain::kUPT * 32) ++lg;
+    d.packed = c.packed;
+    d.gamma = c.gamma;
+    d.x = c.x;
+    d.y = c.y;
+    d.N = static_cast<int>(c.N);
+    d.K = static_cast<int>(c.K);
+    d.rpc = static_cast<int>((c.N + grid - 1) / grid);
+    d.flags = (c.x_dtype == BL_BF16 ? chain::kFlagBf16 : 0) | (c.act == BL_ACT_RELU2 ? chain::kFlagRelu2 : 0) |
+              (barrier[i] ? chain::kFlagBarrier : 0);
+    d.split_log2 = lg;
+    d.chunk = static_cast<int>((units + (int64_t(1) << lg) - 1) >> lg);
+    int64_t sr = chain::kStageBytes / rb;
+    if (lg > 0 && sr > chain::kMaxSplitRows) sr = chain::kMaxSplitRows;
+    d.stage_rows = static_cast<int>(sr);
+    d.src = src[i];
+    d.mb_out = produces[i] ? reinterpret_cast<uint64_t *>(wsb + mb_off[i]) : nullptr;
+    d.mb_in = nullptr;
+  }
+  for (int i = 0; i < n; ++i)
+    if (src[i] >= 0)
+      p->c[i].mb_in = p->c[src[i]].mb_out + (xr[i].lo - yr[src[i]].lo) / 4;
+  return BL_OK;
+}
+
+bl_status bitlinear_chain_workspace_bytes(const bl_chain_call *calls, int n, size_t *bytes) {
+  if (bytes == nullptr) return BL_ERR_NULL;
+  size_t need = 0;
+  bl_status s = chain_plan(calls, n, 1, nullptr, &need, nullptr);
+  if (s != BL_OK) return s;
+  *bytes = need;
+  return BL_OK;
+}
+
+bl_status bitlinear_forward_chain(const bl_chain_call *calls, int n, void *ws, size_t ws_bytes,
+                                  void *stream) {
+  if (calls == nullptr || ws == nullptr) return BL_ERR_NULL;
+  if (!aligned(ws, 256)) return BL_ERR_ALIGN;
+  size_t need = 0;
+  bl_status s = chain_plan(calls, n, 1, nullptr, &need, nullptr);
+  if (s != BL_OK) return s;
+  if (ws_bytes < need) return BL_ERR_WORKSPACE;
   int dev = 0, sms = 0;
-  bl_status s = current_device(&dev, &sms);
+  s = current_device(&dev, &sms);
+  if (s != BL_OK) return s;
+  static chain::Params p;  // about 20 KB: kept off the stack (the launch copies it)
+  static std::mutex p_mu;
+  std::lock_guard<std::mutex> lk(p_mu);
+  s = chain_plan(calls, n, sms, &p, &need, ws);
   if (s != BL_OK) return s;
   s = ensure_smem(dev, reinterpret_cast<const void *>(&chain::chain_kernel), chain::kSmemBytes);
   if (s != BL_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(ws, 0, 256, st) != cudaSuccess) {
-    cudaGetLastError();
-    return BL_ERR_CUDA;
-  }
-  // every block waits for the others at the grid barrier: all must be resident
+  // every block may wait for the others: all must be resident (one per SM)
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(sms));
   cfg.blockDim = dim3(chain::kThreads);
