@@ -320,9 +320,11 @@ typedef struct bl_chain_call {
 } bl_chain_call;
 
 /* Workspace (device bytes) that bitlinear_forward_chain needs for these
- * calls: 256 bytes of control words, plus 8 * N bytes for every call whose
- * output a later call reads.  Host only; the calls' pointers are compared, not
- * dereferenced.  Errors: as bitlinear_forward_chain's argument checks. */
+ * calls: 256 bytes of control words, 256 bytes per call (its weights' TMA
+ * descriptors, rewritten by every launch), plus 8 * N bytes for every call
+ * whose output a later call reads.  Host only; the calls' pointers are
+ * compared, not dereferenced.  Errors: as bitlinear_forward_chain's argument
+ * checks. */
 BL_API bl_status bitlinear_chain_workspace_bytes(const bl_chain_call *calls, int n, size_t *bytes);
 
 /* A decode chain: up to 256 single-token BitLinear forwards run in order in

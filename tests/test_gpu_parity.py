@@ -399,6 +399,25 @@ def test_chain_write_after_read_and_write_after_write(bl):
     assert_bits_equal(C.cpu().numpy(), ref["C"], "C")
 
 
+@pytest.mark.parametrize("N,K", [(50, 64), (333, 100), (4000, 448), (129, 512)])
+def test_chain_short_rows(bl, N, K):
+    """Rows shorter than one 128-byte box (the box reads zeros past the row),
+    a row count that leaves a partial group in every block, chained twice."""
+    mats = [pack_both(bl, N, K, 0.02, 900 + K), pack_both(bl, K, N, 0.02, 901 + K)]
+    x0 = wl.activations(1, K, "normal", 902, "cpu", torch.bfloat16)
+    y0 = torch.empty((1, N), dtype=torch.float32, device=DEV)
+    y1 = torch.empty((1, K), dtype=torch.float32, device=DEV)
+    calls = [dict(packed=mats[0][0], gamma=mats[0][1], x=x0.to(DEV), y=y0, N=N, K=K),
+             dict(packed=mats[1][0], gamma=mats[1][1], x=y0, y=y1, N=K, K=N)]
+    bl.bitlinear_forward_chain(calls)
+    torch.cuda.synchronize()
+    assert bl.device_error() == 0
+    r0 = oracle.forward_packed(mats[0][2], mats[0][3], N, K, x0.float().numpy())
+    r1 = oracle.forward_packed(mats[1][2], mats[1][3], K, N, r0)
+    assert_bits_equal(y0.cpu().numpy(), r0, "short rows 0")
+    assert_bits_equal(y1.cpu().numpy(), r1, "short rows 1")
+
+
 def test_chain_unaligned_and_odd_k(bl):
     """K not a multiple of 8 and an input that starts off a 16-byte boundary
     take the element-by-element activation path."""

@@ -9,6 +9,8 @@
 
 #include <atomic>
 #include <cstdint>
+#include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -90,6 +92,15 @@ bl_status ensure_smem(int dev, const void *func, int bytes) {
   return BL_OK;
 }
 
+// A launch the runtime refused: cleared and reported as BL_ERR_CUDA; with
+// BITLINEAR_DEBUG set in the environment the CUDA error text goes to stderr.
+bl_status launch_failed(const char *what) {
+  const cudaError_t e = cudaGetLastError();
+  static const bool dbg = std::getenv("BITLINEAR_DEBUG") != nullptr;
+  if (dbg) std::fprintf(stderr, "bitlinear: %s: %s\n", what, cudaGetErrorString(e));
+  return BL_ERR_CUDA;
+}
+
 template <typename... KArgs, typename... Args>
 bl_status launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
                  bool overlap, Args &&...args) {
@@ -105,10 +116,7 @@ bl_status launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, c
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  if (cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...) != cudaSuccess) {
-    cudaGetLastError();
-    return BL_ERR_CUDA;
-  }
+  if (cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...) != cudaSuccess) return launch_failed("launch");
   return BL_OK;
 }
 
@@ -786,18 +794,36 @@ bl_status bitlinear_relu2_quant_act(const void *x, int dtype, int64_t M, int64_t
                                     void *stream) {
   return quant_common(x, dtype, nullptr, 0.0f, false, M, K, xq, scale, stream, kActRelu2);
 }
-// Plan of a decode chain (host): each call's rows per block, row split and
-// stage rows; where its input comes from (an earlier call's output words, or
-// memory); which calls need a grid barrier first; the workspace layout.
+// Packed rows [N, rb] bytes as TMA boxes of 128 bytes x box_rows rows with the
+// 128-byte swizzle (the decode chain's one-lane-per-row layout).
+bool make_map_rows(CUtensorMap *m, const void *ptr, int64_t N, int64_t rb, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(rb), static_cast<cuuint64_t>(N)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(rb)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(chain::kBoxBytes), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t es[2] = {1u, 1u};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Plan of a decode chain (host): each call's rows per block and tensor maps;
+// where its input comes from (quantised ahead into a record, an earlier
+// call's output words, or memory after a grid barrier); the workspace layout
+// (control words, two tensor maps per call, records, output words).
 // Dependencies are read off the calls' buffers:
+//   * x written by no earlier call (and no wait_prev): quantised before the
+//     chain starts, into a record;
 //   * x inside an earlier call's y (fp32, the latest earlier writer of any of
 //     x's bytes): read from that call's output words (it writes them);
 //   * any other input byte (x, packed, gamma) written by an earlier call, an
 //     output byte written or read (from memory) by an earlier call, or
 //     wait_prev: a grid barrier before the call.
-// A call's output may not overlap its own inputs.  p may be null (size only).
-static bl_status chain_plan(const bl_chain_call *calls, int n, int grid, chain::Params *p, size_t *ws_need,
-                            void *ws) {
+// A call's output may not overlap its own inputs.  p, maps and q may be null
+// (size only).
+static bl_status chain_plan(const bl_chain_call *calls, int n, int grid, chain::Params *p, CUtensorMap *maps,
+                            chain::QuantParams *q, size_t *ws_need, void *ws) {
   if (calls == nullptr) return BL_ERR_NULL;
   if (n < 1 || n > chain::kMaxCalls) return BL_ERR_SHAPE;
   struct Rng {
@@ -821,7 +847,7 @@ static bl_status chain_plan(const bl_chain_call *calls, int n, int grid, chain::
     if (ovl(yr[i], xr[i]) || ovl(yr[i], pr[i]) || ovl(yr[i], gr[i])) return BL_ERR_SHAPE;
   }
   std::vector<int> src(n, -1);
-  std::vector<char> produces(n, 0), barrier(n, 0);
+  std::vector<char> produces(n, 0), barrier(n, 0), early(n, 0);
   for (int c = 0; c < n; ++c) {
     bool bar = c > 0 && calls[c].wait_prev != 0;
     int j = -1;
@@ -845,9 +871,15 @@ static bl_status chain_plan(const bl_chain_call *calls, int n, int grid, chain::
         bar = true;
     }
     barrier[c] = bar ? 1 : 0;
+    early[c] = (j < 0 && !bar) ? 1 : 0;  // no earlier call writes x: quantised before the chain
   }
-  std::vector<size_t> mb_off(n, 0);
-  size_t off = chain::kMailboxOffset;
+  size_t off = plan::align256(chain::kMapsOffset + static_cast<size_t>(2 * n) * sizeof(CUtensorMap));
+  std::vector<size_t> rec_off(n, 0), mb_off(n, 0);
+  for (int i = 0; i < n; ++i)
+    if (early[i]) {
+      rec_off[i] = off;
+      off = plan::align256(off + static_cast<size_t>(chain::record_bytes(static_cast<int>(plan::row_bytes(calls[i].K)))));
+    }
   for (int i = 0; i < n; ++i)
     if (produces[i]) {
       mb_off[i] = off;
@@ -857,31 +889,48 @@ static bl_status chain_plan(const bl_chain_call *calls, int n, int grid, chain::
   if (p == nullptr) return BL_OK;
   p->n = n;
   p->ctl = static_cast<unsigned *>(ws);
+  q->n = 0;
   uint8_t *wsb = static_cast<uint8_t *>(ws);
+  CUtensorMap *wmaps = reinterpret_cast<CUtensorMap *>(wsb + chain::kMapsOffset);
   for (int i = 0; i < n; ++i) {
     const bl_chain_call &c = calls[i];
     chain::Call &d = p->c[i];
     const int64_t rb = plan::row_bytes(c.K);
-    const int64_t units = rb / 8;
-    int lg = 0;
-    while ((units + (int64_t(1) << lg) - 1) / (int64_t(1) << lg) > chain::kUPT * 32) ++lg;
-    d.packed = c.packed;
+    const int64_t rpc = (c.N + grid - 1) / grid;
+    const int rem = static_cast<int>(rpc % chain::kGroupRows);
+    if (!make_map_rows(&maps[2 * i], c.packed, c.N, rb, chain::kGroupRows)) return BL_ERR_CUDA;
+    if (rem > 0) {
+      if (!make_map_rows(&maps[2 * i + 1], c.packed, c.N, rb, rem)) return BL_ERR_CUDA;
+    } else {
+      maps[2 * i + 1] = maps[2 * i];
+    }
+    d.map = &wmaps[2 * i];
+    d.map_rem = &wmaps[2 * i + 1];
     d.gamma = c.gamma;
     d.x = c.x;
     d.y = c.y;
     d.N = static_cast<int>(c.N);
     d.K = static_cast<int>(c.K);
-    d.rpc = static_cast<int>((c.N + grid - 1) / grid);
-    d.flags = (c.x_dtype == BL_BF16 ? chain::kFlagBf16 : 0) | (c.act == BL_ACT_RELU2 ? chain::kFlagRelu2 : 0) |
-              (barrier[i] ? chain::kFlagBarrier : 0);
-    d.split_log2 = lg;
-    d.chunk = static_cast<int>((units + (int64_t(1) << lg) - 1) >> lg);
-    int64_t sr = chain::kStageBytes / rb;
-    if (lg > 0 && sr > chain::kMaxSplitRows) sr = chain::kMaxSplitRows;
-    d.stage_rows = static_cast<int>(sr);
+    d.rb = static_cast<int>(rb);
+    d.rpc = static_cast<int>(rpc);
+    d.rem = rem;
+    const int flags = (c.x_dtype == BL_BF16 ? chain::kFlagBf16 : 0) | (c.act == BL_ACT_RELU2 ? chain::kFlagRelu2 : 0);
+    d.flags = flags | (barrier[i] ? chain::kFlagBarrier : 0);
     d.src = src[i];
+    d.pad_ = 0;
+    d.rec = early[i] ? wsb + rec_off[i] : nullptr;
     d.mb_out = produces[i] ? reinterpret_cast<uint64_t *>(wsb + mb_off[i]) : nullptr;
     d.mb_in = nullptr;
+    if (early[i]) {
+      chain::QuantJob &jb = q->j[q->n++];
+      jb.x = c.x;
+      jb.gamma = c.gamma;
+      jb.rec = wsb + rec_off[i];
+      jb.K = static_cast<int>(c.K);
+      jb.rb = static_cast<int>(rb);
+      jb.flags = flags;
+      jb.pad_ = 0;
+    }
   }
   for (int i = 0; i < n; ++i)
     if (src[i] >= 0)
@@ -892,7 +941,7 @@ static bl_status chain_plan(const bl_chain_call *calls, int n, int grid, chain::
 bl_status bitlinear_chain_workspace_bytes(const bl_chain_call *calls, int n, size_t *bytes) {
   if (bytes == nullptr) return BL_ERR_NULL;
   size_t need = 0;
-  bl_status s = chain_plan(calls, n, 1, nullptr, &need, nullptr);
+  bl_status s = chain_plan(calls, n, 1, nullptr, nullptr, nullptr, &need, nullptr);
   if (s != BL_OK) return s;
   *bytes = need;
   return BL_OK;
@@ -903,20 +952,40 @@ bl_status bitlinear_forward_chain(const bl_chain_call *calls, int n, void *ws, s
   if (calls == nullptr || ws == nullptr) return BL_ERR_NULL;
   if (!aligned(ws, 256)) return BL_ERR_ALIGN;
   size_t need = 0;
-  bl_status s = chain_plan(calls, n, 1, nullptr, &need, nullptr);
+  bl_status s = chain_plan(calls, n, 1, nullptr, nullptr, nullptr, &need, nullptr);
   if (s != BL_OK) return s;
   if (ws_bytes < need) return BL_ERR_WORKSPACE;
   int dev = 0, sms = 0;
   s = current_device(&dev, &sms);
   if (s != BL_OK) return s;
-  static chain::Params p;  // about 20 KB: kept off the stack (the launch copies it)
+  // about 22 KB of call table, 64 KB of maps and 8 KB of quantisation jobs:
+  // kept off the stack (each launch copies its parameters)
+  static chain::Params p;
+  static chain::MapCopy mc;
+  static chain::QuantParams qp;
+  static CUtensorMap maps[2 * chain::kMaxCalls];
   static std::mutex p_mu;
   std::lock_guard<std::mutex> lk(p_mu);
-  s = chain_plan(calls, n, sms, &p, &need, ws);
+  s = chain_plan(calls, n, sms, &p, maps, &qp, &need, ws);
   if (s != BL_OK) return s;
   s = ensure_smem(dev, reinterpret_cast<const void *>(&chain::chain_kernel), chain::kSmemBytes);
   if (s != BL_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // the tensor maps into the workspace (their parameters are kept by value)
+  CUtensorMap *wmaps = reinterpret_cast<CUtensorMap *>(static_cast<uint8_t *>(ws) + chain::kMapsOffset);
+  for (int m0 = 0; m0 < 2 * n; m0 += chain::kMapsPerCopy) {
+    mc.n = 2 * n - m0 < chain::kMapsPerCopy ? 2 * n - m0 : chain::kMapsPerCopy;
+    mc.dst = wmaps + m0;
+    std::memcpy(mc.maps, maps + m0, sizeof(CUtensorMap) * static_cast<size_t>(mc.n));
+    s = launch(&chain::copy_maps_kernel, dim3(1), dim3(256), 0, st, false, mc);
+    if (s != BL_OK) return s;
+  }
+  // the inputs no earlier call writes, quantised into their records
+  if (qp.n > 0) {
+    s = launch(&chain::chain_quant_kernel, dim3(static_cast<unsigned>(qp.n)), dim3(chain::kQThreads), 0, st, false,
+               qp);
+    if (s != BL_OK) return s;
+  }
   // every block may wait for the others: all must be resident (one per SM)
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(sms));
@@ -928,10 +997,7 @@ bl_status bitlinear_forward_chain(const bl_chain_call *calls, int n, void *ws, s
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, &chain::chain_kernel, p) != cudaSuccess) {
-    cudaGetLastError();
-    return BL_ERR_CUDA;
-  }
+  if (cudaLaunchKernelEx(&cfg, &chain::chain_kernel, p) != cudaSuccess) return launch_failed("chain launch");
   return BL_OK;
 }
 bl_status bitlinear_forward_noalloc(const uint8_t *packed, const float *gamma, int64_t N, int64_t K,

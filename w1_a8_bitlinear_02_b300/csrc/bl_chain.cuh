@@ -8,21 +8,46 @@
 // its packed weights -- static inputs -- are a fraction of a microsecond of
 // HBM time.  Here one block per SM stays resident for the whole chain:
 //   * its producer thread streams the block's rows of every call, call after
-//     call, into one bulk-copy ring: the weights of later calls arrive while
-//     earlier calls compute, limited only by the ring's size ("pack-store-
-//     load-unpack-compute", 微软AI大模型炸场：0.4GB, blog.csdn.net/2401_84494441,
-//     section 3, GPU bullet, carried across calls);
-//   * the consumer warps run the calls in order: quantise the input (per-token
-//     absmax, once per block into shared memory), then run the block's rows
-//     (masked dp4a on the packed codes, exact int32 sums, y = fl32(acc * c),
-//     c = fl32(gamma / s)).
+//     call, into one ring of shared-memory stages by TMA: the weights of later
+//     calls arrive while earlier calls compute, limited only by the ring's
+//     size ("pack-store-load-unpack-compute", 微软AI大模型炸场：0.4GB,
+//     blog.csdn.net/2401_84494441, section 3, GPU bullet, carried across
+//     calls);
+//   * the consumer warps run the calls in order over the block's rows.
+//
+// Rows, one lane each.  A stage is a group of up to 32 consecutive rows and a
+// 1 KB slab of their packed bytes (4096 weights), loaded as 128-byte x 32-row
+// TMA boxes with the 128-byte swizzle, so lane l reading 16 bytes of row l
+// touches a different bank group than the other 7 lanes of its quarter-warp.
+// The 16 consumer warps split each slab's 16-byte pieces (64 weights) among
+// themselves; every lane of a warp needs the same 64 activation codes, which
+// are broadcast from shared memory.  A lane adds its row's pieces with the
+// masked dp4a (the bytes of (word & (3 << 2i)) are the codes c = q + 1 times
+// 4^i; the 4^i factor is removed exactly at the end; sum c*x - X = sum q*x,
+// X = the warp's sum of activation codes) across all slabs of the group; the
+// 16 warps' partial sums then meet in shared memory once per group and one
+// warp writes y = fl32(acc * c), c = fl32(gamma / s).  No per-row reduction,
+// no copy of the activation codes per warp, and K of any length splits the
+// same way.
+//
+// The activation codes (per-token absmax, "20亿参数仅0.4GB" page, section 2,
+// item 2) of a call come one of two ways:
+//   * an input no earlier call writes is quantised before the chain starts
+//     (chain_quant_kernel, one block per such call) into a record in the
+//     workspace -- codes, c and the 16 warps' code sums -- and the producer
+//     loads the record by bulk copy along with the call's weights;
+//   * an input an earlier call writes is quantised by every block when the
+//     call comes up, into the same shared-memory slot.
+// Two slots alternate between consecutive calls, so a call's record arrives
+// while the previous call runs.
+//
 // Dependencies between calls come in two forms, both found by the host from
 // the calls' buffers:
-//   * mailbox: when a call's x lies inside an earlier call's y, that earlier
-//     call also writes each output as one 8-byte word {value, tag} into the
-//     workspace, and the reader polls those words directly: the tag says the
-//     value is there, so no barrier, fence or separate flag is needed (an
-//     aligned 64-bit store is seen whole or not at all).  The tag holds the
+//   * output words: when a call's x lies inside an earlier call's y, that
+//     earlier call also writes each output as one 8-byte word {value, tag}
+//     into the workspace, and the reader polls those words directly: the tag
+//     says the value is there, so no barrier, fence or separate flag is needed
+//     (an aligned 64-bit store is seen whole or not at all).  The tag holds the
 //     producing call and a per-launch sequence number kept in the workspace,
 //     so words left by an earlier launch never match;
 //   * grid barrier: any other overlap (an input read from memory that an
@@ -33,6 +58,7 @@
 // launch is cooperative, one block per SM.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cstdint>
 
@@ -46,41 +72,57 @@ constexpr int kMaxCalls = 256;
 constexpr int kCW = 16;                   // consumer warps
 constexpr int kThreads = (kCW + 1) * 32;  // + one producer warp
 constexpr int kC = kCW * 32;              // consumer threads
-constexpr int kUPT = 8;                   // 8-byte units per lane: a warp's chunk spans 256 units (8192 weights)
-constexpr int kMaxK = 32768;              // longer rows are split over warps (at most 4 per row)
-constexpr int kMaxN = 1 << 30;           // row indices stay far inside int
-constexpr int kStageBytes = 32 * 1024;
-constexpr int kStages = 5;
-constexpr int kMaxSplitRows = 8;          // rows per stage when a row is split over warps
-constexpr int kJM = 2;                    // x vectors of 8 per consumer thread kept in registers
-constexpr int kSmemFixed = 22 * 1024;     // barriers, reductions and the call table
-constexpr int kSmemBytes = kSmemFixed + kStages * kStageBytes + kMaxK;  // + activation codes
+constexpr int kMaxK = 32768;
+constexpr int kMaxN = 1 << 30;            // row indices stay far inside int
+constexpr int kGroupRows = 32;            // rows per group: one per lane
+constexpr int kBoxBytes = 128;            // packed bytes per TMA box row (512 weights)
+constexpr int kBoxSize = kGroupRows * kBoxBytes;  // 4 KB per box
+constexpr int kSlabBoxes = 8;             // a slab: 1 KB of each row (4096 weights)
+constexpr int kSlabBytes = kSlabBoxes * kBoxBytes;
+constexpr int kSlabCodes = kSlabBytes * 4;
+constexpr int kStageBytes = kSlabBoxes * kBoxSize;  // 32 KB
+constexpr int kStages = 3;
+constexpr int kJM = 2;                    // x vectors of 8 per consumer thread kept in registers (K <= 8192)
+// A codes slot (and a record in the workspace): a 128-byte header -- c =
+// gamma / s (fp32) at byte 0, the 16 warps' code sums (int32) at byte 64 --
+// then the codes, zero from K to the end of the last slab.
+constexpr int kHeader = 128;
+constexpr int kSlotBytes = kHeader + kMaxK + kSlabCodes;
+constexpr int kSmemFixed = 30 * 1024;     // barriers, partial sums and the call table
+constexpr int kSmemBytes = 1024 + kSmemFixed + kStages * kStageBytes + 2 * kSlotBytes;
 
-// Control words at the start of the workspace (bytes 0..255).
+// Control words at the start of the workspace (bytes 0..255), then the
+// calls' tensor maps (two per call, 128 bytes each), the records, the output
+// words.
 constexpr int kCtlBar = 0;    // grid-barrier arrivals of this launch
 constexpr int kCtlDone = 1;   // blocks finished with this launch
 constexpr int kCtlSeq = 32;   // launches completed on this workspace (tags)
-constexpr int kMailboxOffset = 256;
+constexpr int kMapsOffset = 256;
 
 // Call flags.
 constexpr int kFlagBf16 = 1;      // x is bf16 (else fp32)
 constexpr int kFlagRelu2 = 2;     // quantise relu2(x)
 constexpr int kFlagBarrier = 4;   // every block finishes all earlier calls first
 
+__host__ __device__ constexpr int slabs_of(int rb) { return (rb + kSlabBytes - 1) / kSlabBytes; }
+__host__ __device__ constexpr int record_bytes(int rb) { return kHeader + slabs_of(rb) * kSlabCodes; }
+
 struct Call {
-  const uint8_t *packed;  // [N, 16 * ceil(K / 64)]
+  const CUtensorMap *map;      // packed [N, rb] bytes, box 128 B x 32 rows, 128-byte swizzle
+  const CUtensorMap *map_rem;  // the same with rem rows per box (a block's last, partial group)
   const float *gamma;
-  const void *x;          // [K] f32 or bf16 (read when mb_in is null)
+  const void *x;          // [K] f32 or bf16 (read when neither rec nor mb_in is set)
   float *y;               // [N]
+  const uint8_t *rec;     // the call's quantised input (record), or null
   uint64_t *mb_out;       // this call's output words [N] {value bits, tag}, or null
   const uint64_t *mb_in;  // the words holding x [K] (inside an earlier call's mb_out), or null
   int N, K;
+  int rb;                 // packed row bytes
   int rpc;                // rows per block
+  int rem;                // rpc % 32: rows of every block's partial group (0: none)
   int flags;
-  int split_log2;         // warps per row: 1 << split_log2
-  int chunk;              // 8-byte units per warp chunk of a row
-  int stage_rows;         // rows per ring stage
   int src;                // the call that wrote mb_in
+  int pad_;
 };
 static_assert(sizeof(Call) % 4 == 0, "call table copied in words");
 
@@ -93,16 +135,122 @@ struct Params {
 struct Smem {
   uint64_t full[kStages];
   uint64_t empty[kStages];
+  uint64_t sfull[2];      // a slot's record has landed
+  uint64_t sempty[2];     // a slot's call is done with it
   float fred[kCW];
-  int32_t part[kStages][kMaxSplitRows];
-  uint32_t cnt[kStages][kMaxSplitRows];
+  int32_t part[2][kCW][kGroupRows];  // a group's partial sums, by group parity
   uint32_t seq_tag;
   int abort_flag;
   Call calls[kMaxCalls];  // the parameters, copied once: indexed reads of the
                           // parameter space go through the constant cache
 };
 static_assert(sizeof(Smem) <= kSmemFixed, "fixed shared-memory region");
+static_assert(kSmemBytes <= 227 * 1024, "shared memory of one block");
 
+// ------------------------------------------------------------ set-up kernels
+// Maps for the workspace, copied there by a separate launch (kernel
+// parameters hold them by value, so a captured graph keeps them).
+constexpr int kMapsPerCopy = 254;  // the whole struct (64-byte aligned) stays under 32764 bytes
+struct MapCopy {
+  int n;
+  CUtensorMap *dst;
+  CUtensorMap maps[kMapsPerCopy];
+};
+__global__ void copy_maps_kernel(const __grid_constant__ MapCopy m) {
+  const uint4 *src = reinterpret_cast<const uint4 *>(m.maps);
+  uint4 *dst = reinterpret_cast<uint4 *>(m.dst);
+  const int words = m.n * static_cast<int>(sizeof(CUtensorMap) / 16);
+  for (int i = threadIdx.x; i < words; i += blockDim.x) dst[i] = src[i];
+  asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
+}
+
+// One input quantised ahead: x [K] (f32 or bf16, relu2 first if flagged) ->
+// record (c = gamma / s, the 16 warps' code sums, codes zero-padded to the
+// last slab).
+struct QuantJob {
+  const void *x;
+  const float *gamma;
+  uint8_t *rec;
+  int K, rb, flags, pad_;
+};
+struct QuantParams {
+  int n;
+  QuantJob j[kMaxCalls];
+};
+constexpr int kQThreads = 256;
+__global__ void __launch_bounds__(kQThreads) chain_quant_kernel(const __grid_constant__ QuantParams q) {
+  __shared__ __align__(16) uint8_t codes[kMaxK + kSlabCodes];
+  __shared__ float red[kQThreads / 32];
+  __shared__ int xsum[kCW];
+  const QuantJob &jb = q.j[blockIdx.x];
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const bool bf = (jb.flags & kFlagBf16) != 0, r2 = (jb.flags & kFlagRelu2) != 0;
+  const int K = jb.K, kend = slabs_of(jb.rb) * kSlabCodes;
+  auto ld = [&](int k) -> float {
+    const float v = bf ? __bfloat162float(static_cast<const __nv_bfloat16 *>(jb.x)[k])
+                       : static_cast<const float *>(jb.x)[k];
+    return r2 ? relu2f(v) : v;
+  };
+  const bool vec = (K % 8) == 0 && al16(jb.x);
+  const int nv = vec ? K / 8 : 0;
+  float a = 0.0f;
+  for (int v = t; v < nv; v += kQThreads) {
+    float f[8];
+    if (bf)
+      load8(static_cast<const __nv_bfloat16 *>(jb.x) + 8 * v, f);
+    else
+      load8(static_cast<const float *>(jb.x) + 8 * v, f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) a = fmaxf(a, fabsf(r2 ? relu2f(f[e]) : f[e]));
+  }
+  for (int k = 8 * nv + t; k < K; k += kQThreads) a = fmaxf(a, fabsf(ld(k)));
+  a = warp_max_nonneg(a);
+  if (lane == 0) red[warp] = a;
+  if (t < kCW) xsum[t] = 0;
+  __syncthreads();
+  a = red[0];
+#pragma unroll
+  for (int w = 1; w < kQThreads / 32; ++w) a = fmaxf(a, red[w]);
+  const float s = act_scale(a);
+  for (int v = t; v < nv; v += kQThreads) {
+    float f[8];
+    if (bf)
+      load8(static_cast<const __nv_bfloat16 *>(jb.x) + 8 * v, f);
+    else
+      load8(static_cast<const float *>(jb.x) + 8 * v, f);
+    uint32_t lo = 0, hi = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      lo |= (static_cast<uint32_t>(quant_one(r2 ? relu2f(f[e]) : f[e], s)) & 0xFFu) << (8 * e);
+      hi |= (static_cast<uint32_t>(quant_one(r2 ? relu2f(f[e + 4]) : f[e + 4], s)) & 0xFFu) << (8 * e);
+    }
+    *reinterpret_cast<uint2 *>(codes + 8 * v) = make_uint2(lo, hi);
+  }
+  for (int k = 8 * nv + t; k < kend; k += kQThreads)
+    codes[k] = k < K ? static_cast<uint8_t>(quant_one(ld(k), s) & 0xFF) : 0u;
+  __syncthreads();
+  // the codes out, and each 64-code piece's sum into its warp's total (piece
+  // p is read by consumer warp p mod 16)
+  uint4 *dst = reinterpret_cast<uint4 *>(jb.rec + kHeader);
+  for (int i = t; i < kend / 16; i += kQThreads) dst[i] = *reinterpret_cast<const uint4 *>(codes + 16 * i);
+  for (int pc = t; pc < kend / 64; pc += kQThreads) {
+    int sm = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 v = *reinterpret_cast<const uint4 *>(codes + 64 * pc + 16 * i);
+      sm = dp4a_us(0x01010101u, v.x, sm);
+      sm = dp4a_us(0x01010101u, v.y, sm);
+      sm = dp4a_us(0x01010101u, v.z, sm);
+      sm = dp4a_us(0x01010101u, v.w, sm);
+    }
+    atomicAdd(&xsum[pc % kCW], sm);
+  }
+  __syncthreads();
+  if (t < kCW) reinterpret_cast<int *>(jb.rec + 64)[t] = xsum[t];
+  if (t == 0) *reinterpret_cast<float *>(jb.rec) = __fdiv_rn(__ldg(jb.gamma), s);
+}
+
+// ------------------------------------------------------------ helpers
 __device__ __forceinline__ void red_release_add(unsigned *p, unsigned v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
@@ -126,96 +274,10 @@ __device__ __forceinline__ uint64_t ld_word(const uint64_t *p) {
   asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(a) : "l"(p) : "memory");
   return a;
 }
-
 // Another block (or kernel) gave up a bounded wait: the words or arrivals
 // this block waits for may never come, so stop waiting.
 __device__ __forceinline__ bool gave_up() {
   return (*static_cast<volatile unsigned *>(&g_dev_error) & kDevErrTimeout) != 0u;
-}
-
-__device__ __forceinline__ uint2 lds_u64(uint32_t addr) {
-  uint2 v;
-  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
-  return v;
-}
-
-// One row's code-weighted sum over this lane's first U units (unit u at
-// lbase + uoff[u]): the masked dp4a loop.  The bytes of (word & (3 << 2i)) are
-// codes c = q + 1 times 4^i, dp4a'd against the activation codes into
-// accumulator i; the 4^i factor is removed exactly at the end.  A unit the
-// lane does not have is read at an existing unit with zero activation codes,
-// so the loop has no per-unit branch.
-template <int U>
-__device__ __forceinline__ int row_sum(uint32_t lbase, const uint32_t (&uoff)[kUPT], const uint32_t (&xa)[kUPT][8]) {
-  int a0 = 0, a1 = 0, a2 = 0, a3 = 0;
-#pragma unroll
-  for (int u = 0; u < U; ++u) {
-    const uint2 wv = lds_u64(lbase + uoff[u]);
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const uint32_t word = h ? wv.y : wv.x;
-      a0 = dp4a_us(word & 0x03030303u, xa[u][4 * h + 0], a0);
-      a1 = dp4a_us(word & 0x0C0C0C0Cu, xa[u][4 * h + 1], a1);
-      a2 = dp4a_us(word & 0x30303030u, xa[u][4 * h + 2], a2);
-      a3 = dp4a_us(word & 0xC0C0C0C0u, xa[u][4 * h + 3], a3);
-    }
-  }
-  return a0 + (a1 >> 2) + (a2 >> 4) + (a3 >> 6);
-}
-
-struct RowCtx {
-  float cm;          // fl32(gamma / s)
-  int xl;            // this lane's sum of activation codes over its units
-  uint32_t laddr;    // this lane's first unit, bytes from the row start
-  int rb;            // packed row bytes
-  float *y;          // y + first row of the stage
-  uint64_t *mb;      // output words + first row of the stage, or null
-  uint32_t tag;
-};
-
-__device__ __forceinline__ void put_out(const RowCtx &x, int r, int t) {
-  const float v = __fmul_rn(static_cast<float>(t), x.cm);
-  x.y[r] = v;
-  if (x.mb != nullptr) st_word(x.mb + r, v, x.tag);
-}
-
-// Whole rows (one warp per row): rows r0 = slot, slot + step, ... of a stage,
-// two in flight per iteration (their loads and dp4a chains interleave).
-template <int U>
-__device__ __forceinline__ void stage_rows_whole(uint32_t sbase, int nr, int slot, int step, int lane,
-                                                 const uint32_t (&uoff)[kUPT], const uint32_t (&xa)[kUPT][8],
-                                                 const RowCtx &x) {
-  for (int r = slot; r < nr; r += 2 * step) {
-    const int r2 = r + step < nr ? r + step : r;
-    int t0 = row_sum<U>(sbase + static_cast<uint32_t>(r * x.rb) + x.laddr, uoff, xa) - x.xl;
-    int t1 = row_sum<U>(sbase + static_cast<uint32_t>(r2 * x.rb) + x.laddr, uoff, xa) - x.xl;
-    t0 = __reduce_add_sync(0xffffffffu, t0);
-    t1 = __reduce_add_sync(0xffffffffu, t1);
-    if (lane == 0) put_out(x, r, t0);
-    if (lane == 1 && r2 != r) put_out(x, r2, t1);
-  }
-}
-
-// Rows split over G warps: warp chunk `cid` of rows slot, slot + step, ...;
-// the chunks' sums meet in shared memory and the last arriver writes.
-template <int U>
-__device__ __forceinline__ void stage_rows_split(uint32_t sbase, int nr, int slot, int step, int lane, int G,
-                                                 int32_t *part, uint32_t *cnt, const uint32_t (&uoff)[kUPT],
-                                                 const uint32_t (&xa)[kUPT][8], const RowCtx &x) {
-  for (int r = slot; r < nr; r += step) {
-    int t = row_sum<U>(sbase + static_cast<uint32_t>(r * x.rb) + x.laddr, uoff, xa) - x.xl;
-    t = __reduce_add_sync(0xffffffffu, t);
-    if (lane == 0) {
-      atomicAdd(&part[r], t);
-      __threadfence_block();
-      if (atomicAdd(&cnt[r], 1u) == static_cast<uint32_t>(G - 1)) {
-        __threadfence_block();
-        const int tot = atomicExch(&part[r], 0);
-        cnt[r] = 0u;
-        put_out(x, r, tot);
-      }
-    }
-  }
 }
 
 // Rows of call c owned by this block: [r0, r0 + rows).
@@ -224,10 +286,15 @@ __device__ __forceinline__ void block_rows(const Call &c, int &r0, int &rows) {
   rows = c.N - r0 < c.rpc ? c.N - r0 : c.rpc;
   if (rows < 0) rows = 0;
 }
-__device__ __forceinline__ int row_bytes_of(int K) { return ((K + 63) / 64) * 16; }
+// 128-byte boxes of slab s (the last slab of a row may be shorter)
+__device__ __forceinline__ int boxes_of(int rb, int s) {
+  int len = rb - s * kSlabBytes;
+  if (len > kSlabBytes) len = kSlabBytes;
+  return (len + kBoxBytes - 1) / kBoxBytes;
+}
 
-// Eight activations of vector v (elements 8v .. 8v+7) into f; false when
-// they come from output words and one of them does not carry `want` yet.
+// Eight activations of vector v into f; false when they come from output
+// words and one of them does not carry `want` yet.
 __device__ __forceinline__ bool load_vec8(const Call &c, int v, uint32_t want, float (&f)[8]) {
   if (c.mb_in != nullptr) {
     uint64_t w[8];
@@ -285,17 +352,172 @@ __device__ __forceinline__ void put_codes8(uint32_t xs, int v, const float (&f)[
   sts_u64(xs + 8 * v, lo, hi);
 }
 
-__global__ void __maxnreg__(120) chain_kernel(const __grid_constant__ Params p) {
-  extern __shared__ __align__(128) uint8_t smem_raw[];
-  Smem &sm = *reinterpret_cast<Smem *>(smem_raw);
-  const uint32_t ring = smem_u32(smem_raw + kSmemFixed);
-  const uint32_t xs = ring + kStages * kStageBytes;  // activation codes of the current call
+// Vectors of 8 the call's input is read in (0: element by element).
+__device__ __forceinline__ int vec_count(const Call &c) {
+  const bool vec = (c.K % 8) == 0 && (c.mb_in != nullptr ? (reinterpret_cast<uintptr_t>(c.mb_in) & 15u) == 0u
+                                                          : (reinterpret_cast<uintptr_t>(c.x) & 15u) == 0u);
+  return vec ? c.K / 8 : 0;
+}
+
+// One 16-byte piece of a lane's row (64 weights) against the 64 activation
+// codes at `act` (broadcast): accumulator i gets the bit-plane-i codes x 4^i.
+__device__ __forceinline__ void piece(uint32_t waddr, uint32_t act, int (&a)[4]) {
+  const uint4 w = lds_u128(waddr);
+  const uint4 x0 = lds_u128(act), x1 = lds_u128(act + 16), x2 = lds_u128(act + 32), x3 = lds_u128(act + 48);
+  const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
+  const uint32_t xv[16] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w,
+                           x2.x, x2.y, x2.z, x2.w, x3.x, x3.y, x3.z, x3.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    a[0] = dp4a_us(wd[j] & 0x03030303u, xv[4 * j + 0], a[0]);
+    a[1] = dp4a_us(wd[j] & 0x0C0C0C0Cu, xv[4 * j + 1], a[1]);
+    a[2] = dp4a_us(wd[j] & 0x30303030u, xv[4 * j + 2], a[2]);
+    a[3] = dp4a_us(wd[j] & 0xC0C0C0C0u, xv[4 * j + 3], a[3]);
+  }
+}
+
+// Quantise the input of call c in every block (it depends on earlier calls)
+// into the codes slot: values polled from output words or read after the grid
+// barrier, per-token absmax over the block, codes zero-padded to the last
+// slab, the warps' code sums and c = gamma / s into the slot's header.
+// Returns false (in every thread) when the block must stop.
+__device__ __forceinline__ bool quantise_in_block(const Call &c, uint32_t slot, uint32_t want, int tid, Smem &sm,
+                                                  volatile int *abort_flag) {
+  const int warp = tid >> 5, lane = tid & 31;
+  const uint32_t xs = slot + kHeader;
+  const int nv = vec_count(c);
+  const bool in_regs = nv <= kJM * kC;
+  float xv[kJM][8];
+  bool timed_out = false;
+  float a = 0.0f;
+  const long long t0 = clock64();
+  // first pass: every value (polling output words until they carry the
+  // producing call's tag); kept in registers when they fit
+  for (int v0 = tid; v0 < nv; v0 += kJM * kC) {
+    bool ok[kJM];
+#pragma unroll
+    for (int j = 0; j < kJM; ++j) {
+      const int v = v0 + j * kC;
+      if (v < nv) {
+        ok[j] = load_vec8(c, v, want, xv[j]);
+      } else {
+        ok[j] = true;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) xv[j][e] = 0.0f;
+      }
+    }
+    bool all = true;
+#pragma unroll
+    for (int j = 0; j < kJM; ++j) all &= ok[j];
+    while (!all) {
+      if (clock64() - t0 > kWaitLimitCycles || gave_up()) {
+        timed_out = true;
+        break;
+      }
+      all = true;
+#pragma unroll
+      for (int j = 0; j < kJM; ++j)
+        if (!ok[j]) {
+          ok[j] = load_vec8(c, v0 + j * kC, want, xv[j]);
+          all &= ok[j];
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < kJM; ++j)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        xv[j][e] = act_of(c, xv[j][e]);
+        a = fmaxf(a, fabsf(xv[j][e]));
+      }
+    if (timed_out) break;
+  }
+  for (int k = 8 * nv + tid; k < c.K && !timed_out; k += kC) {
+    float f;
+    while (!load_one(c, k, want, f)) {
+      if (clock64() - t0 > kWaitLimitCycles || gave_up()) {
+        timed_out = true;
+        break;
+      }
+    }
+    a = fmaxf(a, fabsf(act_of(c, f)));
+  }
+  if (timed_out) atomicOr(&g_dev_error, kDevErrTimeout);
+  a = warp_max_nonneg(a);
+  if (lane == 0) sm.fred[warp] = a;
+  if (named_bar_or(1, kC, timed_out || *abort_flag)) return false;
+  a = sm.fred[0];
+#pragma unroll
+  for (int w = 1; w < kCW; ++w) a = fmaxf(a, sm.fred[w]);
+  const float s = act_scale(a);
+  // codes (every value is present now: a second pass reads plainly), then
+  // zeros from K to the end of the last slab
+  if (in_regs) {
+#pragma unroll
+    for (int j = 0; j < kJM; ++j) {
+      const int v = tid + j * kC;
+      if (v < nv) put_codes8(xs, v, xv[j], s);
+    }
+  } else {
+    for (int v = tid; v < nv; v += kC) {
+      float f[8];
+      load_vec8(c, v, want, f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) f[e] = act_of(c, f[e]);
+      put_codes8(xs, v, f, s);
+    }
+  }
+  const int kz = (c.K + 15) & ~15;
+  for (int k = 8 * nv + tid; k < kz; k += kC) {
+    int q = 0;
+    if (k < c.K) {
+      float f;
+      load_one(c, k, want, f);
+      q = quant_one(act_of(c, f), s);
+    }
+    sts_u8(xs + k, static_cast<uint32_t>(q) & 0xFFu);
+  }
+  for (int k = kz + 16 * tid; k < slabs_of(c.rb) * kSlabCodes; k += 16 * kC) sts_u128(xs + k, 0u, 0u, 0u, 0u);
+  if (tid == 0) asm volatile("st.shared.f32 [%0], %1;" ::"r"(slot), "f"(__fdiv_rn(__ldg(c.gamma), s)) : "memory");
+  named_bar(1, kC);
+  // X for this warp: the sum of the codes of its pieces (pieces w, w + 16,
+  // ... of the whole row: at most 32), one piece per lane
+  const int npieces = slabs_of(c.rb) * (kSlabCodes / 64);
+  int xw = 0;
+  const int pc = warp + kCW * lane;
+  if (pc < npieces) {
+    const uint32_t act = xs + static_cast<uint32_t>(64 * pc);
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+      const uint4 v = lds_u128(act + 16 * q4);
+      xw = dp4a_us(0x01010101u, v.x, xw);
+      xw = dp4a_us(0x01010101u, v.y, xw);
+      xw = dp4a_us(0x01010101u, v.z, xw);
+      xw = dp4a_us(0x01010101u, v.w, xw);
+    }
+  }
+  xw = __reduce_add_sync(0xffffffffu, xw);
+  if (lane == 0) asm volatile("st.shared.u32 [%0], %1;" ::"r"(slot + 64u + 4u * warp), "r"(xw) : "memory");
+  __syncwarp();
+  return true;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constant__ Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;  // the 128-byte swizzle needs 1 KB alignment
+  Smem &sm = *reinterpret_cast<Smem *>(smem_raw + (base - raw));
+  const uint32_t ring = base + kSmemFixed;
+  const uint32_t slots = ring + kStages * kStageBytes;  // two codes slots of kSlotBytes
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&sm.full[s]), 1);
       mbar_init(smem_u32(&sm.empty[s]), kCW);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&sm.sfull[s]), 1);
+      mbar_init(smem_u32(&sm.sempty[s]), 1);
     }
     sm.abort_flag = 0;
     sm.seq_tag = p.ctl[kCtlSeq] << 9;  // tags: (launch sequence << 9) | (call + 1)
@@ -306,56 +528,86 @@ __global__ void __maxnreg__(120) chain_kernel(const __grid_constant__ Params p) 
     uint32_t *dst = reinterpret_cast<uint32_t *>(sm.calls);
     const int words = p.n * static_cast<int>(sizeof(Call) / 4);
     for (int w = tid; w < words; w += kThreads) dst[w] = src[w];
-    for (int i = tid; i < kStages * kMaxSplitRows; i += kThreads) {
-      (&sm.part[0][0])[i] = 0;
-      (&sm.cnt[0][0])[i] = 0u;
-    }
   }
   __syncthreads();
   volatile int *abort_flag = &sm.abort_flag;
   const uint32_t seq_tag = sm.seq_tag;
 
+  // Calls with rows in this block take the codes slots in turn: slot a & 1
+  // for the a-th such call; a slot is reused two calls later.
   if (warp == kCW) {
-    // ------------------------------------------------ producer: every call's rows, in order
+    // ------------------------------------------------ producer: records and weight stages, in order
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
-      int i = 0, issued = 0;
+      int i = 0, issued = 0, a = 0;
+      int rec_n[2] = {0, 0};
       bool go = true;
       for (int ci = 0; ci < p.n && go; ++ci) {
         const Call &c = sm.calls[ci];
         int r0, rows;
         block_rows(c, r0, rows);
-        const int rb = row_bytes_of(c.K);
-        for (int q = 0; q < rows; q += c.stage_rows, ++i) {
-          const int s = i % kStages;
-          if (i >= kStages && (!mbar_wait(smem_u32(&sm.empty[s]), ((i / kStages) - 1) & 1) || *abort_flag)) {
+        if (rows == 0) continue;
+        const int sl = a & 1;
+        if (c.rec != nullptr) {
+          // the slot's previous call (a - 2) must be done with it
+          if (a >= 2 && (!mbar_wait(smem_u32(&sm.sempty[sl]), ((a >> 1) - 1) & 1) || *abort_flag)) {
             *abort_flag = 1;
-            go = false;
             break;
           }
-          const int nr = rows - q < c.stage_rows ? rows - q : c.stage_rows;
-          const uint32_t bytes = static_cast<uint32_t>(nr * rb);
-          const uint32_t fb = smem_u32(&sm.full[s]);
+          const uint32_t bytes = static_cast<uint32_t>(record_bytes(c.rb));
+          const uint32_t fb = smem_u32(&sm.sfull[sl]);
           mbar_arrive_expect_tx(fb, bytes);
-          bulk_g2s(ring + s * kStageBytes, c.packed + static_cast<int64_t>(r0 + q) * rb, bytes, fb, pol);
-          issued = i + 1;
+          bulk_g2s(slots + sl * kSlotBytes, c.rec, bytes, fb, policy_evict_last());
+          ++rec_n[sl];
+        }
+        ++a;
+        asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(c.map) : "memory");
+        if (c.rem > 0)
+          asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(c.map_rem) : "memory");
+        const int nslab = slabs_of(c.rb);
+        for (int g = 0; g < rows && go; g += kGroupRows) {
+          // a full group, or the block's last one: rows past it belong to
+          // the next block unless they lie past N (where the box reads zeros)
+          const bool part = rows - g < kGroupRows && r0 + rows < c.N;
+          const CUtensorMap *map = part ? c.map_rem : c.map;
+          const uint32_t box = static_cast<uint32_t>(part ? c.rem : kGroupRows) * kBoxBytes;
+          for (int s = 0; s < nslab; ++s, ++i) {
+            const int st = i % kStages;
+            if (i >= kStages && (!mbar_wait(smem_u32(&sm.empty[st]), ((i / kStages) - 1) & 1) || *abort_flag)) {
+              *abort_flag = 1;
+              go = false;
+              break;
+            }
+            const int nb = boxes_of(c.rb, s);
+            const uint32_t fb = smem_u32(&sm.full[st]);
+            mbar_arrive_expect_tx(fb, static_cast<uint32_t>(nb) * box);
+            for (int b = 0; b < nb; ++b)
+              tma_load_2d(ring + st * kStageBytes + b * kBoxSize, map, s * kSlabBytes + b * kBoxBytes, r0 + g, fb,
+                          pol);
+            issued = i + 1;
+          }
         }
       }
       // no copy into this block's shared memory may be in flight at exit
       for (int j = issued - kStages < 0 ? 0 : issued - kStages; j < issued; ++j)
         mbar_wait(smem_u32(&sm.full[j % kStages]), (j / kStages) & 1);
+      for (int sl = 0; sl < 2; ++sl)
+        if (rec_n[sl] > 0) mbar_wait(smem_u32(&sm.sfull[sl]), (rec_n[sl] - 1) & 1);
     }
+    __syncwarp();
   } else {
     // -------------------------------------------------- consumers
-    int it = 0;       // ring stage counter, in the producer's order
-    int nbar = 0;     // grid barriers passed
     // Every consumer warp passes the same sequence of block barriers: a
     // decision to stop is taken only from a barrier's reduced predicate (the
-    // same in every warp); a warp that stops streaming rows early still runs
-    // the later calls' barriers.
+    // same in every warp); a warp that stops streaming early still runs the
+    // later calls' barriers.
+    int it = 0;       // ring stage counter, in the producer's order
+    int nbar = 0;     // grid barriers passed
+    int ng = 0;       // row groups done (partial-sum buffer parity)
+    int a = 0;        // calls with rows here so far
+    int rec_n[2] = {0, 0};
     for (int ci = 0; ci < p.n; ++ci) {
       const Call &c = sm.calls[ci];
-      const float gam = __ldg(c.gamma);  // static input: fetched early
       int r0, rows;
       block_rows(c, r0, rows);
 
@@ -384,180 +636,80 @@ __global__ void __maxnreg__(120) chain_kernel(const __grid_constant__ Params p) 
         }
       }
       if (rows == 0) continue;
+      const int sl = a & 1;
+      const uint32_t slot = slots + sl * kSlotBytes;
 
-      // ---- the input: per-token absmax, s, c = gamma / s, codes in shared memory
-      const int rb = row_bytes_of(c.K);
-      const int units = rb / 8;
-      const int kp = rb * 4;
-      const uint32_t want = seq_tag | static_cast<uint32_t>(c.src + 1);
-      const bool vec = (c.K % 8) == 0 &&
-                       (c.mb_in != nullptr ? (reinterpret_cast<uintptr_t>(c.mb_in) & 15u) == 0u
-                                           : (reinterpret_cast<uintptr_t>(c.x) & 15u) == 0u);
-      const int nv = vec ? c.K / 8 : 0;
-      const bool in_regs = nv <= kJM * kC;
-      float xv[kJM][8];
-      bool timed_out = false;
-      float a = 0.0f;
-      {
-        // first pass: every value (polling output words until they carry the
-        // producing call's tag); kept in registers when they fit
-        const long long t0 = clock64();
-        for (int v0 = tid; v0 < nv; v0 += kJM * kC) {
-          bool ok[kJM];
-#pragma unroll
-          for (int j = 0; j < kJM; ++j) {
-            const int v = v0 + j * kC;
-            ok[j] = v < nv ? load_vec8(c, v, want, xv[j]) : true;
-            if (v >= nv)
-#pragma unroll
-              for (int e = 0; e < 8; ++e) xv[j][e] = 0.0f;
-          }
-          bool all = true;
-#pragma unroll
-          for (int j = 0; j < kJM; ++j) all &= ok[j];
-          while (!all) {
-            if (clock64() - t0 > kWaitLimitCycles || gave_up()) {
-              timed_out = true;
-              break;
-            }
-            all = true;
-#pragma unroll
-            for (int j = 0; j < kJM; ++j)
-              if (!ok[j]) {
-                ok[j] = load_vec8(c, v0 + j * kC, want, xv[j]);
-                all &= ok[j];
-              }
-          }
-#pragma unroll
-          for (int j = 0; j < kJM; ++j)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              xv[j][e] = act_of(c, xv[j][e]);
-              a = fmaxf(a, fabsf(xv[j][e]));
-            }
-          if (timed_out) break;
-        }
-        for (int k = 8 * nv + tid; k < c.K && !timed_out; k += kC) {
-          float f;
-          while (!load_one(c, k, want, f)) {
-            if (clock64() - t0 > kWaitLimitCycles || gave_up()) {
-              timed_out = true;
-              break;
-            }
-          }
-          a = fmaxf(a, fabsf(act_of(c, f)));
-        }
-      }
-      if (timed_out) atomicOr(&g_dev_error, kDevErrTimeout);
-      a = warp_max_nonneg(a);
-      if (lane == 0) sm.fred[warp] = a;
-      if (named_bar_or(1, kC, timed_out || *abort_flag)) {
-        *abort_flag = 1;
-        break;
-      }
-      a = sm.fred[0];
-#pragma unroll
-      for (int w = 1; w < kCW; ++w) a = fmaxf(a, sm.fred[w]);
-      const float s = act_scale(a);
-      // codes (every value is present now: a second pass reads plainly)
-      if (in_regs) {
-#pragma unroll
-        for (int j = 0; j < kJM; ++j) {
-          const int v = tid + j * kC;
-          if (v < nv) put_codes8(xs, v, xv[j], s);
-        }
+      // ---- the activation codes, c and the warp's code sum
+      if (c.rec != nullptr) {
+        const bool ok = mbar_wait(smem_u32(&sm.sfull[sl]), rec_n[sl] & 1);
+        ++rec_n[sl];
+        if (!ok) *abort_flag = 1;
       } else {
-        for (int v = tid; v < nv; v += kC) {
-          float f[8];
-          load_vec8(c, v, want, f);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) f[e] = act_of(c, f[e]);
-          put_codes8(xs, v, f, s);
-        }
-      }
-      for (int k = 8 * nv + tid; k < kp; k += kC) {
-        int q = 0;
-        if (k < c.K) {
-          float f;
-          load_one(c, k, want, f);
-          q = quant_one(act_of(c, f), s);
-        }
-        sts_u8(xs + k, static_cast<uint32_t>(q) & 0xFFu);
-      }
-      named_bar(1, kC);
-
-      // ---- this warp's chunk of K: activation codes in registers, and the
-      // lane's share of X = sum of codes (sum c*x - X = sum q*x, lane by lane)
-      const int G = 1 << c.split_log2;
-      const int cid = warp & (G - 1);
-      const int slot = warp >> c.split_log2;
-      const int step = kCW >> c.split_log2;
-      const int ubase = cid * c.chunk;
-      const int uend = ubase + c.chunk < units ? ubase + c.chunk : units;
-      uint32_t xa[kUPT][8];
-      uint32_t uoff[kUPT];
-      int xl = 0;
-      const bool lane_in = ubase + lane < uend;  // otherwise every unit is read at the chunk's first
-#pragma unroll
-      for (int u = 0; u < kUPT; ++u) {
-        const int unit = ubase + lane + 32 * u;
-        uint4 lo4 = make_uint4(0u, 0u, 0u, 0u), hi4 = lo4;
-        uoff[u] = 0u;
-        if (unit < uend) {
-          lo4 = lds_u128(xs + 32 * unit);
-          hi4 = lds_u128(xs + 32 * unit + 16);
-          uoff[u] = 256u * u;
-        }
-        xa[u][0] = lo4.x; xa[u][1] = lo4.y; xa[u][2] = lo4.z; xa[u][3] = lo4.w;
-        xa[u][4] = hi4.x; xa[u][5] = hi4.y; xa[u][6] = hi4.z; xa[u][7] = hi4.w;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) xl = dp4a_us(0x01010101u, xa[u][e], xl);
-      }
-      const int upt = (c.chunk + 31) / 32;  // unit slots this call needs
-      RowCtx x;
-      x.cm = __fdiv_rn(gam, s);
-      x.xl = xl;
-      x.laddr = 8u * static_cast<uint32_t>(lane_in ? ubase + lane : ubase);
-      x.rb = rb;
-      x.tag = seq_tag | static_cast<uint32_t>(ci + 1);
-      // (xs is rewritten by the next call only after its first block barrier)
-
-      // ---- rows, stage by stage
-      for (int q = 0; q < rows; q += c.stage_rows, ++it) {
-        const int st = it % kStages;
-        if (*abort_flag || !mbar_wait(smem_u32(&sm.full[st]), (it / kStages) & 1)) {
+        // the slot is free: its previous call (a - 2) ended at this block's
+        // group barriers, which every warp has passed
+        if (!quantise_in_block(c, slot, seq_tag | static_cast<uint32_t>(c.src + 1), tid, sm, abort_flag)) {
           *abort_flag = 1;
           break;
         }
-        const int nr = rows - q < c.stage_rows ? rows - q : c.stage_rows;
-        const uint32_t sbase = ring + st * kStageBytes;
-        x.y = c.y + r0 + q;
-        x.mb = c.mb_out != nullptr ? c.mb_out + r0 + q : nullptr;
-        if (G == 1) {
-          switch (upt) {
-#define BL_W(U) case U: stage_rows_whole<U>(sbase, nr, slot, step, lane, uoff, xa, x); break;
-            BL_W(1) BL_W(2) BL_W(3) BL_W(4) BL_W(5) BL_W(6) BL_W(7)
-            default: stage_rows_whole<8>(sbase, nr, slot, step, lane, uoff, xa, x); break;
-#undef BL_W
+      }
+      ++a;
+      float cm;
+      int xw;
+      asm volatile("ld.shared.f32 %0, [%1];" : "=f"(cm) : "r"(slot) : "memory");
+      asm volatile("ld.shared.u32 %0, [%1];" : "=r"(xw) : "r"(slot + 64u + 4u * warp) : "memory");
+      const uint32_t xs = slot + kHeader;
+      const int nslab = slabs_of(c.rb);
+      const uint32_t tag = seq_tag | static_cast<uint32_t>(ci + 1);
+      const uint32_t lrow = static_cast<uint32_t>(lane) * kBoxBytes;
+      const uint32_t lsw = static_cast<uint32_t>(lane & 7);
+
+      // ---- row groups: one lane per row, the slabs' pieces split over warps
+      for (int g = 0; g < rows; g += kGroupRows) {
+        int acc[4] = {0, 0, 0, 0};
+        for (int s = 0; s < nslab; ++s, ++it) {
+          const int st = it % kStages;
+          if (*abort_flag || !mbar_wait(smem_u32(&sm.full[st]), (it / kStages) & 1)) {
+            *abort_flag = 1;
+            break;
           }
-        } else {
-          switch (upt) {
-#define BL_S(U) case U: stage_rows_split<U>(sbase, nr, slot, step, lane, G, sm.part[st], sm.cnt[st], uoff, xa, x); break;
-            BL_S(1) BL_S(2) BL_S(3) BL_S(4) BL_S(5) BL_S(6) BL_S(7)
-            default: stage_rows_split<8>(sbase, nr, slot, step, lane, G, sm.part[st], sm.cnt[st], uoff, xa, x); break;
-#undef BL_S
+          const int npc = boxes_of(c.rb, s) * 8;
+          const uint32_t sbase = ring + st * kStageBytes + lrow;
+          const uint32_t abase = xs + static_cast<uint32_t>(s * kSlabCodes);
+          for (int pc = warp; pc < npc; pc += kCW) {
+            const uint32_t waddr = sbase + static_cast<uint32_t>((pc >> 3) * kBoxSize) +
+                                   ((static_cast<uint32_t>(pc & 7) ^ lsw) << 4);
+            piece(waddr, abase + 64u * pc, acc);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&sm.empty[st]));
+        }
+        const int pb = ng & 1;
+        sm.part[pb][warp][lane] = acc[0] + (acc[1] >> 2) + (acc[2] >> 4) + (acc[3] >> 6) - xw;
+        named_bar(2, kC);
+        // every warp is past this group's pieces: after the last group the
+        // slot may take the call two ahead
+        if (tid == 0 && g + kGroupRows >= rows) mbar_arrive(smem_u32(&sm.sempty[sl]));
+        // one warp per group adds the 16 partial sums of each row and writes it
+        if (warp == (ng % kCW)) {
+          const int h = rows - g < kGroupRows ? rows - g : kGroupRows;
+          if (lane < h) {
+            int t = 0;
+#pragma unroll
+            for (int w = 0; w < kCW; ++w) t += sm.part[pb][w][lane];
+            const int r = r0 + g + lane;
+            const float v = __fmul_rn(static_cast<float>(t), cm);
+            c.y[r] = v;
+            if (c.mb_out != nullptr) st_word(c.mb_out + r, v, tag);
           }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&sm.empty[st]));
+        ++ng;
       }
     }
+    __syncwarp();
   }
 
   // ---- the block is done with the launch; the last block to finish resets
-  // the counters and advances the sequence number for the next launch (each
-  // warp reconverges first: the producer's lane 0 may still be streaming)
-  __syncwarp();
+  // the counters and advances the sequence number for the next launch
   __syncthreads();
   if (tid == 0) {
     __threadfence();
