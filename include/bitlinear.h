@@ -320,14 +320,15 @@ typedef struct bl_chain_call {
 } bl_chain_call;
 
 /* Workspace (device bytes) that bitlinear_forward_chain needs for these
- * calls: 256 bytes of control words, 256 bytes per call (its weights' TMA
- * descriptors, rewritten by every launch), plus 8 * N bytes for every call
- * whose output a later call reads.  Host only; the calls' pointers are
+ * calls: 256 bytes of control words, 96 bytes per call (the call table,
+ * rewritten by every launch), a record of about K + 128 bytes for every call
+ * whose input no earlier call writes (its input quantised before the chain
+ * starts), plus 8 * N bytes for every call whose output a later call reads.  Host only; the calls' pointers are
  * compared, not dereferenced.  Errors: as bitlinear_forward_chain's argument
  * checks. */
 BL_API bl_status bitlinear_chain_workspace_bytes(const bl_chain_call *calls, int n, size_t *bytes);
 
-/* A decode chain: up to 256 single-token BitLinear forwards run in order in
+/* A decode chain: up to 240 single-token BitLinear forwards run in order in
  * one persistent launch (one block per SM, all resident).  Each call's
  * result equals, bit for bit, bitlinear_forward (or bitlinear_forward_relu2)
  * of its x as it stands when the call runs in sequence.
@@ -342,7 +343,7 @@ BL_API bl_status bitlinear_chain_workspace_bytes(const bl_chain_call *calls, int
  *     or between its output and an earlier call's inputs or output, and
  *     wait_prev = 1: every block first finishes all earlier calls (a
  *     grid-wide barrier).
- *   calls    host array of n descriptors (copied at the call; 1 <= n <= 256).
+ *   calls    host array of n descriptors (copied at the call; 1 <= n <= 240).
  *   ws       >= bitlinear_chain_workspace_bytes(calls, n) bytes, device,
  *            256-byte aligned, ZERO-FILLED before its first use; the library
  *            keeps its contents valid from launch to launch (a sequence

@@ -197,7 +197,7 @@ def test_chain_invalid_arguments_return_status(lib):
     assert lib.bitlinear_forward_chain(None, 1, ws, 256, None) == capi.BL_ERR_NULL
     assert lib.bitlinear_forward_chain(p, 1, None, 256, None) == capi.BL_ERR_NULL
     assert lib.bitlinear_forward_chain(p, 0, ws, 256, None) == capi.BL_ERR_SHAPE
-    assert lib.bitlinear_forward_chain(p, 257, ws, 256, None) == capi.BL_ERR_SHAPE
+    assert lib.bitlinear_forward_chain(p, 241, ws, 256, None) == capi.BL_ERR_SHAPE
     assert lib.bitlinear_forward_chain(p, 1, ws, 255, None) == capi.BL_ERR_WORKSPACE
     assert lib.bitlinear_forward_chain(p, 1, ctypes.c_void_p(odd), 256, None) == capi.BL_ERR_ALIGN
     for kw, want in ((dict(y=0), capi.BL_ERR_NULL), (dict(K=32769), capi.BL_ERR_SHAPE),

@@ -808,10 +808,11 @@ bool make_map_rows(CUtensorMap *m, const void *ptr, int64_t N, int64_t rb, int b
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Plan of a decode chain (host): each call's rows per block and tensor maps;
-// where its input comes from (quantised ahead into a record, an earlier
-// call's output words, or memory after a grid barrier); the workspace layout
-// (control words, two tensor maps per call, records, output words).
+// Plan of a decode chain (host): each call's rows per block (ng groups of gh
+// <= 32 rows, so one tensor map with box height gh serves every group) and
+// tensor map; where its input comes from (quantised ahead into a record, an
+// earlier call's output words, or memory after a grid barrier); the workspace
+// layout (control words, call table, records, output words).
 // Dependencies are read off the calls' buffers:
 //   * x written by no earlier call (and no wait_prev): quantised before the
 //     chain starts, into a record;
@@ -820,9 +821,9 @@ bool make_map_rows(CUtensorMap *m, const void *ptr, int64_t N, int64_t rb, int b
 //   * any other input byte (x, packed, gamma) written by an earlier call, an
 //     output byte written or read (from memory) by an earlier call, or
 //     wait_prev: a grid barrier before the call.
-// A call's output may not overlap its own inputs.  p, maps and q may be null
+// A call's output may not overlap its own inputs.  p, t and q may be null
 // (size only).
-static bl_status chain_plan(const bl_chain_call *calls, int n, int grid, chain::Params *p, CUtensorMap *maps,
+static bl_status chain_plan(const bl_chain_call *calls, int n, int grid, chain::Params *p, chain::TableCopy *t,
                             chain::QuantParams *q, size_t *ws_need, void *ws) {
   if (calls == nullptr) return BL_ERR_NULL;
   if (n < 1 || n > chain::kMaxCalls) return BL_ERR_SHAPE;
@@ -873,7 +874,7 @@ static bl_status chain_plan(const bl_chain_call *calls, int n, int grid, chain::
     barrier[c] = bar ? 1 : 0;
     early[c] = (j < 0 && !bar) ? 1 : 0;  // no earlier call writes x: quantised before the chain
   }
-  size_t off = plan::align256(chain::kMapsOffset + static_cast<size_t>(2 * n) * sizeof(CUtensorMap));
+  size_t off = plan::align256(chain::kTableOffset + static_cast<size_t>(n) * sizeof(chain::Call));
   std::vector<size_t> rec_off(n, 0), mb_off(n, 0);
   for (int i = 0; i < n; ++i)
     if (early[i]) {
@@ -887,33 +888,29 @@ static bl_status chain_plan(const bl_chain_call *calls, int n, int grid, chain::
     }
   *ws_need = off;
   if (p == nullptr) return BL_OK;
+  uint8_t *wsb = static_cast<uint8_t *>(ws);
   p->n = n;
   p->ctl = static_cast<unsigned *>(ws);
+  p->table = reinterpret_cast<const chain::Call *>(wsb + chain::kTableOffset);
+  t->n = n;
+  t->dst = reinterpret_cast<chain::Call *>(wsb + chain::kTableOffset);
   q->n = 0;
-  uint8_t *wsb = static_cast<uint8_t *>(ws);
-  CUtensorMap *wmaps = reinterpret_cast<CUtensorMap *>(wsb + chain::kMapsOffset);
   for (int i = 0; i < n; ++i) {
     const bl_chain_call &c = calls[i];
-    chain::Call &d = p->c[i];
+    chain::Call &d = t->calls[i];
     const int64_t rb = plan::row_bytes(c.K);
-    const int64_t rpc = (c.N + grid - 1) / grid;
-    const int rem = static_cast<int>(rpc % chain::kGroupRows);
-    if (!make_map_rows(&maps[2 * i], c.packed, c.N, rb, chain::kGroupRows)) return BL_ERR_CUDA;
-    if (rem > 0) {
-      if (!make_map_rows(&maps[2 * i + 1], c.packed, c.N, rb, rem)) return BL_ERR_CUDA;
-    } else {
-      maps[2 * i + 1] = maps[2 * i];
-    }
-    d.map = &wmaps[2 * i];
-    d.map_rem = &wmaps[2 * i + 1];
+    const int64_t rpc0 = (c.N + grid - 1) / grid;
+    const int64_t ng = (rpc0 + chain::kGroupRows - 1) / chain::kGroupRows;
+    const int64_t gh = (rpc0 + ng - 1) / ng;
+    if (!make_map_rows(&p->maps[i], c.packed, c.N, rb, static_cast<int>(gh))) return BL_ERR_CUDA;
     d.gamma = c.gamma;
     d.x = c.x;
     d.y = c.y;
     d.N = static_cast<int>(c.N);
     d.K = static_cast<int>(c.K);
     d.rb = static_cast<int>(rb);
-    d.rpc = static_cast<int>(rpc);
-    d.rem = rem;
+    d.rpc = static_cast<int>(ng * gh);
+    d.gh = static_cast<int>(gh);
     const int flags = (c.x_dtype == BL_BF16 ? chain::kFlagBf16 : 0) | (c.act == BL_ACT_RELU2 ? chain::kFlagRelu2 : 0);
     d.flags = flags | (barrier[i] ? chain::kFlagBarrier : 0);
     d.src = src[i];
@@ -934,7 +931,7 @@ static bl_status chain_plan(const bl_chain_call *calls, int n, int grid, chain::
   }
   for (int i = 0; i < n; ++i)
     if (src[i] >= 0)
-      p->c[i].mb_in = p->c[src[i]].mb_out + (xr[i].lo - yr[src[i]].lo) / 4;
+      t->calls[i].mb_in = t->calls[src[i]].mb_out + (xr[i].lo - yr[src[i]].lo) / 4;
   return BL_OK;
 }
 
@@ -958,28 +955,21 @@ bl_status bitlinear_forward_chain(const bl_chain_call *calls, int n, void *ws, s
   int dev = 0, sms = 0;
   s = current_device(&dev, &sms);
   if (s != BL_OK) return s;
-  // about 22 KB of call table, 64 KB of maps and 8 KB of quantisation jobs:
-  // kept off the stack (each launch copies its parameters)
+  // about 30 KB of tensor maps, 23 KB of call table and 8 KB of
+  // quantisation jobs: kept off the stack (each launch copies its parameters)
   static chain::Params p;
-  static chain::MapCopy mc;
+  static chain::TableCopy tc;
   static chain::QuantParams qp;
-  static CUtensorMap maps[2 * chain::kMaxCalls];
   static std::mutex p_mu;
   std::lock_guard<std::mutex> lk(p_mu);
-  s = chain_plan(calls, n, sms, &p, maps, &qp, &need, ws);
+  s = chain_plan(calls, n, sms, &p, &tc, &qp, &need, ws);
   if (s != BL_OK) return s;
   s = ensure_smem(dev, reinterpret_cast<const void *>(&chain::chain_kernel), chain::kSmemBytes);
   if (s != BL_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // the tensor maps into the workspace (their parameters are kept by value)
-  CUtensorMap *wmaps = reinterpret_cast<CUtensorMap *>(static_cast<uint8_t *>(ws) + chain::kMapsOffset);
-  for (int m0 = 0; m0 < 2 * n; m0 += chain::kMapsPerCopy) {
-    mc.n = 2 * n - m0 < chain::kMapsPerCopy ? 2 * n - m0 : chain::kMapsPerCopy;
-    mc.dst = wmaps + m0;
-    std::memcpy(mc.maps, maps + m0, sizeof(CUtensorMap) * static_cast<size_t>(mc.n));
-    s = launch(&chain::copy_maps_kernel, dim3(1), dim3(256), 0, st, false, mc);
-    if (s != BL_OK) return s;
-  }
+  // the call table into the workspace (its parameters are kept by value)
+  s = launch(&chain::copy_table_kernel, dim3(1), dim3(256), 0, st, false, tc);
+  if (s != BL_OK) return s;
   // the inputs no earlier call writes, quantised into their records
   if (qp.n > 0) {
     s = launch(&chain::chain_quant_kernel, dim3(static_cast<unsigned>(qp.n)), dim3(chain::kQThreads), 0, st, false,

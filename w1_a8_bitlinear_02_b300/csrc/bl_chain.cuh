@@ -15,10 +15,11 @@
 //     calls);
 //   * the consumer warps run the calls in order over the block's rows.
 //
-// Rows, one lane each.  A stage is a group of up to 32 consecutive rows and a
-// 1 KB slab of their packed bytes (4096 weights), loaded as 128-byte x 32-row
-// TMA boxes with the 128-byte swizzle, so lane l reading 16 bytes of row l
-// touches a different bank group than the other 7 lanes of its quarter-warp.
+// Rows, one lane each.  A block's rows form groups of gh <= 32 consecutive
+// rows; a stage is a group and a 1 KB slab of its packed bytes (4096
+// weights), loaded as 128-byte x gh-row TMA boxes with the 128-byte swizzle, so
+// lane l reading 16 bytes of row l touches a different bank group than the
+// other 7 lanes of its quarter-warp.
 // The 16 consumer warps split each slab's 16-byte pieces (64 weights) among
 // themselves; every lane of a warp needs the same 64 activation codes, which
 // are broadcast from shared memory.  A lane adds its row's pieces with the
@@ -34,12 +35,11 @@
 // item 2) of a call come one of two ways:
 //   * an input no earlier call writes is quantised before the chain starts
 //     (chain_quant_kernel, one block per such call) into a record in the
-//     workspace -- codes, c and the 16 warps' code sums -- and the producer
-//     loads the record by bulk copy along with the call's weights;
+//     workspace -- codes, c and the 16 warps' code sums -- and each weight
+//     stage carries the record's codes for its slab (and, for a group's first
+//     slab, the header), so these calls stream with no per-call set-up;
 //   * an input an earlier call writes is quantised by every block when the
-//     call comes up, into the same shared-memory slot.
-// Two slots alternate between consecutive calls, so a call's record arrives
-// while the previous call runs.
+//     call comes up, into a shared-memory area of its own.
 //
 // Dependencies between calls come in two forms, both found by the host from
 // the calls' buffers:
@@ -68,36 +68,39 @@
 namespace bl {
 namespace chain {
 
-constexpr int kMaxCalls = 256;
+constexpr int kMaxCalls = 240;            // one tensor map each in the kernel parameters
 constexpr int kCW = 16;                   // consumer warps
 constexpr int kThreads = (kCW + 1) * 32;  // + one producer warp
 constexpr int kC = kCW * 32;              // consumer threads
 constexpr int kMaxK = 32768;
 constexpr int kMaxN = 1 << 30;            // row indices stay far inside int
-constexpr int kGroupRows = 32;            // rows per group: one per lane
+constexpr int kGroupRows = 32;            // rows per group at most: one per lane
 constexpr int kBoxBytes = 128;            // packed bytes per TMA box row (512 weights)
 constexpr int kBoxSize = kGroupRows * kBoxBytes;  // 4 KB per box
 constexpr int kSlabBoxes = 8;             // a slab: 1 KB of each row (4096 weights)
 constexpr int kSlabBytes = kSlabBoxes * kBoxBytes;
 constexpr int kSlabCodes = kSlabBytes * 4;
-constexpr int kStageBytes = kSlabBoxes * kBoxSize;  // 32 KB
-constexpr int kStages = 3;
 constexpr int kJM = 2;                    // x vectors of 8 per consumer thread kept in registers (K <= 8192)
-// A codes slot (and a record in the workspace): a 128-byte header -- c =
-// gamma / s (fp32) at byte 0, the 16 warps' code sums (int32) at byte 64 --
-// then the codes, zero from K to the end of the last slab.
+// A record in the workspace (and the in-block codes area): a 128-byte header
+// -- c = gamma / s (fp32) at byte 0, the 16 warps' code sums (int32) at byte
+// 64 -- then the codes, zero from K to the end of the last slab.
 constexpr int kHeader = 128;
-constexpr int kSlotBytes = kHeader + kMaxK + kSlabCodes;
+constexpr int kInBlockBytes = kHeader + kMaxK + kSlabCodes;
+// A ring stage: the slab's weight boxes (32 KB), then the record header and
+// the slab's 4096 activation codes (one bulk copy for a group's first slab,
+// whose header travels with it); 1 KB aligned for the next stage's boxes.
+constexpr int kStageW = kSlabBoxes * kBoxSize;
+constexpr int kStageBytes = kStageW + kSlabCodes + 1024;
+constexpr int kStages = 4;
 constexpr int kSmemFixed = 30 * 1024;     // barriers, partial sums and the call table
-constexpr int kSmemBytes = 1024 + kSmemFixed + kStages * kStageBytes + 2 * kSlotBytes;
+constexpr int kSmemBytes = 1024 + kSmemFixed + kStages * kStageBytes + kInBlockBytes;
 
 // Control words at the start of the workspace (bytes 0..255), then the
-// calls' tensor maps (two per call, 128 bytes each), the records, the output
-// words.
+// call table, the records, the output words.
 constexpr int kCtlBar = 0;    // grid-barrier arrivals of this launch
 constexpr int kCtlDone = 1;   // blocks finished with this launch
 constexpr int kCtlSeq = 32;   // launches completed on this workspace (tags)
-constexpr int kMapsOffset = 256;
+constexpr int kTableOffset = 256;
 
 // Call flags.
 constexpr int kFlagBf16 = 1;      // x is bf16 (else fp32)
@@ -108,8 +111,6 @@ __host__ __device__ constexpr int slabs_of(int rb) { return (rb + kSlabBytes - 1
 __host__ __device__ constexpr int record_bytes(int rb) { return kHeader + slabs_of(rb) * kSlabCodes; }
 
 struct Call {
-  const CUtensorMap *map;      // packed [N, rb] bytes, box 128 B x 32 rows, 128-byte swizzle
-  const CUtensorMap *map_rem;  // the same with rem rows per box (a block's last, partial group)
   const float *gamma;
   const void *x;          // [K] f32 or bf16 (read when neither rec nor mb_in is set)
   float *y;               // [N]
@@ -118,50 +119,50 @@ struct Call {
   const uint64_t *mb_in;  // the words holding x [K] (inside an earlier call's mb_out), or null
   int N, K;
   int rb;                 // packed row bytes
-  int rpc;                // rows per block
-  int rem;                // rpc % 32: rows of every block's partial group (0: none)
+  int rpc;                // rows per block: ng groups of gh rows
+  int gh;                 // rows per group (<= 32; the tensor map's box height)
   int flags;
   int src;                // the call that wrote mb_in
   int pad_;
 };
 static_assert(sizeof(Call) % 4 == 0, "call table copied in words");
 
+// The packed weights of call i are read through maps[i]: [N, rb] bytes, box
+// 128 bytes x gh rows, 128-byte swizzle.  Tensor maps in the kernel
+// parameters need no fetch from global memory (a map read from global memory
+// stalled the issuing thread by about an L2 round trip per call).
 struct Params {
   int n;                  // calls
   unsigned *ctl;          // workspace control words
-  Call c[kMaxCalls];
+  const Call *table;      // the call table (in the workspace)
+  CUtensorMap maps[kMaxCalls];
 };
 
 struct Smem {
   uint64_t full[kStages];
   uint64_t empty[kStages];
-  uint64_t sfull[2];      // a slot's record has landed
-  uint64_t sempty[2];     // a slot's call is done with it
   float fred[kCW];
   int32_t part[2][kCW][kGroupRows];  // a group's partial sums, by group parity
   uint32_t seq_tag;
   int abort_flag;
-  Call calls[kMaxCalls];  // the parameters, copied once: indexed reads of the
-                          // parameter space go through the constant cache
+  Call calls[kMaxCalls];  // the call table, copied in once
 };
 static_assert(sizeof(Smem) <= kSmemFixed, "fixed shared-memory region");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory of one block");
 
 // ------------------------------------------------------------ set-up kernels
-// Maps for the workspace, copied there by a separate launch (kernel
-// parameters hold them by value, so a captured graph keeps them).
-constexpr int kMapsPerCopy = 254;  // the whole struct (64-byte aligned) stays under 32764 bytes
-struct MapCopy {
+// The call table into the workspace (a separate launch: its parameters hold
+// the table by value, so a captured graph keeps it).
+struct TableCopy {
   int n;
-  CUtensorMap *dst;
-  CUtensorMap maps[kMapsPerCopy];
+  Call *dst;
+  Call calls[kMaxCalls];
 };
-__global__ void copy_maps_kernel(const __grid_constant__ MapCopy m) {
-  const uint4 *src = reinterpret_cast<const uint4 *>(m.maps);
-  uint4 *dst = reinterpret_cast<uint4 *>(m.dst);
-  const int words = m.n * static_cast<int>(sizeof(CUtensorMap) / 16);
+__global__ void copy_table_kernel(const __grid_constant__ TableCopy t) {
+  const uint32_t *src = reinterpret_cast<const uint32_t *>(t.calls);
+  uint32_t *dst = reinterpret_cast<uint32_t *>(t.dst);
+  const int words = t.n * static_cast<int>(sizeof(Call) / 4);
   for (int i = threadIdx.x; i < words; i += blockDim.x) dst[i] = src[i];
-  asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
 }
 
 // One input quantised ahead: x [K] (f32 or bf16, relu2 first if flagged) ->
@@ -377,10 +378,10 @@ __device__ __forceinline__ void piece(uint32_t waddr, uint32_t act, int (&a)[4])
 }
 
 // Quantise the input of call c in every block (it depends on earlier calls)
-// into the codes slot: values polled from output words or read after the grid
-// barrier, per-token absmax over the block, codes zero-padded to the last
-// slab, the warps' code sums and c = gamma / s into the slot's header.
-// Returns false (in every thread) when the block must stop.
+// into the in-block codes area `slot`: values polled from output words or
+// read after the grid barrier, per-token absmax over the block, codes
+// zero-padded to the last slab, the warps' code sums and c = gamma / s into
+// the area's header.  Returns false (in every thread) when the block must stop.
 __device__ __forceinline__ bool quantise_in_block(const Call &c, uint32_t slot, uint32_t want, int tid, Smem &sm,
                                                   volatile int *abort_flag) {
   const int warp = tid >> 5, lane = tid & 31;
@@ -507,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
   const uint32_t base = (raw + 1023u) & ~1023u;  // the 128-byte swizzle needs 1 KB alignment
   Smem &sm = *reinterpret_cast<Smem *>(smem_raw + (base - raw));
   const uint32_t ring = base + kSmemFixed;
-  const uint32_t slots = ring + kStages * kStageBytes;  // two codes slots of kSlotBytes
+  const uint32_t inb = ring + kStages * kStageBytes;  // codes quantised in this block
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
@@ -515,16 +516,12 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
       mbar_init(smem_u32(&sm.full[s]), 1);
       mbar_init(smem_u32(&sm.empty[s]), kCW);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(smem_u32(&sm.sfull[s]), 1);
-      mbar_init(smem_u32(&sm.sempty[s]), 1);
-    }
     sm.abort_flag = 0;
     sm.seq_tag = p.ctl[kCtlSeq] << 9;  // tags: (launch sequence << 9) | (call + 1)
     fence_barrier_init();
   }
   {
-    const uint32_t *src = reinterpret_cast<const uint32_t *>(p.c);
+    const uint32_t *src = reinterpret_cast<const uint32_t *>(p.table);
     uint32_t *dst = reinterpret_cast<uint32_t *>(sm.calls);
     const int words = p.n * static_cast<int>(sizeof(Call) / 4);
     for (int w = tid; w < words; w += kThreads) dst[w] = src[w];
@@ -533,44 +530,27 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
   volatile int *abort_flag = &sm.abort_flag;
   const uint32_t seq_tag = sm.seq_tag;
 
-  // Calls with rows in this block take the codes slots in turn: slot a & 1
-  // for the a-th such call; a slot is reused two calls later.
   if (warp == kCW) {
     // ------------------------------------------------ producer: records and weight stages, in order
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
-      int i = 0, issued = 0, a = 0;
-      int rec_n[2] = {0, 0};
+      const uint64_t pol_rec = policy_evict_last();  // records are read by every block
+      int i = 0, issued = 0;
       bool go = true;
       for (int ci = 0; ci < p.n && go; ++ci) {
-        const Call &c = sm.calls[ci];
-        int r0, rows;
-        block_rows(c, r0, rows);
+        // the call's fields in registers (the asm statements below clobber
+        // memory, which would make every use a shared-memory reload)
+        const int N = sm.calls[ci].N, rb = sm.calls[ci].rb, rpc = sm.calls[ci].rpc, gh = sm.calls[ci].gh;
+        const uint8_t *rec = sm.calls[ci].rec;
+        const int r0 = static_cast<int>(blockIdx.x) * rpc;
+        const int rows = N - r0 < rpc ? (N - r0 > 0 ? N - r0 : 0) : rpc;
         if (rows == 0) continue;
-        const int sl = a & 1;
-        if (c.rec != nullptr) {
-          // the slot's previous call (a - 2) must be done with it
-          if (a >= 2 && (!mbar_wait(smem_u32(&sm.sempty[sl]), ((a >> 1) - 1) & 1) || *abort_flag)) {
-            *abort_flag = 1;
-            break;
-          }
-          const uint32_t bytes = static_cast<uint32_t>(record_bytes(c.rb));
-          const uint32_t fb = smem_u32(&sm.sfull[sl]);
-          mbar_arrive_expect_tx(fb, bytes);
-          bulk_g2s(slots + sl * kSlotBytes, c.rec, bytes, fb, policy_evict_last());
-          ++rec_n[sl];
-        }
-        ++a;
-        asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(c.map) : "memory");
-        if (c.rem > 0)
-          asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(c.map_rem) : "memory");
-        const int nslab = slabs_of(c.rb);
-        for (int g = 0; g < rows && go; g += kGroupRows) {
-          // a full group, or the block's last one: rows past it belong to
-          // the next block unless they lie past N (where the box reads zeros)
-          const bool part = rows - g < kGroupRows && r0 + rows < c.N;
-          const CUtensorMap *map = part ? c.map_rem : c.map;
-          const uint32_t box = static_cast<uint32_t>(part ? c.rem : kGroupRows) * kBoxBytes;
+        const CUtensorMap *map = &p.maps[ci];
+        const int nslab = slabs_of(rb);
+        // groups of gh rows (the last block's last group may run past N,
+        // where the box reads zeros)
+        const uint32_t box = static_cast<uint32_t>(gh) * kBoxBytes;
+        for (int g = 0; g < rows && go; g += gh) {
           for (int s = 0; s < nslab; ++s, ++i) {
             const int st = i % kStages;
             if (i >= kStages && (!mbar_wait(smem_u32(&sm.empty[st]), ((i / kStages) - 1) & 1) || *abort_flag)) {
@@ -578,12 +558,20 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
               go = false;
               break;
             }
-            const int nb = boxes_of(c.rb, s);
+            const int nb = boxes_of(rb, s);
             const uint32_t fb = smem_u32(&sm.full[st]);
-            mbar_arrive_expect_tx(fb, static_cast<uint32_t>(nb) * box);
+            const uint32_t sb = ring + st * kStageBytes;
+            uint32_t tx = static_cast<uint32_t>(nb) * box;
+            if (rec != nullptr) tx += kSlabCodes + (s == 0 ? kHeader : 0);
+            mbar_arrive_expect_tx(fb, tx);
             for (int b = 0; b < nb; ++b)
-              tma_load_2d(ring + st * kStageBytes + b * kBoxSize, map, s * kSlabBytes + b * kBoxBytes, r0 + g, fb,
-                          pol);
+              tma_load_2d(sb + b * kBoxSize, map, s * kSlabBytes + b * kBoxBytes, r0 + g, fb, pol);
+            if (rec != nullptr) {
+              if (s == 0)
+                bulk_g2s(sb + kStageW, rec, kHeader + kSlabCodes, fb, pol_rec);
+              else
+                bulk_g2s(sb + kStageW + kHeader, rec + kHeader + s * kSlabCodes, kSlabCodes, fb, pol_rec);
+            }
             issued = i + 1;
           }
         }
@@ -591,8 +579,6 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
       // no copy into this block's shared memory may be in flight at exit
       for (int j = issued - kStages < 0 ? 0 : issued - kStages; j < issued; ++j)
         mbar_wait(smem_u32(&sm.full[j % kStages]), (j / kStages) & 1);
-      for (int sl = 0; sl < 2; ++sl)
-        if (rec_n[sl] > 0) mbar_wait(smem_u32(&sm.sfull[sl]), (rec_n[sl] - 1) & 1);
     }
     __syncwarp();
   } else {
@@ -604,8 +590,6 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
     int it = 0;       // ring stage counter, in the producer's order
     int nbar = 0;     // grid barriers passed
     int ng = 0;       // row groups done (partial-sum buffer parity)
-    int a = 0;        // calls with rows here so far
-    int rec_n[2] = {0, 0};
     for (int ci = 0; ci < p.n; ++ci) {
       const Call &c = sm.calls[ci];
       int r0, rows;
@@ -636,70 +620,83 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
         }
       }
       if (rows == 0) continue;
-      const int sl = a & 1;
-      const uint32_t slot = slots + sl * kSlotBytes;
+      // the call's fields in registers (asm statements below clobber memory)
+      const bool has_rec = c.rec != nullptr;
+      const int rb = c.rb, gh = c.gh;
+      float *const yout = c.y;
+      uint64_t *const mbo = c.mb_out;
 
-      // ---- the activation codes, c and the warp's code sum
-      if (c.rec != nullptr) {
-        const bool ok = mbar_wait(smem_u32(&sm.sfull[sl]), rec_n[sl] & 1);
-        ++rec_n[sl];
-        if (!ok) *abort_flag = 1;
-      } else {
-        // the slot is free: its previous call (a - 2) ended at this block's
-        // group barriers, which every warp has passed
-        if (!quantise_in_block(c, slot, seq_tag | static_cast<uint32_t>(c.src + 1), tid, sm, abort_flag)) {
+      // ---- the activation codes, c and the warp's code sum: from the
+      // record (in the call's first stage) or quantised here
+      float cm = 0.0f;
+      int xw = 0;
+      if (!has_rec) {
+        // the area is free: earlier calls ended at this block's group
+        // barriers, which every warp has passed
+        if (!quantise_in_block(c, inb, seq_tag | static_cast<uint32_t>(c.src + 1), tid, sm, abort_flag)) {
           *abort_flag = 1;
           break;
         }
+        asm volatile("ld.shared.f32 %0, [%1];" : "=f"(cm) : "r"(inb) : "memory");
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(xw) : "r"(inb + 64u + 4u * warp) : "memory");
       }
-      ++a;
-      float cm;
-      int xw;
-      asm volatile("ld.shared.f32 %0, [%1];" : "=f"(cm) : "r"(slot) : "memory");
-      asm volatile("ld.shared.u32 %0, [%1];" : "=r"(xw) : "r"(slot + 64u + 4u * warp) : "memory");
-      const uint32_t xs = slot + kHeader;
-      const int nslab = slabs_of(c.rb);
+      const int nslab = slabs_of(rb);
       const uint32_t tag = seq_tag | static_cast<uint32_t>(ci + 1);
       const uint32_t lrow = static_cast<uint32_t>(lane) * kBoxBytes;
       const uint32_t lsw = static_cast<uint32_t>(lane & 7);
 
       // ---- row groups: one lane per row, the slabs' pieces split over warps
-      for (int g = 0; g < rows; g += kGroupRows) {
-        int acc[4] = {0, 0, 0, 0};
+      for (int g = 0; g < rows; g += gh) {
+        int acc[4] = {0, 0, 0, 0}, acc2[4] = {0, 0, 0, 0};
         for (int s = 0; s < nslab; ++s, ++it) {
           const int st = it % kStages;
           if (*abort_flag || !mbar_wait(smem_u32(&sm.full[st]), (it / kStages) & 1)) {
             *abort_flag = 1;
             break;
           }
-          const int npc = boxes_of(c.rb, s) * 8;
-          const uint32_t sbase = ring + st * kStageBytes + lrow;
-          const uint32_t abase = xs + static_cast<uint32_t>(s * kSlabCodes);
-          for (int pc = warp; pc < npc; pc += kCW) {
-            const uint32_t waddr = sbase + static_cast<uint32_t>((pc >> 3) * kBoxSize) +
-                                   ((static_cast<uint32_t>(pc & 7) ^ lsw) << 4);
-            piece(waddr, abase + 64u * pc, acc);
+          const int npc = boxes_of(rb, s) * 8;
+          const uint32_t sb = ring + st * kStageBytes;
+          const uint32_t sbase = sb + lrow;
+          const uint32_t abase = has_rec ? sb + kStageW + kHeader : inb + kHeader + static_cast<uint32_t>(s * kSlabCodes);
+          if (has_rec && g == 0 && s == 0) {
+            asm volatile("ld.shared.f32 %0, [%1];" : "=f"(cm) : "r"(sb + kStageW) : "memory");
+            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(xw) : "r"(sb + kStageW + 64u + 4u * warp) : "memory");
+          }
+          // two pieces at a time, in separate accumulators, so their loads
+          // and dp4a chains overlap
+          int pc = warp;
+          for (; pc + kCW < npc; pc += 2 * kCW) {
+            const uint32_t w0 = sbase + static_cast<uint32_t>((pc >> 3) * kBoxSize) +
+                                ((static_cast<uint32_t>(pc & 7) ^ lsw) << 4);
+            const int pc1 = pc + kCW;
+            const uint32_t w1 = sbase + static_cast<uint32_t>((pc1 >> 3) * kBoxSize) +
+                                ((static_cast<uint32_t>(pc1 & 7) ^ lsw) << 4);
+            piece(w0, abase + 64u * pc, acc);
+            piece(w1, abase + 64u * pc1, acc2);
+          }
+          if (pc < npc) {
+            const uint32_t w0 = sbase + static_cast<uint32_t>((pc >> 3) * kBoxSize) +
+                                ((static_cast<uint32_t>(pc & 7) ^ lsw) << 4);
+            piece(w0, abase + 64u * pc, acc);
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&sm.empty[st]));
         }
         const int pb = ng & 1;
-        sm.part[pb][warp][lane] = acc[0] + (acc[1] >> 2) + (acc[2] >> 4) + (acc[3] >> 6) - xw;
+        sm.part[pb][warp][lane] = (acc[0] + acc2[0]) + ((acc[1] + acc2[1]) >> 2) + ((acc[2] + acc2[2]) >> 4) +
+                                  ((acc[3] + acc2[3]) >> 6) - xw;
         named_bar(2, kC);
-        // every warp is past this group's pieces: after the last group the
-        // slot may take the call two ahead
-        if (tid == 0 && g + kGroupRows >= rows) mbar_arrive(smem_u32(&sm.sempty[sl]));
         // one warp per group adds the 16 partial sums of each row and writes it
         if (warp == (ng % kCW)) {
-          const int h = rows - g < kGroupRows ? rows - g : kGroupRows;
+          const int h = rows - g < gh ? rows - g : gh;
           if (lane < h) {
             int t = 0;
 #pragma unroll
             for (int w = 0; w < kCW; ++w) t += sm.part[pb][w][lane];
             const int r = r0 + g + lane;
             const float v = __fmul_rn(static_cast<float>(t), cm);
-            c.y[r] = v;
-            if (c.mb_out != nullptr) st_word(c.mb_out + r, v, tag);
+            yout[r] = v;
+            if (mbo != nullptr) st_word(mbo + r, v, tag);
           }
         }
         ++ng;
