@@ -4,15 +4,21 @@
 Headline workload, one step: decode at M = 1 over a ~2B-class ternary model's
 projections -- 30 layers x {QKV 2560->3840, O 2560->2560, up 2560->6912,
 down 6912->2560} with distinct weights (388 MB packed, three times the 126 MB
-L2, so every step streams the weights from HBM; no L2 flush is needed).  A
-step is one bitlinear_forward per matrix (120 calls: fused activation
-quantisation + packed-ternary GEMV + rescale), captured once in a CUDA graph
-with launch overlap on and replayed.  Metric: GB/s of algorithmic bytes
-(packed weights + bf16 activations + fp32 outputs + gamma).
+L2, so every step streams the weights from HBM; no L2 flush is needed) and a
+bf16 N(0, 1) input per projection (the down projection's relu(z)^2-shaped).
+A step is the 120 single-token forwards (activation quantisation + packed-
+ternary contraction + rescale) as one bitlinear_forward_chain launch: the
+inputs are independent, so the chain streams the weights of all 120 calls
+without waiting between them.  Captured once in a CUDA graph and replayed.
+Metric: GB/s of algorithmic bytes (packed weights + bf16 activations + fp32
+outputs + gamma).
 
-Extra workloads reported under "extras": batched decode M in {8,16,32,64} on
-the same weights, prefill M = 2048 (tensor-core path; dense-equivalent
-2*M*N*K ops/s) and the 100B-class decode shapes (80 layers, 9.4 GB resident).
+"extras" adds the same weights run as dependent calls (each call waits for
+the one before: per-call launches, the chain with a grid barrier before every
+call, the chain passing each output on as the next input), as independent
+per-call launches, with grouped scales, batched decode M in {8,16,32,64},
+prefill M = 2048 (tensor-core path; dense-equivalent 2*M*N*K ops/s) and the
+100B-class shapes (80 layers, 9.4 GB resident).
 
 --impl reference times the CPU oracle instead (the repository's plain C
 restatement of the method) on a bounded sample of the same workload.
@@ -36,21 +42,22 @@ sys.path.insert(0, ROOT)
 METRIC = "BitLinear GB/s (decode, % HBM peak) and int8 TOPS (prefill, % INT8 peak)"
 WORKLOAD = "decode_2b"
 
-# DRAM bytes (read + write) per decode-GEMV launch, mean over the four ~2B
-# shapes, from one ncu capture of the kernel source whose sha256 starts with
-# `src`; reported as null once that source has changed.
-GEMV_TRAFFIC = {"bytes_per_launch": 3282560.0, "src": "d10bf5d2912effc9",
-                "file": "w1_a8_bitlinear_02_b300/csrc/bl_gemv.cuh"}
+# DRAM bytes (read + write) of one chain launch of the headline step, from
+# one ncu capture of the kernel source whose sha256 starts with `src`;
+# reported as null once that source has changed.
+CHAIN_TRAFFIC = {"bytes_per_launch": None, "src": "",
+                 "file": "w1_a8_bitlinear_02_b300/csrc/bl_chain.cuh"}
 
 
 def measured_traffic():
     import hashlib
-    path = os.path.join(ROOT, GEMV_TRAFFIC["file"])
+    path = os.path.join(ROOT, CHAIN_TRAFFIC["file"])
     try:
         h = hashlib.sha256(open(path, "rb").read()).hexdigest()
     except OSError:
         return None
-    return GEMV_TRAFFIC["bytes_per_launch"] if h.startswith(GEMV_TRAFFIC["src"]) else None
+    ok = CHAIN_TRAFFIC["src"] and h.startswith(CHAIN_TRAFFIC["src"])
+    return CHAIN_TRAFFIC["bytes_per_launch"] if ok else None
 
 
 def load_peaks() -> dict:
@@ -369,6 +376,48 @@ REF_TIMED_S = 6.0
 
 
 # ------------------------------------------------------------------ our arm
+def chain_calls(items, mode="independent"):
+    """Chain descriptors for the items: independent inputs (each call its own
+    x), "barrier" (the same, each call waiting for every earlier one) or
+    "dataflow" (each call's input is the previous call's output, cut to K;
+    the down projection squares its ReLU)."""
+    calls, prev = [], None
+    for it in items:
+        mt = it["mt"]
+        c = dict(packed=it["packed"], gamma=it["gamma"], x=it["x"], y=it["y"], N=mt.N, K=mt.K,
+                 wait_prev=1 if mode == "barrier" else 0)
+        if mode == "dataflow" and prev is not None and prev.shape[1] >= mt.K:
+            c["x"] = prev[:, :mt.K]
+            c["act"] = 1 if mt.name == "down" else 0
+        calls.append(c)
+        prev = it["y"]
+    return calls
+
+
+def capture_chain(bl, calls, ws, stream):
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        bl.bitlinear_forward_chain(calls, ws)  # warm (kernel attributes)
+        stream.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            bl.bitlinear_forward_chain(calls, ws)
+    return g
+
+
+def chain_launches(calls) -> int:
+    """Launches of one chain call: the call table copy, the quantisation of
+    inputs no earlier call writes (when there are any), the chain itself."""
+    ys = [(c["y"].data_ptr(), c["y"].data_ptr() + c["y"].numel() * 4) for c in calls]
+    early = 0
+    for i, c in enumerate(calls):
+        lo = c["x"].data_ptr()
+        hi = lo + c["x"].numel() * c["x"].element_size()
+        if not c.get("wait_prev", 0) and not any(a < hi and lo < b for a, b in ys[:i]):
+            early += 1
+    return 2 + (1 if early else 0)
+
+
 def run_ours(args, rank: int, world: int, local: int):
     import torch
 
@@ -387,8 +436,10 @@ def run_ours(args, rank: int, world: int, local: int):
     x_slab, y_slab = to_slabs(items, torch)
     step_bytes = sum(algorithmic_bytes(1, it["mt"].N, it["mt"].K) for it in items)
     packed_bytes = sum(it["packed"].numel() for it in items)
-    g = capture(bl, items, stream)
-    launches_step = sum(launches_per_call(bl, 1, it["mt"].N, it["mt"].K) for it in items)
+    calls = chain_calls(items)
+    ws = bl.chain_workspace(calls, device)
+    g = capture_chain(bl, calls, ws, stream)
+    launches_step = chain_launches(calls)
 
     with ClockSampler(local) as clk:
         secs = time_graph(g, stream, args.steps, args.warmup, D, device)
@@ -397,22 +448,21 @@ def run_ours(args, rank: int, world: int, local: int):
     ms_step = secs_max / args.steps * 1e3
     assert bl.device_error() == 0, "a kernel reported a device-side failure"
 
-    # the dominant kernel: the M=1 GEMV, the only kernel of the step (one
-    # launch per matrix); with launch overlap consecutive launches overlap, so
-    # the per-launch duration is the step time divided by the launches
-    per_launch_s = secs / (args.steps * len(items))
-    per_launch_bytes = step_bytes / len(items)
-    achieved = per_launch_bytes / per_launch_s / 1e9
+    # the dominant kernel: the chain, one launch per step; its duration is
+    # taken as the whole step's (the two small set-up launches included), so
+    # the achieved rate is a lower bound of the chain kernel's own
+    per_launch_s = secs / args.steps
+    achieved = step_bytes / per_launch_s / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "traffic": measured_traffic(),
                 "traffic_unit": "bytes per launch (dram read + write, ncu)",
-                "algorithmic_bytes_per_launch": per_launch_bytes,
-                "kernel": "bl::gemv::gemv_kernel<1,*,bf16>",
-                "duration": "step time / launches per step (CUDA events on the launching stream; "
-                            "the GEMV is the only kernel in the step)",
+                "algorithmic_bytes_per_launch": step_bytes,
+                "kernel": "bl::chain::chain_kernel",
+                "duration": "step time (CUDA events on the launching stream) per chain launch, the "
+                            "call-table copy and input quantisation launches of the step included",
                 "peak_source": f"{peaks['source']} (copy bandwidth)"}
 
-    # end to end: pinned host x -> device, the sweep, device y -> pinned host
+    # end to end: pinned host x -> device, the step, device y -> pinned host
     # (one copy each way per step: the calls' inputs and outputs are slabs)
     x_host = x_slab.cpu().pin_memory()
     y_host = torch.empty_like(y_slab, device="cpu").pin_memory()
@@ -441,7 +491,8 @@ def run_ours(args, rank: int, world: int, local: int):
     e2e = {"value": e2e_bytes / e2e_s / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": d2h,
            "how": "per step: one pinned-host -> device copy of every call's x (one slab), the "
-                  "120-call graph, one device -> pinned-host copy of every call's y (one slab)"}
+                  "chain launch, one device -> pinned-host copy of every call's y (one slab)"}
+    del g
 
     extras = {}
     if not args.no_extras:
@@ -450,13 +501,12 @@ def run_ours(args, rank: int, world: int, local: int):
     cpu_baseline = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         hi = host_items(items, 4)
-        el, nb, calls, cores = oracle_timing(hi, args.cpu_seconds)
+        el, nb, ncalls, cores = oracle_timing(hi, args.cpu_seconds)
         cpu_baseline = {"value": nb / el / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
-                        "sample": f"{calls} calls of the oracle's forward on layer 0's four "
+                        "sample": f"{ncalls} calls of the oracle's forward on layer 0's four "
                                   "projections at M=1 (host copies of the same packed weights "
-                                  f"and activations), {el:.1f} s"}
+                                  f"and activations), {el:.1f} s after {ORACLE_WARM_S} s of warm-up"}
 
-    del g
     if rank == 0:
         line = {
             "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world,
@@ -464,15 +514,16 @@ def run_ours(args, rank: int, world: int, local: int):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "int8", "data": "synthetic",
             "config": {"workload": f"decode_2b: M=1 over {args.layers} layers x {{qkv 3840x2560, "
-                                   "o 2560x2560, up 6912x2560, down 2560x6912}, x bf16, fused act-quant",
+                                   "o 2560x2560, up 6912x2560, down 2560x6912}, an independent "
+                                   "x bf16 per projection, fused act-quant",
                        "M": 1, "layers": args.layers, "matrices": len(items),
                        "packed_weight_bytes_per_step": packed_bytes,
                        "algorithmic_bytes_per_step": step_bytes,
                        "l2": (f"inputs larger than L2 (packed weights {packed_bytes / 1e6:.0f} MB vs "
                               "126 MB L2); no flush") if packed_bytes > 126e6 else
                              f"packed weights {packed_bytes / 1e6:.0f} MB fit in L2 (reduced run)",
-                       "launch": "CUDA graph of one bitlinear_forward per matrix, launch overlap "
-                                 + ("off" if args.no_overlap else "on"),
+                       "launch": "CUDA graph of one bitlinear_forward_chain of the 120 calls "
+                                 "(independent inputs: no call waits for another)",
                        "parallelism": f"{world} independent replica(s), weak scaling"},
             "roofline": roofline,
             "cpu_baseline": cpu_baseline,
@@ -486,7 +537,6 @@ def run_ours(args, rank: int, world: int, local: int):
 
 
 def run_extras(bl, wl, torch, device, stream, peaks, items2b, args):
-    from w1_a8_bitlinear_02_b300 import dist as D
     out = {}
     reps = max(3, min(args.steps, 50))
 
@@ -503,40 +553,43 @@ def run_extras(bl, wl, torch, device, stream, peaks, items2b, args):
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) / 1e3 / n
 
+    def line(nb, s, how, **kw):
+        return {"GB/s": nb / s / 1e9, "frac_hbm": nb / s / 1e9 / peaks["hbm_gbs"], "ms_per_sweep": s * 1e3,
+                "us_per_call": s * 1e6 / len(items2b), "how": how, **kw}
+
+    nb = sum(algorithmic_bytes(1, it["mt"].N, it["mt"].K) for it in items2b)
     with torch.cuda.stream(stream):
-        # the same M=1 sweep as independent calls (launch overlap mode 2: no
-        # call waits for the previous one; valid because every call has its own
-        # input and output buffers)
+        # dependent calls, per-call launches (launch overlap mode 1: a kernel
+        # may prefetch its weights, then waits for the previous one)
+        bl.set_launch_overlap(0 if args.no_overlap else 1)
+        g = capture(bl, items2b, stream)
+        out["decode_2b_per_call_dependent"] = line(nb, timed(g.replay, max(3, min(args.steps, 200))),
+                                                   "120 bitlinear_forward launches, each waiting for the "
+                                                   "previous (launch overlap mode 1)")
+        del g
+        # independent per-call launches (mode 2: the GEMV does not wait)
         bl.set_launch_overlap(2)
         g = capture(bl, items2b, stream)
-        s = timed(g.replay, max(3, min(args.steps, 200)))
+        out["decode_2b_per_call_independent"] = line(nb, timed(g.replay, max(3, min(args.steps, 200))),
+                                                     "120 bitlinear_forward launches, launch overlap mode 2")
         bl.set_launch_overlap(0 if args.no_overlap else 1)
-        nb = sum(algorithmic_bytes(1, it["mt"].N, it["mt"].K) for it in items2b)
-        out["decode_2b_independent_calls"] = {
-            "GB/s": nb / s / 1e9, "frac_hbm": nb / s / 1e9 / peaks["hbm_gbs"], "ms_per_sweep": s * 1e3,
-            "how": "same 120 calls, launch overlap mode 2 (calls do not wait for each other)"}
         del g
+        # the chain with every call waiting for all earlier ones (grid barrier)
+        for mode, how in (("barrier", "bitlinear_forward_chain, every call waiting for all earlier calls "
+                                      "at a grid barrier (independent inputs)"),
+                          ("dataflow", "bitlinear_forward_chain, each call's input the previous call's "
+                                       "output (fp32, read from its tagged output words as it lands); "
+                                       "without normalisation between layers the values shrink layer "
+                                       "by layer, the work per call is the same")):
+            calls = chain_calls(items2b, mode)
+            ws = bl.chain_workspace(calls, device)
+            g = capture_chain(bl, calls, ws, stream)
+            s = timed(g.replay, max(3, min(args.steps, 200)))
+            out[f"decode_2b_chain_{mode}"] = line(nb, s, how)
+            del g, ws
 
-        # the same 120 calls as one decode-chain launch (each call waits for the
-        # previous one at a grid barrier instead of a kernel boundary)
-        ws_chain = torch.empty(256, dtype=torch.uint8, device=device)
-        chain = [dict(packed=it["packed"], gamma=it["gamma"], x=it["x"], y=it["y"], N=it["mt"].N,
-                      K=it["mt"].K, wait_prev=1) for it in items2b]
-        gch = torch.cuda.CUDAGraph()
-        bl.bitlinear_forward_chain(chain, ws_chain)
-        stream.synchronize()
-        with torch.cuda.graph(gch, stream=stream):
-            bl.bitlinear_forward_chain(chain, ws_chain)
-        s = timed(gch.replay, max(3, min(args.steps, 200)))
-        out["decode_2b_chain"] = {
-            "GB/s": nb / s / 1e9, "frac_hbm": nb / s / 1e9 / peaks["hbm_gbs"], "ms_per_sweep": s * 1e3,
-            "how": "bitlinear_forward_chain: the 120 calls in one persistent launch, each call "
-                   "waiting for the previous at a grid barrier"}
-        del gch
-
-        # the same chained M=1 sweep with one weight scale per 128 output rows
-        # (grouped packing of the same seeded weights; the forward rescales
-        # each row by its group's scale)
+        # grouped scales: one weight scale per 128 output rows, dependent
+        # per-call launches (the grouped forward has no chain form)
         G = 128
         gits = []
         for it in items2b:
@@ -559,13 +612,11 @@ def run_extras(bl, wl, torch, device, stream, peaks, items2b, args):
             grouped_sweep()
         s = timed(gg.replay, max(3, min(args.steps, 200)))
         nbg = nb + sum(4 * (it["mt"].N // G - 1) for it in items2b)  # the scale vectors
-        out["decode_2b_grouped128"] = {
-            "GB/s": nbg / s / 1e9, "frac_hbm": nbg / s / 1e9 / peaks["hbm_gbs"], "ms_per_sweep": s * 1e3,
-            "how": "bitlinear_forward_grouped, one weight scale per 128 output rows, the same "
-                   "120 chained calls (launch overlap on)"}
+        out["decode_2b_grouped128"] = line(nbg, s, "bitlinear_forward_grouped, one weight scale per 128 "
+                                                   "output rows, 120 dependent per-call launches")
         del gg, gits
 
-        # batched decode on the same weights
+        # batched decode on the same weights (dependent per-call launches)
         mats = [it["mt"] for it in items2b]
         bd = {}
         for M in (8, 16, 32, 64):
@@ -579,9 +630,9 @@ def run_extras(bl, wl, torch, device, stream, peaks, items2b, args):
                 its.append(dict(mt=mt, packed=it["packed"], gamma=it["gamma"], x=x, y=y, ws=ws))
             g = capture(bl, its, stream)
             s = timed(g.replay, reps)
-            nb = sum(algorithmic_bytes(M, m.N, m.K) for m in mats)
+            nbm = sum(algorithmic_bytes(M, m.N, m.K) for m in mats)
             ops = sum(2 * M * m.N * m.K for m in mats)
-            bd[f"M={M}"] = {"GB/s": nb / s / 1e9, "frac_hbm": nb / s / 1e9 / peaks["hbm_gbs"],
+            bd[f"M={M}"] = {"GB/s": nbm / s / 1e9, "frac_hbm": nbm / s / 1e9 / peaks["hbm_gbs"],
                             "TOPS_dense_equiv": ops / s / 1e12, "ms_per_sweep": s * 1e3}
             del g, its
         out["decode_2b_batch"] = bd
@@ -620,18 +671,26 @@ def run_extras(bl, wl, torch, device, stream, peaks, items2b, args):
         out["prefill_2b"] = pf
 
         # 100B-class decode: 80 layers x {28672x8192, 8192x28672}, 9.4 GB
-        # resident; M = 1 chained (launch overlap mode 1) and as independent
-        # calls (mode 2: the GEMV's own streaming rate), M = 8 chained
+        # resident: M = 1 as one chain (independent inputs), as dependent and
+        # as independent per-call launches; M = 8 dependent per-call launches
         if not args.no_100b:
             mats = wl.matrices("decode_100b")
             its = prepare(bl, wl, mats, 1, device, torch.bfloat16)
+            nb1 = sum(algorithmic_bytes(1, it["mt"].N, it["mt"].K) for it in its)
             res = {}
+            calls = chain_calls(its)
+            ws = bl.chain_workspace(calls, device)
+            gch = capture_chain(bl, calls, ws, stream)
+            s = timed(gch.replay, max(3, min(args.steps, 20)))
+            res["M=1 chain"] = {"GB/s": nb1 / s / 1e9, "frac_hbm": nb1 / s / 1e9 / peaks["hbm_gbs"],
+                                "ms_per_sweep": s * 1e3, "us_per_call": s * 1e6 / len(its),
+                                "how": "one bitlinear_forward_chain of the 160 calls (independent inputs)"}
+            del gch, ws
             for M, mode in ((1, 1), (1, 2), (8, 1)):
                 if M == 8:
                     for it in its:
                         mt = it["mt"]
-                        it["x"] = wl.activations(8, mt.K, "normal", mt.seed + 508, device,
-                                                 torch.bfloat16)
+                        it["x"] = wl.activations(8, mt.K, "normal", mt.seed + 508, device, torch.bfloat16)
                         it["y"] = torch.empty((8, mt.N), dtype=torch.float32, device=device)
                         wsn = bl.workspace_bytes(8, mt.N, mt.K)
                         it["ws"] = torch.empty(wsn, dtype=torch.uint8, device=device) if wsn else None
@@ -639,13 +698,13 @@ def run_extras(bl, wl, torch, device, stream, peaks, items2b, args):
                 g = capture(bl, its, stream)
                 s = timed(g.replay, max(3, min(args.steps, 20)))
                 bl.set_launch_overlap(0 if args.no_overlap else 1)
-                nb = sum(algorithmic_bytes(M, it["mt"].N, it["mt"].K) for it in its)
-                res[f"M={M}" + ("" if mode == 1 else " independent")] = {
-                    "GB/s": nb / s / 1e9, "frac_hbm": nb / s / 1e9 / peaks["hbm_gbs"],
+                nbm = sum(algorithmic_bytes(M, it["mt"].N, it["mt"].K) for it in its)
+                res[f"M={M} per-call " + ("dependent" if mode == 1 else "independent")] = {
+                    "GB/s": nbm / s / 1e9, "frac_hbm": nbm / s / 1e9 / peaks["hbm_gbs"],
                     "ms_per_sweep": s * 1e3, "us_per_call": s * 1e6 / len(its),
                     "resident_packed_GB": sum(it["packed"].numel() for it in its) / 1e9,
-                    "how": ("chained calls (launch overlap mode 1)" if mode == 1 else
-                            "independent calls (launch overlap mode 2)")}
+                    "how": ("per-call launches, launch overlap mode 1" if mode == 1 else
+                            "per-call launches, launch overlap mode 2")}
                 del g
             del its
             out["decode_100b"] = res
