@@ -616,7 +616,9 @@ def run_extras(bl, wl, torch, device, stream, peaks, items2b, args):
                                                    "output rows, 120 dependent per-call launches")
         del gg, gits
 
-        # batched decode on the same weights (dependent per-call launches)
+        # batched decode on the same weights: dependent per-call launches,
+        # and (8 and 16 tokens) the chain of independent calls -- 16 tokens as
+        # two 8-token calls per projection, each streaming the weights
         mats = [it["mt"] for it in items2b]
         bd = {}
         for M in (8, 16, 32, 64):
@@ -628,13 +630,32 @@ def run_extras(bl, wl, torch, device, stream, peaks, items2b, args):
                 wsn = bl.workspace_bytes(M, mt.N, mt.K)
                 ws = torch.empty(wsn, dtype=torch.uint8, device=device) if wsn else None
                 its.append(dict(mt=mt, packed=it["packed"], gamma=it["gamma"], x=x, y=y, ws=ws))
-            g = capture(bl, its, stream)
-            s = timed(g.replay, reps)
             nbm = sum(algorithmic_bytes(M, m.N, m.K) for m in mats)
             ops = sum(2 * M * m.N * m.K for m in mats)
+            g = capture(bl, its, stream)
+            s = timed(g.replay, reps)
             bd[f"M={M}"] = {"GB/s": nbm / s / 1e9, "frac_hbm": nbm / s / 1e9 / peaks["hbm_gbs"],
-                            "TOPS_dense_equiv": ops / s / 1e12, "ms_per_sweep": s * 1e3}
-            del g, its
+                            "TOPS_dense_equiv": ops / s / 1e12, "ms_per_sweep": s * 1e3,
+                            "how": "120 dependent bitlinear_forward launches (launch overlap mode 1)"}
+            del g
+            if M <= 16:
+                calls = []
+                for it in its:
+                    mt = it["mt"]
+                    for h in range(0, M, 8):
+                        calls.append(dict(packed=it["packed"], gamma=it["gamma"], x=it["x"][h:h + 8],
+                                          y=it["y"][h:h + 8], N=mt.N, K=mt.K))
+                ws = bl.chain_workspace(calls, device)
+                gch = capture_chain(bl, calls, ws, stream)
+                s = timed(gch.replay, reps)
+                bd[f"M={M} chain"] = {"GB/s": nbm / s / 1e9, "frac_hbm": nbm / s / 1e9 / peaks["hbm_gbs"],
+                                      "TOPS_dense_equiv": ops / s / 1e12, "ms_per_sweep": s * 1e3,
+                                      "how": ("one bitlinear_forward_chain of the 120 calls of 8 tokens "
+                                              "(independent inputs)") if M == 8 else
+                                             ("one bitlinear_forward_chain of 240 calls of 8 tokens, two per "
+                                              "projection (the weights stream twice; the bytes count them once)")}
+                del gch, ws, calls
+            del its
         out["decode_2b_batch"] = bd
 
         # prefill M = 2048 on the tensor-core path (forward = activation
@@ -686,6 +707,18 @@ def run_extras(bl, wl, torch, device, stream, peaks, items2b, args):
                                 "ms_per_sweep": s * 1e3, "us_per_call": s * 1e6 / len(its),
                                 "how": "one bitlinear_forward_chain of the 160 calls (independent inputs)"}
             del gch, ws
+            x8 = [wl.activations(8, it["mt"].K, "normal", it["mt"].seed + 508, device, torch.bfloat16) for it in its]
+            y8 = [torch.empty((8, it["mt"].N), dtype=torch.float32, device=device) for it in its]
+            calls = [dict(packed=it["packed"], gamma=it["gamma"], x=x, y=y, N=it["mt"].N, K=it["mt"].K)
+                     for it, x, y in zip(its, x8, y8)]
+            ws = bl.chain_workspace(calls, device)
+            gch = capture_chain(bl, calls, ws, stream)
+            s = timed(gch.replay, max(3, min(args.steps, 20)))
+            nb8 = sum(algorithmic_bytes(8, it["mt"].N, it["mt"].K) for it in its)
+            res["M=8 chain"] = {"GB/s": nb8 / s / 1e9, "frac_hbm": nb8 / s / 1e9 / peaks["hbm_gbs"],
+                                "ms_per_sweep": s * 1e3, "us_per_call": s * 1e6 / len(its),
+                                "how": "one bitlinear_forward_chain of the 160 calls of 8 tokens (independent inputs)"}
+            del gch, ws, calls, x8, y8
             for M, mode in ((1, 1), (1, 2), (8, 1)):
                 if M == 8:
                     for it in its:

@@ -295,12 +295,17 @@ BL_API bl_status bitlinear_forward_noalloc(const uint8_t *packed, const float *g
                                            int64_t N, int64_t K, const void *x, int dtype,
                                            int64_t M, float *y, void *stream);
 
-/* One call of a decode chain (bitlinear_forward_chain), M = 1.
+/* One call of a decode chain (bitlinear_forward_chain).
  *   packed, gamma  as bitlinear_forward (device).
- *   x              [K] of x_dtype, device; may lie inside an earlier call's y.
- *   y              [N] float out, device, 4-byte aligned; must not overlap
+ *   x              [M, K] of x_dtype, device; with M = 1 it may lie inside an
+ *                  earlier call's y.
+ *   y              [M, N] float out, device, 4-byte aligned; must not overlap
  *                  this call's x, packed or gamma.
  *   N, K           sizes; N <= 2^30, K <= 32768.
+ *   M              tokens, 1..8 (0 counts as 1).  A call of more than one
+ *                  token must read an x that no earlier call of the chain
+ *                  writes (its input is quantised before the chain starts);
+ *                  its y is not passed on by output words.
  *   x_dtype        BL_F32 or BL_BF16.
  *   act            BL_ACT_NONE, or BL_ACT_RELU2 for relu2(x) (as
  *                  bitlinear_forward_relu2).
@@ -317,6 +322,7 @@ typedef struct bl_chain_call {
   int x_dtype;
   int act;
   int wait_prev;
+  int M;
 } bl_chain_call;
 
 /* Workspace (device bytes) that bitlinear_forward_chain needs for these
@@ -350,8 +356,9 @@ BL_API bl_status bitlinear_chain_workspace_bytes(const bl_chain_call *calls, int
  *            number in the control words makes each launch's tags new).
  *            Chains that share ws must be ordered.  If bitlinear_device_error
  *            reports a failure, zero ws again before reusing it.
- * Errors: BL_ERR_NULL, BL_ERR_SHAPE (n, N, K or act out of range, or a call
- * whose output overlaps its own inputs), BL_ERR_DTYPE, BL_ERR_ALIGN,
+ * Errors: BL_ERR_NULL, BL_ERR_SHAPE (n, N, K, M or act out of range, a call
+ * whose output overlaps its own inputs, or a call of more than one token
+ * whose x an earlier call writes), BL_ERR_DTYPE, BL_ERR_ALIGN,
  * BL_ERR_WORKSPACE, BL_ERR_UNSUPPORTED, BL_ERR_CUDA (including a launch the
  * device cannot fit on all its SMs).
  * [The layer structure: 0.4GB page, section 2 (ReLU^2 FFN, no bias);

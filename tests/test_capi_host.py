@@ -187,10 +187,10 @@ def test_chain_invalid_arguments_return_status(lib):
 
     def chain(**kw):
         d = dict(packed=fake, gamma=fake, x=fake, y=fake, N=64, K=64, x_dtype=capi.BL_BF16,
-                 act=capi.BL_ACT_NONE, wait_prev=1)
+                 act=capi.BL_ACT_NONE, wait_prev=1, M=1)
         d.update(kw)
         arr = (capi.ChainCall * 1)(capi.ChainCall(d["packed"], d["gamma"], d["x"], d["y"], d["N"],
-                                                  d["K"], d["x_dtype"], d["act"], d["wait_prev"]))
+                                                  d["K"], d["x_dtype"], d["act"], d["wait_prev"], d["M"]))
         return ctypes.cast(arr, ctypes.c_void_p), arr
 
     p, keep = chain(y=0x900000)
@@ -203,7 +203,8 @@ def test_chain_invalid_arguments_return_status(lib):
     for kw, want in ((dict(y=0), capi.BL_ERR_NULL), (dict(K=32769), capi.BL_ERR_SHAPE),
                      (dict(N=0), capi.BL_ERR_SHAPE), (dict(x_dtype=7), capi.BL_ERR_DTYPE),
                      (dict(act=5), capi.BL_ERR_SHAPE), (dict(packed=odd), capi.BL_ERR_ALIGN),
-                     (dict(y=fake + 64), capi.BL_ERR_SHAPE)):  # y over its own x
+                     (dict(y=fake + 64), capi.BL_ERR_SHAPE),  # y over its own x
+                     (dict(M=9), capi.BL_ERR_SHAPE)):
         kw.setdefault("y", 0x900000)
         p2, keep2 = chain(**kw)
         assert lib.bitlinear_forward_chain(p2, 1, ws, 256, None) == want, kw

@@ -374,6 +374,35 @@ def test_chain_subrange_inputs_and_long_rows(bl):
             assert_bits_equal(y.cpu().numpy(), outs[i], f"launch {launch} call {i}")
 
 
+def test_chain_many_tokens(bl):
+    """Calls of 2 to 8 tokens (independent inputs, quantised ahead; half-slab
+    stages) mixed with single-token calls, ragged N and K, bf16 and fp32
+    inputs, a squared-ReLU input, and every ~2B projection at 8 tokens; the
+    chain runs twice on one workspace and each output equals the oracle's."""
+    specs = [(300, 1000, 2, torch.bfloat16, 0), (3840, 2560, 8, torch.bfloat16, 0), (2560, 2560, 8, torch.bfloat16, 0),
+             (6912, 2560, 8, torch.bfloat16, 0), (2560, 6912, 8, torch.bfloat16, 1), (513, 100, 3, torch.float32, 0),
+             (700, 2000, 1, torch.bfloat16, 0), (129, 4608, 5, torch.float32, 1), (1000, 64, 7, torch.bfloat16, 0)]
+    mats = [pack_both(bl, N, K, 0.02, 950 + i) for i, (N, K, _, _, _) in enumerate(specs)]
+    calls, xs, ys = [], [], []
+    for i, ((N, K, M, dt, act), (packed, gamma, _, _)) in enumerate(zip(specs, mats)):
+        x = wl.activations(M, K, "outliers1pct", 960 + i, "cpu", dt)
+        y = torch.full((M, N), float("nan"), dtype=torch.float32, device=DEV)
+        calls.append(dict(packed=packed, gamma=gamma, x=x.to(DEV), y=y, N=N, K=K, act=act))
+        xs.append(x)
+        ys.append(y)
+    ws = bl.chain_workspace(calls, DEV)
+    for launch in range(2):
+        for y in ys:
+            y.fill_(float("nan"))
+        bl.bitlinear_forward_chain(calls, ws)
+        torch.cuda.synchronize()
+        assert bl.device_error() == 0
+        for i, ((N, K, M, dt, act), (_, _, p_ref, g_ref)) in enumerate(zip(specs, mats)):
+            f = oracle.forward_packed_relu2 if act else oracle.forward_packed
+            assert_bits_equal(ys[i].cpu().numpy(), f(p_ref, g_ref, N, K, xs[i].float().numpy()),
+                              f"launch {launch} call {i} M={M} N={N} K={K}")
+
+
 def test_chain_write_after_read_and_write_after_write(bl):
     """Outputs that overwrite an earlier call's input buffer or output buffer:
     the library puts a grid barrier before such calls, so the results are those

@@ -317,7 +317,8 @@ def _chain_array(calls):
         _need_cuda("y", c["y"], torch.float32)
         arr[i] = capi.ChainCall(c["packed"].data_ptr(), c["gamma"].data_ptr(), c["x"].data_ptr(),
                                 c["y"].data_ptr(), int(c["N"]), int(c["K"]), _DTYPES[c["x"].dtype],
-                                int(c.get("act", capi.BL_ACT_NONE)), int(c.get("wait_prev", 0)))
+                                int(c.get("act", capi.BL_ACT_NONE)), int(c.get("wait_prev", 0)),
+                                int(c.get("M", c["x"].shape[0] if c["x"].dim() == 2 else 1)))
     return calls, arr
 
 
@@ -338,8 +339,8 @@ def chain_workspace(calls, device) -> torch.Tensor:
 def bitlinear_forward_chain(calls, workspace: torch.Tensor | None = None) -> None:
     """A decode chain of single-token forwards in one launch.
 
-    calls: sequence of dicts with packed, gamma, x [1, K] (fp32 / bf16), y [1, N]
-    fp32 (written), N, K and optionally act (capi.BL_ACT_RELU2 for relu2(x))
+    calls: sequence of dicts with packed, gamma, x [M, K] (fp32 / bf16, M <= 8),
+    y [M, N] fp32 (written), N, K and optionally act (capi.BL_ACT_RELU2 for relu2(x))
     and wait_prev (default 0: the library orders dependent calls itself).
     workspace: from chain_workspace (zero-filled before its first use; reuse it
     across launches); allocated when None."""

@@ -33,7 +33,8 @@ class ChainCall(ctypes.Structure):
     """bl_chain_call (include/bitlinear.h)."""
     _fields_ = [("packed", ctypes.c_void_p), ("gamma", ctypes.c_void_p), ("x", ctypes.c_void_p),
                 ("y", ctypes.c_void_p), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
-                ("x_dtype", ctypes.c_int), ("act", ctypes.c_int), ("wait_prev", ctypes.c_int)]
+                ("x_dtype", ctypes.c_int), ("act", ctypes.c_int), ("wait_prev", ctypes.c_int),
+                ("M", ctypes.c_int)]
 
 
 # name -> (restype, argtypes)

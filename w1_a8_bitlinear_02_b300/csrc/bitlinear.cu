@@ -823,6 +823,8 @@ bool make_map_rows(CUtensorMap *m, const void *ptr, int64_t N, int64_t rb, int b
 //     wait_prev: a grid barrier before the call.
 // A call's output may not overlap its own inputs.  p, t and q may be null
 // (size only).
+static int toks(const bl_chain_call &c) { return c.M < 1 ? 1 : c.M; }
+
 static bl_status chain_plan(const bl_chain_call *calls, int n, int grid, chain::Params *p, chain::TableCopy *t,
                             chain::QuantParams *q, size_t *ws_need, void *ws) {
   if (calls == nullptr) return BL_ERR_NULL;
@@ -838,10 +840,12 @@ static bl_status chain_plan(const bl_chain_call *calls, int n, int grid, chain::
     if (c.x_dtype != BL_F32 && c.x_dtype != BL_BF16) return BL_ERR_DTYPE;
     if (c.N < 1 || c.N > chain::kMaxN || c.K < 1 || c.K > chain::kMaxK) return BL_ERR_SHAPE;
     if (c.act != BL_ACT_NONE && c.act != BL_ACT_RELU2) return BL_ERR_SHAPE;
+    if (c.M < 0 || c.M > chain::kMaxTok) return BL_ERR_SHAPE;
     if (!aligned(c.packed, 16) || !aligned(c.gamma, 4) || !aligned(c.y, 4)) return BL_ERR_ALIGN;
     const uintptr_t es = c.x_dtype == BL_BF16 ? 2 : 4;
-    xr[i] = {reinterpret_cast<uintptr_t>(c.x), reinterpret_cast<uintptr_t>(c.x) + static_cast<uintptr_t>(c.K) * es};
-    yr[i] = {reinterpret_cast<uintptr_t>(c.y), reinterpret_cast<uintptr_t>(c.y) + static_cast<uintptr_t>(c.N) * 4};
+    const uintptr_t m = static_cast<uintptr_t>(toks(c));
+    xr[i] = {reinterpret_cast<uintptr_t>(c.x), reinterpret_cast<uintptr_t>(c.x) + m * static_cast<uintptr_t>(c.K) * es};
+    yr[i] = {reinterpret_cast<uintptr_t>(c.y), reinterpret_cast<uintptr_t>(c.y) + m * static_cast<uintptr_t>(c.N) * 4};
     pr[i] = {reinterpret_cast<uintptr_t>(c.packed),
              reinterpret_cast<uintptr_t>(c.packed) + static_cast<uintptr_t>(c.N * plan::row_bytes(c.K))};
     gr[i] = {reinterpret_cast<uintptr_t>(c.gamma), reinterpret_cast<uintptr_t>(c.gamma) + 4};
@@ -858,8 +862,8 @@ static bl_status chain_plan(const bl_chain_call *calls, int n, int grid, chain::
         break;
       }
     if (j >= 0) {
-      if (calls[c].x_dtype == BL_F32 && xr[c].lo >= yr[j].lo && xr[c].hi <= yr[j].hi &&
-          (xr[c].lo - yr[j].lo) % 4 == 0) {
+      if (calls[c].x_dtype == BL_F32 && toks(calls[c]) == 1 && toks(calls[j]) == 1 && xr[c].lo >= yr[j].lo &&
+          xr[c].hi <= yr[j].hi && (xr[c].lo - yr[j].lo) % 4 == 0) {
         src[c] = j;
         produces[j] = 1;
       } else {
@@ -873,13 +877,15 @@ static bl_status chain_plan(const bl_chain_call *calls, int n, int grid, chain::
     }
     barrier[c] = bar ? 1 : 0;
     early[c] = (j < 0 && !bar) ? 1 : 0;  // no earlier call writes x: quantised before the chain
+    if (toks(calls[c]) > 1 && !early[c]) return BL_ERR_SHAPE;  // many tokens: only a quantised-ahead input
   }
   size_t off = plan::align256(chain::kTableOffset + static_cast<size_t>(n) * sizeof(chain::Call));
   std::vector<size_t> rec_off(n, 0), mb_off(n, 0);
   for (int i = 0; i < n; ++i)
     if (early[i]) {
       rec_off[i] = off;
-      off = plan::align256(off + static_cast<size_t>(chain::record_bytes(static_cast<int>(plan::row_bytes(calls[i].K)))));
+      off = plan::align256(off + static_cast<size_t>(chain::record_bytes(static_cast<int>(plan::row_bytes(calls[i].K)),
+                                                                         toks(calls[i]))));
     }
   for (int i = 0; i < n; ++i)
     if (produces[i]) {
@@ -914,7 +920,7 @@ static bl_status chain_plan(const bl_chain_call *calls, int n, int grid, chain::
     const int flags = (c.x_dtype == BL_BF16 ? chain::kFlagBf16 : 0) | (c.act == BL_ACT_RELU2 ? chain::kFlagRelu2 : 0);
     d.flags = flags | (barrier[i] ? chain::kFlagBarrier : 0);
     d.src = src[i];
-    d.pad_ = 0;
+    d.M = toks(c);
     d.rec = early[i] ? wsb + rec_off[i] : nullptr;
     d.mb_out = produces[i] ? reinterpret_cast<uint64_t *>(wsb + mb_off[i]) : nullptr;
     d.mb_in = nullptr;
@@ -926,7 +932,7 @@ static bl_status chain_plan(const bl_chain_call *calls, int n, int grid, chain::
       jb.K = static_cast<int>(c.K);
       jb.rb = static_cast<int>(rb);
       jb.flags = flags;
-      jb.pad_ = 0;
+      jb.M = toks(c);
     }
   }
   for (int i = 0; i < n; ++i)
@@ -964,7 +970,10 @@ bl_status bitlinear_forward_chain(const bl_chain_call *calls, int n, void *ws, s
   std::lock_guard<std::mutex> lk(p_mu);
   s = chain_plan(calls, n, sms, &p, &tc, &qp, &need, ws);
   if (s != BL_OK) return s;
-  s = ensure_smem(dev, reinterpret_cast<const void *>(&chain::chain_kernel), chain::kSmemBytes);
+  bool many = false;
+  for (int i = 0; i < n; ++i) many = many || toks(calls[i]) > 1;
+  void (*kern)(chain::Params) = many ? &chain::chain_kernel<true> : &chain::chain_kernel<false>;
+  s = ensure_smem(dev, reinterpret_cast<const void *>(kern), chain::kSmemBytes);
   if (s != BL_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // the call table into the workspace (its parameters are kept by value)
@@ -972,8 +981,10 @@ bl_status bitlinear_forward_chain(const bl_chain_call *calls, int n, void *ws, s
   if (s != BL_OK) return s;
   // the inputs no earlier call writes, quantised into their records
   if (qp.n > 0) {
-    s = launch(&chain::chain_quant_kernel, dim3(static_cast<unsigned>(qp.n)), dim3(chain::kQThreads), 0, st, false,
-               qp);
+    int mt = 1;
+    for (int i = 0; i < qp.n; ++i) mt = qp.j[i].M > mt ? qp.j[i].M : mt;
+    s = launch(&chain::chain_quant_kernel, dim3(static_cast<unsigned>(qp.n), static_cast<unsigned>(mt)),
+               dim3(chain::kQThreads), 0, st, false, qp);
     if (s != BL_OK) return s;
   }
   // every block may wait for the others: all must be resident (one per SM)
@@ -987,7 +998,7 @@ bl_status bitlinear_forward_chain(const bl_chain_call *calls, int n, void *ws, s
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, &chain::chain_kernel, p) != cudaSuccess) return launch_failed("chain launch");
+  if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) return launch_failed("chain launch");
   return BL_OK;
 }
 bl_status bitlinear_forward_noalloc(const uint8_t *packed, const float *gamma, int64_t N, int64_t K,

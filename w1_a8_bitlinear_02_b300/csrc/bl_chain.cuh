@@ -107,8 +107,20 @@ constexpr int kFlagBf16 = 1;      // x is bf16 (else fp32)
 constexpr int kFlagRelu2 = 2;     // quantise relu2(x)
 constexpr int kFlagBarrier = 4;   // every block finishes all earlier calls first
 
-__host__ __device__ constexpr int slabs_of(int rb) { return (rb + kSlabBytes - 1) / kSlabBytes; }
-__host__ __device__ constexpr int record_bytes(int rb) { return kHeader + slabs_of(rb) * kSlabCodes; }
+// Calls of more than one token (up to kMaxTok) use half slabs (512 bytes of
+// each row, 2048 weights), so a stage holds the weights (16 KB) and every
+// token's codes for them (M x 2 KB); their record header holds c[m] (fp32)
+// at 4m and the 16 warps' code sums of token m at 64 + 64m.
+constexpr int kMaxTok = 8;
+__host__ __device__ constexpr int slab_bytes(int M) { return M > 1 ? kSlabBytes / 2 : kSlabBytes; }
+__host__ __device__ constexpr int slabs_of(int rb, int M = 1) { return (rb + slab_bytes(M) - 1) / slab_bytes(M); }
+__host__ __device__ constexpr int header_bytes(int M) { return M > 1 ? ((64 + 64 * M + 127) / 128) * 128 : kHeader; }
+// a record: the header, then slab by slab each token's codes (4 per weight byte)
+__host__ __device__ constexpr int record_bytes(int rb, int M = 1) {
+  return header_bytes(M) + slabs_of(rb, M) * M * 4 * slab_bytes(M);
+}
+static_assert(kSlabBoxes / 2 * kBoxSize + header_bytes(kMaxTok) + kMaxTok * 4 * (kSlabBytes / 2) <=
+                  kStageBytes, "a stage of a many-token call");
 
 struct Call {
   const float *gamma;
@@ -123,7 +135,7 @@ struct Call {
   int gh;                 // rows per group (<= 32; the tensor map's box height)
   int flags;
   int src;                // the call that wrote mb_in
-  int pad_;
+  int M;                  // tokens (x [M, K], y [M, N]); more than one only with a record
 };
 static_assert(sizeof(Call) % 4 == 0, "call table copied in words");
 
@@ -143,6 +155,7 @@ struct Smem {
   uint64_t empty[kStages];
   float fred[kCW];
   int32_t part[2][kCW][kGroupRows];  // a group's partial sums, by group parity
+  int32_t msum[2][kMaxTok][kGroupRows];  // the same, many-token calls (added into)
   uint32_t seq_tag;
   int abort_flag;
   Call calls[kMaxCalls];  // the call table, copied in once
@@ -165,14 +178,15 @@ __global__ void copy_table_kernel(const __grid_constant__ TableCopy t) {
   for (int i = threadIdx.x; i < words; i += blockDim.x) dst[i] = src[i];
 }
 
-// One input quantised ahead: x [K] (f32 or bf16, relu2 first if flagged) ->
-// record (c = gamma / s, the 16 warps' code sums, codes zero-padded to the
-// last slab).
+// One input quantised ahead: token m of x [M, K] (f32 or bf16, relu2 first
+// if flagged) -> its part of the record (c[m] = gamma / s_m, the 16 warps'
+// code sums, codes zero-padded to the last slab).  One block per (call,
+// token).
 struct QuantJob {
   const void *x;
   const float *gamma;
   uint8_t *rec;
-  int K, rb, flags, pad_;
+  int K, rb, flags, M;
 };
 struct QuantParams {
   int n;
@@ -184,23 +198,26 @@ __global__ void __launch_bounds__(kQThreads) chain_quant_kernel(const __grid_con
   __shared__ float red[kQThreads / 32];
   __shared__ int xsum[kCW];
   const QuantJob &jb = q.j[blockIdx.x];
+  const int m = blockIdx.y;
+  if (m >= jb.M) return;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const bool bf = (jb.flags & kFlagBf16) != 0, r2 = (jb.flags & kFlagRelu2) != 0;
-  const int K = jb.K, kend = slabs_of(jb.rb) * kSlabCodes;
+  const int K = jb.K, M = jb.M, SB4 = 4 * slab_bytes(M), nsl = slabs_of(jb.rb, M), kend = nsl * SB4;
+  const void *xr = bf ? static_cast<const void *>(static_cast<const __nv_bfloat16 *>(jb.x) + static_cast<int64_t>(m) * K)
+                      : static_cast<const void *>(static_cast<const float *>(jb.x) + static_cast<int64_t>(m) * K);
   auto ld = [&](int k) -> float {
-    const float v = bf ? __bfloat162float(static_cast<const __nv_bfloat16 *>(jb.x)[k])
-                       : static_cast<const float *>(jb.x)[k];
+    const float v = bf ? __bfloat162float(static_cast<const __nv_bfloat16 *>(xr)[k]) : static_cast<const float *>(xr)[k];
     return r2 ? relu2f(v) : v;
   };
-  const bool vec = (K % 8) == 0 && al16(jb.x);
+  const bool vec = (K % 8) == 0 && al16(xr);
   const int nv = vec ? K / 8 : 0;
   float a = 0.0f;
   for (int v = t; v < nv; v += kQThreads) {
     float f[8];
     if (bf)
-      load8(static_cast<const __nv_bfloat16 *>(jb.x) + 8 * v, f);
+      load8(static_cast<const __nv_bfloat16 *>(xr) + 8 * v, f);
     else
-      load8(static_cast<const float *>(jb.x) + 8 * v, f);
+      load8(static_cast<const float *>(xr) + 8 * v, f);
 #pragma unroll
     for (int e = 0; e < 8; ++e) a = fmaxf(a, fabsf(r2 ? relu2f(f[e]) : f[e]));
   }
@@ -216,9 +233,9 @@ __global__ void __launch_bounds__(kQThreads) chain_quant_kernel(const __grid_con
   for (int v = t; v < nv; v += kQThreads) {
     float f[8];
     if (bf)
-      load8(static_cast<const __nv_bfloat16 *>(jb.x) + 8 * v, f);
+      load8(static_cast<const __nv_bfloat16 *>(xr) + 8 * v, f);
     else
-      load8(static_cast<const float *>(jb.x) + 8 * v, f);
+      load8(static_cast<const float *>(xr) + 8 * v, f);
     uint32_t lo = 0, hi = 0;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -230,10 +247,15 @@ __global__ void __launch_bounds__(kQThreads) chain_quant_kernel(const __grid_con
   for (int k = 8 * nv + t; k < kend; k += kQThreads)
     codes[k] = k < K ? static_cast<uint8_t>(quant_one(ld(k), s) & 0xFF) : 0u;
   __syncthreads();
-  // the codes out, and each 64-code piece's sum into its warp's total (piece
-  // p is read by consumer warp p mod 16)
-  uint4 *dst = reinterpret_cast<uint4 *>(jb.rec + kHeader);
-  for (int i = t; i < kend / 16; i += kQThreads) dst[i] = *reinterpret_cast<const uint4 *>(codes + 16 * i);
+  // the codes out, slab by slab after the header (token m's share of each
+  // slab), and each 64-code piece's sum into its warp's total (piece p is
+  // read by consumer warp p mod 16)
+  const int H = header_bytes(M);
+  for (int i = t; i < kend / 16; i += kQThreads) {
+    const int sl = (16 * i) / SB4, off = (16 * i) % SB4;
+    *reinterpret_cast<uint4 *>(jb.rec + H + (static_cast<size_t>(sl) * M + m) * SB4 + off) =
+        *reinterpret_cast<const uint4 *>(codes + 16 * i);
+  }
   for (int pc = t; pc < kend / 64; pc += kQThreads) {
     int sm = 0;
 #pragma unroll
@@ -247,8 +269,8 @@ __global__ void __launch_bounds__(kQThreads) chain_quant_kernel(const __grid_con
     atomicAdd(&xsum[pc % kCW], sm);
   }
   __syncthreads();
-  if (t < kCW) reinterpret_cast<int *>(jb.rec + 64)[t] = xsum[t];
-  if (t == 0) *reinterpret_cast<float *>(jb.rec) = __fdiv_rn(__ldg(jb.gamma), s);
+  if (t < kCW) reinterpret_cast<int *>(jb.rec + 64 + 64 * m)[t] = xsum[t];
+  if (t == 0) reinterpret_cast<float *>(jb.rec)[m] = __fdiv_rn(__ldg(jb.gamma), s);
 }
 
 // ------------------------------------------------------------ helpers
@@ -288,9 +310,10 @@ __device__ __forceinline__ void block_rows(const Call &c, int &r0, int &rows) {
   if (rows < 0) rows = 0;
 }
 // 128-byte boxes of slab s (the last slab of a row may be shorter)
-__device__ __forceinline__ int boxes_of(int rb, int s) {
-  int len = rb - s * kSlabBytes;
-  if (len > kSlabBytes) len = kSlabBytes;
+__device__ __forceinline__ int boxes_of(int rb, int s, int M = 1) {
+  const int sb = slab_bytes(M);
+  int len = rb - s * sb;
+  if (len > sb) len = sb;
   return (len + kBoxBytes - 1) / kBoxBytes;
 }
 
@@ -502,6 +525,41 @@ __device__ __forceinline__ bool quantise_in_block(const Call &c, uint32_t slot, 
   return true;
 }
 
+// One 16-byte piece against MT tokens' activation codes (token m's 64 codes
+// at act + m * tstride, broadcast): the codes are shifted down once per word
+// and shared by the tokens; acc[m] += sum c * x.
+template <int MT>
+__device__ __forceinline__ void piece_multi(uint32_t waddr, uint32_t act, uint32_t tstride, int (&acc)[kMaxTok]) {
+  const uint4 w = lds_u128(waddr);
+  const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
+  uint32_t cw[16];
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) cw[4 * j + i] = (wd[j] >> (2 * i)) & 0x03030303u;
+#pragma unroll
+  for (int m = 0; m < MT; ++m) {
+    const uint32_t at = act + m * tstride;
+    const uint4 x0 = lds_u128(at), x1 = lds_u128(at + 16), x2 = lds_u128(at + 32), x3 = lds_u128(at + 48);
+    const uint32_t xv[16] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w,
+                             x2.x, x2.y, x2.z, x2.w, x3.x, x3.y, x3.z, x3.w};
+#pragma unroll
+    for (int t = 0; t < 16; ++t) acc[m] = dp4a_us(cw[t], xv[t], acc[m]);
+  }
+}
+
+// The pieces of one stage of a many-token call (this warp's: warp, warp + 16).
+template <int MT>
+__device__ __forceinline__ void stage_multi(uint32_t sbase, uint32_t abase, uint32_t tstride, int npc, int warp,
+                                            uint32_t lsw, int (&acc)[kMaxTok]) {
+  for (int pc = warp; pc < npc; pc += kCW)
+    piece_multi<MT>(sbase + static_cast<uint32_t>((pc >> 3) * kBoxSize) + ((static_cast<uint32_t>(pc & 7) ^ lsw) << 4),
+                    abase + 64u * pc, tstride, acc);
+}
+
+// MANY: the chain has calls of more than one token (a separate instantiation,
+// so single-token chains keep their register budget).
+template <bool MANY>
 __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constant__ Params p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -525,6 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
     uint32_t *dst = reinterpret_cast<uint32_t *>(sm.calls);
     const int words = p.n * static_cast<int>(sizeof(Call) / 4);
     for (int w = tid; w < words; w += kThreads) dst[w] = src[w];
+    for (int i = tid; i < 2 * kMaxTok * kGroupRows; i += kThreads) (&sm.msum[0][0][0])[i] = 0;
   }
   __syncthreads();
   volatile int *abort_flag = &sm.abort_flag;
@@ -541,12 +600,16 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
         // the call's fields in registers (the asm statements below clobber
         // memory, which would make every use a shared-memory reload)
         const int N = sm.calls[ci].N, rb = sm.calls[ci].rb, rpc = sm.calls[ci].rpc, gh = sm.calls[ci].gh;
+        const int M = sm.calls[ci].M;
         const uint8_t *rec = sm.calls[ci].rec;
+        const int SB = slab_bytes(M), H = header_bytes(M);
+        const uint32_t cbytes = static_cast<uint32_t>(M * 4 * SB);  // every token's codes of one slab
+        const uint32_t cofs = static_cast<uint32_t>(SB / kBoxBytes) * kBoxSize;  // codes after the boxes
         const int r0 = static_cast<int>(blockIdx.x) * rpc;
         const int rows = N - r0 < rpc ? (N - r0 > 0 ? N - r0 : 0) : rpc;
         if (rows == 0) continue;
         const CUtensorMap *map = &p.maps[ci];
-        const int nslab = slabs_of(rb);
+        const int nslab = slabs_of(rb, M);
         // groups of gh rows (the last block's last group may run past N,
         // where the box reads zeros)
         const uint32_t box = static_cast<uint32_t>(gh) * kBoxBytes;
@@ -558,19 +621,19 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
               go = false;
               break;
             }
-            const int nb = boxes_of(rb, s);
+            const int nb = boxes_of(rb, s, M);
             const uint32_t fb = smem_u32(&sm.full[st]);
             const uint32_t sb = ring + st * kStageBytes;
             uint32_t tx = static_cast<uint32_t>(nb) * box;
-            if (rec != nullptr) tx += kSlabCodes + (s == 0 ? kHeader : 0);
+            if (rec != nullptr) tx += cbytes + (s == 0 ? H : 0);
             mbar_arrive_expect_tx(fb, tx);
             for (int b = 0; b < nb; ++b)
-              tma_load_2d(sb + b * kBoxSize, map, s * kSlabBytes + b * kBoxBytes, r0 + g, fb, pol);
+              tma_load_2d(sb + b * kBoxSize, map, s * SB + b * kBoxBytes, r0 + g, fb, pol);
             if (rec != nullptr) {
               if (s == 0)
-                bulk_g2s(sb + kStageW, rec, kHeader + kSlabCodes, fb, pol_rec);
+                bulk_g2s(sb + cofs, rec, H + cbytes, fb, pol_rec);
               else
-                bulk_g2s(sb + kStageW + kHeader, rec + kHeader + s * kSlabCodes, kSlabCodes, fb, pol_rec);
+                bulk_g2s(sb + cofs + H, rec + H + s * cbytes, cbytes, fb, pol_rec);
             }
             issued = i + 1;
           }
@@ -622,9 +685,80 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
       if (rows == 0) continue;
       // the call's fields in registers (asm statements below clobber memory)
       const bool has_rec = c.rec != nullptr;
-      const int rb = c.rb, gh = c.gh;
+      const int rb = c.rb, gh = c.gh, M = c.M, N = c.N;
       float *const yout = c.y;
       uint64_t *const mbo = c.mb_out;
+      const uint32_t lrow = static_cast<uint32_t>(lane) * kBoxBytes;
+      const uint32_t lsw = static_cast<uint32_t>(lane & 7);
+
+      if (MANY && M > 1) {
+        // ---- many tokens (their codes come with the record in every stage)
+        const int SB = slab_bytes(M), H = header_bytes(M), nslab = slabs_of(rb, M);
+        const uint32_t cofs = static_cast<uint32_t>(SB / kBoxBytes) * kBoxSize;
+        const uint32_t tstride = static_cast<uint32_t>(4 * SB);
+        float cmv[kMaxTok];  // the tokens' output scales (used by the writing warp)
+        int xwv[kMaxTok];
+#pragma unroll
+        for (int m = 0; m < kMaxTok; ++m) {
+          cmv[m] = 0.0f;
+          xwv[m] = 0;
+        }
+        for (int g = 0; g < rows; g += gh) {
+          int acc[kMaxTok];
+#pragma unroll
+          for (int m = 0; m < kMaxTok; ++m) acc[m] = 0;
+          for (int s = 0; s < nslab; ++s, ++it) {
+            const int st = it % kStages;
+            if (*abort_flag || !mbar_wait(smem_u32(&sm.full[st]), (it / kStages) & 1)) {
+              *abort_flag = 1;
+              break;
+            }
+            const int npc = boxes_of(rb, s, M) * 8;
+            const uint32_t sb = ring + st * kStageBytes;
+            if (g == 0 && s == 0) {
+#pragma unroll
+              for (int m = 0; m < kMaxTok; ++m)
+                if (m < M) {
+                  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(cmv[m]) : "r"(sb + cofs + 4u * m) : "memory");
+                  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(xwv[m]) : "r"(sb + cofs + 64u + 64u * m + 4u * warp)
+                               : "memory");
+                }
+            }
+            const uint32_t sbase = sb + lrow, abase = sb + cofs + static_cast<uint32_t>(H);
+            switch (M) {
+              case 2: stage_multi<2>(sbase, abase, tstride, npc, warp, lsw, acc); break;
+              case 3: stage_multi<3>(sbase, abase, tstride, npc, warp, lsw, acc); break;
+              case 4: stage_multi<4>(sbase, abase, tstride, npc, warp, lsw, acc); break;
+              case 5: stage_multi<5>(sbase, abase, tstride, npc, warp, lsw, acc); break;
+              case 6: stage_multi<6>(sbase, abase, tstride, npc, warp, lsw, acc); break;
+              case 7: stage_multi<7>(sbase, abase, tstride, npc, warp, lsw, acc); break;
+              default: stage_multi<8>(sbase, abase, tstride, npc, warp, lsw, acc); break;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&sm.empty[st]));
+          }
+          // the 16 warps' sums meet by shared-memory adds into this group's
+          // buffer; one warp writes the rows and clears it for two groups on
+          const int pb = ng & 1;
+#pragma unroll
+          for (int m = 0; m < kMaxTok; ++m)
+            if (m < M) atomicAdd(&sm.msum[pb][m][lane], acc[m] - xwv[m]);
+          named_bar(2, kC);
+          if (warp == (ng % kCW)) {
+            const int h = rows - g < gh ? rows - g : gh;
+#pragma unroll
+            for (int m = 0; m < kMaxTok; ++m)
+              if (m < M) {
+                const int t = sm.msum[pb][m][lane];
+                sm.msum[pb][m][lane] = 0;
+                if (lane < h)
+                  yout[static_cast<int64_t>(m) * N + r0 + g + lane] = __fmul_rn(static_cast<float>(t), cmv[m]);
+              }
+          }
+          ++ng;
+        }
+        continue;
+      }
 
       // ---- the activation codes, c and the warp's code sum: from the
       // record (in the call's first stage) or quantised here
@@ -642,8 +776,6 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
       }
       const int nslab = slabs_of(rb);
       const uint32_t tag = seq_tag | static_cast<uint32_t>(ci + 1);
-      const uint32_t lrow = static_cast<uint32_t>(lane) * kBoxBytes;
-      const uint32_t lsw = static_cast<uint32_t>(lane & 7);
 
       // ---- row groups: one lane per row, the slabs' pieces split over warps
       for (int g = 0; g < rows; g += gh) {
