@@ -204,6 +204,8 @@ def sweep_calls(bl, items):
 
 def capture(bl, items, stream):
     import torch
+    # the inputs, outputs and workspaces were made on the current stream
+    stream.wait_stream(torch.cuda.current_stream())
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
         sweep_calls(bl, items)  # warm (first launches set kernel attributes)
@@ -298,11 +300,41 @@ PROFILE_CASES = {
 }
 
 
+# decode-chain cases: (workload, layers, tokens, launches)
+PROFILE_CHAINS = {
+    "chain_2b": ("decode_2b", 30, 1, 4),       # the headline step
+    "chain_2b_10": ("decode_2b", 10, 1, 4),    # 130 MB of weights (above L2), for full captures
+    "chain_2b_m8": ("decode_2b", 10, 8, 4),
+    "chain_100b_8": ("decode_100b", 8, 1, 4),  # 8 layers, 470 MB
+}
+
+
+def run_profile_chain(name: str):
+    """A few untimed chain launches of one case on cuda:0 (for ncu captures)."""
+    import torch
+    import w1_a8_bitlinear_02_b300 as bl
+    from w1_a8_bitlinear_02_b300 import workloads as wl
+    wname, layers, M, n = PROFILE_CHAINS[name]
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    items = prepare(bl, wl, wl.matrices(wname, layers=layers), M, dev, torch.bfloat16)
+    calls = chain_calls(items)
+    ws = bl.chain_workspace(calls, dev)
+    for _ in range(n):
+        bl.bitlinear_forward_chain(calls, ws)
+    torch.cuda.synchronize()
+    assert bl.device_error() == 0
+    print(json.dumps({"profile_chain": name, "calls": len(calls), "launches": n}), flush=True)
+
+
 def run_profile_case(name: str):
     """A few untimed forward calls of one case on cuda:0 (for ncu captures)."""
     import torch
     import w1_a8_bitlinear_02_b300 as bl
     from w1_a8_bitlinear_02_b300 import workloads as wl
+    if name in PROFILE_CHAINS:
+        run_profile_chain(name)
+        return
     M, N, K, kind, std, calls = PROFILE_CASES[name]
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
@@ -396,6 +428,8 @@ def chain_calls(items, mode="independent"):
 
 def capture_chain(bl, calls, ws, stream):
     import torch
+    # the workspace was zero-filled (and the inputs made) on the current stream
+    stream.wait_stream(torch.cuda.current_stream())
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
         bl.bitlinear_forward_chain(calls, ws)  # warm (kernel attributes)
@@ -757,7 +791,7 @@ def main():
     ap.add_argument("--no-100b", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--profile", choices=sorted(PROFILE_CASES),
+    ap.add_argument("--profile", choices=sorted(PROFILE_CASES) + sorted(PROFILE_CHAINS),
                     help="run one case a few times untimed (for ncu) and exit")
     args = ap.parse_args()
     if args.profile:

@@ -326,12 +326,13 @@ typedef struct bl_chain_call {
 } bl_chain_call;
 
 /* Workspace (device bytes) that bitlinear_forward_chain needs for these
- * calls: 256 bytes of control words, 96 bytes per call (the call table,
- * rewritten by every launch), a record of about K + 128 bytes for every call
- * whose input no earlier call writes (its input quantised before the chain
- * starts), plus 8 * N bytes for every call whose output a later call reads.  Host only; the calls' pointers are
- * compared, not dereferenced.  Errors: as bitlinear_forward_chain's argument
- * checks. */
+ * calls: 256 bytes of control words, 88 bytes per call (the call table,
+ * rewritten by every launch), a record of about M * K + 128 bytes (K rounded
+ * up to the call's weight slabs) for every call whose input no earlier call
+ * writes (its input quantised before the chain starts), plus 8 * N bytes for
+ * every call whose output a later call reads; each part 256-byte aligned.
+ * Host only; the calls' pointers are compared, not dereferenced.  Errors: as
+ * bitlinear_forward_chain's argument checks. */
 BL_API bl_status bitlinear_chain_workspace_bytes(const bl_chain_call *calls, int n, size_t *bytes);
 
 /* A decode chain: up to 240 single-token BitLinear forwards run in order in

@@ -794,17 +794,19 @@ bl_status bitlinear_relu2_quant_act(const void *x, int dtype, int64_t M, int64_t
                                     void *stream) {
   return quant_common(x, dtype, nullptr, 0.0f, false, M, K, xq, scale, stream, kActRelu2);
 }
-// Packed rows [N, rb] bytes as TMA boxes of 128 bytes x box_rows rows with the
-// 128-byte swizzle (the decode chain's one-lane-per-row layout).
-bool make_map_rows(CUtensorMap *m, const void *ptr, int64_t N, int64_t rb, int box_rows) {
+// Packed rows [N, rb] bytes as 8-byte elements, read in boxes of `pieces`
+// 16-byte pieces (2 elements each) x box_rows rows, unswizzled (the decode
+// chain's one-lane-per-row layout: an odd piece count per row keeps the
+// lanes' reads on different bank groups), zeros outside the rows.
+bool make_map_rows(CUtensorMap *m, const void *ptr, int64_t N, int64_t rb, int pieces, int box_rows) {
   auto fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(rb), static_cast<cuuint64_t>(N)};
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(rb / 8), static_cast<cuuint64_t>(N)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(rb)};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(chain::kBoxBytes), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(pieces * (chain::kPiece / 8)), static_cast<cuuint32_t>(box_rows)};
   cuuint32_t es[2] = {1u, 1u};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void *>(ptr), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -908,7 +910,8 @@ static bl_status chain_plan(const bl_chain_call *calls, int n, int grid, chain::
     const int64_t rpc0 = (c.N + grid - 1) / grid;
     const int64_t ng = (rpc0 + chain::kGroupRows - 1) / chain::kGroupRows;
     const int64_t gh = (rpc0 + ng - 1) / ng;
-    if (!make_map_rows(&p->maps[i], c.packed, c.N, rb, static_cast<int>(gh))) return BL_ERR_CUDA;
+    const int P = chain::slab_pieces(static_cast<int>(rb), toks(c));
+    if (!make_map_rows(&p->maps[i], c.packed, c.N, rb, P, static_cast<int>(gh))) return BL_ERR_CUDA;
     d.gamma = c.gamma;
     d.x = c.x;
     d.y = c.y;
@@ -921,6 +924,8 @@ static bl_status chain_plan(const bl_chain_call *calls, int n, int grid, chain::
     d.flags = flags | (barrier[i] ? chain::kFlagBarrier : 0);
     d.src = src[i];
     d.M = toks(c);
+    d.P = P;
+    d.ns = chain::slabs_of(static_cast<int>(rb), toks(c));
     d.rec = early[i] ? wsb + rec_off[i] : nullptr;
     d.mb_out = produces[i] ? reinterpret_cast<uint64_t *>(wsb + mb_off[i]) : nullptr;
     d.mb_in = nullptr;
@@ -933,6 +938,7 @@ static bl_status chain_plan(const bl_chain_call *calls, int n, int grid, chain::
       jb.rb = static_cast<int>(rb);
       jb.flags = flags;
       jb.M = toks(c);
+      jb.P = P;
     }
   }
   for (int i = 0; i < n; ++i)

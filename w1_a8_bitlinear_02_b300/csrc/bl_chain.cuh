@@ -16,12 +16,16 @@
 //   * the consumer warps run the calls in order over the block's rows.
 //
 // Rows, one lane each.  A block's rows form groups of gh <= 32 consecutive
-// rows; a stage is a group and a 1 KB slab of its packed bytes (4096
-// weights), loaded as 128-byte x gh-row TMA boxes with the 128-byte swizzle, so
-// lane l reading 16 bytes of row l touches a different bank group than the
-// other 7 lanes of its quarter-warp.
-// The 16 consumer warps split each slab's 16-byte pieces (64 weights) among
-// themselves; every lane of a warp needs the same 64 activation codes, which
+// rows; a stage is a group and a slab of its packed bytes: P 16-byte pieces
+// (64 weights each) of every row, P odd and at most 65 (1040 bytes, 4160
+// weights; the row's slabs as even as that allows), loaded as ONE TMA box of
+// 2P 8-byte elements x gh rows.  Rows land P * 16
+// bytes apart, an odd number of 16-byte units, so the 8 lanes of a
+// quarter-warp reading piece p of their own rows touch 8 different bank
+// groups with no swizzle; and one copy per stage keeps the producer's issue
+// cost (a TMA instruction waits behind the consumers' shared-memory traffic)
+// to two instructions per stage with the record's.
+// The 16 consumer warps split each slab's pieces among themselves; every lane of a warp needs the same 64 activation codes, which
 // are broadcast from shared memory.  A lane adds its row's pieces with the
 // masked dp4a (the bytes of (word & (3 << 2i)) are the codes c = q + 1 times
 // 4^i; the 4^i factor is removed exactly at the end; sum c*x - X = sum q*x,
@@ -70,27 +74,39 @@ namespace chain {
 
 constexpr int kMaxCalls = 240;            // one tensor map each in the kernel parameters
 constexpr int kCW = 16;                   // consumer warps
-constexpr int kThreads = (kCW + 1) * 32;  // + one producer warp
+constexpr int kTeams = 2;                 // one-token row groups alternate between two teams
+constexpr int kTW = kCW / kTeams;         // warps of a team
+constexpr int kProd = 2;                  // producer warps (one thread each): alternate stages
+constexpr int kThreads = (kCW + kProd) * 32;
 constexpr int kC = kCW * 32;              // consumer threads
 constexpr int kMaxK = 32768;
 constexpr int kMaxN = 1 << 30;            // row indices stay far inside int
 constexpr int kGroupRows = 32;            // rows per group at most: one per lane
-constexpr int kBoxBytes = 128;            // packed bytes per TMA box row (512 weights)
-constexpr int kBoxSize = kGroupRows * kBoxBytes;  // 4 KB per box
-constexpr int kSlabBoxes = 8;             // a slab: 1 KB of each row (4096 weights)
-constexpr int kSlabBytes = kSlabBoxes * kBoxBytes;
-constexpr int kSlabCodes = kSlabBytes * 4;
+constexpr int kPiece = 16;                // packed bytes of a piece (64 weights)
 constexpr int kJM = 2;                    // x vectors of 8 per consumer thread kept in registers (K <= 8192)
-// A record in the workspace (and the in-block codes area): a 128-byte header
-// -- c = gamma / s (fp32) at byte 0, the 16 warps' code sums (int32) at byte
-// 64 -- then the codes, zero from K to the end of the last slab.
+// Pieces per slab: odd (conflict-free rows, see above), at most 65 for one
+// token and 31 for more (their stage also holds every token's codes); a row
+// of np pieces takes the fewest slabs the cap allows, split evenly.
+__host__ __device__ constexpr int piece_cap(int M) { return M > 1 ? 31 : 65; }
+__host__ __device__ constexpr int slab_pieces(int rb, int M = 1) {
+  return ((rb / kPiece + (rb / kPiece + piece_cap(M) - 1) / piece_cap(M) - 1) /
+          ((rb / kPiece + piece_cap(M) - 1) / piece_cap(M))) | 1;
+}
+__host__ __device__ constexpr int slabs_of(int rb, int M = 1) {
+  return (rb / kPiece + slab_pieces(rb, M) - 1) / slab_pieces(rb, M);
+}
+// A record in the workspace: a 128-byte header -- c = gamma / s (fp32) at
+// byte 0, the code sums of the 16 piece classes (slab piece p mod 16; int32)
+// at byte 64 -- then the codes, zero from K to the end of the last slab.  The
+// in-block codes area has the same header (c only) and the codes zero to the
+// end of the row's last piece.
 constexpr int kHeader = 128;
-constexpr int kInBlockBytes = kHeader + kMaxK + kSlabCodes;
-// A ring stage: the slab's weight boxes (32 KB), then the record header and
-// the slab's 4096 activation codes (one bulk copy for a group's first slab,
-// whose header travels with it); 1 KB aligned for the next stage's boxes.
-constexpr int kStageW = kSlabBoxes * kBoxSize;
-constexpr int kStageBytes = kStageW + kSlabCodes + 1024;
+constexpr int kInBlockBytes = kHeader + kMaxK;
+// A ring stage: the slab's weights (gh rows of P pieces), then at codes_ofs
+// the record header and the slab's activation codes (one bulk copy for a
+// group's first slab, whose header travels with it).
+__host__ __device__ constexpr int codes_ofs(int M) { return kGroupRows * kPiece * piece_cap(M); }
+constexpr int kStageBytes = 37 * 1024;
 constexpr int kStages = 4;
 constexpr int kSmemFixed = 30 * 1024;     // barriers, partial sums and the call table
 constexpr int kSmemBytes = 1024 + kSmemFixed + kStages * kStageBytes + kInBlockBytes;
@@ -107,20 +123,21 @@ constexpr int kFlagBf16 = 1;      // x is bf16 (else fp32)
 constexpr int kFlagRelu2 = 2;     // quantise relu2(x)
 constexpr int kFlagBarrier = 4;   // every block finishes all earlier calls first
 
-// Calls of more than one token (up to kMaxTok) use half slabs (512 bytes of
-// each row, 2048 weights), so a stage holds the weights (16 KB) and every
-// token's codes for them (M x 2 KB); their record header holds c[m] (fp32)
+// Calls of more than one token (up to kMaxTok) use slabs of at most 31
+// pieces, so a stage holds the weights (at most 15.5 KB) and every token's
+// codes for them (M x 31 x 64 bytes); their record header holds c[m] (fp32)
 // at 4m and the 16 warps' code sums of token m at 64 + 64m.
 constexpr int kMaxTok = 8;
-__host__ __device__ constexpr int slab_bytes(int M) { return M > 1 ? kSlabBytes / 2 : kSlabBytes; }
-__host__ __device__ constexpr int slabs_of(int rb, int M = 1) { return (rb + slab_bytes(M) - 1) / slab_bytes(M); }
 __host__ __device__ constexpr int header_bytes(int M) { return M > 1 ? ((64 + 64 * M + 127) / 128) * 128 : kHeader; }
-// a record: the header, then slab by slab each token's codes (4 per weight byte)
+// a record: the header, then slab by slab each token's codes (64 per piece)
 __host__ __device__ constexpr int record_bytes(int rb, int M = 1) {
-  return header_bytes(M) + slabs_of(rb, M) * M * 4 * slab_bytes(M);
+  return header_bytes(M) + slabs_of(rb, M) * M * 64 * slab_pieces(rb, M);
 }
-static_assert(kSlabBoxes / 2 * kBoxSize + header_bytes(kMaxTok) + kMaxTok * 4 * (kSlabBytes / 2) <=
-                  kStageBytes, "a stage of a many-token call");
+static_assert(codes_ofs(1) + kHeader + 64 * piece_cap(1) <= kStageBytes, "a stage of a one-token call");
+static_assert(codes_ofs(kMaxTok) + header_bytes(kMaxTok) + kMaxTok * 64 * piece_cap(kMaxTok) <= kStageBytes,
+              "a stage of a many-token call");
+static_assert(kStageBytes % 1024 == 0 && codes_ofs(1) % 128 == 0 && codes_ofs(kMaxTok) % 128 == 0,
+              "stage and codes alignment");
 
 struct Call {
   const float *gamma;
@@ -136,13 +153,16 @@ struct Call {
   int flags;
   int src;                // the call that wrote mb_in
   int M;                  // tokens (x [M, K], y [M, N]); more than one only with a record
+  int P;                  // pieces per slab (slab_pieces(rb, M); the box is 4P words wide)
+  int ns;                 // slabs per row (slabs_of(rb, M))
 };
 static_assert(sizeof(Call) % 4 == 0, "call table copied in words");
 
-// The packed weights of call i are read through maps[i]: [N, rb] bytes, box
-// 128 bytes x gh rows, 128-byte swizzle.  Tensor maps in the kernel
-// parameters need no fetch from global memory (a map read from global memory
-// stalled the issuing thread by about an L2 round trip per call).
+// The packed weights of call i are read through maps[i]: [N, rb / 8] 8-byte
+// elements, box 2P elements x gh rows, no swizzle, zeros outside.  Tensor maps in
+// the kernel parameters need no fetch from global memory (a map read from
+// global memory stalled the issuing thread by about an L2 round trip per
+// call).
 struct Params {
   int n;                  // calls
   unsigned *ctl;          // workspace control words
@@ -150,11 +170,23 @@ struct Params {
   CUtensorMap maps[kMaxCalls];
 };
 
+// Row sums of one-token groups meet in one of kGB buffers, each with an
+// mbarrier the group's warps arrive on once their shares are added; only the
+// warp that writes the group's rows waits.  No warp can be kStages + 1 groups
+// ahead of another (each group takes at least one stage), so kGB > kStages + 1
+// keeps a buffer from being reused before its group is written.
+constexpr int kGB = 8;
+static_assert(kGB > kStages + 1, "group buffers");
+static_assert(kGB % kTeams == 0 && kCW % kTeams == 0, "teams");
+static_assert(kStages % kProd == 0, "each producer owns whole ring slots");
+static_assert(kThreads <= 20 * 32, "the kernel's register budget assumes at most 20 warps");
+
 struct Smem {
   uint64_t full[kStages];
   uint64_t empty[kStages];
+  uint64_t gbar[kGB];
   float fred[kCW];
-  int32_t part[2][kCW][kGroupRows];  // a group's partial sums, by group parity
+  int32_t gsum[kGB][kGroupRows];
   int32_t msum[2][kMaxTok][kGroupRows];  // the same, many-token calls (added into)
   uint32_t seq_tag;
   int abort_flag;
@@ -186,7 +218,7 @@ struct QuantJob {
   const void *x;
   const float *gamma;
   uint8_t *rec;
-  int K, rb, flags, M;
+  int K, rb, flags, M, P;
 };
 struct QuantParams {
   int n;
@@ -194,7 +226,7 @@ struct QuantParams {
 };
 constexpr int kQThreads = 256;
 __global__ void __launch_bounds__(kQThreads) chain_quant_kernel(const __grid_constant__ QuantParams q) {
-  __shared__ __align__(16) uint8_t codes[kMaxK + kSlabCodes];
+  __shared__ __align__(16) uint8_t codes[kMaxK + 64 * piece_cap(1)];
   __shared__ float red[kQThreads / 32];
   __shared__ int xsum[kCW];
   const QuantJob &jb = q.j[blockIdx.x];
@@ -202,7 +234,7 @@ __global__ void __launch_bounds__(kQThreads) chain_quant_kernel(const __grid_con
   if (m >= jb.M) return;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const bool bf = (jb.flags & kFlagBf16) != 0, r2 = (jb.flags & kFlagRelu2) != 0;
-  const int K = jb.K, M = jb.M, SB4 = 4 * slab_bytes(M), nsl = slabs_of(jb.rb, M), kend = nsl * SB4;
+  const int K = jb.K, M = jb.M, P = jb.P, SB4 = 64 * P, nsl = slabs_of(jb.rb, M), kend = nsl * SB4;
   const void *xr = bf ? static_cast<const void *>(static_cast<const __nv_bfloat16 *>(jb.x) + static_cast<int64_t>(m) * K)
                       : static_cast<const void *>(static_cast<const float *>(jb.x) + static_cast<int64_t>(m) * K);
   auto ld = [&](int k) -> float {
@@ -248,8 +280,8 @@ __global__ void __launch_bounds__(kQThreads) chain_quant_kernel(const __grid_con
     codes[k] = k < K ? static_cast<uint8_t>(quant_one(ld(k), s) & 0xFF) : 0u;
   __syncthreads();
   // the codes out, slab by slab after the header (token m's share of each
-  // slab), and each 64-code piece's sum into its warp's total (piece p is
-  // read by consumer warp p mod 16)
+  // slab), and each 64-code piece's sum into its warp's total (piece p of a
+  // slab is read by consumer warp p mod 16)
   const int H = header_bytes(M);
   for (int i = t; i < kend / 16; i += kQThreads) {
     const int sl = (16 * i) / SB4, off = (16 * i) % SB4;
@@ -266,7 +298,7 @@ __global__ void __launch_bounds__(kQThreads) chain_quant_kernel(const __grid_con
       sm = dp4a_us(0x01010101u, v.z, sm);
       sm = dp4a_us(0x01010101u, v.w, sm);
     }
-    atomicAdd(&xsum[pc % kCW], sm);
+    atomicAdd(&xsum[(pc % P) % kCW], sm);
   }
   __syncthreads();
   if (t < kCW) reinterpret_cast<int *>(jb.rec + 64 + 64 * m)[t] = xsum[t];
@@ -309,12 +341,10 @@ __device__ __forceinline__ void block_rows(const Call &c, int &r0, int &rows) {
   rows = c.N - r0 < c.rpc ? c.N - r0 : c.rpc;
   if (rows < 0) rows = 0;
 }
-// 128-byte boxes of slab s (the last slab of a row may be shorter)
-__device__ __forceinline__ int boxes_of(int rb, int s, int M = 1) {
-  const int sb = slab_bytes(M);
-  int len = rb - s * sb;
-  if (len > sb) len = sb;
-  return (len + kBoxBytes - 1) / kBoxBytes;
+// Pieces of slab s that lie inside the row (the last slab may be shorter).
+__device__ __forceinline__ int pieces_in(int rb, int P, int s) {
+  const int left = rb / kPiece - s * P;
+  return left < P ? left : P;
 }
 
 // Eight activations of vector v into f; false when they come from output
@@ -403,10 +433,12 @@ __device__ __forceinline__ void piece(uint32_t waddr, uint32_t act, int (&a)[4])
 // Quantise the input of call c in every block (it depends on earlier calls)
 // into the in-block codes area `slot`: values polled from output words or
 // read after the grid barrier, per-token absmax over the block, codes
-// zero-padded to the last slab, the warps' code sums and c = gamma / s into
-// the area's header.  Returns false (in every thread) when the block must stop.
-__device__ __forceinline__ bool quantise_in_block(const Call &c, uint32_t slot, uint32_t want, int tid, Smem &sm,
-                                                  volatile int *abort_flag) {
+// zero-padded to the end of the row's last piece and c = gamma / s into the
+// area's header; xw = the code sum of piece class cls (slab pieces p with
+// p mod kTW == cls).  Returns false (in every thread) when the block must
+// stop.
+__device__ __forceinline__ bool quantise_in_block(const Call &c, uint32_t slot, uint32_t want, int tid, int cls,
+                                                  Smem &sm, volatile int *abort_flag, int &xw) {
   const int warp = tid >> 5, lane = tid & 31;
   const uint32_t xs = slot + kHeader;
   const int nv = vec_count(c);
@@ -500,28 +532,28 @@ __device__ __forceinline__ bool quantise_in_block(const Call &c, uint32_t slot, 
     }
     sts_u8(xs + k, static_cast<uint32_t>(q) & 0xFFu);
   }
-  for (int k = kz + 16 * tid; k < slabs_of(c.rb) * kSlabCodes; k += 16 * kC) sts_u128(xs + k, 0u, 0u, 0u, 0u);
+  for (int k = kz + 16 * tid; k < 4 * c.rb; k += 16 * kC) sts_u128(xs + k, 0u, 0u, 0u, 0u);
   if (tid == 0) asm volatile("st.shared.f32 [%0], %1;" ::"r"(slot), "f"(__fdiv_rn(__ldg(c.gamma), s)) : "memory");
   named_bar(1, kC);
-  // X for this warp: the sum of the codes of its pieces (pieces w, w + 16,
-  // ... of the whole row: at most 32), one piece per lane
-  const int npieces = slabs_of(c.rb) * (kSlabCodes / 64);
-  int xw = 0;
-  const int pc = warp + kCW * lane;
-  if (pc < npieces) {
-    const uint32_t act = xs + static_cast<uint32_t>(64 * pc);
+  // X of piece class cls: the sum of the codes of slab pieces cls, cls + kTW,
+  // ... of every slab, a piece per lane at a time
+  const int npieces = c.rb / kPiece, P = c.P, per = (P + kTW - 1) / kTW;
+  xw = 0;
+  for (int idx = lane; idx < per * c.ns; idx += 32) {
+    const int p = cls + kTW * (idx % per), g = (idx / per) * P + p;
+    if (p < P && g < npieces) {
+      const uint32_t act = xs + static_cast<uint32_t>(64 * g);
 #pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4) {
-      const uint4 v = lds_u128(act + 16 * q4);
-      xw = dp4a_us(0x01010101u, v.x, xw);
-      xw = dp4a_us(0x01010101u, v.y, xw);
-      xw = dp4a_us(0x01010101u, v.z, xw);
-      xw = dp4a_us(0x01010101u, v.w, xw);
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const uint4 v = lds_u128(act + 16 * q4);
+        xw = dp4a_us(0x01010101u, v.x, xw);
+        xw = dp4a_us(0x01010101u, v.y, xw);
+        xw = dp4a_us(0x01010101u, v.z, xw);
+        xw = dp4a_us(0x01010101u, v.w, xw);
+      }
     }
   }
   xw = __reduce_add_sync(0xffffffffu, xw);
-  if (lane == 0) asm volatile("st.shared.u32 [%0], %1;" ::"r"(slot + 64u + 4u * warp), "r"(xw) : "memory");
-  __syncwarp();
   return true;
 }
 
@@ -551,19 +583,21 @@ __device__ __forceinline__ void piece_multi(uint32_t waddr, uint32_t act, uint32
 // The pieces of one stage of a many-token call (this warp's: warp, warp + 16).
 template <int MT>
 __device__ __forceinline__ void stage_multi(uint32_t sbase, uint32_t abase, uint32_t tstride, int npc, int warp,
-                                            uint32_t lsw, int (&acc)[kMaxTok]) {
+                                            int (&acc)[kMaxTok]) {
   for (int pc = warp; pc < npc; pc += kCW)
-    piece_multi<MT>(sbase + static_cast<uint32_t>((pc >> 3) * kBoxSize) + ((static_cast<uint32_t>(pc & 7) ^ lsw) << 4),
-                    abase + 64u * pc, tstride, acc);
+    piece_multi<MT>(sbase + static_cast<uint32_t>(pc * kPiece), abase + 64u * pc, tstride, acc);
 }
 
 // MANY: the chain has calls of more than one token (a separate instantiation,
 // so single-token chains keep their register budget).
+// The register budget is set as for 20 warps (at most 96 registers a thread):
+// with 18 warps, two of the four schedulers hold 5 warps, and each
+// scheduler's share of the register file must fit 5 x 32 x the count.
 template <bool MANY>
-__global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constant__ Params p) {
+__global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant__ Params p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;  // the 128-byte swizzle needs 1 KB alignment
+  const uint32_t base = (raw + 1023u) & ~1023u;  // stages start 1 KB aligned (TMA needs 128 bytes)
   Smem &sm = *reinterpret_cast<Smem *>(smem_raw + (base - raw));
   const uint32_t ring = base + kSmemFixed;
   const uint32_t inb = ring + kStages * kStageBytes;  // codes quantised in this block
@@ -574,6 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
       mbar_init(smem_u32(&sm.full[s]), 1);
       mbar_init(smem_u32(&sm.empty[s]), kCW);
     }
+    for (int b = 0; b < kGB; ++b) mbar_init(smem_u32(&sm.gbar[b]), kCW);
     sm.abort_flag = 0;
     sm.seq_tag = p.ctl[kCtlSeq] << 9;  // tags: (launch sequence << 9) | (call + 1)
     fence_barrier_init();
@@ -584,51 +619,73 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
     const int words = p.n * static_cast<int>(sizeof(Call) / 4);
     for (int w = tid; w < words; w += kThreads) dst[w] = src[w];
     for (int i = tid; i < 2 * kMaxTok * kGroupRows; i += kThreads) (&sm.msum[0][0][0])[i] = 0;
+    for (int i = tid; i < kGB * kGroupRows; i += kThreads) (&sm.gsum[0][0])[i] = 0;
   }
   __syncthreads();
   volatile int *abort_flag = &sm.abort_flag;
   const uint32_t seq_tag = sm.seq_tag;
 
-  if (warp == kCW) {
-    // ------------------------------------------------ producer: records and weight stages, in order
+  if (warp >= kCW) {
+    // ------------------------------------------------ producers: records and weight stages, in order;
+    // producer q issues the stages i with i mod kProd == q (its own ring
+    // slots, as kStages is a multiple of kProd), so two threads on two
+    // schedulers share the per-stage issue work
+    const int q = warp - kCW;
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
       const uint64_t pol_rec = policy_evict_last();  // records are read by every block
       int i = 0, issued = 0;
       bool go = true;
+      // the call's fields in registers, read one call ahead (shared-memory
+      // loads wait behind the consumers' traffic; the asm statements below
+      // clobber memory, which would make every later use a reload)
+      struct Fields {
+        int N, rpc, gh, M, P, ns;
+        const uint8_t *rec;
+      };
+      auto fields = [&](int ci) {
+        Fields f;
+        f.N = sm.calls[ci].N;
+        f.rpc = sm.calls[ci].rpc;
+        f.gh = sm.calls[ci].gh;
+        f.M = sm.calls[ci].M;
+        f.P = sm.calls[ci].P;
+        f.ns = sm.calls[ci].ns;
+        f.rec = sm.calls[ci].rec;
+        return f;
+      };
+      Fields nxt = fields(0);
       for (int ci = 0; ci < p.n && go; ++ci) {
-        // the call's fields in registers (the asm statements below clobber
-        // memory, which would make every use a shared-memory reload)
-        const int N = sm.calls[ci].N, rb = sm.calls[ci].rb, rpc = sm.calls[ci].rpc, gh = sm.calls[ci].gh;
-        const int M = sm.calls[ci].M;
-        const uint8_t *rec = sm.calls[ci].rec;
-        const int SB = slab_bytes(M), H = header_bytes(M);
-        const uint32_t cbytes = static_cast<uint32_t>(M * 4 * SB);  // every token's codes of one slab
-        const uint32_t cofs = static_cast<uint32_t>(SB / kBoxBytes) * kBoxSize;  // codes after the boxes
+        const Fields cur = nxt;
+        if (ci + 1 < p.n) nxt = fields(ci + 1);
+        const int N = cur.N, rpc = cur.rpc, gh = cur.gh, M = cur.M, P = cur.P;
+        const uint8_t *rec = cur.rec;
+        const int H = header_bytes(M);
+        const uint32_t cbytes = static_cast<uint32_t>(M * 64 * P);  // every token's codes of one slab
+        const uint32_t cofs = static_cast<uint32_t>(codes_ofs(M));
         const int r0 = static_cast<int>(blockIdx.x) * rpc;
         const int rows = N - r0 < rpc ? (N - r0 > 0 ? N - r0 : 0) : rpc;
         if (rows == 0) continue;
         const CUtensorMap *map = &p.maps[ci];
-        const int nslab = slabs_of(rb, M);
+        const int nslab = cur.ns;
         // groups of gh rows (the last block's last group may run past N,
-        // where the box reads zeros)
-        const uint32_t box = static_cast<uint32_t>(gh) * kBoxBytes;
+        // where the box reads zeros; so does the last slab past the row)
+        const uint32_t box = static_cast<uint32_t>(gh * kPiece * P);
         for (int g = 0; g < rows && go; g += gh) {
           for (int s = 0; s < nslab; ++s, ++i) {
+            if (i % kProd != q) continue;
             const int st = i % kStages;
             if (i >= kStages && (!mbar_wait(smem_u32(&sm.empty[st]), ((i / kStages) - 1) & 1) || *abort_flag)) {
               *abort_flag = 1;
               go = false;
               break;
             }
-            const int nb = boxes_of(rb, s, M);
             const uint32_t fb = smem_u32(&sm.full[st]);
             const uint32_t sb = ring + st * kStageBytes;
-            uint32_t tx = static_cast<uint32_t>(nb) * box;
+            uint32_t tx = box;
             if (rec != nullptr) tx += cbytes + (s == 0 ? H : 0);
             mbar_arrive_expect_tx(fb, tx);
-            for (int b = 0; b < nb; ++b)
-              tma_load_2d(sb + b * kBoxSize, map, s * SB + b * kBoxBytes, r0 + g, fb, pol);
+            tma_load_2d(sb, map, s * P * (kPiece / 8), r0 + g, fb, pol);
             if (rec != nullptr) {
               if (s == 0)
                 bulk_g2s(sb + cofs, rec, H + cbytes, fb, pol_rec);
@@ -641,7 +698,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
       }
       // no copy into this block's shared memory may be in flight at exit
       for (int j = issued - kStages < 0 ? 0 : issued - kStages; j < issued; ++j)
-        mbar_wait(smem_u32(&sm.full[j % kStages]), (j / kStages) & 1);
+        if (j % kProd == q) mbar_wait(smem_u32(&sm.full[j % kStages]), (j / kStages) & 1);
     }
     __syncwarp();
   } else {
@@ -652,7 +709,8 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
     // later calls' barriers.
     int it = 0;       // ring stage counter, in the producer's order
     int nbar = 0;     // grid barriers passed
-    int ng = 0;       // row groups done (partial-sum buffer parity)
+    int ng = 0;       // many-token row groups done (partial-sum buffer parity)
+    int ng1 = 0;      // one-token row groups done (group buffer, writer and phase)
     for (int ci = 0; ci < p.n; ++ci) {
       const Call &c = sm.calls[ci];
       int r0, rows;
@@ -685,17 +743,16 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
       if (rows == 0) continue;
       // the call's fields in registers (asm statements below clobber memory)
       const bool has_rec = c.rec != nullptr;
-      const int rb = c.rb, gh = c.gh, M = c.M, N = c.N;
+      const int rb = c.rb, gh = c.gh, M = c.M, N = c.N, P = c.P;
       float *const yout = c.y;
       uint64_t *const mbo = c.mb_out;
-      const uint32_t lrow = static_cast<uint32_t>(lane) * kBoxBytes;
-      const uint32_t lsw = static_cast<uint32_t>(lane & 7);
+      const uint32_t lrow = static_cast<uint32_t>(lane * kPiece * P);  // this lane's row in a stage
 
       if (MANY && M > 1) {
         // ---- many tokens (their codes come with the record in every stage)
-        const int SB = slab_bytes(M), H = header_bytes(M), nslab = slabs_of(rb, M);
-        const uint32_t cofs = static_cast<uint32_t>(SB / kBoxBytes) * kBoxSize;
-        const uint32_t tstride = static_cast<uint32_t>(4 * SB);
+        const int H = header_bytes(M), nslab = c.ns;
+        const uint32_t cofs = static_cast<uint32_t>(codes_ofs(M));
+        const uint32_t tstride = static_cast<uint32_t>(64 * P);
         float cmv[kMaxTok];  // the tokens' output scales (used by the writing warp)
         int xwv[kMaxTok];
 #pragma unroll
@@ -713,7 +770,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
               *abort_flag = 1;
               break;
             }
-            const int npc = boxes_of(rb, s, M) * 8;
+            const int npc = pieces_in(rb, P, s);
             const uint32_t sb = ring + st * kStageBytes;
             if (g == 0 && s == 0) {
 #pragma unroll
@@ -726,13 +783,13 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
             }
             const uint32_t sbase = sb + lrow, abase = sb + cofs + static_cast<uint32_t>(H);
             switch (M) {
-              case 2: stage_multi<2>(sbase, abase, tstride, npc, warp, lsw, acc); break;
-              case 3: stage_multi<3>(sbase, abase, tstride, npc, warp, lsw, acc); break;
-              case 4: stage_multi<4>(sbase, abase, tstride, npc, warp, lsw, acc); break;
-              case 5: stage_multi<5>(sbase, abase, tstride, npc, warp, lsw, acc); break;
-              case 6: stage_multi<6>(sbase, abase, tstride, npc, warp, lsw, acc); break;
-              case 7: stage_multi<7>(sbase, abase, tstride, npc, warp, lsw, acc); break;
-              default: stage_multi<8>(sbase, abase, tstride, npc, warp, lsw, acc); break;
+              case 2: stage_multi<2>(sbase, abase, tstride, npc, warp, acc); break;
+              case 3: stage_multi<3>(sbase, abase, tstride, npc, warp, acc); break;
+              case 4: stage_multi<4>(sbase, abase, tstride, npc, warp, acc); break;
+              case 5: stage_multi<5>(sbase, abase, tstride, npc, warp, acc); break;
+              case 6: stage_multi<6>(sbase, abase, tstride, npc, warp, acc); break;
+              case 7: stage_multi<7>(sbase, abase, tstride, npc, warp, acc); break;
+              default: stage_multi<8>(sbase, abase, tstride, npc, warp, acc); break;
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&sm.empty[st]));
@@ -761,77 +818,106 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(const __grid_constan
       }
 
       // ---- the activation codes, c and the warp's code sum: from the
-      // record (in the call's first stage) or quantised here
+      // record (in each group's first stage) or quantised here.  Row groups
+      // alternate between the two teams of kTW warps (group ng1 goes to team
+      // ng1 mod 2), so each warp takes more pieces of a stage for the same
+      // per-stage work; within its team a warp takes the slab pieces of
+      // class cls (p mod kTW == cls), rotated from call to call so the
+      // classes with one piece more fall to different warps.
+      const int team = warp / kTW, tw = warp % kTW;
+      const int cls = (tw + ci) & (kTW - 1);
       float cm = 0.0f;
       int xw = 0;
       if (!has_rec) {
-        // the area is free: earlier calls ended at this block's group
-        // barriers, which every warp has passed
-        if (!quantise_in_block(c, inb, seq_tag | static_cast<uint32_t>(c.src + 1), tid, sm, abort_flag)) {
+        // the area is rewritten only after the block barrier inside, which
+        // every warp reaches once it is done with the earlier calls
+        if (!quantise_in_block(c, inb, seq_tag | static_cast<uint32_t>(c.src + 1), tid, cls, sm, abort_flag, xw)) {
           *abort_flag = 1;
           break;
         }
         asm volatile("ld.shared.f32 %0, [%1];" : "=f"(cm) : "r"(inb) : "memory");
-        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(xw) : "r"(inb + 64u + 4u * warp) : "memory");
       }
-      const int nslab = slabs_of(rb);
+      const int nslab = c.ns;
       const uint32_t tag = seq_tag | static_cast<uint32_t>(ci + 1);
 
-      // ---- row groups: one lane per row, the slabs' pieces split over warps
+      // ---- row groups: one lane per row, the slabs' pieces split over the
+      // warps of the group's team (the other team moves on to its next group)
       for (int g = 0; g < rows; g += gh) {
+        if ((ng1 & 1) != team) {
+          it += nslab;
+          ++ng1;
+          continue;
+        }
         int acc[4] = {0, 0, 0, 0}, acc2[4] = {0, 0, 0, 0};
         for (int s = 0; s < nslab; ++s, ++it) {
           const int st = it % kStages;
-          if (*abort_flag || !mbar_wait(smem_u32(&sm.full[st]), (it / kStages) & 1)) {
+          // (the stop flag is read only when the stage is not there yet)
+          if (!mbar_try_wait(smem_u32(&sm.full[st]), (it / kStages) & 1) &&
+              (*abort_flag || !mbar_wait_slow(smem_u32(&sm.full[st]), (it / kStages) & 1))) {
             *abort_flag = 1;
             break;
           }
-          const int npc = boxes_of(rb, s) * 8;
+          const int npc = pieces_in(rb, P, s);
           const uint32_t sb = ring + st * kStageBytes;
           const uint32_t sbase = sb + lrow;
-          const uint32_t abase = has_rec ? sb + kStageW + kHeader : inb + kHeader + static_cast<uint32_t>(s * kSlabCodes);
-          if (has_rec && g == 0 && s == 0) {
-            asm volatile("ld.shared.f32 %0, [%1];" : "=f"(cm) : "r"(sb + kStageW) : "memory");
-            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(xw) : "r"(sb + kStageW + 64u + 4u * warp) : "memory");
+          const uint32_t abase = has_rec ? sb + codes_ofs(1) + kHeader : inb + kHeader + static_cast<uint32_t>(s * 64 * P);
+          if (has_rec && s == 0) {
+            // c and X of class cls (the header holds the sums of the 16
+            // classes p mod 16; classes cls and cls + kTW make p mod kTW)
+            uint32_t x0, x1;
+            asm volatile("ld.shared.f32 %0, [%1];" : "=f"(cm) : "r"(sb + codes_ofs(1)) : "memory");
+            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(x0) : "r"(sb + codes_ofs(1) + 64u + 4u * cls) : "memory");
+            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(x1) : "r"(sb + codes_ofs(1) + 64u + 4u * (cls + kTW))
+                         : "memory");
+            xw = static_cast<int>(x0 + x1);
           }
           // two pieces at a time, in separate accumulators, so their loads
           // and dp4a chains overlap
-          int pc = warp;
-          for (; pc + kCW < npc; pc += 2 * kCW) {
-            const uint32_t w0 = sbase + static_cast<uint32_t>((pc >> 3) * kBoxSize) +
-                                ((static_cast<uint32_t>(pc & 7) ^ lsw) << 4);
-            const int pc1 = pc + kCW;
-            const uint32_t w1 = sbase + static_cast<uint32_t>((pc1 >> 3) * kBoxSize) +
-                                ((static_cast<uint32_t>(pc1 & 7) ^ lsw) << 4);
+          int pc = cls;
+          for (; pc + kTW < npc; pc += 2 * kTW) {
+            const uint32_t w0 = sbase + static_cast<uint32_t>(pc * kPiece);
+            const int pc1 = pc + kTW;
+            const uint32_t w1 = sbase + static_cast<uint32_t>(pc1 * kPiece);
             piece(w0, abase + 64u * pc, acc);
             piece(w1, abase + 64u * pc1, acc2);
           }
           if (pc < npc) {
-            const uint32_t w0 = sbase + static_cast<uint32_t>((pc >> 3) * kBoxSize) +
-                                ((static_cast<uint32_t>(pc & 7) ^ lsw) << 4);
+            const uint32_t w0 = sbase + static_cast<uint32_t>(pc * kPiece);
             piece(w0, abase + 64u * pc, acc);
           }
+          // the stage's empty barrier counts kCW arrivals: a team's warps
+          // arrive twice each
           __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&sm.empty[st]));
+          if (lane == 0) mbar_arrive_n(smem_u32(&sm.empty[st]), kTeams);
         }
-        const int pb = ng & 1;
-        sm.part[pb][warp][lane] = (acc[0] + acc2[0]) + ((acc[1] + acc2[1]) >> 2) + ((acc[2] + acc2[2]) >> 4) +
-                                  ((acc[3] + acc2[3]) >> 6) - xw;
-        named_bar(2, kC);
-        // one warp per group adds the 16 partial sums of each row and writes it
-        if (warp == (ng % kCW)) {
+        // the warps' sums meet in the group's buffer (no block barrier: a
+        // warp done with its share goes on to the next group); the writing
+        // warp waits for every thread's share, writes the rows and clears
+        // the buffer
+        const int gb = ng1 & (kGB - 1);
+        atomicAdd(&sm.gsum[gb][lane], (acc[0] + acc2[0]) + ((acc[1] + acc2[1]) >> 2) +
+                                          ((acc[2] + acc2[2]) >> 4) + ((acc[3] + acc2[3]) >> 6) - xw);
+        __syncwarp();  // orders the lanes' adds before lane 0's release
+        if (lane == 0) mbar_arrive_n(smem_u32(&sm.gbar[gb]), kTeams);
+        // (once the block is stopping, nothing more is waited for or written;
+        // every warp still walks the same calls, so later block barriers match)
+        if (tw == ((ng1 / kTeams) % kTW) && !*abort_flag) {
+          if (!mbar_wait(smem_u32(&sm.gbar[gb]), (ng1 / kGB) & 1)) {
+            *abort_flag = 1;
+            ++ng1;
+            continue;
+          }
+          const int t = sm.gsum[gb][lane];
+          sm.gsum[gb][lane] = 0;
           const int h = rows - g < gh ? rows - g : gh;
           if (lane < h) {
-            int t = 0;
-#pragma unroll
-            for (int w = 0; w < kCW; ++w) t += sm.part[pb][w][lane];
             const int r = r0 + g + lane;
             const float v = __fmul_rn(static_cast<float>(t), cm);
             yout[r] = v;
             if (mbo != nullptr) st_word(mbo + r, v, tag);
           }
         }
-        ++ng;
+        ++ng1;
       }
     }
     __syncwarp();
