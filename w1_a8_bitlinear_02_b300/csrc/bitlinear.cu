@@ -810,9 +810,9 @@ bool make_map_rows(CUtensorMap *m, const void *ptr, int64_t N, int64_t rb, int p
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Plan of a decode chain (host): each call's rows per block (ng groups of gh
-// <= 32 rows, so one tensor map with box height gh serves every group) and
-// tensor map; where its input comes from (quantised ahead into a record, an
+// Plan of a decode chain (host): each call's 32-row groups, dealt to the
+// blocks round-robin from where the previous call's deal ended (group j of
+// call i goes to block (g0_i + j) mod grid), and its tensor map; where its input comes from (quantised ahead into a record, an
 // earlier call's output words, or memory after a grid barrier); the workspace
 // layout (control words, call table, records, output words).
 // Dependencies are read off the calls' buffers:
@@ -903,23 +903,23 @@ static bl_status chain_plan(const bl_chain_call *calls, int n, int grid, chain::
   t->n = n;
   t->dst = reinterpret_cast<chain::Call *>(wsb + chain::kTableOffset);
   q->n = 0;
+  int64_t deal = 0;  // the block that takes the next call's group 0
   for (int i = 0; i < n; ++i) {
     const bl_chain_call &c = calls[i];
     chain::Call &d = t->calls[i];
     const int64_t rb = plan::row_bytes(c.K);
-    const int64_t rpc0 = (c.N + grid - 1) / grid;
-    const int64_t ng = (rpc0 + chain::kGroupRows - 1) / chain::kGroupRows;
-    const int64_t gh = (rpc0 + ng - 1) / ng;
+    const int64_t ng = (c.N + chain::kGroupRows - 1) / chain::kGroupRows;
     const int P = chain::slab_pieces(static_cast<int>(rb), toks(c));
-    if (!make_map_rows(&p->maps[i], c.packed, c.N, rb, P, static_cast<int>(gh))) return BL_ERR_CUDA;
+    if (!make_map_rows(&p->maps[i], c.packed, c.N, rb, P, chain::kGroupRows)) return BL_ERR_CUDA;
     d.gamma = c.gamma;
     d.x = c.x;
     d.y = c.y;
     d.N = static_cast<int>(c.N);
     d.K = static_cast<int>(c.K);
     d.rb = static_cast<int>(rb);
-    d.rpc = static_cast<int>(ng * gh);
-    d.gh = static_cast<int>(gh);
+    d.g0 = static_cast<int>(deal);
+    d.ng = static_cast<int>(ng);
+    deal = (deal + ng) % grid;
     const int flags = (c.x_dtype == BL_BF16 ? chain::kFlagBf16 : 0) | (c.act == BL_ACT_RELU2 ? chain::kFlagRelu2 : 0);
     d.flags = flags | (barrier[i] ? chain::kFlagBarrier : 0);
     d.src = src[i];

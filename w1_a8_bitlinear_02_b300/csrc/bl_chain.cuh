@@ -15,11 +15,13 @@
 //     calls);
 //   * the consumer warps run the calls in order over the block's rows.
 //
-// Rows, one lane each.  A block's rows form groups of gh <= 32 consecutive
-// rows; a stage is a group and a slab of its packed bytes: P 16-byte pieces
-// (64 weights each) of every row, P odd and at most 65 (1040 bytes, 4160
-// weights; the row's slabs as even as that allows), loaded as ONE TMA box of
-// 2P 8-byte elements x gh rows.  Rows land P * 16
+// Rows, one lane each.  A call's rows form groups of 32 consecutive rows,
+// dealt out to the blocks round-robin, each call's deal continuing where the
+// previous call's ended, so the lanes are full and the blocks' loads even out
+// over the chain.  A stage is a group and a slab of its packed bytes: P
+// 16-byte pieces (64 weights each) of every row, P odd and at most 65 (1040
+// bytes, 4160 weights; the row's slabs as even as that allows), loaded as ONE
+// TMA box of 2P 8-byte elements x 32 rows.  Rows land P * 16
 // bytes apart, an odd number of 16-byte units, so the 8 lanes of a
 // quarter-warp reading piece p of their own rows touch 8 different bank
 // groups with no swizzle; and one copy per stage keeps the producer's issue
@@ -102,7 +104,7 @@ __host__ __device__ constexpr int slabs_of(int rb, int M = 1) {
 // end of the row's last piece.
 constexpr int kHeader = 128;
 constexpr int kInBlockBytes = kHeader + kMaxK;
-// A ring stage: the slab's weights (gh rows of P pieces), then at codes_ofs
+// A ring stage: the slab's weights (32 rows of P pieces), then at codes_ofs
 // the record header and the slab's activation codes (one bulk copy for a
 // group's first slab, whose header travels with it).
 __host__ __device__ constexpr int codes_ofs(int M) { return kGroupRows * kPiece * piece_cap(M); }
@@ -148,8 +150,8 @@ struct Call {
   const uint64_t *mb_in;  // the words holding x [K] (inside an earlier call's mb_out), or null
   int N, K;
   int rb;                 // packed row bytes
-  int rpc;                // rows per block: ng groups of gh rows
-  int gh;                 // rows per group (<= 32; the tensor map's box height)
+  int g0;                 // the block that takes group 0 (group j goes to block (g0 + j) mod grid)
+  int ng;                 // 32-row groups: ceil(N / 32)
   int flags;
   int src;                // the call that wrote mb_in
   int M;                  // tokens (x [M, K], y [M, N]); more than one only with a record
@@ -159,7 +161,7 @@ struct Call {
 static_assert(sizeof(Call) % 4 == 0, "call table copied in words");
 
 // The packed weights of call i are read through maps[i]: [N, rb / 8] 8-byte
-// elements, box 2P elements x gh rows, no swizzle, zeros outside.  Tensor maps in
+// elements, box 2P elements x 32 rows, no swizzle, zeros outside.  Tensor maps in
 // the kernel parameters need no fetch from global memory (a map read from
 // global memory stalled the issuing thread by about an L2 round trip per
 // call).
@@ -335,11 +337,11 @@ __device__ __forceinline__ bool gave_up() {
   return (*static_cast<volatile unsigned *>(&g_dev_error) & kDevErrTimeout) != 0u;
 }
 
-// Rows of call c owned by this block: [r0, r0 + rows).
-__device__ __forceinline__ void block_rows(const Call &c, int &r0, int &rows) {
-  r0 = static_cast<int>(blockIdx.x) * c.rpc;
-  rows = c.N - r0 < c.rpc ? c.N - r0 : c.rpc;
-  if (rows < 0) rows = 0;
+// This block's first group of call c (it takes groups j, j + grid, ...;
+// none when j >= c.ng).
+__device__ __forceinline__ int first_group(const Call &c) {
+  const int j = static_cast<int>(blockIdx.x) - c.g0;
+  return j < 0 ? j + static_cast<int>(gridDim.x) : j;
 }
 // Pieces of slab s that lie inside the row (the last slab may be shorter).
 __device__ __forceinline__ int pieces_in(int rb, int P, int s) {
@@ -640,14 +642,13 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
       // loads wait behind the consumers' traffic; the asm statements below
       // clobber memory, which would make every later use a reload)
       struct Fields {
-        int N, rpc, gh, M, P, ns;
+        int g0, ng, M, P, ns;
         const uint8_t *rec;
       };
       auto fields = [&](int ci) {
         Fields f;
-        f.N = sm.calls[ci].N;
-        f.rpc = sm.calls[ci].rpc;
-        f.gh = sm.calls[ci].gh;
+        f.g0 = sm.calls[ci].g0;
+        f.ng = sm.calls[ci].ng;
         f.M = sm.calls[ci].M;
         f.P = sm.calls[ci].P;
         f.ns = sm.calls[ci].ns;
@@ -658,20 +659,20 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
       for (int ci = 0; ci < p.n && go; ++ci) {
         const Fields cur = nxt;
         if (ci + 1 < p.n) nxt = fields(ci + 1);
-        const int N = cur.N, rpc = cur.rpc, gh = cur.gh, M = cur.M, P = cur.P;
+        const int M = cur.M, P = cur.P, G = static_cast<int>(gridDim.x);
         const uint8_t *rec = cur.rec;
         const int H = header_bytes(M);
         const uint32_t cbytes = static_cast<uint32_t>(M * 64 * P);  // every token's codes of one slab
         const uint32_t cofs = static_cast<uint32_t>(codes_ofs(M));
-        const int r0 = static_cast<int>(blockIdx.x) * rpc;
-        const int rows = N - r0 < rpc ? (N - r0 > 0 ? N - r0 : 0) : rpc;
-        if (rows == 0) continue;
+        int j = static_cast<int>(blockIdx.x) - cur.g0;
+        if (j < 0) j += G;
+        if (j >= cur.ng) continue;
         const CUtensorMap *map = &p.maps[ci];
         const int nslab = cur.ns;
-        // groups of gh rows (the last block's last group may run past N,
-        // where the box reads zeros; so does the last slab past the row)
-        const uint32_t box = static_cast<uint32_t>(gh * kPiece * P);
-        for (int g = 0; g < rows && go; g += gh) {
+        // this block's groups (the last group may run past N, where the box
+        // reads zeros; so does the last slab past the row)
+        const uint32_t box = static_cast<uint32_t>(kGroupRows * kPiece * P);
+        for (; j < cur.ng && go; j += G) {
           for (int s = 0; s < nslab; ++s, ++i) {
             if (i % kProd != q) continue;
             const int st = i % kStages;
@@ -685,7 +686,7 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
             uint32_t tx = box;
             if (rec != nullptr) tx += cbytes + (s == 0 ? H : 0);
             mbar_arrive_expect_tx(fb, tx);
-            tma_load_2d(sb, map, s * P * (kPiece / 8), r0 + g, fb, pol);
+            tma_load_2d(sb, map, s * P * (kPiece / 8), j * kGroupRows, fb, pol);
             if (rec != nullptr) {
               if (s == 0)
                 bulk_g2s(sb + cofs, rec, H + cbytes, fb, pol_rec);
@@ -713,8 +714,7 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
     int ng1 = 0;      // one-token row groups done (group buffer, writer and phase)
     for (int ci = 0; ci < p.n; ++ci) {
       const Call &c = sm.calls[ci];
-      int r0, rows;
-      block_rows(c, r0, rows);
+      const int j0 = first_group(c), G = static_cast<int>(gridDim.x);
 
       if (c.flags & kFlagBarrier) {
         // every consumer warp of this block is done with the earlier calls;
@@ -740,10 +740,10 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
           break;
         }
       }
-      if (rows == 0) continue;
+      if (j0 >= c.ng) continue;  // no group of this call here (nor its input quantisation)
       // the call's fields in registers (asm statements below clobber memory)
       const bool has_rec = c.rec != nullptr;
-      const int rb = c.rb, gh = c.gh, M = c.M, N = c.N, P = c.P;
+      const int rb = c.rb, M = c.M, N = c.N, P = c.P, ngr = c.ng;
       float *const yout = c.y;
       uint64_t *const mbo = c.mb_out;
       const uint32_t lrow = static_cast<uint32_t>(lane * kPiece * P);  // this lane's row in a stage
@@ -760,7 +760,8 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
           cmv[m] = 0.0f;
           xwv[m] = 0;
         }
-        for (int g = 0; g < rows; g += gh) {
+        for (int j = j0; j < ngr; j += G) {
+          const int r0 = j * kGroupRows, h = N - r0 < kGroupRows ? N - r0 : kGroupRows;
           int acc[kMaxTok];
 #pragma unroll
           for (int m = 0; m < kMaxTok; ++m) acc[m] = 0;
@@ -772,7 +773,7 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
             }
             const int npc = pieces_in(rb, P, s);
             const uint32_t sb = ring + st * kStageBytes;
-            if (g == 0 && s == 0) {
+            if (s == 0) {
 #pragma unroll
               for (int m = 0; m < kMaxTok; ++m)
                 if (m < M) {
@@ -802,14 +803,13 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
             if (m < M) atomicAdd(&sm.msum[pb][m][lane], acc[m] - xwv[m]);
           named_bar(2, kC);
           if (warp == (ng % kCW)) {
-            const int h = rows - g < gh ? rows - g : gh;
 #pragma unroll
             for (int m = 0; m < kMaxTok; ++m)
               if (m < M) {
                 const int t = sm.msum[pb][m][lane];
                 sm.msum[pb][m][lane] = 0;
                 if (lane < h)
-                  yout[static_cast<int64_t>(m) * N + r0 + g + lane] = __fmul_rn(static_cast<float>(t), cmv[m]);
+                  yout[static_cast<int64_t>(m) * N + r0 + lane] = __fmul_rn(static_cast<float>(t), cmv[m]);
               }
           }
           ++ng;
@@ -842,7 +842,7 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
 
       // ---- row groups: one lane per row, the slabs' pieces split over the
       // warps of the group's team (the other team moves on to its next group)
-      for (int g = 0; g < rows; g += gh) {
+      for (int j = j0; j < ngr; j += G) {
         if ((ng1 & 1) != team) {
           it += nslab;
           ++ng1;
@@ -909,9 +909,8 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
           }
           const int t = sm.gsum[gb][lane];
           sm.gsum[gb][lane] = 0;
-          const int h = rows - g < gh ? rows - g : gh;
-          if (lane < h) {
-            const int r = r0 + g + lane;
+          const int r = j * kGroupRows + lane;
+          if (r < N) {
             const float v = __fmul_rn(static_cast<float>(t), cm);
             yout[r] = v;
             if (mbo != nullptr) st_word(mbo + r, v, tag);
