@@ -447,6 +447,40 @@ def test_chain_short_rows(bl, N, K):
     assert_bits_equal(y1.cpu().numpy(), r1, "short rows 1")
 
 
+def test_chain_long_row_groups_alternating_teams(bl):
+    """Row groups of many slabs (K = 28672: seven stages a group) next to
+    groups of two, one-token and many-token: the warps of one team skip the
+    other team's long group and must not take a ring slot's earlier phase
+    for the stage they wait for.  Independent and dependent inputs; whole
+    outputs against the oracle, repeated launches on one workspace."""
+    specs = [(4736, 28672, -1, 1), (4736, 8192, -1, 1), (4736, 28672, -1, 1), (9472, 4736, 2, 1),
+             (4736, 28672, -1, 3), (300, 9472, 3, 1)]
+    mats = [pack_both(bl, N, K, 0.01, 1100 + i) for i, (N, K, _, _) in enumerate(specs)]
+    xs, ys, calls = [], [], []
+    for i, ((N, K, src, M), (packed, gamma, _, _)) in enumerate(zip(specs, mats)):
+        y = torch.full((M, N), float("nan"), dtype=torch.float32, device=DEV)
+        if src < 0:
+            x = wl.activations(M, K, "outliers1pct", 1110 + i, "cpu", torch.bfloat16)
+            xd = x.to(DEV)
+        else:
+            x, xd = None, ys[src][:, :K]
+        xs.append(x)
+        ys.append(y)
+        calls.append(dict(packed=packed, gamma=gamma, x=xd, y=y, N=N, K=K))
+    ws = bl.chain_workspace(calls, DEV)
+    for _ in range(3):
+        for y in ys:
+            y.fill_(float("nan"))
+        bl.bitlinear_forward_chain(calls, ws)
+        torch.cuda.synchronize()
+        assert bl.device_error() == 0
+        outs = []
+        for i, ((N, K, src, M), (_, _, p_ref, g_ref)) in enumerate(zip(specs, mats)):
+            xin = xs[i].float().numpy() if src < 0 else np.ascontiguousarray(outs[src][:, :K], np.float32)
+            outs.append(oracle.forward_packed(p_ref, g_ref, N, K, xin))
+            assert_bits_equal(ys[i].cpu().numpy(), outs[i], f"long groups call {i}")
+
+
 def test_chain_unaligned_and_odd_k(bl):
     """K not a multiple of 8 and an input that starts off a 16-byte boundary
     take the element-by-element activation path."""

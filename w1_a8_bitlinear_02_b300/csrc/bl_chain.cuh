@@ -192,6 +192,7 @@ struct Smem {
   int32_t msum[2][kMaxTok][kGroupRows];  // the same, many-token calls (added into)
   uint32_t seq_tag;
   int abort_flag;
+  int stage_tag[kStages];  // the stage each ring slot was last armed for (written by its producer)
   Call calls[kMaxCalls];  // the call table, copied in once
 };
 static_assert(sizeof(Smem) <= kSmemFixed, "fixed shared-memory region");
@@ -335,6 +336,34 @@ __device__ __forceinline__ uint64_t ld_word(const uint64_t *p) {
 // this block waits for may never come, so stop waiting.
 __device__ __forceinline__ bool gave_up() {
   return (*static_cast<volatile unsigned *>(&g_dev_error) & kDevErrTimeout) != 0u;
+}
+
+// Wait for ring stage `it` to land.  A parity wait on a slot is only sound
+// once the slot's previous stage (it - kStages) has landed: before that, the
+// phase two back has the same parity and the wait would pass at once.  A
+// warp that processed stage it - kStages saw it land (bit 3 of `seen`, the
+// warp's record of which of the last four stages it processed); a warp that
+// skipped it (another team's row group) first waits for the producer to
+// arm the slot for `it`, which it does only after the slot's previous stage
+// was consumed.  Bounded; false when the block must stop.
+__device__ __forceinline__ bool stage_ready(const uint64_t *full, const int *stage_tag, int it, uint32_t seen,
+                                            volatile int *abort_flag) {
+  const int st = it % kStages;
+  if (!(seen & 8u)) {
+    const long long t0 = clock64();
+    while (true) {
+      int tag;
+      asm volatile("ld.acquire.cta.shared.s32 %0, [%1];" : "=r"(tag) : "r"(smem_u32(&stage_tag[st])) : "memory");
+      if (tag == it) break;
+      if (*abort_flag || clock64() - t0 > kWaitLimitCycles || gave_up()) {
+        atomicOr(&g_dev_error, kDevErrTimeout);
+        return false;
+      }
+    }
+  }
+  const uint32_t bar = smem_u32(&full[st]);
+  if (mbar_try_wait(bar, (it / kStages) & 1)) return true;
+  return !*abort_flag && mbar_wait_slow(bar, (it / kStages) & 1);
 }
 
 // This block's first group of call c (it takes groups j, j + grid, ...;
@@ -612,6 +641,7 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
     }
     for (int b = 0; b < kGB; ++b) mbar_init(smem_u32(&sm.gbar[b]), kCW);
     sm.abort_flag = 0;
+    for (int s = 0; s < kStages; ++s) sm.stage_tag[s] = s;
     sm.seq_tag = p.ctl[kCtlSeq] << 9;  // tags: (launch sequence << 9) | (call + 1)
     fence_barrier_init();
   }
@@ -681,6 +711,10 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
               go = false;
               break;
             }
+            // the slot's previous stage has landed and been consumed: say so
+            // before arming it (see stage_ready)
+            if (i >= kStages)
+              asm volatile("st.release.cta.shared.s32 [%0], %1;" ::"r"(smem_u32(&sm.stage_tag[st])), "r"(i) : "memory");
             const uint32_t fb = smem_u32(&sm.full[st]);
             const uint32_t sb = ring + st * kStageBytes;
             uint32_t tx = box;
@@ -712,6 +746,7 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
     int nbar = 0;     // grid barriers passed
     int ng = 0;       // many-token row groups done (partial-sum buffer parity)
     int ng1 = 0;      // one-token row groups done (group buffer, writer and phase)
+    uint32_t seen = 0xFu;  // bit b: this warp processed stage it - 1 - b (stages before 0 count as seen)
     for (int ci = 0; ci < p.n; ++ci) {
       const Call &c = sm.calls[ci];
       const int j0 = first_group(c), G = static_cast<int>(gridDim.x);
@@ -767,10 +802,11 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
           for (int m = 0; m < kMaxTok; ++m) acc[m] = 0;
           for (int s = 0; s < nslab; ++s, ++it) {
             const int st = it % kStages;
-            if (*abort_flag || !mbar_wait(smem_u32(&sm.full[st]), (it / kStages) & 1)) {
+            if (*abort_flag || !stage_ready(sm.full, sm.stage_tag, it, seen, abort_flag)) {
               *abort_flag = 1;
               break;
             }
+            seen = (seen << 1) | 1u;
             const int npc = pieces_in(rb, P, s);
             const uint32_t sb = ring + st * kStageBytes;
             if (s == 0) {
@@ -845,18 +881,18 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
       for (int j = j0; j < ngr; j += G) {
         if ((ng1 & 1) != team) {
           it += nslab;
+          seen = nslab >= 32 ? 0u : seen << nslab;
           ++ng1;
           continue;
         }
         int acc[4] = {0, 0, 0, 0}, acc2[4] = {0, 0, 0, 0};
         for (int s = 0; s < nslab; ++s, ++it) {
           const int st = it % kStages;
-          // (the stop flag is read only when the stage is not there yet)
-          if (!mbar_try_wait(smem_u32(&sm.full[st]), (it / kStages) & 1) &&
-              (*abort_flag || !mbar_wait_slow(smem_u32(&sm.full[st]), (it / kStages) & 1))) {
+          if (!stage_ready(sm.full, sm.stage_tag, it, seen, abort_flag)) {
             *abort_flag = 1;
             break;
           }
+          seen = (seen << 1) | 1u;
           const int npc = pieces_in(rb, P, s);
           const uint32_t sb = ring + st * kStageBytes;
           const uint32_t sbase = sb + lrow;
