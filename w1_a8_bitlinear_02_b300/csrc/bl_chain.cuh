@@ -188,8 +188,7 @@ struct Smem {
   uint64_t empty[kStages];
   uint64_t gbar[kGB];
   float fred[kCW];
-  int32_t gsum[kGB][kGroupRows];
-  int32_t msum[2][kMaxTok][kGroupRows];  // the same, many-token calls (added into)
+  int32_t gsum[kGB][kMaxTok][kGroupRows];  // by group buffer, token, row
   uint32_t seq_tag;
   int abort_flag;
   int stage_tag[kStages];  // the stage each ring slot was last armed for (written by its producer)
@@ -611,11 +610,12 @@ __device__ __forceinline__ void piece_multi(uint32_t waddr, uint32_t act, uint32
   }
 }
 
-// The pieces of one stage of a many-token call (this warp's: warp, warp + 16).
+// The pieces of one stage of a many-token call (this warp's: class cls,
+// cls + kTW, ...).
 template <int MT>
-__device__ __forceinline__ void stage_multi(uint32_t sbase, uint32_t abase, uint32_t tstride, int npc, int warp,
+__device__ __forceinline__ void stage_multi(uint32_t sbase, uint32_t abase, uint32_t tstride, int npc, int cls,
                                             int (&acc)[kMaxTok]) {
-  for (int pc = warp; pc < npc; pc += kCW)
+  for (int pc = cls; pc < npc; pc += kTW)
     piece_multi<MT>(sbase + static_cast<uint32_t>(pc * kPiece), abase + 64u * pc, tstride, acc);
 }
 
@@ -650,8 +650,7 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
     uint32_t *dst = reinterpret_cast<uint32_t *>(sm.calls);
     const int words = p.n * static_cast<int>(sizeof(Call) / 4);
     for (int w = tid; w < words; w += kThreads) dst[w] = src[w];
-    for (int i = tid; i < 2 * kMaxTok * kGroupRows; i += kThreads) (&sm.msum[0][0][0])[i] = 0;
-    for (int i = tid; i < kGB * kGroupRows; i += kThreads) (&sm.gsum[0][0])[i] = 0;
+    for (int i = tid; i < kGB * kMaxTok * kGroupRows; i += kThreads) (&sm.gsum[0][0][0])[i] = 0;
   }
   __syncthreads();
   volatile int *abort_flag = &sm.abort_flag;
@@ -744,8 +743,7 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
     // later calls' barriers.
     int it = 0;       // ring stage counter, in the producer's order
     int nbar = 0;     // grid barriers passed
-    int ng = 0;       // many-token row groups done (partial-sum buffer parity)
-    int ng1 = 0;      // one-token row groups done (group buffer, writer and phase)
+    int ng1 = 0;      // row groups done (team, group buffer, writer and phase)
     uint32_t seen = 0xFu;  // bit b: this warp processed stage it - 1 - b (stages before 0 count as seen)
     for (int ci = 0; ci < p.n; ++ci) {
       const Call &c = sm.calls[ci];
@@ -782,6 +780,14 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
       float *const yout = c.y;
       uint64_t *const mbo = c.mb_out;
       const uint32_t lrow = static_cast<uint32_t>(lane * kPiece * P);  // this lane's row in a stage
+      // Row groups alternate between the two teams of kTW warps (group ng1
+      // goes to team ng1 mod 2), so each warp takes more pieces of a stage
+      // for the same per-stage work; within its team a warp takes the slab
+      // pieces of class cls (p mod kTW == cls), rotated from call to call so
+      // the classes with one piece more fall to different warps.  A group's
+      // sums meet in a group buffer (gsum, gbar): no block barrier.
+      const int team = warp / kTW, tw = warp % kTW;
+      const int cls = (tw + ci) & (kTW - 1);
 
       if (MANY && M > 1) {
         // ---- many tokens (their codes come with the record in every stage)
@@ -796,7 +802,13 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
           xwv[m] = 0;
         }
         for (int j = j0; j < ngr; j += G) {
-          const int r0 = j * kGroupRows, h = N - r0 < kGroupRows ? N - r0 : kGroupRows;
+          if ((ng1 & 1) != team) {
+            it += nslab;
+            seen = nslab >= 32 ? 0u : seen << nslab;
+            ++ng1;
+            continue;
+          }
+          const int r0 = j * kGroupRows;
           int acc[kMaxTok];
 #pragma unroll
           for (int m = 0; m < kMaxTok; ++m) acc[m] = 0;
@@ -813,55 +825,59 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
 #pragma unroll
               for (int m = 0; m < kMaxTok; ++m)
                 if (m < M) {
+                  uint32_t x0, x1;
                   asm volatile("ld.shared.f32 %0, [%1];" : "=f"(cmv[m]) : "r"(sb + cofs + 4u * m) : "memory");
-                  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(xwv[m]) : "r"(sb + cofs + 64u + 64u * m + 4u * warp)
+                  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(x0) : "r"(sb + cofs + 64u + 64u * m + 4u * cls)
                                : "memory");
+                  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(x1)
+                               : "r"(sb + cofs + 64u + 64u * m + 4u * (cls + kTW))
+                               : "memory");
+                  xwv[m] = static_cast<int>(x0 + x1);
                 }
             }
             const uint32_t sbase = sb + lrow, abase = sb + cofs + static_cast<uint32_t>(H);
             switch (M) {
-              case 2: stage_multi<2>(sbase, abase, tstride, npc, warp, acc); break;
-              case 3: stage_multi<3>(sbase, abase, tstride, npc, warp, acc); break;
-              case 4: stage_multi<4>(sbase, abase, tstride, npc, warp, acc); break;
-              case 5: stage_multi<5>(sbase, abase, tstride, npc, warp, acc); break;
-              case 6: stage_multi<6>(sbase, abase, tstride, npc, warp, acc); break;
-              case 7: stage_multi<7>(sbase, abase, tstride, npc, warp, acc); break;
-              default: stage_multi<8>(sbase, abase, tstride, npc, warp, acc); break;
+              case 2: stage_multi<2>(sbase, abase, tstride, npc, cls, acc); break;
+              case 3: stage_multi<3>(sbase, abase, tstride, npc, cls, acc); break;
+              case 4: stage_multi<4>(sbase, abase, tstride, npc, cls, acc); break;
+              case 5: stage_multi<5>(sbase, abase, tstride, npc, cls, acc); break;
+              case 6: stage_multi<6>(sbase, abase, tstride, npc, cls, acc); break;
+              case 7: stage_multi<7>(sbase, abase, tstride, npc, cls, acc); break;
+              default: stage_multi<8>(sbase, abase, tstride, npc, cls, acc); break;
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&sm.empty[st]));
+            if (lane == 0) mbar_arrive_n(smem_u32(&sm.empty[st]), kTeams);
           }
-          // the 16 warps' sums meet by shared-memory adds into this group's
-          // buffer; one warp writes the rows and clears it for two groups on
-          const int pb = ng & 1;
+          // the team's sums meet in the group's buffer; its writing warp
+          // waits for them, writes the rows and clears the buffer
+          const int gb = ng1 & (kGB - 1);
 #pragma unroll
           for (int m = 0; m < kMaxTok; ++m)
-            if (m < M) atomicAdd(&sm.msum[pb][m][lane], acc[m] - xwv[m]);
-          named_bar(2, kC);
-          if (warp == (ng % kCW)) {
+            if (m < M) atomicAdd(&sm.gsum[gb][m][lane], acc[m] - xwv[m]);
+          __syncwarp();
+          if (lane == 0) mbar_arrive_n(smem_u32(&sm.gbar[gb]), kTeams);
+          if (tw == ((ng1 / kTeams) % kTW) && !*abort_flag) {
+            if (!mbar_wait(smem_u32(&sm.gbar[gb]), (ng1 / kGB) & 1)) {
+              *abort_flag = 1;
+              ++ng1;
+              continue;
+            }
 #pragma unroll
             for (int m = 0; m < kMaxTok; ++m)
               if (m < M) {
-                const int t = sm.msum[pb][m][lane];
-                sm.msum[pb][m][lane] = 0;
-                if (lane < h)
+                const int t = sm.gsum[gb][m][lane];
+                sm.gsum[gb][m][lane] = 0;
+                if (r0 + lane < N)
                   yout[static_cast<int64_t>(m) * N + r0 + lane] = __fmul_rn(static_cast<float>(t), cmv[m]);
               }
           }
-          ++ng;
+          ++ng1;
         }
         continue;
       }
 
       // ---- the activation codes, c and the warp's code sum: from the
-      // record (in each group's first stage) or quantised here.  Row groups
-      // alternate between the two teams of kTW warps (group ng1 goes to team
-      // ng1 mod 2), so each warp takes more pieces of a stage for the same
-      // per-stage work; within its team a warp takes the slab pieces of
-      // class cls (p mod kTW == cls), rotated from call to call so the
-      // classes with one piece more fall to different warps.
-      const int team = warp / kTW, tw = warp % kTW;
-      const int cls = (tw + ci) & (kTW - 1);
+      // record (in each group's first stage) or quantised here.
       float cm = 0.0f;
       int xw = 0;
       if (!has_rec) {
@@ -931,7 +947,7 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
         // warp waits for every thread's share, writes the rows and clears
         // the buffer
         const int gb = ng1 & (kGB - 1);
-        atomicAdd(&sm.gsum[gb][lane], (acc[0] + acc2[0]) + ((acc[1] + acc2[1]) >> 2) +
+        atomicAdd(&sm.gsum[gb][0][lane], (acc[0] + acc2[0]) + ((acc[1] + acc2[1]) >> 2) +
                                           ((acc[2] + acc2[2]) >> 4) + ((acc[3] + acc2[3]) >> 6) - xw);
         __syncwarp();  // orders the lanes' adds before lane 0's release
         if (lane == 0) mbar_arrive_n(smem_u32(&sm.gbar[gb]), kTeams);
@@ -943,8 +959,8 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
             ++ng1;
             continue;
           }
-          const int t = sm.gsum[gb][lane];
-          sm.gsum[gb][lane] = 0;
+          const int t = sm.gsum[gb][0][lane];
+          sm.gsum[gb][0][lane] = 0;
           const int r = j * kGroupRows + lane;
           if (r < N) {
             const float v = __fmul_rn(static_cast<float>(t), cm);
