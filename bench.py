@@ -277,6 +277,75 @@ def oracle_timing(items_host, budget_s: float):
             return el, nbytes, calls, oracle.get_threads()
 
 
+def oracle_table(wl, torch) -> list:
+    """The CPU oracle on bounded samples of every workload configuration, at
+    one thread and at all host threads (the cpu_baseline leg, --cpu-table):
+    weights packed and activations drawn on the host by the oracle and the
+    seeded generators; per entry the seconds per unit and the rate."""
+    import oracle
+
+    def rate(fn, min_s=0.5):
+        fn()
+        t0 = time.perf_counter()
+        n = 0
+        while True:
+            fn()
+            n += 1
+            el = time.perf_counter() - t0
+            if el >= min_s:
+                return el / n
+
+    def packed_host(mt):
+        W = wl.weight(mt.N, mt.K, mt.std, mt.seed, "cpu").numpy()
+        p, g = oracle.pack_weights(W)
+        del W
+        return p, float(g)
+
+    rows = []
+    all_threads = os.cpu_count() or 1
+    plans = []
+    t = wl.matrices("tiny")[0]
+    tp = packed_host(t)
+    tx = wl.activations(4, t.K, t.x_kind, t.seed + 500, "cpu", torch.float32).numpy()
+    plans.append(("1 tiny", "one forward, M=4, 256x512", [(tp, t.N, t.K, tx)], "GB/s"))
+    mats = wl.matrices(WORKLOAD, layers=1)
+    packs = [packed_host(mt) for mt in mats]
+    x1 = [wl.activations(1, mt.K, mt.x_kind, mt.seed + 500, "cpu", torch.bfloat16).float().numpy() for mt in mats]
+    plans.append(("2 decode M=1", "layer 0's four projections (QKV, O, up, down), M=1",
+                  [(p, mt.N, mt.K, x) for p, mt, x in zip(packs, mats, x1)], "GB/s"))
+    for M in (8, 16, 32, 64):
+        xm = [wl.activations(M, mt.K, "outliers1pct", mt.seed + 500, "cpu", torch.bfloat16).float().numpy()
+              for mt in mats]
+        plans.append((f"3 decode M={M}", f"layer 0's four projections, M={M}",
+                      [(p, mt.N, mt.K, x) for p, mt, x in zip(packs, mats, xm)], "GB/s"))
+    T = 16
+    for name, mt, kind in (("up", mats[2], "normal"), ("down", mats[3], "relu2")):
+        p = packs[2] if name == "up" else packs[3]
+        xt = wl.activations(T, mt.K, kind, mt.seed + 900, "cpu", torch.bfloat16).float().numpy()
+        plans.append((f"4 prefill {name}", f"{T} of the 2048 tokens (tokens are independent) on "
+                      f"{mt.N}x{mt.K}", [(p, mt.N, mt.K, xt)], "TOPS"))
+    big = wl.matrices("decode_100b", layers=1)
+    bpk = [packed_host(mt) for mt in big]
+    for M in (1, 8):
+        xb = [wl.activations(M, mt.K, "normal", mt.seed + 500, "cpu", torch.bfloat16).float().numpy() for mt in big]
+        plans.append((f"5 100B M={M}", f"layer 0's two matrices (28672x8192, 8192x28672), M={M}",
+                      [(p, mt.N, mt.K, x) for p, mt, x in zip(bpk, big, xb)], "GB/s"))
+    for cfg, sample, calls, unit in plans:
+        ent = {"config": cfg, "sample": sample, "unit": unit}
+        for th in (1, all_threads):
+            oracle.set_threads(th)
+            sec = rate(lambda: [oracle.forward_packed(p[0], p[1], N, K, x) for (p, N, K, x) in calls])
+            if unit == "GB/s":
+                v = sum(algorithmic_bytes(x.shape[0], N, K) for (_, N, K, x) in calls) / sec / 1e9
+            else:
+                v = sum(2.0 * x.shape[0] * N * K for (_, N, K, x) in calls) / sec / 1e12
+            ent[f"threads_{th}"] = {"s_per_sample": sec, unit: v}
+        rows.append(ent)
+        print(json.dumps(ent), file=sys.stderr, flush=True)
+    oracle.set_threads(all_threads)
+    return rows
+
+
 def host_items(items, limit: int):
     out = []
     for it in items[:limit]:
@@ -540,6 +609,8 @@ def run_ours(args, rank: int, world: int, local: int):
                         "sample": f"{ncalls} calls of the oracle's forward on layer 0's four "
                                   "projections at M=1 (host copies of the same packed weights "
                                   f"and activations), {el:.1f} s after {ORACLE_WARM_S} s of warm-up"}
+        if args.cpu_table:
+            cpu_baseline["table"] = oracle_table(wl, torch)
 
     if rank == 0:
         line = {
@@ -725,6 +796,24 @@ def run_extras(bl, wl, torch, device, stream, peaks, items2b, args):
             del packed, gamma, x, y, ws, xq, sc
         out["prefill_2b"] = pf
 
+        # the tiny configuration: one forward, M = 4, 256 x 512, fp32 x
+        t = wl.matrices("tiny")[0]
+        Wt = wl.weight(t.N, t.K, t.std, t.seed, device)
+        tp, tg = bl.bitlinear_pack_weights(Wt)
+        tx = wl.activations(4, t.K, t.x_kind, t.seed + 500, device, torch.float32)
+        ty = torch.empty((4, t.N), dtype=torch.float32, device=device)
+        gt = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            bl.bitlinear_forward(tp, tg, t.N, t.K, tx, y=ty)
+            stream.synchronize()
+            with torch.cuda.graph(gt, stream=stream):
+                for _ in range(100):
+                    bl.bitlinear_forward(tp, tg, t.N, t.K, tx, y=ty)
+            st = timed(gt.replay, max(3, min(args.steps, 50))) / 100
+        out["tiny"] = {"us_per_call": st * 1e6, "GB/s": algorithmic_bytes(4, t.N, t.K) / st / 1e9,
+                       "how": "100 dependent bitlinear_forward calls (M=4, 256x512, fp32 x) in one graph"}
+        del gt, Wt, tp, tg, tx, ty
+
         # 100B-class decode: 80 layers x {28672x8192, 8192x28672}, 9.4 GB
         # resident: M = 1 as one chain (independent inputs), as dependent and
         # as independent per-call launches; M = 8 dependent per-call launches
@@ -791,6 +880,8 @@ def main():
     ap.add_argument("--no-100b", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-table", action="store_true",
+                    help="also time the CPU oracle on every configuration at 1 and all threads")
     ap.add_argument("--profile", choices=sorted(PROFILE_CASES) + sorted(PROFILE_CHAINS),
                     help="run one case a few times untimed (for ncu) and exit")
     args = ap.parse_args()
