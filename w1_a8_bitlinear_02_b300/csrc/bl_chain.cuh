@@ -130,6 +130,7 @@ constexpr int kFlagBarrier = 4;   // every block finishes all earlier calls firs
 // codes for them (M x 31 x 64 bytes); their record header holds c[m] (fp32)
 // at 4m and the 16 warps' code sums of token m at 64 + 64m.
 constexpr int kMaxTok = 8;
+constexpr int kMmaTok = 5;  // calls of kMmaTok..kMaxTok tokens run their pieces on the tensor cores
 __host__ __device__ constexpr int header_bytes(int M) { return M > 1 ? ((64 + 64 * M + 127) / 128) * 128 : kHeader; }
 // a record: the header, then slab by slab each token's codes (64 per piece)
 __host__ __device__ constexpr int record_bytes(int rb, int M = 1) {
@@ -619,6 +620,40 @@ __device__ __forceinline__ void stage_multi(uint32_t sbase, uint32_t abase, uint
     piece_multi<MT>(sbase + static_cast<uint32_t>(pc * kPiece), abase + 64u * pc, tstride, acc);
 }
 
+// The pieces of one stage of a call of 5-8 tokens on the tensor cores
+// (legacy mma.sync, m16n8k32, u8 codes x s8 activation codes -> exact s32):
+// this warp's 16-row tile (trow = the tile's first row in the stage) and
+// piece class pcls (p mod 4).  Lane (g, t) = (lane / 4, lane % 4) holds word t
+// of rows g and g + 8 of each piece; plane i of a word (its bytes masked by
+// 3 << 2i, shifted down) is four codes c = q + 1 for k = 16t + 4i .. 16t + 4i + 3,
+// so planes 0-1 feed one MMA's A (fragment k 4t.. and 16 + 4t..) and planes
+// 2-3 the next; B is the same k range of token g's codes (one 16-byte load),
+// the 8 MMA columns being the tokens (columns past M are discarded).
+// d[0..1]: rows g, tokens 2t, 2t + 1; d[2..3]: row g + 8.
+__device__ __forceinline__ void stage_mma(uint32_t trow, uint32_t act, int npc, int pcls, int P, int lane,
+                                          int (&d)[4]) {
+  const int g = lane >> 2, t = lane & 3;
+  const uint32_t ra = trow + static_cast<uint32_t>(g * kPiece * P + 4 * t);
+  const uint32_t rbo = ra + static_cast<uint32_t>(8 * kPiece * P);
+  const uint32_t xa = act + static_cast<uint32_t>(16 * t);
+  for (int pc = pcls; pc < npc; pc += 4) {
+    uint32_t wa, wb;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(wa) : "r"(ra + static_cast<uint32_t>(pc * kPiece)));
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(wb) : "r"(rbo + static_cast<uint32_t>(pc * kPiece)));
+    const uint4 x = lds_u128(xa + 64u * pc);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t a0 = (wa >> (4 * h)) & 0x03030303u, a2 = (wa >> (4 * h + 2)) & 0x03030303u;
+      const uint32_t a1 = (wb >> (4 * h)) & 0x03030303u, a3 = (wb >> (4 * h + 2)) & 0x03030303u;
+      const uint32_t b0 = h ? x.z : x.x, b1 = h ? x.w : x.y;
+      asm volatile(
+          "mma.sync.aligned.m16n8k32.row.col.s32.u8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+          : "+r"(d[0]), "+r"(d[1]), "+r"(d[2]), "+r"(d[3])
+          : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    }
+  }
+}
+
 // MANY: the chain has calls of more than one token (a separate instantiation,
 // so single-token chains keep their register budget).
 // The register budget is set as for 20 warps (at most 96 registers a thread):
@@ -809,6 +844,59 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
             continue;
           }
           const int r0 = j * kGroupRows;
+          const int gb = ng1 & (kGB - 1);
+          if (M >= kMmaTok) {
+            // ---- 5-8 tokens: tensor cores, warp tw takes tile tw & 1 and
+            // piece class ((tw >> 1) + call) mod 4
+            const int tile = tw & 1, pcls = ((tw >> 1) + ci) & 3;
+            const int gg = lane >> 2, tt = lane & 3;
+            int d[4] = {0, 0, 0, 0};
+            int xs0 = 0, xs1 = 0;  // the code sums of tokens 2tt, 2tt + 1 over this warp's pieces
+            for (int s = 0; s < nslab; ++s, ++it) {
+              const int st = it % kStages;
+              if (*abort_flag || !stage_ready(sm.full, sm.stage_tag, it, seen, abort_flag)) {
+                *abort_flag = 1;
+                break;
+              }
+              seen = (seen << 1) | 1u;
+              const int npc = pieces_in(rb, P, s);
+              const uint32_t sb = ring + st * kStageBytes;
+              if (s == 0) {
+#pragma unroll
+                for (int m = 0; m < kMaxTok; ++m)
+                  if (m < M) asm volatile("ld.shared.f32 %0, [%1];" : "=f"(cmv[m]) : "r"(sb + cofs + 4u * m) : "memory");
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                  const int m = 2 * tt + q;
+                  int xs = 0;
+                  if (m < M) {
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                      uint32_t v;
+                      asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v)
+                                   : "r"(sb + cofs + 64u + 64u * m + 4u * (pcls + 4 * c4)) : "memory");
+                      xs += static_cast<int>(v);
+                    }
+                  }
+                  if (q == 0) xs0 = xs; else xs1 = xs;
+                }
+              }
+              stage_mma(sb + static_cast<uint32_t>(tile * 16 * kPiece * P),
+                        sb + cofs + static_cast<uint32_t>(H) + static_cast<uint32_t>(gg) * tstride, npc, pcls, P,
+                        lane, d);
+              __syncwarp();
+              if (lane == 0) mbar_arrive_n(smem_u32(&sm.empty[st]), kTeams);
+            }
+            const int row = tile * 16 + gg;
+            if (2 * tt < M) {
+              atomicAdd(&sm.gsum[gb][2 * tt][row], d[0] - xs0);
+              atomicAdd(&sm.gsum[gb][2 * tt][row + 8], d[2] - xs0);
+            }
+            if (2 * tt + 1 < M) {
+              atomicAdd(&sm.gsum[gb][2 * tt + 1][row], d[1] - xs1);
+              atomicAdd(&sm.gsum[gb][2 * tt + 1][row + 8], d[3] - xs1);
+            }
+          } else {
           int acc[kMaxTok];
 #pragma unroll
           for (int m = 0; m < kMaxTok; ++m) acc[m] = 0;
@@ -848,12 +936,12 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
             __syncwarp();
             if (lane == 0) mbar_arrive_n(smem_u32(&sm.empty[st]), kTeams);
           }
-          // the team's sums meet in the group's buffer; its writing warp
-          // waits for them, writes the rows and clears the buffer
-          const int gb = ng1 & (kGB - 1);
 #pragma unroll
           for (int m = 0; m < kMaxTok; ++m)
             if (m < M) atomicAdd(&sm.gsum[gb][m][lane], acc[m] - xwv[m]);
+          }
+          // the team's sums meet in the group's buffer; its writing warp
+          // waits for them, writes the rows and clears the buffer
           __syncwarp();
           if (lane == 0) mbar_arrive_n(smem_u32(&sm.gbar[gb]), kTeams);
           if (tw == ((ng1 / kTeams) % kTW) && !*abort_flag) {
