@@ -978,7 +978,11 @@ bl_status bitlinear_forward_chain(const bl_chain_call *calls, int n, void *ws, s
   if (s != BL_OK) return s;
   bool many = false;
   for (int i = 0; i < n; ++i) many = many || toks(calls[i]) > 1;
-  void (*kern)(chain::Params) = many ? &chain::chain_kernel<true> : &chain::chain_kernel<false>;
+  bool dep = false;  // a call whose input an earlier call writes (quantised in the block)
+  for (int i = 0; i < n; ++i) dep = dep || tc.calls[i].rec == nullptr;
+  void (*kern)(chain::Params) =
+      many ? (dep ? &chain::chain_kernel<true, true> : &chain::chain_kernel<true, false>)
+           : (dep ? &chain::chain_kernel<false, true> : &chain::chain_kernel<false, false>);
   s = ensure_smem(dev, reinterpret_cast<const void *>(kern), chain::kSmemBytes);
   if (s != BL_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

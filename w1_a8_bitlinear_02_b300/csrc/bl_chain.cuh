@@ -67,6 +67,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cstdint>
+#include <type_traits>
 
 #include "bl_pack_quant.cuh"
 #include "bl_ptx.cuh"
@@ -189,6 +190,7 @@ struct Smem {
   uint64_t empty[kStages];
   uint64_t gbar[kGB];
   float fred[kCW];
+  int xcls[2][kCW];  // code sums of in-block inputs by piece class (p mod 16), by call parity
   int32_t gsum[kGB][kMaxTok][kGroupRows];  // by group buffer, token, row
   uint32_t seq_tag;
   int abort_flag;
@@ -427,7 +429,8 @@ __device__ __forceinline__ float act_of(const Call &c, float v) {
   return (c.flags & kFlagRelu2) ? relu2f(v) : v;
 }
 
-__device__ __forceinline__ void put_codes8(uint32_t xs, int v, const float (&f)[8], float s) {
+// Codes of vector v into the codes area; returns their sum.
+__device__ __forceinline__ int put_codes8(uint32_t xs, int v, const float (&f)[8], float s) {
   uint32_t lo = 0, hi = 0;
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
@@ -435,6 +438,7 @@ __device__ __forceinline__ void put_codes8(uint32_t xs, int v, const float (&f)[
     hi |= (static_cast<uint32_t>(quant_one(f[e + 4], s)) & 0xFFu) << (8 * e);
   }
   sts_u64(xs + 8 * v, lo, hi);
+  return dp4a_us(0x01010101u, hi, dp4a_us(0x01010101u, lo, 0));
 }
 
 // Vectors of 8 the call's input is read in (0: element by element).
@@ -461,19 +465,37 @@ __device__ __forceinline__ void piece(uint32_t waddr, uint32_t act, int (&a)[4])
   }
 }
 
-// Quantise the input of call c in every block (it depends on earlier calls)
-// into the in-block codes area `slot`: values polled from output words or
-// read after the grid barrier, per-token absmax over the block, codes
-// zero-padded to the end of the row's last piece and c = gamma / s into the
-// area's header; xw = the code sum of piece class cls (slab pieces p with
-// p mod kTW == cls).  Returns false (in every thread) when the block must
-// stop.
+// The pieces of one stage of a one-token group taken by this warp: class
+// pcls, pcls + STEP, ..., two at a time in separate accumulators so their
+// loads and dp4a chains overlap.
+template <int STEP>
+__device__ __forceinline__ void stage_one(uint32_t sbase, uint32_t abase, int pcls, int npc, int (&acc)[4],
+                                          int (&acc2)[4]) {
+  int pc = pcls;
+  for (; pc + STEP < npc; pc += 2 * STEP) {
+    piece(sbase + static_cast<uint32_t>(pc * kPiece), abase + 64u * pc, acc);
+    piece(sbase + static_cast<uint32_t>((pc + STEP) * kPiece), abase + 64u * (pc + STEP), acc2);
+  }
+  if (pc < npc) piece(sbase + static_cast<uint32_t>(pc * kPiece), abase + 64u * pc, acc);
+}
+
+// Quantise the input of call c in every block that has rows of it (it
+// depends on earlier calls) into the in-block codes area `slot`: values
+// polled from output words or read after the grid barrier, per-token absmax
+// over the block, codes zero-padded to the end of the row's last piece and
+// c = gamma / s into the area's header; xw = the code sum of piece class cls
+// (slab pieces p with p mod 16 == cls), added up per class while the codes
+// are written (nq: the block's count of such calls, picking the class-sum
+// buffer).  Returns false (in every thread) when the block must stop.
 __device__ __forceinline__ bool quantise_in_block(const Call &c, uint32_t slot, uint32_t want, int tid, int cls,
-                                                  Smem &sm, volatile int *abort_flag, int &xw) {
+                                                  int nq, Smem &sm, volatile int *abort_flag, int &xw) {
   const int warp = tid >> 5, lane = tid & 31;
   const uint32_t xs = slot + kHeader;
   const int nv = vec_count(c);
   const bool in_regs = nv <= kJM * kC;
+  const float gam = __ldg(c.gamma);  // off the critical path: needed after the last value arrives
+  int *const xcls = sm.xcls[nq & 1];  // last used two such calls ago
+  const int P = c.P;
   float xv[kJM][8];
   bool timed_out = false;
   float a = 0.0f;
@@ -531,6 +553,7 @@ __device__ __forceinline__ bool quantise_in_block(const Call &c, uint32_t slot, 
   if (timed_out) atomicOr(&g_dev_error, kDevErrTimeout);
   a = warp_max_nonneg(a);
   if (lane == 0) sm.fred[warp] = a;
+  if (tid < kCW) xcls[tid] = 0;
   if (named_bar_or(1, kC, timed_out || *abort_flag)) return false;
   a = sm.fred[0];
 #pragma unroll
@@ -538,11 +561,12 @@ __device__ __forceinline__ bool quantise_in_block(const Call &c, uint32_t slot, 
   const float s = act_scale(a);
   // codes (every value is present now: a second pass reads plainly), then
   // zeros from K to the end of the last slab
+  // (vector v lies in global piece v / 8, slab piece (v / 8) mod P)
   if (in_regs) {
 #pragma unroll
     for (int j = 0; j < kJM; ++j) {
       const int v = tid + j * kC;
-      if (v < nv) put_codes8(xs, v, xv[j], s);
+      if (v < nv) atomicAdd(&xcls[((v >> 3) % P) & (kCW - 1)], put_codes8(xs, v, xv[j], s));
     }
   } else {
     for (int v = tid; v < nv; v += kC) {
@@ -550,7 +574,7 @@ __device__ __forceinline__ bool quantise_in_block(const Call &c, uint32_t slot, 
       load_vec8(c, v, want, f);
 #pragma unroll
       for (int e = 0; e < 8; ++e) f[e] = act_of(c, f[e]);
-      put_codes8(xs, v, f, s);
+      atomicAdd(&xcls[((v >> 3) % P) & (kCW - 1)], put_codes8(xs, v, f, s));
     }
   }
   const int kz = (c.K + 15) & ~15;
@@ -560,31 +584,14 @@ __device__ __forceinline__ bool quantise_in_block(const Call &c, uint32_t slot, 
       float f;
       load_one(c, k, want, f);
       q = quant_one(act_of(c, f), s);
+      atomicAdd(&xcls[((k >> 6) % P) & (kCW - 1)], q);
     }
     sts_u8(xs + k, static_cast<uint32_t>(q) & 0xFFu);
   }
   for (int k = kz + 16 * tid; k < 4 * c.rb; k += 16 * kC) sts_u128(xs + k, 0u, 0u, 0u, 0u);
-  if (tid == 0) asm volatile("st.shared.f32 [%0], %1;" ::"r"(slot), "f"(__fdiv_rn(__ldg(c.gamma), s)) : "memory");
+  if (tid == 0) asm volatile("st.shared.f32 [%0], %1;" ::"r"(slot), "f"(__fdiv_rn(gam, s)) : "memory");
   named_bar(1, kC);
-  // X of piece class cls: the sum of the codes of slab pieces cls, cls + kTW,
-  // ... of every slab, a piece per lane at a time
-  const int npieces = c.rb / kPiece, P = c.P, per = (P + kTW - 1) / kTW;
-  xw = 0;
-  for (int idx = lane; idx < per * c.ns; idx += 32) {
-    const int p = cls + kTW * (idx % per), g = (idx / per) * P + p;
-    if (p < P && g < npieces) {
-      const uint32_t act = xs + static_cast<uint32_t>(64 * g);
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const uint4 v = lds_u128(act + 16 * q4);
-        xw = dp4a_us(0x01010101u, v.x, xw);
-        xw = dp4a_us(0x01010101u, v.y, xw);
-        xw = dp4a_us(0x01010101u, v.z, xw);
-        xw = dp4a_us(0x01010101u, v.w, xw);
-      }
-    }
-  }
-  xw = __reduce_add_sync(0xffffffffu, xw);
+  xw = xcls[cls];
   return true;
 }
 
@@ -659,7 +666,10 @@ __device__ __forceinline__ void stage_mma(uint32_t trow, uint32_t act, int npc, 
 // The register budget is set as for 20 warps (at most 96 registers a thread):
 // with 18 warps, two of the four schedulers hold 5 warps, and each
 // scheduler's share of the register file must fit 5 x 32 x the count.
-template <bool MANY>
+// DEP: the chain has calls whose input is quantised in the block (an
+// earlier call writes it); only those take the all-warps form of a group,
+// so chains without them keep the streaming form's register allocation.
+template <bool MANY, bool DEP>
 __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant__ Params p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -779,6 +789,7 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
     int it = 0;       // ring stage counter, in the producer's order
     int nbar = 0;     // grid barriers passed
     int ng1 = 0;      // row groups done (team, group buffer, writer and phase)
+    int nq = 0;       // calls whose input this block quantised
     uint32_t seen = 0xFu;  // bit b: this warp processed stage it - 1 - b (stages before 0 count as seen)
     for (int ci = 0; ci < p.n; ++ci) {
       const Call &c = sm.calls[ci];
@@ -965,25 +976,35 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
       }
 
       // ---- the activation codes, c and the warp's code sum: from the
-      // record (in each group's first stage) or quantised here.
+      // record (in each group's first stage) or quantised here.  A call whose
+      // input is quantised here waits for an earlier call, so its latency
+      // counts: all 16 warps take each of its groups (pieces of class p mod 16).
+      const bool all = DEP && !has_rec;
+      const int pcls = all ? ((warp + ci) & (kCW - 1)) : cls;
       float cm = 0.0f;
       int xw = 0;
       if (!has_rec) {
         // the area is rewritten only after the block barrier inside, which
         // every warp reaches once it is done with the earlier calls
-        if (!quantise_in_block(c, inb, seq_tag | static_cast<uint32_t>(c.src + 1), tid, cls, sm, abort_flag, xw)) {
+        if (!quantise_in_block(c, inb, seq_tag | static_cast<uint32_t>(c.src + 1), tid, pcls, nq, sm, abort_flag,
+                               xw)) {
           *abort_flag = 1;
           break;
         }
+        ++nq;
         asm volatile("ld.shared.f32 %0, [%1];" : "=f"(cm) : "r"(inb) : "memory");
       }
       const int nslab = c.ns;
       const uint32_t tag = seq_tag | static_cast<uint32_t>(ci + 1);
 
       // ---- row groups: one lane per row, the slabs' pieces split over the
-      // warps of the group's team (the other team moves on to its next group)
+      // warps of the group's team (the other team moves on to its next group),
+      // or over all warps (ALL); one instantiation each, so the streaming form
+      // keeps its register allocation
+      auto groups = [&](auto all_c) {
+      constexpr bool ALL = decltype(all_c)::value;
       for (int j = j0; j < ngr; j += G) {
-        if ((ng1 & 1) != team) {
+        if (!ALL && (ng1 & 1) != team) {
           it += nslab;
           seen = nslab >= 32 ? 0u : seen << nslab;
           ++ng1;
@@ -1000,8 +1021,8 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
           const int npc = pieces_in(rb, P, s);
           const uint32_t sb = ring + st * kStageBytes;
           const uint32_t sbase = sb + lrow;
-          const uint32_t abase = has_rec ? sb + codes_ofs(1) + kHeader : inb + kHeader + static_cast<uint32_t>(s * 64 * P);
-          if (has_rec && s == 0) {
+          const uint32_t abase = !ALL ? sb + codes_ofs(1) + kHeader : inb + kHeader + static_cast<uint32_t>(s * 64 * P);
+          if (!ALL && s == 0) {
             // c and X of class cls (the header holds the sums of the 16
             // classes p mod 16; classes cls and cls + kTW make p mod kTW)
             uint32_t x0, x1;
@@ -1011,24 +1032,11 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
                          : "memory");
             xw = static_cast<int>(x0 + x1);
           }
-          // two pieces at a time, in separate accumulators, so their loads
-          // and dp4a chains overlap
-          int pc = cls;
-          for (; pc + kTW < npc; pc += 2 * kTW) {
-            const uint32_t w0 = sbase + static_cast<uint32_t>(pc * kPiece);
-            const int pc1 = pc + kTW;
-            const uint32_t w1 = sbase + static_cast<uint32_t>(pc1 * kPiece);
-            piece(w0, abase + 64u * pc, acc);
-            piece(w1, abase + 64u * pc1, acc2);
-          }
-          if (pc < npc) {
-            const uint32_t w0 = sbase + static_cast<uint32_t>(pc * kPiece);
-            piece(w0, abase + 64u * pc, acc);
-          }
+          stage_one<ALL ? kCW : kTW>(sbase, abase, pcls, npc, acc, acc2);
           // the stage's empty barrier counts kCW arrivals: a team's warps
           // arrive twice each
           __syncwarp();
-          if (lane == 0) mbar_arrive_n(smem_u32(&sm.empty[st]), kTeams);
+          if (lane == 0) mbar_arrive_n(smem_u32(&sm.empty[st]), ALL ? 1u : static_cast<uint32_t>(kTeams));
         }
         // the warps' sums meet in the group's buffer (no block barrier: a
         // warp done with its share goes on to the next group); the writing
@@ -1038,10 +1046,10 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
         atomicAdd(&sm.gsum[gb][0][lane], (acc[0] + acc2[0]) + ((acc[1] + acc2[1]) >> 2) +
                                           ((acc[2] + acc2[2]) >> 4) + ((acc[3] + acc2[3]) >> 6) - xw);
         __syncwarp();  // orders the lanes' adds before lane 0's release
-        if (lane == 0) mbar_arrive_n(smem_u32(&sm.gbar[gb]), kTeams);
+        if (lane == 0) mbar_arrive_n(smem_u32(&sm.gbar[gb]), ALL ? 1u : static_cast<uint32_t>(kTeams));
         // (once the block is stopping, nothing more is waited for or written;
         // every warp still walks the same calls, so later block barriers match)
-        if (tw == ((ng1 / kTeams) % kTW) && !*abort_flag) {
+        if ((ALL ? warp == (ng1 % kCW) : tw == ((ng1 / kTeams) % kTW)) && !*abort_flag) {
           if (!mbar_wait(smem_u32(&sm.gbar[gb]), (ng1 / kGB) & 1)) {
             *abort_flag = 1;
             ++ng1;
@@ -1058,6 +1066,11 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
         }
         ++ng1;
       }
+      };
+      if (all)
+        groups(std::true_type{});
+      else
+        groups(std::false_type{});
     }
     __syncwarp();
   }
