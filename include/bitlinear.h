@@ -302,7 +302,7 @@ BL_API bl_status bitlinear_forward_noalloc(const uint8_t *packed, const float *g
  *   y              [M, N] float out, device, 4-byte aligned; must not overlap
  *                  this call's x, packed or gamma.
  *   N, K           sizes; N <= 2^30, K <= 32768.
- *   M              tokens, 1..8 (0 counts as 1).  A call of more than one
+ *   M              tokens, 1..16 (0 counts as 1).  A call of more than one
  *                  token must read an x that no earlier call of the chain
  *                  writes (its input is quantised before the chain starts);
  *                  its y is not passed on by output words.

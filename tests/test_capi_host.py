@@ -204,7 +204,7 @@ def test_chain_invalid_arguments_return_status(lib):
                      (dict(N=0), capi.BL_ERR_SHAPE), (dict(x_dtype=7), capi.BL_ERR_DTYPE),
                      (dict(act=5), capi.BL_ERR_SHAPE), (dict(packed=odd), capi.BL_ERR_ALIGN),
                      (dict(y=fake + 64), capi.BL_ERR_SHAPE),  # y over its own x
-                     (dict(M=9), capi.BL_ERR_SHAPE)):
+                     (dict(M=17), capi.BL_ERR_SHAPE)):
         kw.setdefault("y", 0x900000)
         p2, keep2 = chain(**kw)
         assert lib.bitlinear_forward_chain(p2, 1, ws, 256, None) == want, kw

@@ -375,15 +375,16 @@ def test_chain_subrange_inputs_and_long_rows(bl):
 
 
 def test_chain_many_tokens(bl):
-    """Calls of 2 to 8 tokens (independent inputs, quantised ahead; stages of
-    at most 31 pieces; 2-4 tokens on dp4a, 5-8 on the tensor cores) mixed with
+    """Calls of 2 to 16 tokens (independent inputs, quantised ahead; stages of
+    at most 31 or 23 pieces; 2-4 tokens on dp4a, 5-16 on the tensor cores) mixed with
     single-token calls, ragged N and K, bf16 and fp32 inputs, a squared-ReLU
     input, every ~2B projection at 8 tokens and a five-slab row at 6 tokens;
     the chain runs twice on one workspace and each output equals the oracle's."""
     specs = [(300, 1000, 2, torch.bfloat16, 0), (3840, 2560, 8, torch.bfloat16, 0), (2560, 2560, 8, torch.bfloat16, 0),
              (6912, 2560, 8, torch.bfloat16, 0), (2560, 6912, 8, torch.bfloat16, 1), (513, 100, 3, torch.float32, 0),
              (700, 2000, 1, torch.bfloat16, 0), (129, 4608, 5, torch.float32, 1), (1000, 64, 7, torch.bfloat16, 0),
-             (4736, 9000, 6, torch.bfloat16, 0), (333, 512, 4, torch.bfloat16, 0)]
+             (4736, 9000, 6, torch.bfloat16, 0), (333, 512, 4, torch.bfloat16, 0),
+             (2560, 6912, 16, torch.bfloat16, 1), (3840, 2560, 12, torch.bfloat16, 0), (777, 1000, 9, torch.float32, 0)]
     mats = [pack_both(bl, N, K, 0.02, 950 + i) for i, (N, K, _, _, _) in enumerate(specs)]
     calls, xs, ys = [], [], []
     for i, ((N, K, M, dt, act), (packed, gamma, _, _)) in enumerate(zip(specs, mats)):

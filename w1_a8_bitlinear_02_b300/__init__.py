@@ -339,7 +339,7 @@ def chain_workspace(calls, device) -> torch.Tensor:
 def bitlinear_forward_chain(calls, workspace: torch.Tensor | None = None) -> None:
     """A decode chain of single-token forwards in one launch.
 
-    calls: sequence of dicts with packed, gamma, x [M, K] (fp32 / bf16, M <= 8),
+    calls: sequence of dicts with packed, gamma, x [M, K] (fp32 / bf16, M <= 16),
     y [M, N] fp32 (written), N, K and optionally act (capi.BL_ACT_RELU2 for relu2(x))
     and wait_prev (default 0: the library orders dependent calls itself).
     workspace: from chain_workspace (zero-filled before its first use; reuse it

@@ -88,9 +88,10 @@ constexpr int kGroupRows = 32;            // rows per group at most: one per lan
 constexpr int kPiece = 16;                // packed bytes of a piece (64 weights)
 constexpr int kJM = 2;                    // x vectors of 8 per consumer thread kept in registers (K <= 8192)
 // Pieces per slab: odd (conflict-free rows, see above), at most 65 for one
-// token and 31 for more (their stage also holds every token's codes); a row
+// token, 31 for 2-8 and 23 for 9-16 (their stage also holds every token's
+// codes); a row
 // of np pieces takes the fewest slabs the cap allows, split evenly.
-__host__ __device__ constexpr int piece_cap(int M) { return M > 1 ? 31 : 65; }
+__host__ __device__ constexpr int piece_cap(int M) { return M > 8 ? 23 : (M > 1 ? 31 : 65); }
 __host__ __device__ constexpr int slab_pieces(int rb, int M = 1) {
   return ((rb / kPiece + (rb / kPiece + piece_cap(M) - 1) / piece_cap(M) - 1) /
           ((rb / kPiece + piece_cap(M) - 1) / piece_cap(M))) | 1;
@@ -111,7 +112,7 @@ constexpr int kInBlockBytes = kHeader + kMaxK;
 __host__ __device__ constexpr int codes_ofs(int M) { return kGroupRows * kPiece * piece_cap(M); }
 constexpr int kStageBytes = 37 * 1024;
 constexpr int kStages = 4;
-constexpr int kSmemFixed = 30 * 1024;     // barriers, partial sums and the call table
+constexpr int kSmemFixed = 40 * 1024;     // barriers, partial sums and the call table
 constexpr int kSmemBytes = 1024 + kSmemFixed + kStages * kStageBytes + kInBlockBytes;
 
 // Control words at the start of the workspace (bytes 0..255), then the
@@ -126,21 +127,24 @@ constexpr int kFlagBf16 = 1;      // x is bf16 (else fp32)
 constexpr int kFlagRelu2 = 2;     // quantise relu2(x)
 constexpr int kFlagBarrier = 4;   // every block finishes all earlier calls first
 
-// Calls of more than one token (up to kMaxTok) use slabs of at most 31
+// Calls of more than one token (up to kMaxTok) use slabs of at most 31 (23)
 // pieces, so a stage holds the weights (at most 15.5 KB) and every token's
 // codes for them (M x 31 x 64 bytes); their record header holds c[m] (fp32)
 // at 4m and the 16 warps' code sums of token m at 64 + 64m.
-constexpr int kMaxTok = 8;
+constexpr int kMaxTok = 16;
 constexpr int kMmaTok = 5;  // calls of kMmaTok..kMaxTok tokens run their pieces on the tensor cores
+constexpr int kDp4aTok = kMmaTok - 1;  // 2..kDp4aTok tokens on dp4a
 __host__ __device__ constexpr int header_bytes(int M) { return M > 1 ? ((64 + 64 * M + 127) / 128) * 128 : kHeader; }
 // a record: the header, then slab by slab each token's codes (64 per piece)
 __host__ __device__ constexpr int record_bytes(int rb, int M = 1) {
   return header_bytes(M) + slabs_of(rb, M) * M * 64 * slab_pieces(rb, M);
 }
 static_assert(codes_ofs(1) + kHeader + 64 * piece_cap(1) <= kStageBytes, "a stage of a one-token call");
+static_assert(codes_ofs(8) + header_bytes(8) + 8 * 64 * piece_cap(8) <= kStageBytes, "a stage of 8 tokens");
 static_assert(codes_ofs(kMaxTok) + header_bytes(kMaxTok) + kMaxTok * 64 * piece_cap(kMaxTok) <= kStageBytes,
               "a stage of a many-token call");
-static_assert(kStageBytes % 1024 == 0 && codes_ofs(1) % 128 == 0 && codes_ofs(kMaxTok) % 128 == 0,
+static_assert(kStageBytes % 1024 == 0 && codes_ofs(1) % 128 == 0 && codes_ofs(8) % 128 == 0 &&
+                  codes_ofs(kMaxTok) % 128 == 0,
               "stage and codes alignment");
 
 struct Call {
@@ -192,6 +196,7 @@ struct Smem {
   float fred[kCW];
   int xcls[2][kCW];  // code sums of in-block inputs by piece class (p mod 16), by call parity
   int32_t gsum[kGB][kMaxTok][kGroupRows];  // by group buffer, token, row
+  float gcm[kGB][kMaxTok];                 // the tokens' output scales c, by group buffer
   uint32_t seq_tag;
   int abort_flag;
   int stage_tag[kStages];  // the stage each ring slot was last armed for (written by its producer)
@@ -599,7 +604,7 @@ __device__ __forceinline__ bool quantise_in_block(const Call &c, uint32_t slot, 
 // at act + m * tstride, broadcast): the codes are shifted down once per word
 // and shared by the tokens; acc[m] += sum c * x.
 template <int MT>
-__device__ __forceinline__ void piece_multi(uint32_t waddr, uint32_t act, uint32_t tstride, int (&acc)[kMaxTok]) {
+__device__ __forceinline__ void piece_multi(uint32_t waddr, uint32_t act, uint32_t tstride, int (&acc)[kDp4aTok]) {
   const uint4 w = lds_u128(waddr);
   const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
   uint32_t cw[16];
@@ -622,7 +627,7 @@ __device__ __forceinline__ void piece_multi(uint32_t waddr, uint32_t act, uint32
 // cls + kTW, ...).
 template <int MT>
 __device__ __forceinline__ void stage_multi(uint32_t sbase, uint32_t abase, uint32_t tstride, int npc, int cls,
-                                            int (&acc)[kMaxTok]) {
+                                            int (&acc)[kDp4aTok]) {
   for (int pc = cls; pc < npc; pc += kTW)
     piece_multi<MT>(sbase + static_cast<uint32_t>(pc * kPiece), abase + 64u * pc, tstride, acc);
 }
@@ -636,9 +641,12 @@ __device__ __forceinline__ void stage_multi(uint32_t sbase, uint32_t abase, uint
 // so planes 0-1 feed one MMA's A (fragment k 4t.. and 16 + 4t..) and planes
 // 2-3 the next; B is the same k range of token g's codes (one 16-byte load),
 // the 8 MMA columns being the tokens (columns past M are discarded).
-// d[0..1]: rows g, tokens 2t, 2t + 1; d[2..3]: row g + 8.
-__device__ __forceinline__ void stage_mma(uint32_t trow, uint32_t act, int npc, int pcls, int P, int lane,
-                                          int (&d)[4]) {
+// d[4u + 0..1]: row g, tokens 8u + 2t, 8u + 2t + 1; d[4u + 2..3]: row g + 8
+// (u: the token tile, NT tiles of 8 tokens, sharing the weight fragments;
+// tile u's codes are act + 8u * tstride).
+template <int NT>
+__device__ __forceinline__ void stage_mma(uint32_t trow, uint32_t act, uint32_t tstride, int npc, int pcls, int P,
+                                          int lane, int (&d)[8]) {
   const int g = lane >> 2, t = lane & 3;
   const uint32_t ra = trow + static_cast<uint32_t>(g * kPiece * P + 4 * t);
   const uint32_t rbo = ra + static_cast<uint32_t>(8 * kPiece * P);
@@ -647,16 +655,21 @@ __device__ __forceinline__ void stage_mma(uint32_t trow, uint32_t act, int npc, 
     uint32_t wa, wb;
     asm volatile("ld.shared.u32 %0, [%1];" : "=r"(wa) : "r"(ra + static_cast<uint32_t>(pc * kPiece)));
     asm volatile("ld.shared.u32 %0, [%1];" : "=r"(wb) : "r"(rbo + static_cast<uint32_t>(pc * kPiece)));
-    const uint4 x = lds_u128(xa + 64u * pc);
+    uint4 x[NT];
+#pragma unroll
+    for (int u = 0; u < NT; ++u) x[u] = lds_u128(xa + 8u * u * tstride + 64u * pc);
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const uint32_t a0 = (wa >> (4 * h)) & 0x03030303u, a2 = (wa >> (4 * h + 2)) & 0x03030303u;
       const uint32_t a1 = (wb >> (4 * h)) & 0x03030303u, a3 = (wb >> (4 * h + 2)) & 0x03030303u;
-      const uint32_t b0 = h ? x.z : x.x, b1 = h ? x.w : x.y;
-      asm volatile(
-          "mma.sync.aligned.m16n8k32.row.col.s32.u8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-          : "+r"(d[0]), "+r"(d[1]), "+r"(d[2]), "+r"(d[3])
-          : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+#pragma unroll
+      for (int u = 0; u < NT; ++u) {
+        const uint32_t b0 = h ? x[u].z : x[u].x, b1 = h ? x[u].w : x[u].y;
+        asm volatile(
+            "mma.sync.aligned.m16n8k32.row.col.s32.u8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+            : "+r"(d[4 * u + 0]), "+r"(d[4 * u + 1]), "+r"(d[4 * u + 2]), "+r"(d[4 * u + 3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+      }
     }
   }
 }
@@ -840,13 +853,6 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
         const int H = header_bytes(M), nslab = c.ns;
         const uint32_t cofs = static_cast<uint32_t>(codes_ofs(M));
         const uint32_t tstride = static_cast<uint32_t>(64 * P);
-        float cmv[kMaxTok];  // the tokens' output scales (used by the writing warp)
-        int xwv[kMaxTok];
-#pragma unroll
-        for (int m = 0; m < kMaxTok; ++m) {
-          cmv[m] = 0.0f;
-          xwv[m] = 0;
-        }
         for (int j = j0; j < ngr; j += G) {
           if ((ng1 & 1) != team) {
             it += nslab;
@@ -857,12 +863,12 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
           const int r0 = j * kGroupRows;
           const int gb = ng1 & (kGB - 1);
           if (M >= kMmaTok) {
-            // ---- 5-8 tokens: tensor cores, warp tw takes tile tw & 1 and
-            // piece class ((tw >> 1) + call) mod 4
-            const int tile = tw & 1, pcls = ((tw >> 1) + ci) & 3;
+            // ---- 5-16 tokens: tensor cores, warp tw takes tile tw & 1 and
+            // piece class ((tw >> 1) + call) mod 4; tokens in tiles of 8
+            const int tile = tw & 1, pcls4 = ((tw >> 1) + ci) & 3;
             const int gg = lane >> 2, tt = lane & 3;
-            int d[4] = {0, 0, 0, 0};
-            int xs0 = 0, xs1 = 0;  // the code sums of tokens 2tt, 2tt + 1 over this warp's pieces
+            int d[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+            int xs[4] = {0, 0, 0, 0};  // code sums of tokens 8u + 2tt + q over this warp's pieces (u, q)
             for (int s = 0; s < nslab; ++s, ++it) {
               const int st = it % kStages;
               if (*abort_flag || !stage_ready(sm.full, sm.stage_tag, it, seen, abort_flag)) {
@@ -873,86 +879,88 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
               const int npc = pieces_in(rb, P, s);
               const uint32_t sb = ring + st * kStageBytes;
               if (s == 0) {
+                if (tw == 0 && lane < M)
+                  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(sm.gcm[gb][lane]) : "r"(sb + cofs + 4u * lane)
+                               : "memory");
 #pragma unroll
-                for (int m = 0; m < kMaxTok; ++m)
-                  if (m < M) asm volatile("ld.shared.f32 %0, [%1];" : "=f"(cmv[m]) : "r"(sb + cofs + 4u * m) : "memory");
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                  const int m = 2 * tt + q;
-                  int xs = 0;
+                for (int e = 0; e < 4; ++e) {
+                  const int m = 8 * (e >> 1) + 2 * tt + (e & 1);
+                  int x = 0;
                   if (m < M) {
 #pragma unroll
                     for (int c4 = 0; c4 < 4; ++c4) {
                       uint32_t v;
                       asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v)
-                                   : "r"(sb + cofs + 64u + 64u * m + 4u * (pcls + 4 * c4)) : "memory");
-                      xs += static_cast<int>(v);
+                                   : "r"(sb + cofs + 64u + 64u * m + 4u * (pcls4 + 4 * c4)) : "memory");
+                      x += static_cast<int>(v);
                     }
                   }
-                  if (q == 0) xs0 = xs; else xs1 = xs;
+                  xs[e] = x;
                 }
               }
-              stage_mma(sb + static_cast<uint32_t>(tile * 16 * kPiece * P),
-                        sb + cofs + static_cast<uint32_t>(H) + static_cast<uint32_t>(gg) * tstride, npc, pcls, P,
-                        lane, d);
+              const uint32_t trow = sb + static_cast<uint32_t>(tile * 16 * kPiece * P);
+              const uint32_t act = sb + cofs + static_cast<uint32_t>(H) + static_cast<uint32_t>(gg) * tstride;
+              if (M > 8)
+                stage_mma<2>(trow, act, tstride, npc, pcls4, P, lane, d);
+              else
+                stage_mma<1>(trow, act, tstride, npc, pcls4, P, lane, d);
               __syncwarp();
               if (lane == 0) mbar_arrive_n(smem_u32(&sm.empty[st]), kTeams);
             }
             const int row = tile * 16 + gg;
-            if (2 * tt < M) {
-              atomicAdd(&sm.gsum[gb][2 * tt][row], d[0] - xs0);
-              atomicAdd(&sm.gsum[gb][2 * tt][row + 8], d[2] - xs0);
-            }
-            if (2 * tt + 1 < M) {
-              atomicAdd(&sm.gsum[gb][2 * tt + 1][row], d[1] - xs1);
-              atomicAdd(&sm.gsum[gb][2 * tt + 1][row + 8], d[3] - xs1);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int m = 8 * (e >> 1) + 2 * tt + (e & 1);
+              if (m < M) {
+                atomicAdd(&sm.gsum[gb][m][row], d[4 * (e >> 1) + (e & 1)] - xs[e]);
+                atomicAdd(&sm.gsum[gb][m][row + 8], d[4 * (e >> 1) + 2 + (e & 1)] - xs[e]);
+              }
             }
           } else {
-          int acc[kMaxTok];
-#pragma unroll
-          for (int m = 0; m < kMaxTok; ++m) acc[m] = 0;
-          for (int s = 0; s < nslab; ++s, ++it) {
-            const int st = it % kStages;
-            if (*abort_flag || !stage_ready(sm.full, sm.stage_tag, it, seen, abort_flag)) {
-              *abort_flag = 1;
-              break;
-            }
-            seen = (seen << 1) | 1u;
-            const int npc = pieces_in(rb, P, s);
-            const uint32_t sb = ring + st * kStageBytes;
-            if (s == 0) {
-#pragma unroll
-              for (int m = 0; m < kMaxTok; ++m)
-                if (m < M) {
-                  uint32_t x0, x1;
-                  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(cmv[m]) : "r"(sb + cofs + 4u * m) : "memory");
-                  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(x0) : "r"(sb + cofs + 64u + 64u * m + 4u * cls)
+            // ---- 2-4 tokens: dp4a, the shifted code planes shared by the tokens
+            int acc[kDp4aTok] = {0, 0, 0, 0};
+            int xwv[kDp4aTok] = {0, 0, 0, 0};
+            for (int s = 0; s < nslab; ++s, ++it) {
+              const int st = it % kStages;
+              if (*abort_flag || !stage_ready(sm.full, sm.stage_tag, it, seen, abort_flag)) {
+                *abort_flag = 1;
+                break;
+              }
+              seen = (seen << 1) | 1u;
+              const int npc = pieces_in(rb, P, s);
+              const uint32_t sb = ring + st * kStageBytes;
+              if (s == 0) {
+                if (tw == 0 && lane < M)
+                  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(sm.gcm[gb][lane]) : "r"(sb + cofs + 4u * lane)
                                : "memory");
-                  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(x1)
-                               : "r"(sb + cofs + 64u + 64u * m + 4u * (cls + kTW))
-                               : "memory");
-                  xwv[m] = static_cast<int>(x0 + x1);
-                }
-            }
-            const uint32_t sbase = sb + lrow, abase = sb + cofs + static_cast<uint32_t>(H);
-            switch (M) {
-              case 2: stage_multi<2>(sbase, abase, tstride, npc, cls, acc); break;
-              case 3: stage_multi<3>(sbase, abase, tstride, npc, cls, acc); break;
-              case 4: stage_multi<4>(sbase, abase, tstride, npc, cls, acc); break;
-              case 5: stage_multi<5>(sbase, abase, tstride, npc, cls, acc); break;
-              case 6: stage_multi<6>(sbase, abase, tstride, npc, cls, acc); break;
-              case 7: stage_multi<7>(sbase, abase, tstride, npc, cls, acc); break;
-              default: stage_multi<8>(sbase, abase, tstride, npc, cls, acc); break;
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive_n(smem_u32(&sm.empty[st]), kTeams);
-          }
 #pragma unroll
-          for (int m = 0; m < kMaxTok; ++m)
-            if (m < M) atomicAdd(&sm.gsum[gb][m][lane], acc[m] - xwv[m]);
+                for (int m = 0; m < kDp4aTok; ++m)
+                  if (m < M) {
+                    uint32_t x0, x1;
+                    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(x0) : "r"(sb + cofs + 64u + 64u * m + 4u * cls)
+                                 : "memory");
+                    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(x1)
+                                 : "r"(sb + cofs + 64u + 64u * m + 4u * (cls + kTW))
+                                 : "memory");
+                    xwv[m] = static_cast<int>(x0 + x1);
+                  }
+              }
+              const uint32_t sbase = sb + lrow, abase = sb + cofs + static_cast<uint32_t>(H);
+              switch (M) {
+                case 2: stage_multi<2>(sbase, abase, tstride, npc, cls, acc); break;
+                case 3: stage_multi<3>(sbase, abase, tstride, npc, cls, acc); break;
+                default: stage_multi<4>(sbase, abase, tstride, npc, cls, acc); break;
+              }
+              __syncwarp();
+              if (lane == 0) mbar_arrive_n(smem_u32(&sm.empty[st]), kTeams);
+            }
+#pragma unroll
+            for (int m = 0; m < kDp4aTok; ++m)
+              if (m < M) atomicAdd(&sm.gsum[gb][m][lane], acc[m] - xwv[m]);
           }
           // the team's sums meet in the group's buffer; its writing warp
-          // waits for them, writes the rows and clears the buffer
+          // waits for them, writes the rows and clears the buffer (the
+          // output scales c came with the group's first stage into gcm)
           __syncwarp();
           if (lane == 0) mbar_arrive_n(smem_u32(&sm.gbar[gb]), kTeams);
           if (tw == ((ng1 / kTeams) % kTW) && !*abort_flag) {
@@ -961,14 +969,12 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
               ++ng1;
               continue;
             }
-#pragma unroll
-            for (int m = 0; m < kMaxTok; ++m)
-              if (m < M) {
-                const int t = sm.gsum[gb][m][lane];
-                sm.gsum[gb][m][lane] = 0;
-                if (r0 + lane < N)
-                  yout[static_cast<int64_t>(m) * N + r0 + lane] = __fmul_rn(static_cast<float>(t), cmv[m]);
-              }
+            for (int m = 0; m < M; ++m) {
+              const int t = sm.gsum[gb][m][lane];
+              sm.gsum[gb][m][lane] = 0;
+              if (r0 + lane < N)
+                yout[static_cast<int64_t>(m) * N + r0 + lane] = __fmul_rn(static_cast<float>(t), sm.gcm[gb][m]);
+            }
           }
           ++ng1;
         }
