@@ -339,6 +339,70 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const XT *__restrict__ x
   zero_fill(m, zrows, zn, zcnt, ncnt);
 }
 
+// The same quantisation into bf16 codes (the tensor-core path's operand) in
+// one pass: TPR threads per row, 256 / TPR rows per block, every value of a
+// row held in registers between its absmax and its codes (K % 8 == 0,
+// K <= 32 * TPR, x, xb 16-byte aligned, ld % 8 == 0; no gain vector; used
+// for rows of up to 4096).  The
+// results equal quant_act_kernel's (the max does not depend on the order).
+template <typename XT, int TPR>
+__global__ void __launch_bounds__(256) quant_rows_bf16_kernel(const XT *__restrict__ x, int64_t M, int64_t K,
+                                                              int64_t ld, __nv_bfloat16 *__restrict__ xb,
+                                                              float *__restrict__ scale,
+                                                              int32_t *__restrict__ zrows, int64_t zn,
+                                                              unsigned *__restrict__ zcnt, int ncnt, int act) {
+  constexpr int RPB = 256 / TPR, NV = 4, NW = TPR / 32;
+  __shared__ float red[8];
+  pdl_wait_primary();
+  pdl_launch_dependents();
+  const int t = threadIdx.x, r = t / TPR, tr = t % TPR, lane = t & 31, warp = t >> 5;
+  const int64_t m = static_cast<int64_t>(blockIdx.x) * RPB + r;
+  const bool live = m < M;
+  const int nvec = static_cast<int>(K / 8);
+  const XT *xr = x + (live ? m : 0) * K;
+  float v[NV][8];
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int c = tr + i * TPR;
+    if (live && c < nvec) {
+      load8(xr + 8 * c, v[i]);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (act == kActRelu2) v[i][j] = relu2f(v[i][j]);
+        amax = fmaxf(amax, fabsf(v[i][j]));
+      }
+    }
+  }
+  amax = warp_max_nonneg(amax);
+  if (lane == 0) red[warp] = amax;
+  __syncthreads();
+  float a = red[r * NW];
+#pragma unroll
+  for (int w = 1; w < NW; ++w) a = fmaxf(a, red[r * NW + w]);
+  const float s = act_scale(a);
+  if (!live) return;
+  if (tr == 0) scale[m] = s;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int c = tr + i * TPR;
+    if (c < nvec) {
+      uint32_t w[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        w[j] = (__float_as_uint(static_cast<float>(quant_one(v[i][2 * j], s))) >> 16) |
+               (__float_as_uint(static_cast<float>(quant_one(v[i][2 * j + 1], s))) & 0xFFFF0000u);
+      *reinterpret_cast<uint4 *>(xb + m * ld + 8 * c) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+  for (int64_t c = nvec + tr; c < ld / 8; c += TPR)
+    *reinterpret_cast<uint4 *>(xb + m * ld + 8 * c) = make_uint4(0u, 0u, 0u, 0u);
+  if (zrows != nullptr)
+    for (int64_t k = tr; k < zn; k += TPR) zrows[m * zn + k] = 0;
+  if (zcnt != nullptr && m == 0)
+    for (int i = tr; i < ncnt; i += TPR) zcnt[i] = 0u;
+}
+
 // int8 codes [M, K] -> bf16 [M, ld] (exact), zero padded; one block per row.
 __global__ void __launch_bounds__(256) codes_to_bf16_kernel(const int8_t *__restrict__ xq,
                                                             int64_t K, int64_t ld,
