@@ -844,12 +844,12 @@ bool make_map_rows(CUtensorMap *m, const void *ptr, int64_t N, int64_t rb, int p
 //   * any other input byte (x, packed, gamma) written by an earlier call, an
 //     output byte written or read (from memory) by an earlier call, or
 //     wait_prev: a grid barrier before the call.
-// A call's output may not overlap its own inputs.  p, t and q may be null
+// A call's output may not overlap its own inputs.  p and t may be null
 // (size only).
 static int toks(const bl_chain_call &c) { return c.M < 1 ? 1 : c.M; }
 
 static bl_status chain_plan(const bl_chain_call *calls, int n, int grid, chain::Params *p, chain::TableCopy *t,
-                            chain::QuantParams *q, size_t *ws_need, void *ws) {
+                            size_t *ws_need, void *ws) {
   if (calls == nullptr) return BL_ERR_NULL;
   if (n < 1 || n > chain::kMaxCalls) return BL_ERR_SHAPE;
   struct Rng {
@@ -923,7 +923,6 @@ static bl_status chain_plan(const bl_chain_call *calls, int n, int grid, chain::
   p->table = reinterpret_cast<const chain::Call *>(wsb + chain::kTableOffset);
   t->n = n;
   t->dst = reinterpret_cast<chain::Call *>(wsb + chain::kTableOffset);
-  q->n = 0;
   int64_t deal = 0;  // the block that takes the next call's group 0
   for (int i = 0; i < n; ++i) {
     const bl_chain_call &c = calls[i];
@@ -950,17 +949,6 @@ static bl_status chain_plan(const bl_chain_call *calls, int n, int grid, chain::
     d.rec = early[i] ? wsb + rec_off[i] : nullptr;
     d.mb_out = produces[i] ? reinterpret_cast<uint64_t *>(wsb + mb_off[i]) : nullptr;
     d.mb_in = nullptr;
-    if (early[i]) {
-      chain::QuantJob &jb = q->j[q->n++];
-      jb.x = c.x;
-      jb.gamma = c.gamma;
-      jb.rec = wsb + rec_off[i];
-      jb.K = static_cast<int>(c.K);
-      jb.rb = static_cast<int>(rb);
-      jb.flags = flags;
-      jb.M = toks(c);
-      jb.P = P;
-    }
   }
   for (int i = 0; i < n; ++i)
     if (src[i] >= 0)
@@ -971,7 +959,7 @@ static bl_status chain_plan(const bl_chain_call *calls, int n, int grid, chain::
 bl_status bitlinear_chain_workspace_bytes(const bl_chain_call *calls, int n, size_t *bytes) {
   if (bytes == nullptr) return BL_ERR_NULL;
   size_t need = 0;
-  bl_status s = chain_plan(calls, n, 1, nullptr, nullptr, nullptr, &need, nullptr);
+  bl_status s = chain_plan(calls, n, 1, nullptr, nullptr, &need, nullptr);
   if (s != BL_OK) return s;
   *bytes = need;
   return BL_OK;
@@ -982,20 +970,19 @@ bl_status bitlinear_forward_chain(const bl_chain_call *calls, int n, void *ws, s
   if (calls == nullptr || ws == nullptr) return BL_ERR_NULL;
   if (!aligned(ws, 256)) return BL_ERR_ALIGN;
   size_t need = 0;
-  bl_status s = chain_plan(calls, n, 1, nullptr, nullptr, nullptr, &need, nullptr);
+  bl_status s = chain_plan(calls, n, 1, nullptr, nullptr, &need, nullptr);
   if (s != BL_OK) return s;
   if (ws_bytes < need) return BL_ERR_WORKSPACE;
   int dev = 0, sms = 0;
   s = current_device(&dev, &sms);
   if (s != BL_OK) return s;
-  // about 30 KB of tensor maps, 23 KB of call table and 8 KB of
-  // quantisation jobs: kept off the stack (each launch copies its parameters)
+  // about 30 KB of tensor maps and 21 KB of call table: kept off the stack
+  // (each launch copies its parameters)
   static chain::Params p;
   static chain::TableCopy tc;
-  static chain::QuantParams qp;
   static std::mutex p_mu;
   std::lock_guard<std::mutex> lk(p_mu);
-  s = chain_plan(calls, n, sms, &p, &tc, &qp, &need, ws);
+  s = chain_plan(calls, n, sms, &p, &tc, &need, ws);
   if (s != BL_OK) return s;
   bool many = false;
   for (int i = 0; i < n; ++i) many = many || toks(calls[i]) > 1;
@@ -1008,16 +995,14 @@ bl_status bitlinear_forward_chain(const bl_chain_call *calls, int n, void *ws, s
   if (s != BL_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // the call table into the workspace (its parameters are kept by value)
-  s = launch(&chain::copy_table_kernel, dim3(1), dim3(256), 0, st, false, tc);
+  // and the inputs no earlier call writes quantised into their records, one
+  // launch: block (i, m) takes token m of call i
+  int mt = 1;
+  for (int i = 0; i < n; ++i)
+    if (tc.calls[i].rec != nullptr && tc.calls[i].M > mt) mt = tc.calls[i].M;
+  s = launch(&chain::chain_setup_kernel, dim3(static_cast<unsigned>(n), static_cast<unsigned>(mt)),
+             dim3(chain::kQThreads), 0, st, false, tc);
   if (s != BL_OK) return s;
-  // the inputs no earlier call writes, quantised into their records
-  if (qp.n > 0) {
-    int mt = 1;
-    for (int i = 0; i < qp.n; ++i) mt = qp.j[i].M > mt ? qp.j[i].M : mt;
-    s = launch(&chain::chain_quant_kernel, dim3(static_cast<unsigned>(qp.n), static_cast<unsigned>(mt)),
-               dim3(chain::kQThreads), 0, st, false, qp);
-    if (s != BL_OK) return s;
-  }
   // every block may wait for the others: all must be resident (one per SM)
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(sms));

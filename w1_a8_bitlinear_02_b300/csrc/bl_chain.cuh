@@ -40,7 +40,7 @@
 // The activation codes (per-token absmax, "20亿参数仅0.4GB" page, section 2,
 // item 2) of a call come one of two ways:
 //   * an input no earlier call writes is quantised before the chain starts
-//     (chain_quant_kernel, one block per such call) into a record in the
+//     (chain_setup_kernel, one block per such call and token) into a record in the
 //     workspace -- codes, c and the 16 warps' code sums -- and each weight
 //     stage carries the record's codes for its slab (and, for a group's first
 //     slab, the header), so these calls stream with no per-call set-up;
@@ -206,42 +206,43 @@ static_assert(sizeof(Smem) <= kSmemFixed, "fixed shared-memory region");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory of one block");
 
 // ------------------------------------------------------------ set-up kernels
-// The call table into the workspace (a separate launch: its parameters hold
-// the table by value, so a captured graph keeps it).
+// The set-up launch before each chain: the call table into the workspace
+// (its parameters hold the table by value, so a captured graph keeps it; each
+// block copies a slice), then the inputs no earlier call writes quantised
+// into their records: token m of x [M, K] (f32 or bf16, relu2 first if
+// flagged) -> its part of the record (c[m] = gamma / s_m, the code sums of
+// the 16 piece classes, codes zero-padded to the last slab).  Grid (calls,
+// most tokens); block (i, m) takes token m of call i if it has a record.
 struct TableCopy {
   int n;
   Call *dst;
   Call calls[kMaxCalls];
 };
-__global__ void copy_table_kernel(const __grid_constant__ TableCopy t) {
-  const uint32_t *src = reinterpret_cast<const uint32_t *>(t.calls);
-  uint32_t *dst = reinterpret_cast<uint32_t *>(t.dst);
-  const int words = t.n * static_cast<int>(sizeof(Call) / 4);
-  for (int i = threadIdx.x; i < words; i += blockDim.x) dst[i] = src[i];
-}
-
-// One input quantised ahead: token m of x [M, K] (f32 or bf16, relu2 first
-// if flagged) -> its part of the record (c[m] = gamma / s_m, the 16 warps'
-// code sums, codes zero-padded to the last slab).  One block per (call,
-// token).
-struct QuantJob {
-  const void *x;
-  const float *gamma;
-  uint8_t *rec;
-  int K, rb, flags, M, P;
-};
-struct QuantParams {
-  int n;
-  QuantJob j[kMaxCalls];
-};
 constexpr int kQThreads = 256;
-__global__ void __launch_bounds__(kQThreads) chain_quant_kernel(const __grid_constant__ QuantParams q) {
+__global__ void __launch_bounds__(kQThreads) chain_setup_kernel(const __grid_constant__ TableCopy q) {
   __shared__ __align__(16) uint8_t codes[kMaxK + 64 * piece_cap(1)];
   __shared__ float red[kQThreads / 32];
   __shared__ int xsum[kCW];
-  const QuantJob &jb = q.j[blockIdx.x];
+  {
+    const uint32_t *src = reinterpret_cast<const uint32_t *>(q.calls);
+    uint32_t *dst = reinterpret_cast<uint32_t *>(q.dst);
+    const int words = q.n * static_cast<int>(sizeof(Call) / 4);
+    const int nb = static_cast<int>(gridDim.x * gridDim.y);
+    const int b = static_cast<int>(blockIdx.y * gridDim.x + blockIdx.x);
+    for (int i = b * kQThreads + static_cast<int>(threadIdx.x); i < words; i += nb * kQThreads) dst[i] = src[i];
+  }
+  struct {
+    const void *x;
+    const float *gamma;
+    uint8_t *rec;
+    int K, rb, flags, M, P;
+  } jb;
+  {
+    const Call &c = q.calls[blockIdx.x];
+    jb = {c.x, c.gamma, const_cast<uint8_t *>(c.rec), c.K, c.rb, c.flags, c.M, c.P};
+  }
   const int m = blockIdx.y;
-  if (m >= jb.M) return;
+  if (jb.rec == nullptr || m >= jb.M) return;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const bool bf = (jb.flags & kFlagBf16) != 0, r2 = (jb.flags & kFlagRelu2) != 0;
   const int K = jb.K, M = jb.M, P = jb.P, SB4 = 64 * P, nsl = slabs_of(jb.rb, M), kend = nsl * SB4;
