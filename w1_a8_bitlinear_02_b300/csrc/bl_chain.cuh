@@ -218,7 +218,7 @@ struct TableCopy {
   Call *dst;
   Call calls[kMaxCalls];
 };
-constexpr int kQThreads = 256;
+constexpr int kQThreads = 512;
 __global__ void __launch_bounds__(kQThreads) chain_setup_kernel(const __grid_constant__ TableCopy q) {
   __shared__ __align__(16) uint8_t codes[kMaxK + 64 * piece_cap(1)];
   __shared__ float red[kQThreads / 32];
