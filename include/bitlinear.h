@@ -326,11 +326,17 @@ typedef struct bl_chain_call {
 } bl_chain_call;
 
 /* Workspace (device bytes) that bitlinear_forward_chain needs for these
- * calls: 256 bytes of control words, 88 bytes per call (the call table,
- * rewritten by every launch), a record of about M * K + 128 bytes (K rounded
- * up to the call's weight slabs) for every call whose input no earlier call
- * writes (its input quantised before the chain starts), plus 8 * N bytes for
- * every call whose output a later call reads; each part 256-byte aligned.
+ * calls, each part rounded up to 256 bytes:
+ *   - 256 bytes of control words;
+ *   - 88 bytes per call (the call table, rewritten by every launch);
+ *   - a record for every call whose input no earlier call writes and that
+ *     does not wait (its input is quantised before the chain starts): a
+ *     header (128 bytes for one token, 64 + 64 M rounded up to 128 for more),
+ *     then M * 64 * P bytes for each of the row's slabs.  A row of
+ *     ceil(K / 64) pieces takes the fewest slabs of at most 65 (M = 1), 31
+ *     (M = 2..8) or 23 (M = 9..16) pieces, split evenly with an odd piece
+ *     count P per slab, so the codes take M * K bytes and a little more;
+ *   - 8 * N bytes for every call whose output a later call reads as its x.
  * Host only; the calls' pointers are compared, not dereferenced.  Errors: as
  * bitlinear_forward_chain's argument checks. */
 BL_API bl_status bitlinear_chain_workspace_bytes(const bl_chain_call *calls, int n, size_t *bytes);

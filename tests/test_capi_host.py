@@ -208,3 +208,79 @@ def test_chain_invalid_arguments_return_status(lib):
         kw.setdefault("y", 0x900000)
         p2, keep2 = chain(**kw)
         assert lib.bitlinear_forward_chain(p2, 1, ws, 256, None) == want, kw
+
+
+def _chain_record_bytes(K, M):
+    """A record as the header describes it: a header (128 bytes for one token,
+    64 + 64 M rounded up to 128 for more), then M x 64 code bytes per piece of
+    every slab.  A row of ceil(K/64) pieces takes the fewest slabs of at most
+    65 (one token), 31 (2-8) or 23 (9-16) pieces, split evenly, with an odd
+    piece count per slab."""
+    M = max(M, 1)
+    pieces = -(-K // 64)
+    cap = 65 if M == 1 else (31 if M <= 8 else 23)
+    ns = -(-pieces // cap)
+    P = -(-pieces // ns) | 1
+    slabs = -(-pieces // P)
+    assert P % 2 == 1 and P <= cap and slabs * P >= pieces and (slabs - 1) * cap < pieces
+    head = 128 if M == 1 else -(-(64 + 64 * M) // 128) * 128
+    return head + slabs * M * 64 * P
+
+
+def test_chain_workspace_layout(lib):
+    """bitlinear_chain_workspace_bytes adds up the parts its header lists: the
+    control words, the call table, a record per call quantised before the chain
+    and the output words of every call a later call reads -- and nothing for a
+    call that waits or reads an earlier output."""
+    from w1_a8_bitlinear_02_b300 import capi
+    al = lambda b: -(-b // 256) * 256
+    nxt = [0x10000000]
+
+    def region(nbytes):  # disjoint fake device ranges, never dereferenced
+        a = nxt[0]
+        nxt[0] += al(nbytes) + 4096
+        return a
+
+    def call(N, K, M=1, x=None, dt=capi.BL_BF16, wait=0):
+        M1 = max(M, 1)
+        return capi.ChainCall(region(N * 16 * -(-K // 64)), region(4),
+                              x if x is not None else region(M1 * K * 4), region(M1 * N * 4),
+                              N, K, dt, capi.BL_ACT_NONE, wait, M)
+
+    def need(calls):
+        arr = (capi.ChainCall * len(calls))(*calls)
+        sz = ctypes.c_size_t(0)
+        st = lib.bitlinear_chain_workspace_bytes(ctypes.cast(arr, ctypes.c_void_p), len(calls), ctypes.byref(sz))
+        return st, sz.value
+
+    base = lambda n: 256 + al(88 * n)
+
+    # independent calls of every token class, ragged and maximal K
+    shapes = [(2560, 2560, 1), (6912, 2560, 0), (2560, 6912, 1), (640, 1000, 1), (64, 64, 1),
+              (128, 32768, 1), (8192, 8192, 2), (28672, 8192, 8), (8192, 28672, 9),
+              (333, 4160, 16), (777, 63, 4), (4096, 4095, 12)]
+    calls = [call(N, K, M) for N, K, M in shapes]
+    assert need(calls) == (capi.BL_OK, base(len(calls)) + sum(al(_chain_record_bytes(K, M)) for _, K, M in shapes))
+    for N, K, M in shapes:
+        assert _chain_record_bytes(K, M) >= max(M, 1) * K + 128
+
+    # a dataflow chain: call 1 reads call 0's fp32 y, call 2 reads call 1's
+    c0 = call(2560, 2560)
+    c1 = call(6912, 2560, x=c0.y, dt=capi.BL_F32)
+    c2 = call(2560, 6912, x=c1.y, dt=capi.BL_F32)
+    assert need([c0, c1, c2]) == (capi.BL_OK, base(3) + al(_chain_record_bytes(2560, 1)) + al(8 * 2560) + al(8 * 6912))
+    # a row inside a larger output still takes output words (offset x, shorter K)
+    c3 = call(640, 1024, x=c1.y + 4 * 512, dt=capi.BL_F32)
+    assert need([c0, c1, c3]) == (capi.BL_OK, base(3) + al(_chain_record_bytes(2560, 1)) + al(8 * 2560) + al(8 * 6912))
+
+    # bf16 x over an earlier output, and wait_prev: a barrier, no record and no output words
+    d0 = call(2560, 2560)
+    d1 = call(2560, 1280, x=d0.y, dt=capi.BL_BF16)
+    assert need([d0, d1]) == (capi.BL_OK, base(2) + al(_chain_record_bytes(2560, 1)))
+    e0, e1 = call(2560, 2560), call(1024, 2560, wait=1)
+    assert need([e0, e1]) == (capi.BL_OK, base(2) + al(_chain_record_bytes(2560, 1)))
+
+    # several tokens whose x an earlier call writes: refused
+    f0 = call(2560, 2560)
+    f1 = call(640, 1280, M=2, x=f0.y, dt=capi.BL_F32)
+    assert need([f0, f1])[0] == capi.BL_ERR_SHAPE
