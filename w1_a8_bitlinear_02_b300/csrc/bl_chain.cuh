@@ -112,7 +112,7 @@ constexpr int kInBlockBytes = kHeader + kMaxK;
 __host__ __device__ constexpr int codes_ofs(int M) { return kGroupRows * kPiece * piece_cap(M); }
 constexpr int kStageBytes = 37 * 1024;
 constexpr int kStages = 4;
-constexpr int kSmemFixed = 40 * 1024;     // barriers, partial sums and the call table
+constexpr int kSmemFixed = 42 * 1024;     // barriers, partial sums and the call table
 constexpr int kSmemBytes = 1024 + kSmemFixed + kStages * kStageBytes + kInBlockBytes;
 
 // Control words at the start of the workspace (bytes 0..255), then the
@@ -189,6 +189,18 @@ static_assert(kGB % kTeams == 0 && kCW % kTeams == 0, "teams");
 static_assert(kStages % kProd == 0, "each producer owns whole ring slots");
 static_assert(kThreads <= 20 * 32, "the kernel's register budget assumes at most 20 warps");
 
+// This block's share of a call, built once per launch: the first of its
+// row groups (j0), how many it takes (cnt: j0, j0 + grid, ... below the
+// call's group count), N, and packed: pieces per slab (bits 0-7), slabs per
+// row (8-15), pieces per row (16-25), tokens - 1 (26-29), kCbFast (30: one
+// token, input quantised ahead, no barrier) and kCbRec (31: a record).
+struct __align__(16) CallBlk {
+  int j0, cnt, N;
+  uint32_t pk;
+};
+constexpr uint32_t kCbFast = 1u << 30;
+constexpr uint32_t kCbRec = 1u << 31;
+
 struct Smem {
   uint64_t full[kStages];
   uint64_t empty[kStages];
@@ -200,8 +212,10 @@ struct Smem {
   uint32_t seq_tag;
   int abort_flag;
   int stage_tag[kStages];  // the stage each ring slot was last armed for (written by its producer)
+  CallBlk cb[kMaxCalls];  // this block's share of each call
   Call calls[kMaxCalls];  // the call table, copied in once
 };
+static_assert(sizeof(CallBlk) == 16, "one 16-byte load a call");
 static_assert(sizeof(Smem) <= kSmemFixed, "fixed shared-memory region");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory of one block");
 
@@ -712,6 +726,22 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
     for (int i = tid; i < kGB * kMaxTok * kGroupRows; i += kThreads) (&sm.gsum[0][0][0])[i] = 0;
   }
   __syncthreads();
+  for (int i = tid; i < p.n; i += kThreads) {
+    const Call &c = sm.calls[i];
+    const int G = static_cast<int>(gridDim.x);
+    int j0 = static_cast<int>(blockIdx.x) - c.g0;
+    if (j0 < 0) j0 += G;
+    CallBlk e;
+    e.j0 = j0;
+    e.cnt = j0 < c.ng ? (c.ng - j0 + G - 1) / G : 0;
+    e.N = c.N;
+    const bool fast = c.M == 1 && c.rec != nullptr && (c.flags & kFlagBarrier) == 0;
+    e.pk = static_cast<uint32_t>(c.P) | (static_cast<uint32_t>(c.ns) << 8) |
+           (static_cast<uint32_t>(c.rb / kPiece) << 16) | (static_cast<uint32_t>(c.M - 1) << 26) |
+           (fast ? kCbFast : 0u) | (c.rec != nullptr ? kCbRec : 0u);
+    sm.cb[i] = e;
+  }
+  __syncthreads();
   volatile int *abort_flag = &sm.abort_flag;
   const uint32_t seq_tag = sm.seq_tag;
 
@@ -730,16 +760,12 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
       // loads wait behind the consumers' traffic; the asm statements below
       // clobber memory, which would make every later use a reload)
       struct Fields {
-        int g0, ng, M, P, ns;
+        uint4 e;  // CallBlk
         const uint8_t *rec;
       };
       auto fields = [&](int ci) {
         Fields f;
-        f.g0 = sm.calls[ci].g0;
-        f.ng = sm.calls[ci].ng;
-        f.M = sm.calls[ci].M;
-        f.P = sm.calls[ci].P;
-        f.ns = sm.calls[ci].ns;
+        f.e = lds_u128(smem_u32(&sm.cb[ci]));
         f.rec = sm.calls[ci].rec;
         return f;
       };
@@ -747,20 +773,22 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
       for (int ci = 0; ci < p.n && go; ++ci) {
         const Fields cur = nxt;
         if (ci + 1 < p.n) nxt = fields(ci + 1);
-        const int M = cur.M, P = cur.P, G = static_cast<int>(gridDim.x);
+        const int cnt = static_cast<int>(cur.e.y);
+        if (cnt == 0) continue;
+        const uint32_t pk = cur.e.w;
+        const int M = static_cast<int>((pk >> 26) & 0xFu) + 1, P = static_cast<int>(pk & 0xFFu);
+        const int G = static_cast<int>(gridDim.x);
         const uint8_t *rec = cur.rec;
         const int H = header_bytes(M);
         const uint32_t cbytes = static_cast<uint32_t>(M * 64 * P);  // every token's codes of one slab
         const uint32_t cofs = static_cast<uint32_t>(codes_ofs(M));
-        int j = static_cast<int>(blockIdx.x) - cur.g0;
-        if (j < 0) j += G;
-        if (j >= cur.ng) continue;
         const CUtensorMap *map = &p.maps[ci];
-        const int nslab = cur.ns;
+        const int nslab = static_cast<int>((pk >> 8) & 0xFFu);
         // this block's groups (the last group may run past N, where the box
         // reads zeros; so does the last slab past the row)
         const uint32_t box = static_cast<uint32_t>(kGroupRows * kPiece * P);
-        for (; j < cur.ng && go; j += G) {
+        int j = static_cast<int>(cur.e.x);
+        for (int g = 0; g < cnt && go; ++g, j += G) {
           for (int s = 0; s < nslab; ++s, ++i) {
             if (i % kProd != q) continue;
             const int st = i % kStages;
@@ -806,6 +834,89 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
     int nq = 0;       // calls whose input this block quantised
     uint32_t seen = 0xFu;  // bit b: this warp processed stage it - 1 - b (stages before 0 count as seen)
     for (int ci = 0; ci < p.n; ++ci) {
+      {
+        // ---- one token, input quantised ahead, no barrier: the block's
+        // share of the call from one 16-byte entry; this team's groups are
+        // every other one of the block's (group ng1 + g goes to team
+        // (ng1 + g) mod 2), the other team's stages are stepped over
+        const uint4 e = lds_u128(smem_u32(&sm.cb[ci]));
+        if (e.w & kCbFast) {
+          const int cnt = static_cast<int>(e.y);
+          if (cnt == 0) continue;
+          const int G = static_cast<int>(gridDim.x), N = static_cast<int>(e.z);
+          const int P = static_cast<int>(e.w & 0xFFu), nslab = static_cast<int>((e.w >> 8) & 0xFFu);
+          const int np = static_cast<int>((e.w >> 16) & 0x3FFu);
+          float *const yout = sm.calls[ci].y;
+          uint64_t *const mbo = sm.calls[ci].mb_out;
+          const int team = warp / kTW, tw = warp % kTW;
+          const int cls = (tw + ci) & (kTW - 1);
+          const uint32_t lrow = static_cast<uint32_t>(lane * kPiece * P);
+          const uint32_t tag = seq_tag | static_cast<uint32_t>(ci + 1);
+          const uint32_t skip_seen = nslab >= 32 ? 0u : ~0u;
+          int g = (ng1 ^ team) & 1;
+          if (g != 0) {  // the block's first group of the call is the other team's
+            it += nslab;
+            seen = (seen << (nslab & 31)) & skip_seen;
+          }
+          for (; g < cnt; g += 2) {
+            const int o = ng1 + g;  // the group's ordinal in the block
+            int acc[4] = {0, 0, 0, 0}, acc2[4] = {0, 0, 0, 0};
+            float cm = 0.0f;
+            int xw = 0;
+            for (int s = 0; s < nslab; ++s, ++it) {
+              const int st = it % kStages;
+              if (!stage_ready(sm.full, sm.stage_tag, it, seen, abort_flag)) {
+                *abort_flag = 1;
+                break;
+              }
+              seen = (seen << 1) | 1u;
+              const int left = np - s * P;
+              const int npc = left < P ? left : P;
+              const uint32_t sb = ring + st * kStageBytes;
+              if (s == 0) {
+                // c and X of class cls (the header holds the sums of the 16
+                // classes p mod 16; classes cls and cls + kTW make p mod kTW)
+                uint32_t x0, x1;
+                asm volatile("ld.shared.f32 %0, [%1];" : "=f"(cm) : "r"(sb + codes_ofs(1)) : "memory");
+                asm volatile("ld.shared.u32 %0, [%1];" : "=r"(x0) : "r"(sb + codes_ofs(1) + 64u + 4u * cls) : "memory");
+                asm volatile("ld.shared.u32 %0, [%1];" : "=r"(x1) : "r"(sb + codes_ofs(1) + 64u + 4u * (cls + kTW))
+                             : "memory");
+                xw = static_cast<int>(x0 + x1);
+              }
+              stage_one<kTW>(sb + lrow, sb + codes_ofs(1) + kHeader, cls, npc, acc, acc2);
+              // the stage's empty barrier counts kCW arrivals: a team's warps
+              // arrive twice each
+              __syncwarp();
+              if (lane == 0) mbar_arrive_n(smem_u32(&sm.empty[st]), static_cast<uint32_t>(kTeams));
+            }
+            const int gb = o & (kGB - 1);
+            atomicAdd(&sm.gsum[gb][0][lane], (acc[0] + acc2[0]) + ((acc[1] + acc2[1]) >> 2) +
+                                              ((acc[2] + acc2[2]) >> 4) + ((acc[3] + acc2[3]) >> 6) - xw);
+            __syncwarp();  // orders the lanes' adds before lane 0's release
+            if (lane == 0) mbar_arrive_n(smem_u32(&sm.gbar[gb]), static_cast<uint32_t>(kTeams));
+            if (tw == ((o / kTeams) % kTW) && !*abort_flag) {
+              if (mbar_wait(smem_u32(&sm.gbar[gb]), (o / kGB) & 1)) {
+                const int t = sm.gsum[gb][0][lane];
+                sm.gsum[gb][0][lane] = 0;
+                const int r = (static_cast<int>(e.x) + g * G) * kGroupRows + lane;
+                if (r < N) {
+                  const float v = __fmul_rn(static_cast<float>(t), cm);
+                  yout[r] = v;
+                  if (mbo != nullptr) st_word(mbo + r, v, tag);
+                }
+              } else {
+                *abort_flag = 1;
+              }
+            }
+            if (g + 1 < cnt) {  // the other team's next group
+              it += nslab;
+              seen = (seen << (nslab & 31)) & skip_seen;
+            }
+          }
+          ng1 += cnt;
+          continue;
+        }
+      }
       const Call &c = sm.calls[ci];
       const int j0 = first_group(c), G = static_cast<int>(gridDim.x);
 
