@@ -79,7 +79,7 @@ constexpr int kMaxCalls = 240;            // one tensor map each in the kernel p
 constexpr int kCW = 16;                   // consumer warps
 constexpr int kTeams = 2;                 // one-token row groups alternate between two teams
 constexpr int kTW = kCW / kTeams;         // warps of a team
-constexpr int kProd = 2;                  // producer warps (one thread each): alternate stages
+constexpr int kProd = 4;                  // producer warps (one thread each): stage i is producer i mod kProd's
 constexpr int kThreads = (kCW + kProd) * 32;
 constexpr int kC = kCW * 32;              // consumer threads
 constexpr int kMaxK = 32768;
@@ -112,7 +112,7 @@ constexpr int kInBlockBytes = kHeader + kMaxK;
 __host__ __device__ constexpr int codes_ofs(int M) { return kGroupRows * kPiece * piece_cap(M); }
 constexpr int kStageBytes = 37 * 1024;
 constexpr int kStages = 4;
-constexpr int kSmemFixed = 42 * 1024;     // barriers, partial sums and the call table
+constexpr int kSmemFixed = 45 * 1024;     // barriers, partial sums and the call table
 constexpr int kSmemBytes = 1024 + kSmemFixed + kStages * kStageBytes + kInBlockBytes;
 
 // Control words at the start of the workspace (bytes 0..255), then the
@@ -201,6 +201,29 @@ struct __align__(16) CallBlk {
 constexpr uint32_t kCbFast = 1u << 30;
 constexpr uint32_t kCbRec = 1u << 31;
 
+// When every call of the chain takes the fast form (one token, input
+// quantised ahead, no barrier), the producers hand the block's row groups to
+// the two teams through one queue per team (group o of the block goes to
+// team o mod 2 as its entry o / 2; seq = entry + 1 once written, released
+// after the other fields), so the consumers read one entry per group and
+// never walk the call table.  A queue slot is rewritten only kTQ entries
+// later, after its group was summed: no stage is issued before the stage
+// kStages earlier was released, so the producers run at most kStages stages
+// ahead of the oldest stage a team still holds.
+struct __align__(16) Item {
+  float *y;
+  uint64_t *mbo;  // output words, or null
+  int it;         // the group's first ring stage
+  int r0;         // its first row
+  int N;
+  uint32_t pk;    // CallBlk::pk of the call
+  int ci;         // the call
+  int seq;
+  int pad[2];
+};
+constexpr int kTQ = 16;
+constexpr int kTB = 8;  // group-sum buffers per team (a team's warps are at most 4 of its groups apart)
+
 struct Smem {
   uint64_t full[kStages];
   uint64_t empty[kStages];
@@ -213,8 +236,16 @@ struct Smem {
   int abort_flag;
   int stage_tag[kStages];  // the stage each ring slot was last armed for (written by its producer)
   CallBlk cb[kMaxCalls];  // this block's share of each call
+  Item tq[kTeams][kTQ];   // the teams' group queues (every call in the fast form)
+  uint64_t tbar[kTeams][kTB];  // their group-sum barriers (the sums in gsum, flat)
+  int tq_end[kTeams];     // the number of groups of each team
+  int ib[kMaxCalls];      // each call's first ring stage in this block
+  int og[kMaxCalls];      // and the block's ordinal of its first group
+  uint32_t scan_w[kThreads / 32][2];
   Call calls[kMaxCalls];  // the call table, copied in once
 };
+static_assert(sizeof(Item) == 48, "queue entry");
+static_assert(kTeams * kTB * kGroupRows <= kGB * kMaxTok * kGroupRows, "team sums inside gsum");
 static_assert(sizeof(CallBlk) == 16, "one 16-byte load a call");
 static_assert(sizeof(Smem) <= kSmemFixed, "fixed shared-memory region");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory of one block");
@@ -713,6 +744,11 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
       mbar_init(smem_u32(&sm.empty[s]), kCW);
     }
     for (int b = 0; b < kGB; ++b) mbar_init(smem_u32(&sm.gbar[b]), kCW);
+    for (int t = 0; t < kTeams; ++t) {
+      for (int b = 0; b < kTB; ++b) mbar_init(smem_u32(&sm.tbar[t][b]), kTW);
+      for (int k = 0; k < kTQ; ++k) sm.tq[t][k].seq = 0;
+      sm.tq_end[t] = -1;
+    }
     sm.abort_flag = 0;
     for (int s = 0; s < kStages; ++s) sm.stage_tag[s] = s;
     sm.seq_tag = p.ctl[kCtlSeq] << 9;  // tags: (launch sequence << 9) | (call + 1)
@@ -726,7 +762,13 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
     for (int i = tid; i < kGB * kMaxTok * kGroupRows; i += kThreads) (&sm.gsum[0][0][0])[i] = 0;
   }
   __syncthreads();
-  for (int i = tid; i < p.n; i += kThreads) {
+  // this block's share of each call (one thread a call), then the calls'
+  // first stages and group ordinals in the block (prefix sums over the calls)
+  static_assert(kMaxCalls <= kThreads, "one thread a call");
+  bool mine_fast = true;
+  uint32_t vs = 0, vg = 0;  // the call's stages and groups in this block
+  if (tid < p.n) {
+    const int i = tid;
     const Call &c = sm.calls[i];
     const int G = static_cast<int>(gridDim.x);
     int j0 = static_cast<int>(blockIdx.x) - c.g0;
@@ -740,33 +782,74 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
            (static_cast<uint32_t>(c.rb / kPiece) << 16) | (static_cast<uint32_t>(c.M - 1) << 26) |
            (fast ? kCbFast : 0u) | (c.rec != nullptr ? kCbRec : 0u);
     sm.cb[i] = e;
+    mine_fast = fast;
+    vs = static_cast<uint32_t>(e.cnt) * static_cast<uint32_t>(c.ns);
+    vg = static_cast<uint32_t>(e.cnt);
   }
-  __syncthreads();
+  {
+    uint32_t is = vs, ig = vg;  // inclusive prefix sums within the warp
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const uint32_t a = __shfl_up_sync(0xffffffffu, is, d), b = __shfl_up_sync(0xffffffffu, ig, d);
+      if (lane >= d) {
+        is += a;
+        ig += b;
+      }
+    }
+    if (lane == 31) {
+      sm.scan_w[warp][0] = is;
+      sm.scan_w[warp][1] = ig;
+    }
+    __syncthreads();
+    if (tid < p.n) {
+      for (int w = 0; w < warp; ++w) {
+        is += sm.scan_w[w][0];
+        ig += sm.scan_w[w][1];
+      }
+      sm.ib[tid] = static_cast<int>(is - vs);
+      sm.og[tid] = static_cast<int>(ig - vg);
+      if (tid == p.n - 1) {
+        sm.tq_end[0] = static_cast<int>((ig + 1) / 2);
+        sm.tq_end[1] = static_cast<int>(ig / 2);
+      }
+    }
+  }
+  const bool qmode = __syncthreads_and(mine_fast) != 0 && !MANY && !DEP;
   volatile int *abort_flag = &sm.abort_flag;
   const uint32_t seq_tag = sm.seq_tag;
 
   if (warp >= kCW) {
-    // ------------------------------------------------ producers: records and weight stages, in order;
-    // producer q issues the stages i with i mod kProd == q (its own ring
-    // slots, as kStages is a multiple of kProd), so two threads on two
-    // schedulers share the per-stage issue work
+    // ------------------------------------------------ producers: records and weight stages.
+    // Stage i of the block is issued by producer i mod kProd (its ring slot,
+    // as kStages is a multiple of kProd); each producer takes up only the
+    // calls that hold one of its stages (from the stage prefix sums), so the
+    // per-call and per-stage issue work is spread over kProd threads on
+    // different schedulers.
+    static_assert((kProd & (kProd - 1)) == 0, "stage owner by mask");
     const int q = warp - kCW;
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
       const uint64_t pol_rec = policy_evict_last();  // records are read by every block
-      int i = 0, issued = 0;
+      int issued = 0;
       bool go = true;
       // the call's fields in registers, read one call ahead (shared-memory
       // loads wait behind the consumers' traffic; the asm statements below
       // clobber memory, which would make every later use a reload)
       struct Fields {
         uint4 e;  // CallBlk
+        int ib, og;
         const uint8_t *rec;
+        float *y;
+        uint64_t *mbo;
       };
       auto fields = [&](int ci) {
         Fields f;
         f.e = lds_u128(smem_u32(&sm.cb[ci]));
+        f.ib = sm.ib[ci];
+        f.og = sm.og[ci];
         f.rec = sm.calls[ci].rec;
+        f.y = qmode ? sm.calls[ci].y : nullptr;
+        f.mbo = qmode ? sm.calls[ci].mb_out : nullptr;
         return f;
       };
       Fields nxt = fields(0);
@@ -774,8 +857,10 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
         const Fields cur = nxt;
         if (ci + 1 < p.n) nxt = fields(ci + 1);
         const int cnt = static_cast<int>(cur.e.y);
-        if (cnt == 0) continue;
         const uint32_t pk = cur.e.w;
+        const int nslab = static_cast<int>((pk >> 8) & 0xFFu), len = cnt * nslab;
+        const int d = (q - cur.ib) & (kProd - 1);  // this producer's first stage of the call, from its first
+        if (d >= len) continue;
         const int M = static_cast<int>((pk >> 26) & 0xFu) + 1, P = static_cast<int>(pk & 0xFFu);
         const int G = static_cast<int>(gridDim.x);
         const uint8_t *rec = cur.rec;
@@ -783,37 +868,53 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
         const uint32_t cbytes = static_cast<uint32_t>(M * 64 * P);  // every token's codes of one slab
         const uint32_t cofs = static_cast<uint32_t>(codes_ofs(M));
         const CUtensorMap *map = &p.maps[ci];
-        const int nslab = static_cast<int>((pk >> 8) & 0xFFu);
-        // this block's groups (the last group may run past N, where the box
-        // reads zeros; so does the last slab past the row)
+        // this block's groups j0, j0 + G, ... (the last group may run past N,
+        // where the box reads zeros; so does the last slab past the row)
         const uint32_t box = static_cast<uint32_t>(kGroupRows * kPiece * P);
-        int j = static_cast<int>(cur.e.x);
-        for (int g = 0; g < cnt && go; ++g, j += G) {
-          for (int s = 0; s < nslab; ++s, ++i) {
-            if (i % kProd != q) continue;
-            const int st = i % kStages;
-            if (i >= kStages && (!mbar_wait(smem_u32(&sm.empty[st]), ((i / kStages) - 1) & 1) || *abort_flag)) {
-              *abort_flag = 1;
-              go = false;
-              break;
-            }
-            // the slot's previous stage has landed and been consumed: say so
-            // before arming it (see stage_ready)
-            if (i >= kStages)
-              asm volatile("st.release.cta.shared.s32 [%0], %1;" ::"r"(smem_u32(&sm.stage_tag[st])), "r"(i) : "memory");
-            const uint32_t fb = smem_u32(&sm.full[st]);
-            const uint32_t sb = ring + st * kStageBytes;
-            uint32_t tx = box;
-            if (rec != nullptr) tx += cbytes + (s == 0 ? H : 0);
-            mbar_arrive_expect_tx(fb, tx);
-            tma_load_2d(sb, map, s * P * (kPiece / 8), j * kGroupRows, fb, pol);
-            if (rec != nullptr) {
-              if (s == 0)
-                bulk_g2s(sb + cofs, rec, H + cbytes, fb, pol_rec);
-              else
-                bulk_g2s(sb + cofs + H, rec + H + s * cbytes, cbytes, fb, pol_rec);
-            }
-            issued = i + 1;
+        int g = d / nslab, s = d - g * nslab;  // the stage's group (of the block's) and slab
+        for (int i = cur.ib + d; i < cur.ib + len; i += kProd) {
+          const int j = static_cast<int>(cur.e.x) + g * G;
+          const int st = i % kStages;
+          if (i >= kStages && (!mbar_wait(smem_u32(&sm.empty[st]), ((i / kStages) - 1) & 1) || *abort_flag)) {
+            *abort_flag = 1;
+            go = false;
+            break;
+          }
+          // the slot's previous stage has landed and been consumed: say so
+          // before arming it (see stage_ready)
+          if (i >= kStages)
+            asm volatile("st.release.cta.shared.s32 [%0], %1;" ::"r"(smem_u32(&sm.stage_tag[st])), "r"(i) : "memory");
+          if (qmode && s == 0) {
+            // the group's queue entry (its slot's previous entry was
+            // consumed: see Item)
+            const int o = cur.og + g, k = o >> 1;
+            Item &e = sm.tq[o & 1][k % kTQ];
+            e.y = cur.y;
+            e.mbo = cur.mbo;
+            e.it = i;
+            e.r0 = j * kGroupRows;
+            e.N = static_cast<int>(cur.e.z);
+            e.pk = pk;
+            e.ci = ci;
+            asm volatile("st.release.cta.shared.s32 [%0], %1;" ::"r"(smem_u32(&e.seq)), "r"(k + 1) : "memory");
+          }
+          const uint32_t fb = smem_u32(&sm.full[st]);
+          const uint32_t sb = ring + st * kStageBytes;
+          uint32_t tx = box;
+          if (rec != nullptr) tx += cbytes + (s == 0 ? H : 0);
+          mbar_arrive_expect_tx(fb, tx);
+          tma_load_2d(sb, map, s * P * (kPiece / 8), j * kGroupRows, fb, pol);
+          if (rec != nullptr) {
+            if (s == 0)
+              bulk_g2s(sb + cofs, rec, H + cbytes, fb, pol_rec);
+            else
+              bulk_g2s(sb + cofs + H, rec + H + s * cbytes, cbytes, fb, pol_rec);
+          }
+          issued = i + 1;
+          s += kProd;
+          while (s >= nslab) {
+            s -= nslab;
+            ++g;
           }
         }
       }
@@ -833,7 +934,94 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
     int ng1 = 0;      // row groups done (team, group buffer, writer and phase)
     int nq = 0;       // calls whose input this block quantised
     uint32_t seen = 0xFu;  // bit b: this warp processed stage it - 1 - b (stages before 0 count as seen)
-    for (int ci = 0; ci < p.n; ++ci) {
+    if (qmode) {
+      // ---- every call in the fast form: this team's groups from its queue
+      const int team = warp / kTW, tw = warp % kTW;
+      int last = -1;  // the last stage this warp processed
+      int *const tsum = &sm.gsum[0][0][0];
+      for (int k = 0;; ++k) {
+        const Item &E = sm.tq[team][k % kTQ];
+        bool end = false;
+        {
+          const long long t0 = clock64();
+          while (true) {
+            int sq, en;
+            asm volatile("ld.acquire.cta.shared.s32 %0, [%1];" : "=r"(sq) : "r"(smem_u32(&E.seq)) : "memory");
+            if (sq == k + 1) break;
+            asm volatile("ld.acquire.cta.shared.s32 %0, [%1];" : "=r"(en) : "r"(smem_u32(&sm.tq_end[team])) : "memory");
+            if (en == k) {
+              end = true;
+              break;
+            }
+            if (*abort_flag || clock64() - t0 > kWaitLimitCycles || gave_up()) {
+              atomicOr(&g_dev_error, kDevErrTimeout);
+              *abort_flag = 1;
+              end = true;
+              break;
+            }
+          }
+        }
+        if (end) break;
+        const int it0 = E.it, r0 = E.r0, N = E.N, ci = E.ci;
+        const uint32_t pk = E.pk;
+        float *const yout = E.y;
+        uint64_t *const mbo = E.mbo;
+        const int P = static_cast<int>(pk & 0xFFu), nslab = static_cast<int>((pk >> 8) & 0xFFu);
+        const int np = static_cast<int>((pk >> 16) & 0x3FFu);
+        const int cls = (tw + ci) & (kTW - 1);
+        const uint32_t lrow = static_cast<uint32_t>(lane * kPiece * P);
+        const int gap = it0 - last - 1;  // the other team's stages since this warp's last one
+        seen = gap >= 32 ? 0u : seen << gap;
+        int acc[4] = {0, 0, 0, 0}, acc2[4] = {0, 0, 0, 0};
+        float cm = 0.0f;
+        int xw = 0;
+        for (int s = 0; s < nslab; ++s) {
+          const int it = it0 + s, st = it % kStages;
+          if (!stage_ready(sm.full, sm.stage_tag, it, seen, abort_flag)) {
+            *abort_flag = 1;
+            break;
+          }
+          seen = (seen << 1) | 1u;
+          const int left = np - s * P;
+          const int npc = left < P ? left : P;
+          const uint32_t sb = ring + st * kStageBytes;
+          if (s == 0) {
+            uint32_t x0, x1;
+            asm volatile("ld.shared.f32 %0, [%1];" : "=f"(cm) : "r"(sb + codes_ofs(1)) : "memory");
+            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(x0) : "r"(sb + codes_ofs(1) + 64u + 4u * cls) : "memory");
+            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(x1) : "r"(sb + codes_ofs(1) + 64u + 4u * (cls + kTW))
+                         : "memory");
+            xw = static_cast<int>(x0 + x1);
+          }
+          stage_one<kTW>(sb + lrow, sb + codes_ofs(1) + kHeader, cls, npc, acc, acc2);
+          __syncwarp();
+          if (lane == 0) mbar_arrive_n(smem_u32(&sm.empty[st]), static_cast<uint32_t>(kTeams));
+        }
+        last = it0 + nslab - 1;
+        // the team's sums meet in buffer k mod kTB; warp k mod kTW writes the rows
+        const int b = k & (kTB - 1);
+        int *const sum = tsum + (team * kTB + b) * kGroupRows;
+        atomicAdd(sum + lane, (acc[0] + acc2[0]) + ((acc[1] + acc2[1]) >> 2) + ((acc[2] + acc2[2]) >> 4) +
+                                  ((acc[3] + acc2[3]) >> 6) - xw);
+        __syncwarp();
+        if (lane == 0) mbar_arrive_n(smem_u32(&sm.tbar[team][b]), 1u);
+        if (tw == (k % kTW) && !*abort_flag) {
+          if (mbar_wait(smem_u32(&sm.tbar[team][b]), (k / kTB) & 1)) {
+            const int t = sum[lane];
+            sum[lane] = 0;
+            const int r = r0 + lane;
+            if (r < N) {
+              const float v = __fmul_rn(static_cast<float>(t), cm);
+              yout[r] = v;
+              if (mbo != nullptr) st_word(mbo + r, v, seq_tag | static_cast<uint32_t>(ci + 1));
+            }
+          } else {
+            *abort_flag = 1;
+          }
+        }
+      }
+    }
+    for (int ci = 0; ci < (qmode ? 0 : p.n); ++ci) {
       {
         // ---- one token, input quantised ahead, no barrier: the block's
         // share of the call from one 16-byte entry; this team's groups are
