@@ -1009,12 +1009,20 @@ bl_status bitlinear_forward_chain(const bl_chain_call *calls, int n, void *ws, s
   cfg.blockDim = dim3(chain::kThreads);
   cfg.dynamicSmemBytes = chain::kSmemBytes;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  // and it may start while the set-up kernel runs: it waits for it
+  // (griddepcontrol) after initialising its barriers
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) return launch_failed("chain launch");
+  cfg.numAttrs = 2;
+  if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) {
+    cudaGetLastError();  // not taken with the overlap: launch in plain stream order
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) return launch_failed("chain launch");
+  }
   return BL_OK;
 }
 bl_status bitlinear_forward_noalloc(const uint8_t *packed, const float *gamma, int64_t N, int64_t K,

@@ -268,6 +268,7 @@ __global__ void __launch_bounds__(kQThreads) chain_setup_kernel(const __grid_con
   __shared__ __align__(16) uint8_t codes[kMaxK + 64 * piece_cap(1)];
   __shared__ float red[kQThreads / 32];
   __shared__ int xsum[kCW];
+  pdl_launch_dependents();  // the chain may set up its barriers meanwhile
   {
     const uint32_t *src = reinterpret_cast<const uint32_t *>(q.calls);
     uint32_t *dst = reinterpret_cast<uint32_t *>(q.dst);
@@ -299,6 +300,68 @@ __global__ void __launch_bounds__(kQThreads) chain_setup_kernel(const __grid_con
   };
   const bool vec = (K % 8) == 0 && al16(xr);
   const int nv = vec ? K / 8 : 0;
+  if (vec && nv <= 2 * kQThreads) {
+    // one read of x, kept in registers; each thread writes its vectors' codes
+    // straight into the record, and the 8 lanes holding one 64-code piece
+    // add its sum into the piece's class
+    const float gam = t == 0 ? __ldg(jb.gamma) : 0.0f;
+    float f[2][8];
+    float a = 0.0f;
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int v = t + r * kQThreads;
+      if (v < nv) {
+        if (bf)
+          load8(static_cast<const __nv_bfloat16 *>(xr) + 8 * v, f[r]);
+        else
+          load8(static_cast<const float *>(xr) + 8 * v, f[r]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          if (r2) f[r][e] = relu2f(f[r][e]);
+          a = fmaxf(a, fabsf(f[r][e]));
+        }
+      }
+    }
+    a = warp_max_nonneg(a);
+    if (lane == 0) red[warp] = a;
+    if (t < kCW) xsum[t] = 0;
+    __syncthreads();
+    a = red[0];
+#pragma unroll
+    for (int w = 1; w < kQThreads / 32; ++w) a = fmaxf(a, red[w]);
+    const float s = act_scale(a);
+    const int H = header_bytes(M);
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int v = t + r * kQThreads;  // lanes 8i..8i+7 hold one piece (kQThreads is a multiple of 8)
+      int sum = 0, cls = 0;
+      if (v < nv) {
+        uint32_t lo = 0, hi = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          lo |= (static_cast<uint32_t>(quant_one(f[r][e], s)) & 0xFFu) << (8 * e);
+          hi |= (static_cast<uint32_t>(quant_one(f[r][e + 4], s)) & 0xFFu) << (8 * e);
+        }
+        const int k = 8 * v, sl = k / SB4, off = k - sl * SB4;
+        *reinterpret_cast<uint2 *>(jb.rec + H + (static_cast<size_t>(sl) * M + m) * SB4 + off) = make_uint2(lo, hi);
+        sum = dp4a_us(0x01010101u, hi, dp4a_us(0x01010101u, lo, 0));
+        cls = (off / 64) % kCW;
+      }
+      sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+      sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+      sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+      if ((lane & 7) == 0 && v < nv) atomicAdd(&xsum[cls], sum);
+    }
+    // zeros from K to the end of the last slab
+    for (int k = 8 * (nv + t); k < kend; k += 8 * kQThreads) {
+      const int sl = k / SB4, off = k - sl * SB4;
+      *reinterpret_cast<uint2 *>(jb.rec + H + (static_cast<size_t>(sl) * M + m) * SB4 + off) = make_uint2(0u, 0u);
+    }
+    __syncthreads();
+    if (t < kCW) reinterpret_cast<int *>(jb.rec + 64 + 64 * m)[t] = xsum[t];
+    if (t == 0) reinterpret_cast<float *>(jb.rec)[m] = __fdiv_rn(gam, s);
+    return;
+  }
   float a = 0.0f;
   for (int v = t; v < nv; v += kQThreads) {
     float f[8];
@@ -751,9 +814,12 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
     }
     sm.abort_flag = 0;
     for (int s = 0; s < kStages; ++s) sm.stage_tag[s] = s;
-    sm.seq_tag = p.ctl[kCtlSeq] << 9;  // tags: (launch sequence << 9) | (call + 1)
     fence_barrier_init();
   }
+  // the set-up launch writes the call table and the records: wait for it (a
+  // no-op when the launch does not overlap it)
+  pdl_wait_primary();
+  if (tid == 0) sm.seq_tag = p.ctl[kCtlSeq] << 9;  // tags: (launch sequence << 9) | (call + 1)
   {
     const uint32_t *src = reinterpret_cast<const uint32_t *>(p.table);
     uint32_t *dst = reinterpret_cast<uint32_t *>(sm.calls);
@@ -880,8 +946,18 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
             go = false;
             break;
           }
-          // the slot's previous stage has landed and been consumed: say so
-          // before arming it (see stage_ready)
+          const uint32_t fb = smem_u32(&sm.full[st]);
+          const uint32_t sb = ring + st * kStageBytes;
+          uint32_t tx = box;
+          if (rec != nullptr) tx += cbytes + (s == 0 ? H : 0);
+          mbar_arrive_expect_tx(fb, tx);
+          tma_load_2d(sb, map, s * P * (kPiece / 8), j * kGroupRows, fb, pol);
+          if (rec != nullptr) {
+            if (s == 0)
+              bulk_g2s(sb + cofs, rec, H + cbytes, fb, pol_rec);
+            else
+              bulk_g2s(sb + cofs + H, rec + H + s * cbytes, cbytes, fb, pol_rec);
+          }
           if (i >= kStages)
             asm volatile("st.release.cta.shared.s32 [%0], %1;" ::"r"(smem_u32(&sm.stage_tag[st])), "r"(i) : "memory");
           if (qmode && s == 0) {
@@ -897,18 +973,6 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
             e.pk = pk;
             e.ci = ci;
             asm volatile("st.release.cta.shared.s32 [%0], %1;" ::"r"(smem_u32(&e.seq)), "r"(k + 1) : "memory");
-          }
-          const uint32_t fb = smem_u32(&sm.full[st]);
-          const uint32_t sb = ring + st * kStageBytes;
-          uint32_t tx = box;
-          if (rec != nullptr) tx += cbytes + (s == 0 ? H : 0);
-          mbar_arrive_expect_tx(fb, tx);
-          tma_load_2d(sb, map, s * P * (kPiece / 8), j * kGroupRows, fb, pol);
-          if (rec != nullptr) {
-            if (s == 0)
-              bulk_g2s(sb + cofs, rec, H + cbytes, fb, pol_rec);
-            else
-              bulk_g2s(sb + cofs + H, rec + H + s * cbytes, cbytes, fb, pol_rec);
           }
           issued = i + 1;
           s += kProd;
