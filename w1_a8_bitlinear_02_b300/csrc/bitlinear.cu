@@ -991,7 +991,8 @@ bl_status bitlinear_forward_chain(const bl_chain_call *calls, int n, void *ws, s
   void (*kern)(chain::Params) =
       many ? (dep ? &chain::chain_kernel<true, true> : &chain::chain_kernel<true, false>)
            : (dep ? &chain::chain_kernel<false, true> : &chain::chain_kernel<false, false>);
-  s = ensure_smem(dev, reinterpret_cast<const void *>(kern), chain::kSmemBytes);
+  const int smem = chain::smem_bytes(many, dep);
+  s = ensure_smem(dev, reinterpret_cast<const void *>(kern), smem);
   if (s != BL_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // the call table into the workspace (its parameters are kept by value)
@@ -1007,7 +1008,7 @@ bl_status bitlinear_forward_chain(const bl_chain_call *calls, int n, void *ws, s
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(sms));
   cfg.blockDim = dim3(chain::kThreads);
-  cfg.dynamicSmemBytes = chain::kSmemBytes;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   // and it may start while the set-up kernel runs: it waits for it
   // (griddepcontrol) after initialising its barriers

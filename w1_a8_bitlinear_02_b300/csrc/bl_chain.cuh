@@ -111,9 +111,19 @@ constexpr int kInBlockBytes = kHeader + kMaxK;
 // group's first slab, whose header travels with it).
 __host__ __device__ constexpr int codes_ofs(int M) { return kGroupRows * kPiece * piece_cap(M); }
 constexpr int kStageBytes = 37 * 1024;
-constexpr int kStages = 4;
-constexpr int kSmemFixed = 45 * 1024;     // barriers, partial sums and the call table
-constexpr int kSmemBytes = 1024 + kSmemFixed + kStages * kStageBytes + kInBlockBytes;
+// Ring stages: five in the one-token streaming form (no many-token call, no
+// input quantised in the block), whose fixed region is small and which needs
+// no in-block codes area; four in the other forms.
+constexpr int kStagesMax = 5;
+__host__ __device__ constexpr int stages_of(bool many, bool dep) { return (!many && !dep) ? 5 : 4; }
+// Token rows of the group-sum buffers: every token of a many-token call, else
+// the two teams' one-token sums (see Item).
+__host__ __device__ constexpr int sum_rows(bool many) { return many ? 16 : 2; }
+// Barriers, partial sums and the call table.
+__host__ __device__ constexpr int smem_fixed(bool many) { return (many ? 45 : 31) * 1024; }
+__host__ __device__ constexpr int smem_bytes(bool many, bool dep) {
+  return 1024 + smem_fixed(many) + stages_of(many, dep) * kStageBytes + (dep ? kInBlockBytes : 0);
+}
 
 // Control words at the start of the workspace (bytes 0..255), then the
 // call table, the records, the output words.
@@ -181,12 +191,11 @@ struct Params {
 // Row sums of one-token groups meet in one of kGB buffers, each with an
 // mbarrier the group's warps arrive on once their shares are added; only the
 // warp that writes the group's rows waits.  No warp can be kStages + 1 groups
-// ahead of another (each group takes at least one stage), so kGB > kStages + 1
+// ahead of another (each group takes at least one stage), so kGB > kStagesMax + 1
 // keeps a buffer from being reused before its group is written.
 constexpr int kGB = 8;
-static_assert(kGB > kStages + 1, "group buffers");
+static_assert(kGB > kStagesMax + 1, "group buffers");
 static_assert(kGB % kTeams == 0 && kCW % kTeams == 0, "teams");
-static_assert(kStages % kProd == 0, "each producer owns whole ring slots");
 static_assert(kThreads <= 20 * 32, "the kernel's register budget assumes at most 20 warps");
 
 // This block's share of a call, built once per launch: the first of its
@@ -222,19 +231,20 @@ struct __align__(16) Item {
   int pad[2];
 };
 constexpr int kTQ = 16;
-constexpr int kTB = 8;  // group-sum buffers per team (a team's warps are at most 4 of its groups apart)
+constexpr int kTB = 8;  // group-sum buffers per team (a team's warps are at most kStages of its groups apart)
 
-struct Smem {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+template <bool MANY>
+struct SmemT {
+  uint64_t full[kStagesMax];
+  uint64_t empty[kStagesMax];
   uint64_t gbar[kGB];
   float fred[kCW];
   int xcls[2][kCW];  // code sums of in-block inputs by piece class (p mod 16), by call parity
-  int32_t gsum[kGB][kMaxTok][kGroupRows];  // by group buffer, token, row
-  float gcm[kGB][kMaxTok];                 // the tokens' output scales c, by group buffer
+  int32_t gsum[kGB][sum_rows(MANY)][kGroupRows];  // by group buffer, token, row
+  float gcm[kGB][sum_rows(MANY)];                 // the tokens' output scales c, by group buffer
   uint32_t seq_tag;
   int abort_flag;
-  int stage_tag[kStages];  // the stage each ring slot was last armed for (written by its producer)
+  int stage_tag[kStagesMax];  // the stage each ring slot was last armed for (written by the producer that armed it)
   CallBlk cb[kMaxCalls];  // this block's share of each call
   Item tq[kTeams][kTQ];   // the teams' group queues (every call in the fast form)
   uint64_t tbar[kTeams][kTB];  // their group-sum barriers (the sums in gsum, flat)
@@ -245,10 +255,14 @@ struct Smem {
   Call calls[kMaxCalls];  // the call table, copied in once
 };
 static_assert(sizeof(Item) == 48, "queue entry");
-static_assert(kTeams * kTB * kGroupRows <= kGB * kMaxTok * kGroupRows, "team sums inside gsum");
+static_assert(kTeams * kTB <= kGB * sum_rows(false), "team sums inside gsum");
+static_assert(kMaxTok <= sum_rows(true), "every token's sums");
 static_assert(sizeof(CallBlk) == 16, "one 16-byte load a call");
-static_assert(sizeof(Smem) <= kSmemFixed, "fixed shared-memory region");
-static_assert(kSmemBytes <= 227 * 1024, "shared memory of one block");
+static_assert(sizeof(SmemT<false>) <= smem_fixed(false) && sizeof(SmemT<true>) <= smem_fixed(true),
+              "fixed shared-memory region");
+static_assert(smem_bytes(false, false) <= 227 * 1024 && smem_bytes(false, true) <= 227 * 1024 &&
+                  smem_bytes(true, false) <= 227 * 1024 && smem_bytes(true, true) <= 227 * 1024,
+              "shared memory of one block");
 
 // ------------------------------------------------------------ set-up kernels
 // The set-up launch before each chain: the call table into the workspace
@@ -457,15 +471,16 @@ __device__ __forceinline__ bool gave_up() {
 // Wait for ring stage `it` to land.  A parity wait on a slot is only sound
 // once the slot's previous stage (it - kStages) has landed: before that, the
 // phase two back has the same parity and the wait would pass at once.  A
-// warp that processed stage it - kStages saw it land (bit 3 of `seen`, the
-// warp's record of which of the last four stages it processed); a warp that
-// skipped it (another team's row group) first waits for the producer to
-// arm the slot for `it`, which it does only after the slot's previous stage
-// was consumed.  Bounded; false when the block must stop.
+// warp that processed stage it - kStages saw it land (bit kStages - 1 of
+// `seen`, the warp's record of which of the last kStages stages it
+// processed); a warp that skipped it (another team's row group) first waits
+// for the slot to be armed for `it`, which happens only after the slot's
+// previous stage was consumed.  Bounded; false when the block must stop.
+template <int kStages>
 __device__ __forceinline__ bool stage_ready(const uint64_t *full, const int *stage_tag, int it, uint32_t seen,
                                             volatile int *abort_flag) {
   const int st = it % kStages;
-  if (!(seen & 8u)) {
+  if (!(seen & (1u << (kStages - 1)))) {
     const long long t0 = clock64();
     while (true) {
       int tag;
@@ -601,6 +616,7 @@ __device__ __forceinline__ void stage_one(uint32_t sbase, uint32_t abase, int pc
 // (slab pieces p with p mod 16 == cls), added up per class while the codes
 // are written (nq: the block's count of such calls, picking the class-sum
 // buffer).  Returns false (in every thread) when the block must stop.
+template <class Smem>
 __device__ __forceinline__ bool quantise_in_block(const Call &c, uint32_t slot, uint32_t want, int tid, int cls,
                                                   int nq, Smem &sm, volatile int *abort_flag, int &xw) {
   const int warp = tid >> 5, lane = tid & 31;
@@ -793,11 +809,13 @@ __device__ __forceinline__ void stage_mma(uint32_t trow, uint32_t act, uint32_t 
 // so chains without them keep the streaming form's register allocation.
 template <bool MANY, bool DEP>
 __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant__ Params p) {
+  constexpr int kStages = stages_of(MANY, DEP);
+  using Smem = SmemT<MANY>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;  // stages start 1 KB aligned (TMA needs 128 bytes)
   Smem &sm = *reinterpret_cast<Smem *>(smem_raw + (base - raw));
-  const uint32_t ring = base + kSmemFixed;
+  const uint32_t ring = base + smem_fixed(MANY);
   const uint32_t inb = ring + kStages * kStageBytes;  // codes quantised in this block
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -825,7 +843,7 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
     uint32_t *dst = reinterpret_cast<uint32_t *>(sm.calls);
     const int words = p.n * static_cast<int>(sizeof(Call) / 4);
     for (int w = tid; w < words; w += kThreads) dst[w] = src[w];
-    for (int i = tid; i < kGB * kMaxTok * kGroupRows; i += kThreads) (&sm.gsum[0][0][0])[i] = 0;
+    for (int i = tid; i < static_cast<int>(sizeof(sm.gsum) / 4); i += kThreads) (&sm.gsum[0][0][0])[i] = 0;
   }
   __syncthreads();
   // this block's share of each call (one thread a call), then the calls'
@@ -886,11 +904,14 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
 
   if (warp >= kCW) {
     // ------------------------------------------------ producers: records and weight stages.
-    // Stage i of the block is issued by producer i mod kProd (its ring slot,
-    // as kStages is a multiple of kProd); each producer takes up only the
-    // calls that hold one of its stages (from the stage prefix sums), so the
-    // per-call and per-stage issue work is spread over kProd threads on
-    // different schedulers.
+    // Stage i of the block is issued by producer i mod kProd into ring slot
+    // i mod kStages; each producer takes up only the calls that hold one of
+    // its stages (from the stage prefix sums), so the per-call and per-stage
+    // issue work is spread over kProd threads on different schedulers.  A
+    // slot's stages may belong to different producers, so a producer first
+    // waits until the slot was armed for its previous stage (the slot's tag)
+    // and only then waits on that stage's empty phase: never a parity wait
+    // two phases behind.
     static_assert((kProd & (kProd - 1)) == 0, "stage owner by mask");
     const int q = warp - kCW;
     if (lane == 0) {
@@ -941,7 +962,21 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
         for (int i = cur.ib + d; i < cur.ib + len; i += kProd) {
           const int j = static_cast<int>(cur.e.x) + g * G;
           const int st = i % kStages;
-          if (i >= kStages && (!mbar_wait(smem_u32(&sm.empty[st]), ((i / kStages) - 1) & 1) || *abort_flag)) {
+          bool armed = true;
+          if (i >= kStages) {
+            const long long t0 = clock64();
+            while (true) {
+              int tag;
+              asm volatile("ld.acquire.cta.shared.s32 %0, [%1];" : "=r"(tag) : "r"(smem_u32(&sm.stage_tag[st])) : "memory");
+              if (tag == i - kStages) break;
+              if (*abort_flag || clock64() - t0 > kWaitLimitCycles || gave_up()) {
+                atomicOr(&g_dev_error, kDevErrTimeout);
+                armed = false;
+                break;
+              }
+            }
+          }
+          if (i >= kStages && (!armed || !mbar_wait(smem_u32(&sm.empty[st]), ((i / kStages) - 1) & 1) || *abort_flag)) {
             *abort_flag = 1;
             go = false;
             break;
@@ -982,9 +1017,21 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
           }
         }
       }
-      // no copy into this block's shared memory may be in flight at exit
+      // no copy into this block's shared memory may be in flight at exit:
+      // done once stage j landed, or once its slot was armed again (which
+      // needs stage j consumed; never a parity wait two phases behind)
       for (int j = issued - kStages < 0 ? 0 : issued - kStages; j < issued; ++j)
-        if (j % kProd == q) mbar_wait(smem_u32(&sm.full[j % kStages]), (j / kStages) & 1);
+        if (j % kProd == q) {
+          const uint32_t bar = smem_u32(&sm.full[j % kStages]);
+          const long long t0 = clock64();
+          while (!mbar_try_wait(bar, (j / kStages) & 1)) {
+            if (*static_cast<volatile int *>(&sm.stage_tag[j % kStages]) != j) break;
+            if (clock64() - t0 > kWaitLimitCycles) {
+              atomicOr(&g_dev_error, kDevErrTimeout);
+              break;
+            }
+          }
+        }
     }
     __syncwarp();
   } else {
@@ -997,7 +1044,7 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
     int nbar = 0;     // grid barriers passed
     int ng1 = 0;      // row groups done (team, group buffer, writer and phase)
     int nq = 0;       // calls whose input this block quantised
-    uint32_t seen = 0xFu;  // bit b: this warp processed stage it - 1 - b (stages before 0 count as seen)
+    uint32_t seen = (1u << kStages) - 1u;  // bit b: this warp processed stage it - 1 - b (stages before 0 count as seen)
     if (qmode) {
       // ---- every call in the fast form: this team's groups from its queue
       const int team = warp / kTW, tw = warp % kTW;
@@ -1041,7 +1088,7 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
         int xw = 0;
         for (int s = 0; s < nslab; ++s) {
           const int it = it0 + s, st = it % kStages;
-          if (!stage_ready(sm.full, sm.stage_tag, it, seen, abort_flag)) {
+          if (!stage_ready<kStages>(sm.full, sm.stage_tag, it, seen, abort_flag)) {
             *abort_flag = 1;
             break;
           }
@@ -1117,7 +1164,7 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
             int xw = 0;
             for (int s = 0; s < nslab; ++s, ++it) {
               const int st = it % kStages;
-              if (!stage_ready(sm.full, sm.stage_tag, it, seen, abort_flag)) {
+              if (!stage_ready<kStages>(sm.full, sm.stage_tag, it, seen, abort_flag)) {
                 *abort_flag = 1;
                 break;
               }
@@ -1235,7 +1282,7 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
             int xs[4] = {0, 0, 0, 0};  // code sums of tokens 8u + 2tt + q over this warp's pieces (u, q)
             for (int s = 0; s < nslab; ++s, ++it) {
               const int st = it % kStages;
-              if (*abort_flag || !stage_ready(sm.full, sm.stage_tag, it, seen, abort_flag)) {
+              if (*abort_flag || !stage_ready<kStages>(sm.full, sm.stage_tag, it, seen, abort_flag)) {
                 *abort_flag = 1;
                 break;
               }
@@ -1286,7 +1333,7 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
             int xwv[kDp4aTok] = {0, 0, 0, 0};
             for (int s = 0; s < nslab; ++s, ++it) {
               const int st = it % kStages;
-              if (*abort_flag || !stage_ready(sm.full, sm.stage_tag, it, seen, abort_flag)) {
+              if (*abort_flag || !stage_ready<kStages>(sm.full, sm.stage_tag, it, seen, abort_flag)) {
                 *abort_flag = 1;
                 break;
               }
@@ -1383,7 +1430,7 @@ __global__ void __launch_bounds__(20 * 32, 1) chain_kernel(const __grid_constant
         int acc[4] = {0, 0, 0, 0}, acc2[4] = {0, 0, 0, 0};
         for (int s = 0; s < nslab; ++s, ++it) {
           const int st = it % kStages;
-          if (!stage_ready(sm.full, sm.stage_tag, it, seen, abort_flag)) {
+          if (!stage_ready<kStages>(sm.full, sm.stage_tag, it, seen, abort_flag)) {
             *abort_flag = 1;
             break;
           }
