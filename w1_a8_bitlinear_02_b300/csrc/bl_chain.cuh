@@ -1,5 +1,5 @@
-// Decode chain: a sequence of M = 1 BitLinear forwards in one persistent
-// launch.  A call may read an earlier call's output as its input.
+// Decode chain: a sequence of BitLinear forwards of 1 to 16 tokens in one
+// persistent launch.  A call may read an earlier call's output as its input.
 //
 // A decode step runs the projections of every layer one after another
 // ("BitNet b1.58 2B4T" architecture: QKV, O, FFN up, FFN down per layer;
@@ -7,13 +7,14 @@
 // section 2).  As separate launches each call pays a kernel boundary although
 // its packed weights -- static inputs -- are a fraction of a microsecond of
 // HBM time.  Here one block per SM stays resident for the whole chain:
-//   * its producer thread streams the block's rows of every call, call after
-//     call, into one ring of shared-memory stages by TMA: the weights of later
-//     calls arrive while earlier calls compute, limited only by the ring's
-//     size ("pack-store-load-unpack-compute", 微软AI大模型炸场：0.4GB,
-//     blog.csdn.net/2401_84494441, section 3, GPU bullet, carried across
-//     calls);
-//   * the consumer warps run the calls in order over the block's rows.
+//   * its four producer threads stream the block's rows of every call, call
+//     after call, into one ring of shared-memory stages by TMA (stage i is
+//     producer i mod 4's): the weights of later calls arrive while earlier
+//     calls compute, limited only by the ring's size ("pack-store-load-
+//     unpack-compute", 微软AI大模型炸场：0.4GB, blog.csdn.net/2401_84494441,
+//     section 3, GPU bullet, carried across calls);
+//   * the 16 consumer warps, in two teams of 8, run the calls in order over
+//     the block's rows.
 //
 // Rows, one lane each.  A call's rows form groups of 32 consecutive rows,
 // dealt out to the blocks round-robin, each call's deal continuing where the
@@ -27,15 +28,18 @@
 // groups with no swizzle; and one copy per stage keeps the producer's issue
 // cost (a TMA instruction waits behind the consumers' shared-memory traffic)
 // to two instructions per stage with the record's.
-// The 16 consumer warps split each slab's pieces among themselves; every lane of a warp needs the same 64 activation codes, which
-// are broadcast from shared memory.  A lane adds its row's pieces with the
+// Row groups alternate between the two teams; the 8 warps of a team split
+// each slab's pieces by class (piece p mod 8, rotated from call to call);
+// every lane of a warp needs the same 64 activation codes, which are
+// broadcast from shared memory.  A lane adds its row's pieces with the
 // masked dp4a (the bytes of (word & (3 << 2i)) are the codes c = q + 1 times
 // 4^i; the 4^i factor is removed exactly at the end; sum c*x - X = sum q*x,
 // X = the warp's sum of activation codes) across all slabs of the group; the
-// 16 warps' partial sums then meet in shared memory once per group and one
-// warp writes y = fl32(acc * c), c = fl32(gamma / s).  No per-row reduction,
-// no copy of the activation codes per warp, and K of any length splits the
-// same way.
+// team's partial sums then meet in shared memory once per group and one warp
+// writes y = fl32(acc * c), c = fl32(gamma / s).  No per-row reduction, no
+// copy of the activation codes per warp, and K of any length splits the same
+// way.  Calls of 2-4 tokens share the code planes across the tokens' dp4a;
+// calls of 5-16 tokens run their pieces on the int8 mma.sync form.
 //
 // The activation codes (per-token absmax, "20亿参数仅0.4GB" page, section 2,
 // item 2) of a call come one of two ways:
