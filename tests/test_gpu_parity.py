@@ -484,6 +484,50 @@ def test_chain_long_row_groups_alternating_teams(bl):
             assert_bits_equal(ys[i].cpu().numpy(), outs[i], f"long groups call {i}")
 
 
+def _independent_chain(bl, specs, seed, launches=1):
+    """A chain of independent one-token calls (their own x, their own y): every
+    call takes the fast form, so the producers hand row groups to the two
+    teams through their queues.  Whole outputs against the oracle after each
+    launch on one workspace."""
+    calls, refs = [], []
+    for i, (N, K, dtype, act) in enumerate(specs):
+        packed, gamma, p_ref, g_ref = pack_both(bl, N, K, 0.02, seed + i)
+        x = wl.activations(1, K, "outliers1pct", seed + 500 + i, "cpu", dtype)
+        y = torch.empty((1, N), dtype=torch.float32, device=DEV)
+        calls.append(dict(packed=packed, gamma=gamma, x=x.to(DEV), y=y, N=N, K=K, act=act))
+        f = oracle.forward_packed_relu2 if act else oracle.forward_packed
+        refs.append(f(p_ref, g_ref, N, K, x.float().numpy()))
+    ws = bl.chain_workspace(calls, DEV)
+    for _ in range(launches):
+        for c in calls:
+            c["y"].fill_(float("nan"))
+        bl.bitlinear_forward_chain(calls, ws)
+        torch.cuda.synchronize()
+        assert bl.device_error() == 0
+        for i, (c, r) in enumerate(zip(calls, refs)):
+            assert_bits_equal(c["y"].cpu().numpy(), r, f"independent chain call {i}")
+
+
+def test_chain_independent_team_queues(bl):
+    """Independent one-token calls of one, two and seven slabs a group; calls
+    with fewer row groups than blocks (most blocks and one team idle) and with
+    two groups a block; ragged N, bf16 and fp32 x, ReLU2 inputs and a K that is
+    not a multiple of 8; three launches on one workspace."""
+    bf, f32 = torch.bfloat16, torch.float32
+    specs = [(64, 2560, bf, 0), (300, 6912, bf, 1), (9472, 2560, bf, 0), (640, 28672, bf, 0),
+             (2560, 6912, f32, 0), (1000, 999, f32, 0), (4736, 8192, bf, 0), (33, 64, bf, 1)]
+    _independent_chain(bl, specs, 1300, launches=3)
+
+
+def test_chain_independent_most_calls(bl):
+    """The most calls a chain takes (240), all independent and small: the
+    blocks' per-call entries and the stage and group prefix sums over the
+    whole call table."""
+    shapes = [(64, 64), (96, 448), (200, 1000), (320, 2560), (37, 130)]
+    specs = [(shapes[i % 5][0], shapes[i % 5][1], torch.bfloat16, i % 7 == 3) for i in range(240)]
+    _independent_chain(bl, specs, 1400)
+
+
 def test_chain_unaligned_and_odd_k(bl):
     """K not a multiple of 8 and an input that starts off a 16-byte boundary
     take the element-by-element activation path."""
