@@ -342,7 +342,9 @@ typedef struct bl_chain_call {
 BL_API bl_status bitlinear_chain_workspace_bytes(const bl_chain_call *calls, int n, size_t *bytes);
 
 /* A decode chain: up to 240 BitLinear forwards of 1 to 16 tokens run in order
- * in one persistent launch (one block per SM, all resident).  Each call's
+ * in one persistent launch (one block per SM, all resident), after a short
+ * set-up launch on the same stream (the call table into ws, the inputs no
+ * earlier call writes quantised) that the persistent launch overlaps.  Each call's
  * result equals, bit for bit, bitlinear_forward (or bitlinear_forward_relu2)
  * of its x as it stands when the call runs in sequence.
  * The packed weights of later calls stream in while earlier calls compute
