@@ -528,6 +528,33 @@ def test_chain_independent_most_calls(bl):
     _independent_chain(bl, specs, 1400)
 
 
+def test_chain_headline_step_full(bl):
+    """The decode step the bench times, as it times it: the 30 layers' 120
+    projections of the ~2B workload (391 MB of packed weights, each call its
+    own x, drawn as the bench draws them), one chain launch on a reused
+    workspace; every call's whole output against the oracle."""
+    calls = []
+    for mt in wl.matrices("decode_2b", layers=30):
+        W = wl.weight(mt.N, mt.K, mt.std, mt.seed, DEV)
+        packed, gamma = bl.bitlinear_pack_weights(W)
+        del W
+        x = wl.activations(1, mt.K, mt.x_kind, mt.seed + 500, DEV, torch.bfloat16)
+        y = torch.empty((1, mt.N), dtype=torch.float32, device=DEV)
+        calls.append(dict(packed=packed, gamma=gamma, x=x, y=y, N=mt.N, K=mt.K))
+    assert len(calls) == 120
+    ws = bl.chain_workspace(calls, DEV)
+    for _ in range(2):
+        for c in calls:
+            c["y"].fill_(float("nan"))
+        bl.bitlinear_forward_chain(calls, ws)
+        torch.cuda.synchronize()
+        assert bl.device_error() == 0
+    for i, c in enumerate(calls):
+        ref = oracle.forward_packed(c["packed"].cpu().numpy(), float(c["gamma"].item()), c["N"], c["K"],
+                                    c["x"].float().cpu().numpy())
+        assert_bits_equal(c["y"].cpu().numpy(), ref, f"headline step call {i}")
+
+
 def test_chain_unaligned_and_odd_k(bl):
     """K not a multiple of 8 and an input that starts off a 16-byte boundary
     take the element-by-element activation path."""
