@@ -555,6 +555,39 @@ def test_chain_headline_step_full(bl):
         assert_bits_equal(c["y"].cpu().numpy(), ref, f"headline step call {i}")
 
 
+def test_chain_100b_sweep_sampled(bl):
+    """The 100B-class sweep the bench times: 80 layers' 160 calls (9.4 GB of
+    packed weights resident), one chain launch at one token and one at eight;
+    the first and last call of each shape (whole outputs) against the oracle
+    (the oracle needs seconds per 100B-class call, so the rest is sampled)."""
+    mats = wl.matrices("decode_100b")
+    assert len(mats) == 160
+    packs = []
+    for mt in mats:
+        W = wl.weight(mt.N, mt.K, mt.std, mt.seed, DEV)
+        packs.append(bl.bitlinear_pack_weights(W))
+        del W
+    checked = [0, 1, len(mats) - 2, len(mats) - 1]
+    for M in (1, 8):
+        calls = []
+        for mt, (packed, gamma) in zip(mats, packs):
+            x = wl.activations(M, mt.K, mt.x_kind if M == 1 else "outliers1pct", mt.seed + 500 + M, DEV,
+                               torch.bfloat16)
+            y = torch.full((M, mt.N), float("nan"), dtype=torch.float32, device=DEV)
+            calls.append(dict(packed=packed, gamma=gamma, x=x, y=y, N=mt.N, K=mt.K))
+        bl.bitlinear_forward_chain(calls)
+        torch.cuda.synchronize()
+        assert bl.device_error() == 0
+        for i in (checked if M == 1 else checked[1:3]):
+            c = calls[i]
+            ref = oracle.forward_packed(c["packed"].cpu().numpy(), float(c["gamma"].item()), c["N"], c["K"],
+                                        c["x"].float().cpu().numpy())
+            assert_bits_equal(c["y"].cpu().numpy(), ref, f"100B sweep M={M} call {i}")
+        for c in calls:
+            assert not torch.isnan(c["y"]).any(), "an output left unwritten"
+        del calls
+
+
 def test_chain_unaligned_and_odd_k(bl):
     """K not a multiple of 8 and an input that starts off a 16-byte boundary
     take the element-by-element activation path."""
