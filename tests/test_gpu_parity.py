@@ -588,6 +588,37 @@ def test_chain_100b_sweep_sampled(bl):
         del calls
 
 
+@pytest.mark.parametrize("M", [8, 16, 64])
+def test_chain_batched_step_sampled(bl, M):
+    """Batched decode as the bench times it through the chain: the 30 layers'
+    120 projections with M tokens (1 % outlier channels), the token rows in
+    slices of 16 (each slice its own call), at most 240 calls a launch; the
+    whole outputs of a sample of calls (every projection kind, first and last
+    layers) against the oracle, every output written."""
+    mats = wl.matrices("decode_2b", layers=30)
+    items = []
+    for mt in mats:
+        W = wl.weight(mt.N, mt.K, mt.std, mt.seed, DEV)
+        packed, gamma = bl.bitlinear_pack_weights(W)
+        del W
+        x = wl.activations(M, mt.K, "outliers1pct", mt.seed + 600 + M, DEV, torch.bfloat16)
+        y = torch.full((M, mt.N), float("nan"), dtype=torch.float32, device=DEV)
+        items.append(dict(packed=packed, gamma=gamma, x=x, y=y, N=mt.N, K=mt.K))
+    calls = [dict(packed=it["packed"], gamma=it["gamma"], x=it["x"][h:h + 16], y=it["y"][h:h + 16],
+                  N=it["N"], K=it["K"]) for it in items for h in range(0, M, 16)]
+    for i in range(0, len(calls), 240):
+        bl.bitlinear_forward_chain(calls[i:i + 240])
+    torch.cuda.synchronize()
+    assert bl.device_error() == 0
+    for i in (0, 1, 2, 3, len(items) - 4, len(items) - 3, len(items) - 2, len(items) - 1):
+        it = items[i]
+        ref = oracle.forward_packed(it["packed"].cpu().numpy(), float(it["gamma"].item()), it["N"], it["K"],
+                                    it["x"].float().cpu().numpy())
+        assert_bits_equal(it["y"].cpu().numpy(), ref, f"batched step M={M} projection {i}")
+    for it in items:
+        assert not torch.isnan(it["y"]).any(), "an output left unwritten"
+
+
 def test_chain_unaligned_and_odd_k(bl):
     """K not a multiple of 8 and an input that starts off a 16-byte boundary
     take the element-by-element activation path."""
