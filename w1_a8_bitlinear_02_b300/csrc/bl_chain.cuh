@@ -213,6 +213,10 @@ struct __align__(16) CallBlk {
 };
 constexpr uint32_t kCbFast = 1u << 30;
 constexpr uint32_t kCbRec = 1u << 31;
+static_assert(piece_cap(1) < 256 && piece_cap(2) < 256 && piece_cap(kMaxTok) < 256 &&
+                  slabs_of(kPiece * (kMaxK / 64), 1) < 256 && slabs_of(kPiece * (kMaxK / 64), 2) < 256 &&
+                  slabs_of(kPiece * (kMaxK / 64), kMaxTok) < 256 && kMaxK / 64 < 1024 && kMaxTok <= 16,
+              "CallBlk::pk's fields hold the largest call");
 
 // When every call of the chain takes the fast form (one token, input
 // quantised ahead, no barrier), the producers hand the block's row groups to
